@@ -1,0 +1,129 @@
+"""fp64 CPU oracle for row-wise softmax -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU
+baseline / reference leg may import this package.  The CUDA library and its
+Python binding never do; the two sides share no code.
+
+The arithmetic lives in ``oracle.c`` (plain C, double precision):
+
+* ``softmax_rows`` -- the three-pass safe softmax of each row, the definition
+  in "5.2 CUDA Online Softmax 实现优化" §1.1 and "Softmax 数值稳定性与
+  IO-Aware Attention" §三, plus LSE = m + log d ("从原始Softmax到在线Softmax",
+  section "softmax形式推导").
+* ``online_state`` -- the element-by-element (m, d) recurrence,
+  "5.2 CUDA Online Softmax 实现优化" §2.1.
+* ``merge_state`` -- the merge of two partial states,
+  "5.2 CUDA Online Softmax 实现优化" §4.1.
+
+Readings where the pages are silent (also listed in the C source): the empty
+state (-inf, 0) is the merge identity (exp(-inf - b) := 0); an all -inf row
+gives y = 0, m = -inf, d = 0, LSE = -inf.
+
+Every function is pinned by ``tests/test_oracle.py`` to values the pages print,
+closed forms, mpmath brute force and library special cases.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F32 = 0
+BF16 = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so next to it (plain gcc, -O2)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", tmp, _SRC, "-lm"]
+        )
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i64, dp, vp = ctypes.c_int64, ctypes.POINTER(ctypes.c_double), ctypes.c_void_p
+            lib.oracle_softmax_rows.argtypes = [vp, ctypes.c_int, i64, vp, i64, vp, vp, vp, vp, ctypes.c_int]
+            lib.oracle_softmax_rows.restype = ctypes.c_int
+            lib.oracle_online_state.argtypes = [vp, i64, dp, dp]
+            lib.oracle_online_state.restype = None
+            lib.oracle_merge_state.argtypes = [ctypes.c_double] * 4 + [dp, dp]
+            lib.oracle_merge_state.restype = None
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else ctypes.c_void_p(a.ctypes.data)
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def softmax_rows(x: np.ndarray, dtype: int | None = None, rows=None, *, want_y: bool = True,
+                 nthreads: int | None = None):
+    """Three-pass fp64 softmax of rows of a row-major matrix.
+
+    ``x`` is a 2-D float32 array, or a 2-D uint16 array of bf16 bit patterns.
+    ``rows`` selects rows (default: all).  Returns ``(y, m, d, lse)`` as
+    float64 arrays; ``y`` is None when ``want_y`` is False.
+    """
+    x = np.ascontiguousarray(x)
+    if x.ndim != 2:
+        raise ValueError("x must be 2-D")
+    if dtype is None:
+        dtype = F32 if x.dtype == np.float32 else BF16 if x.dtype == np.uint16 else None
+    if dtype is None or (dtype == F32 and x.dtype != np.float32) or (dtype == BF16 and x.dtype != np.uint16):
+        raise TypeError("x must be float32 (F32) or uint16 bf16 bits (BF16)")
+    M, N = x.shape
+    if rows is None:
+        idx = None
+        nrows = M
+    else:
+        idx = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        if idx.size and (idx.min() < 0 or idx.max() >= M):
+            raise IndexError("row index out of range")
+        nrows = idx.size
+    y = np.empty((nrows, N), np.float64) if want_y else None
+    m = np.empty(nrows, np.float64)
+    d = np.empty(nrows, np.float64)
+    lse = np.empty(nrows, np.float64)
+    if nrows == 0:
+        return y, m, d, lse
+    rc = _load().oracle_softmax_rows(_ptr(x), dtype, N, _ptr(idx), nrows, _ptr(y), _ptr(m), _ptr(d),
+                                     _ptr(lse), nthreads or default_threads())
+    if rc != 0:
+        raise RuntimeError("oracle_softmax_rows rejected its arguments")
+    return y, m, d, lse
+
+
+def online_state(xs) -> tuple[float, float]:
+    """The (m, d) recurrence over a 1-D sequence, starting from (-inf, 0)."""
+    a = np.ascontiguousarray(np.asarray(xs, dtype=np.float64).reshape(-1))
+    m, d = ctypes.c_double(), ctypes.c_double()
+    _load().oracle_online_state(_ptr(a) if a.size else None, a.size, ctypes.byref(m), ctypes.byref(d))
+    return m.value, d.value
+
+
+def merge_state(a, b) -> tuple[float, float]:
+    """Merge two partial states ``a = (m_a, d_a)`` and ``b = (m_b, d_b)``."""
+    m, d = ctypes.c_double(), ctypes.c_double()
+    _load().oracle_merge_state(float(a[0]), float(a[1]), float(b[0]), float(b[1]), ctypes.byref(m),
+                               ctypes.byref(d))
+    return m.value, d.value

@@ -1,0 +1,185 @@
+/*
+ * oracle.c -- fp64 CPU oracle for row-wise softmax.
+ *
+ * TEST INFRASTRUCTURE ONLY.  The test suite, the package smoke check and the
+ * benchmark's CPU-baseline / reference leg are the only callers.  The CUDA
+ * library never calls, links or includes anything here, and nothing here is
+ * taken from the CUDA library: the two share no code.
+ *
+ * What it computes, in double precision, written as the plain definitions:
+ *
+ *  oracle_softmax_rows -- the three-pass safe softmax of a row
+ *      ("5.2 CUDA Online Softmax 实现优化", §1.1; "Softmax 数值稳定性与
+ *       IO-Aware Attention", §三):
+ *          pass 1:  m   = max_j x_j
+ *          pass 2:  d   = sum_j exp(x_j - m)
+ *          pass 3:  y_j = exp(x_j - m) / d
+ *      and the log-sum-exp  LSE = m + log(d)
+ *      ("从原始Softmax到在线Softmax", section "softmax形式推导").
+ *
+ *  oracle_online_state -- the element-by-element (m, d) recurrence
+ *      ("5.2 CUDA Online Softmax 实现优化", §2.1):
+ *          m_{k+1} = max(m_k, x_k)
+ *          d_{k+1} = d_k * exp(m_k - m_{k+1}) + exp(x_k - m_{k+1})
+ *
+ *  oracle_merge_state -- the merge of two partial states
+ *      ("5.2 CUDA Online Softmax 实现优化", §4.1; "Softmax 数值稳定性与
+ *       IO-Aware Attention", §4.1):
+ *          m = max(m_a, m_b)
+ *          d = d_a * exp(m_a - m) + d_b * exp(m_b - m)
+ *
+ * Readings where the pages are silent:
+ *  - exp(a - b) is taken as 0 whenever a = -inf.  So the empty state
+ *    (-inf, 0) is the identity of the merge and of the recurrence, as in the
+ *    worked merge of "从原始Softmax到在线Softmax" (section "手推小例子": the
+ *    first merge uses scale_old = 0 for m_old = -inf), and no -inf - (-inf)
+ *    is ever evaluated.
+ *  - A row whose entries are all -inf has y = 0, m = -inf, d = 0, LSE = -inf.
+ *  - bf16 inputs are widened exactly (bf16 -> fp32 -> fp64).
+ *
+ * Rows are independent, so they are spread over POSIX threads; inside a row
+ * the three passes run in plain index order.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_F32 0
+#define ORACLE_BF16 1
+
+/* Element i of a row-major matrix of the given dtype, widened exactly. */
+static double load_elem(const void* x, int dtype, int64_t i) {
+  if (dtype == ORACLE_F32) return (double)((const float*)x)[i];
+  uint32_t bits = (uint32_t)((const uint16_t*)x)[i] << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+/* exp(a - b), with exp(-inf - b) := 0 (the empty-state reading above). */
+static double scaled_exp(double a, double b) {
+  if (a == -INFINITY) return 0.0;
+  return exp(a - b);
+}
+
+/* Three-pass safe softmax of row `row`; y may be NULL (state only). */
+static void softmax_one_row(const void* x, int dtype, int64_t N, int64_t row,
+                            double* y, double* m_out, double* d_out,
+                            double* lse_out) {
+  const int64_t base = row * N;
+
+  /* pass 1: the row maximum */
+  double m = -INFINITY;
+  for (int64_t j = 0; j < N; ++j) {
+    double v = load_elem(x, dtype, base + j);
+    if (v > m) m = v;
+  }
+
+  /* pass 2: the denominator */
+  double d = 0.0;
+  for (int64_t j = 0; j < N; ++j) d += scaled_exp(load_elem(x, dtype, base + j), m);
+
+  /* pass 3: normalise */
+  if (y) {
+    for (int64_t j = 0; j < N; ++j) {
+      y[j] = (m == -INFINITY) ? 0.0 : scaled_exp(load_elem(x, dtype, base + j), m) / d;
+    }
+  }
+  if (m_out) *m_out = m;
+  if (d_out) *d_out = d;
+  if (lse_out) *lse_out = (m == -INFINITY) ? -INFINITY : m + log(d);
+}
+
+typedef struct {
+  const void* x;
+  int dtype;
+  int64_t N;
+  const int64_t* rows;
+  int64_t nrows;
+  double *y, *m, *d, *lse;
+  int64_t begin, end; /* slice of [0, nrows) handled by this thread */
+} oracle_job;
+
+static void* oracle_worker(void* arg) {
+  oracle_job* job = (oracle_job*)arg;
+  for (int64_t i = job->begin; i < job->end; ++i) {
+    int64_t row = job->rows ? job->rows[i] : i;
+    softmax_one_row(job->x, job->dtype, job->N, row,
+                    job->y ? job->y + i * job->N : NULL,
+                    job->m ? job->m + i : NULL, job->d ? job->d + i : NULL,
+                    job->lse ? job->lse + i : NULL);
+  }
+  return NULL;
+}
+
+/*
+ * Softmax of selected rows of a row-major matrix x (dtype ORACLE_F32 or
+ * ORACLE_BF16, N columns).  rows[i] is the i-th row to compute, or rows ==
+ * NULL for rows 0..nrows-1.  Outputs are indexed by i: y is nrows x N,
+ * m / d / lse have nrows entries; each output may be NULL.  Returns 0, or -1
+ * on a bad argument.
+ */
+int oracle_softmax_rows(const void* x, int dtype, int64_t N,
+                        const int64_t* rows, int64_t nrows, double* y,
+                        double* m, double* d, double* lse, int nthreads) {
+  if (!x || N < 1 || nrows < 0) return -1;
+  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return -1;
+  if (nrows == 0) return 0;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > nrows) nthreads = (int)nrows;
+
+  pthread_t* tids = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+  oracle_job* jobs = (oracle_job*)calloc((size_t)nthreads, sizeof(oracle_job));
+  if (!tids || !jobs) {
+    free(tids);
+    free(jobs);
+    return -1;
+  }
+  for (int t = 0; t < nthreads; ++t) {
+    oracle_job job = {x, dtype, N, rows, nrows, y, m, d, lse,
+                      nrows * t / nthreads, nrows * (t + 1) / nthreads};
+    jobs[t] = job;
+    if (t == 0) continue; /* the calling thread takes slice 0 */
+    if (pthread_create(&tids[t], NULL, oracle_worker, &jobs[t]) != 0) {
+      oracle_worker(&jobs[t]); /* no thread available: do it inline */
+      tids[t] = (pthread_t)0;
+    }
+  }
+  oracle_worker(&jobs[0]);
+  for (int t = 1; t < nthreads; ++t)
+    if (tids[t] != (pthread_t)0) pthread_join(tids[t], NULL);
+  free(tids);
+  free(jobs);
+  return 0;
+}
+
+/*
+ * The online recurrence over xs[0..n), one element at a time, starting from
+ * the empty state (m, d) = (-inf, 0).
+ */
+void oracle_online_state(const double* xs, int64_t n, double* m_out, double* d_out) {
+  double m = -INFINITY, d = 0.0;
+  for (int64_t k = 0; k < n; ++k) {
+    double m_new = xs[k] > m ? xs[k] : m;
+    if (m_new == -INFINITY) continue; /* -inf element into an empty state: still empty */
+    d = d * scaled_exp(m, m_new) + scaled_exp(xs[k], m_new);
+    m = m_new;
+  }
+  *m_out = m;
+  *d_out = d;
+}
+
+/* Merge of two partial states (m_a, d_a) and (m_b, d_b). */
+void oracle_merge_state(double m_a, double d_a, double m_b, double d_b,
+                        double* m_out, double* d_out) {
+  double m = m_a > m_b ? m_a : m_b;
+  if (m == -INFINITY) {
+    *m_out = -INFINITY;
+    *d_out = 0.0;
+    return;
+  }
+  *m_out = m;
+  *d_out = d_a * scaled_exp(m_a, m) + d_b * scaled_exp(m_b, m);
+}

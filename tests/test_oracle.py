@@ -1,0 +1,330 @@
+"""Pins of the fp64 oracle to things other than itself (CPU only).
+
+Each test ties one part of the oracle to a value the pages print, a closed
+form, an exact invariant, a library special case, or a 50-digit brute force,
+so that a dropped term, a wrong sign, a wrong row index or a transposed
+operand fails at least one of them.
+"""
+import itertools
+import math
+import os
+import random
+
+import mpmath
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "p3_worked_examples.txt")
+
+
+def _parse_golden():
+    cases = []
+    with open(GOLDEN, encoding="utf-8") as fh:
+        for line in fh:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            kind, *fields = line.split()
+            kv = {}
+            for f in fields:
+                k, v = f.split("=", 1)
+                kv[k] = v
+            cases.append((kind, kv))
+    return cases
+
+
+def _vec(s):
+    return [float(t) for t in s.split(",")]
+
+
+def _f32(rows):
+    return np.asarray(rows, dtype=np.float32).reshape(len(rows), -1)
+
+
+def test_golden_worked_examples():
+    """Every worked example of "从原始Softmax到在线Softmax" (section "手推小例子")."""
+    cases = _parse_golden()
+    assert len(cases) >= 10
+    for kind, kv in cases:
+        tol = float(kv["tol"])
+        if kind == "softmax":
+            x = np.asarray(_vec(kv["x"]), dtype=np.float64)
+            # the printed inputs are decimal; feed the fp32 nearest (what a kernel would see)
+            y, m, d, lse = oracle.softmax_rows(_f32([x]))
+            assert np.allclose(y[0], _vec(kv["p"]), rtol=0, atol=tol), (kv, y)
+            if "sum" in kv:
+                assert abs(y[0].sum() - float(kv["sum"])) <= tol
+        elif kind == "cross_entropy":
+            x = _vec(kv["x"])
+            label = int(kv["label"])
+            y, m, d, lse = oracle.softmax_rows(_f32([x]))
+            xl = float(np.float32(x[label]))
+            assert abs((lse[0] - xl) - float(kv["loss"])) <= tol
+            assert abs(-math.log(y[0][label]) - float(kv["loss"])) <= tol
+        elif kind == "state":
+            x = _vec(kv["x"])
+            m, d = oracle.online_state(x)
+            assert m == float(kv["m"])
+            assert abs(d - float(kv["d"])) <= tol
+            _, m3, d3, _ = oracle.softmax_rows(np.asarray([x], dtype=np.float32), want_y=False)
+            assert abs(d3[0] - float(kv["d"])) <= tol
+        elif kind == "merge":
+            a = _vec(kv["a"])
+            b = _vec(kv["b"])
+            m, d = oracle.merge_state(a, b)
+            assert m == float(kv["m"])
+            assert abs(d - float(kv["d"])) <= tol
+            if "scale_old" in kv:
+                assert abs(math.exp(a[0] - m) - float(kv["scale_old"])) <= tol
+        else:  # pragma: no cover
+            raise AssertionError(f"unknown golden kind {kind}")
+
+
+def _mp_softmax(row):
+    """50-digit softmax of one row of finite values (brute force, independent of the oracle)."""
+    with mpmath.workdps(50):
+        xs = [mpmath.mpf(float(v)) for v in row]
+        m = max(xs)
+        es = [mpmath.e ** (v - m) for v in xs]
+        d = mpmath.fsum(es)
+        return [float(e / d) for e in es], float(m), float(d), float(m + mpmath.log(d))
+
+
+def test_mpmath_brute_force_rectangular():
+    """Non-square random inputs, each row against a 50-digit brute force (catches transposes and row indexing)."""
+    rng = np.random.default_rng(7)
+    for M, N in [(3, 5), (5, 3), (4, 17), (1, 1), (2, 64)]:
+        x = (rng.standard_normal((M, N)) * 4).astype(np.float32)
+        y, m, d, lse = oracle.softmax_rows(x)
+        for r in range(M):
+            ym, mm, dm, lm = _mp_softmax(x[r])
+            np.testing.assert_allclose(y[r], ym, rtol=1e-14, atol=0)
+            assert m[r] == mm
+            assert abs(d[r] - dm) <= 1e-14 * dm
+            assert abs(lse[r] - lm) <= 1e-14 * max(1.0, abs(lm))
+
+
+def test_row_sum_is_one():
+    x = synth.generate(synth.WORKLOADS["fp32_64x1024"])
+    y, m, d, lse = oracle.softmax_rows(x)
+    assert np.all(np.abs(y.sum(axis=1) - 1.0) <= 1e-12)
+    assert np.all(y >= 0)
+
+
+def test_shift_invariance_exact_shift():
+    """softmax(x + c) = softmax(x); m shifts by c, d is unchanged ("Softmax 数值稳定性与 IO-Aware Attention" §2.1)."""
+    rng = np.random.default_rng(1)
+    base = (np.round(rng.uniform(-8, 8, size=(6, 257)) * 1024) / 1024).astype(np.float32)
+    y0, m0, d0, l0 = oracle.softmax_rows(base)
+    for c in (1024.0, -1024.0):
+        shifted = (base.astype(np.float64) + c).astype(np.float32)
+        assert np.array_equal(shifted.astype(np.float64) - c, base.astype(np.float64))  # shift is exact
+        y1, m1, d1, l1 = oracle.softmax_rows(shifted)
+        np.testing.assert_allclose(y1, y0, rtol=1e-12, atol=0)
+        assert np.array_equal(m1, m0 + c)
+        np.testing.assert_allclose(d1, d0, rtol=1e-12)
+        np.testing.assert_allclose(l1, l0 + c, rtol=1e-14)
+
+
+def test_uniform_row_closed_form():
+    for N in (1, 2, 64, 1024, 4096):
+        x = np.full((2, N), 3.25, dtype=np.float32)
+        y, m, d, lse = oracle.softmax_rows(x)
+        assert np.all(y == 1.0 / N)
+        assert np.all(m == 3.25) and np.all(d == N)
+        np.testing.assert_allclose(lse, 3.25 + math.log(N), rtol=1e-15)
+
+
+def test_two_elements_logistic():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((50, 2)).astype(np.float32) * 5
+    y, _, _, _ = oracle.softmax_rows(x)
+    x64 = x.astype(np.float64)
+    expect = 1.0 / (1.0 + np.exp(x64[:, 1] - x64[:, 0]))
+    np.testing.assert_allclose(y[:, 0], expect, rtol=1e-14)
+    np.testing.assert_allclose(y[:, 1], 1.0 / (1.0 + np.exp(x64[:, 0] - x64[:, 1])), rtol=1e-14)
+
+
+def test_one_huge_value_is_one_hot_without_overflow():
+    """A single huge entry ("5.2 CUDA Online Softmax 实现优化" §2.3: exponents stay <= 0)."""
+    rng = np.random.default_rng(4)
+    for big in (1e4, 1e30):
+        x = rng.standard_normal((3, 100)).astype(np.float32)
+        x[:, 37] = big
+        y, m, d, lse = oracle.softmax_rows(x)
+        assert np.all(np.isfinite(y)) and np.all(np.isfinite(d))
+        assert np.all(y[:, 37] == 1.0)
+        assert np.all(np.delete(y, 37, axis=1) == 0.0)
+        assert np.all(m == np.float32(big)) and np.all(d == 1.0)
+
+
+def test_huge_negative_rows():
+    """Very negative entries ("Softmax 数值稳定性与 IO-Aware Attention" §9.2): behaves like the shifted row."""
+    x = np.full((1, 33), -1e30, dtype=np.float32)
+    y, m, d, lse = oracle.softmax_rows(x)
+    assert np.all(y == 1.0 / 33) and d[0] == 33.0
+    rng = np.random.default_rng(5)
+    z = (np.round(rng.uniform(-4, 4, size=(2, 40)) * 256) / 256).astype(np.float32)
+    shifted = (z.astype(np.float64) - 30000.0).astype(np.float32)
+    assert np.array_equal(shifted.astype(np.float64) + 30000.0, z.astype(np.float64))
+    y1, _, d1, _ = oracle.softmax_rows(shifted)
+    y0, _, d0, _ = oracle.softmax_rows(z)
+    np.testing.assert_allclose(y1, y0, rtol=1e-10)
+    np.testing.assert_allclose(d1, d0, rtol=1e-10)
+
+
+def test_masked_entries_reduce_to_shorter_row():
+    """-inf entries carry zero weight; the rest is the softmax of the unmasked entries."""
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((4, 20)).astype(np.float32)
+    mask = rng.random((4, 20)) < 0.4
+    mask[:, 3] = False
+    xm = np.where(mask, -np.inf, x).astype(np.float32)
+    y, m, d, lse = oracle.softmax_rows(xm)
+    for r in range(4):
+        keep = ~mask[r]
+        ym, mm, dm, lm = _mp_softmax(x[r][keep])
+        assert np.all(y[r][mask[r]] == 0.0)
+        np.testing.assert_allclose(y[r][keep], ym, rtol=1e-14)
+        assert m[r] == mm and abs(d[r] - dm) <= 1e-14 * dm
+
+
+def test_fully_masked_row_reading():
+    x = np.full((2, 7), -np.inf, dtype=np.float32)
+    x[1, 2] = 0.5
+    y, m, d, lse = oracle.softmax_rows(x)
+    assert np.all(y[0] == 0.0) and m[0] == -np.inf and d[0] == 0.0 and lse[0] == -np.inf
+    assert y[1, 2] == 1.0 and np.sum(y[1]) == 1.0 and d[1] == 1.0 and lse[1] == 0.5
+
+
+def test_log_softmax_identity():
+    """log y_j = x_j - LSE ("从原始Softmax到在线Softmax", log-softmax)."""
+    x = synth.generate(synth.WORKLOADS["fp32_64x1024"], nrows=8)
+    y, m, d, lse = oracle.softmax_rows(x)
+    np.testing.assert_allclose(np.log(y), x.astype(np.float64) - lse[:, None], rtol=0, atol=1e-12)
+
+
+def test_library_special_case_torch_and_scipy():
+    import scipy.special
+    import torch
+
+    x = synth.generate(synth.WORKLOADS["fp32_4096x4096"], row0=10, nrows=6)
+    y, m, d, lse = oracle.softmax_rows(x)
+    ref = torch.softmax(torch.from_numpy(x).double(), dim=-1).numpy()
+    np.testing.assert_allclose(y, ref, rtol=1e-13, atol=1e-300)
+    np.testing.assert_allclose(y, scipy.special.softmax(x.astype(np.float64), axis=1), rtol=1e-13, atol=1e-300)
+    np.testing.assert_allclose(lse, scipy.special.logsumexp(x.astype(np.float64), axis=1), rtol=1e-14)
+
+
+def test_online_recurrence_equals_three_pass():
+    """"5.2 CUDA Online Softmax 实现优化" §2.3: the online d equals the three-pass d."""
+    x = synth.generate(synth.WORKLOADS["fp32_64x1024"])
+    _, m3, d3, _ = oracle.softmax_rows(x, want_y=False)
+    for r in range(x.shape[0]):
+        m, d = oracle.online_state(x[r].astype(np.float64))
+        assert m == m3[r]
+        assert abs(d - d3[r]) <= 1e-13 * d3[r]
+    rng = np.random.default_rng(8)
+    for n in range(1, 65):
+        row = (rng.standard_normal(n) * 10).astype(np.float32)
+        m, d = oracle.online_state(row.astype(np.float64))
+        _, mm, dm, _ = _mp_softmax(row)
+        assert m == mm and abs(d - dm) <= 1e-13 * dm
+
+
+def test_online_state_of_empty_and_masked_sequences():
+    assert oracle.online_state([]) == (-math.inf, 0.0)
+    assert oracle.online_state([-math.inf, -math.inf]) == (-math.inf, 0.0)
+    m, d = oracle.online_state([-math.inf, 1.0, -math.inf])
+    assert m == 1.0 and d == 1.0
+
+
+def _bracketings(states):
+    """Every full binary bracketing of the sequence, each merged with the oracle merge."""
+    if len(states) == 1:
+        yield states[0]
+        return
+    for k in range(1, len(states)):
+        for left in _bracketings(states[:k]):
+            for right in _bracketings(states[k:]):
+                yield oracle.merge_state(left, right)
+
+
+def test_merge_of_random_chunks_equals_whole_row():
+    """"Softmax 数值稳定性与 IO-Aware Attention" §4.1: cut a row at random, merge the chunk states in any
+    bracketing and either order; the result is the whole-row state."""
+    rng = random.Random(11)
+    nprng = np.random.default_rng(11)
+    for trial in range(60):
+        n = rng.randint(1, 40)
+        row = (nprng.standard_normal(n) * rng.choice([1.0, 5.0, 30.0])).astype(np.float64)
+        if trial % 5 == 0:
+            row[: n // 2] = -np.inf  # an all -inf chunk
+        _, mw, dw, _ = oracle.softmax_rows(row.astype(np.float32)[None, :], want_y=False)
+        row = row.astype(np.float32).astype(np.float64)
+        nchunks = rng.randint(1, 8 if trial % 2 else 5)
+        cuts = sorted(rng.randint(0, n) for _ in range(nchunks - 1))  # repeated cuts = empty chunks
+        bounds = [0] + cuts + [n]
+        states = [oracle.online_state(row[a:b]) for a, b in zip(bounds[:-1], bounds[1:])]
+        if all(s[0] == -math.inf for s in states):
+            continue
+        results = list(_bracketings(states)) if len(states) <= 5 else []
+        # left fold, right fold, and reversed order
+        acc = (-math.inf, 0.0)
+        for s in states:
+            acc = oracle.merge_state(acc, s)
+        results.append(acc)
+        acc = (-math.inf, 0.0)
+        for s in reversed(states):
+            acc = oracle.merge_state(s, acc)
+        results.append(acc)
+        for m, d in results:
+            assert m == mw[0]
+            assert abs(d - dw[0]) <= 1e-13 * dw[0], (trial, d, dw[0])
+
+
+def test_merge_identity_and_commutativity():
+    e = (-math.inf, 0.0)
+    assert oracle.merge_state(e, e) == e
+    assert oracle.merge_state(e, (2.0, 3.5)) == (2.0, 3.5)
+    assert oracle.merge_state((2.0, 3.5), e) == (2.0, 3.5)
+    a, b = (1.25, 2.0), (-0.5, 7.0)
+    assert oracle.merge_state(a, b) == oracle.merge_state(b, a)
+    m, d = oracle.merge_state(a, b)
+    assert m == 1.25 and abs(d - (2.0 + 7.0 * math.exp(-1.75))) <= 1e-15 * d
+
+
+def test_bf16_input_is_widened_exactly():
+    rng = np.random.default_rng(9)
+    f = (rng.standard_normal((5, 300)) * 3).astype(np.float32)
+    bits = synth.f32_to_bf16(f)
+    widened = synth.bf16_to_f32(bits)
+    yb, mb, db, lb = oracle.softmax_rows(bits)
+    yf, mf, df, lf = oracle.softmax_rows(widened)
+    assert np.array_equal(yb, yf) and np.array_equal(mb, mf) and np.array_equal(db, df)
+
+
+def test_row_selection_matches_full_computation():
+    x = synth.generate(synth.WORKLOADS["fp32_64x1024"])
+    y, m, d, lse = oracle.softmax_rows(x)
+    sel = [63, 0, 17, 17, 5]
+    ys, ms, ds, ls = oracle.softmax_rows(x, rows=sel)
+    assert np.array_equal(ys, y[sel]) and np.array_equal(ms, m[sel]) and np.array_equal(ds, d[sel])
+
+
+def test_threads_do_not_change_results():
+    x = synth.generate(synth.WORKLOADS["fp32_64x1024"])
+    a = oracle.softmax_rows(x, nthreads=1)
+    b = oracle.softmax_rows(x, nthreads=7)
+    for u, v in zip(a, b):
+        assert np.array_equal(u, v)
+
+
+def test_bad_arguments_are_rejected():
+    with pytest.raises(TypeError):
+        oracle.softmax_rows(np.zeros((2, 2), np.float64))
+    with pytest.raises(IndexError):
+        oracle.softmax_rows(np.zeros((2, 2), np.float32), rows=[2])
