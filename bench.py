@@ -1,0 +1,424 @@
+"""Benchmark: row-wise online softmax on GB300, one JSON line on rank 0.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one softmax over the whole workload matrix (every kernel the path launches for it).
+The default workload is fp32 4096 x 4096 (x = 3 N(0,1), seed 1), the shape measured on
+"5.2 CUDA Online Softmax 实现优化" §2.4.  Inputs are synthetic (synth/) and already resident in
+HBM when timing starts.
+
+Metric: effective HBM GB/s with minimum bytes = read x once + write y once (2 M N s), plus
+rows/s and the fraction of the HBM roofline.  L2: steps rotate over enough input/output buffer
+sets that every step's operands are evicted from L2 (126 MB) before they are used again; each
+batch of steps is one CUDA graph replay, timed with CUDA events on the launching stream.
+
+Multi-GPU (torchrun): rows are independent, so each rank processes its own shard (its own
+rows of the same seeded matrix) with no data-path collective: weak scaling, max time over ranks.
+
+--impl reference times the fp64 CPU oracle (oracle/) on the host cores, on a bounded sample of
+the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "softmax effective HBM GB/s (read+write once) and % of GB300 HBM peak, rows/s"
+DEFAULT_WORKLOAD = "fp32_4096x4096"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES_NOMINAL = 126 * 2 ** 20
+# The pages' best number on this workload: V3 register-cached one-pass, A100 80GB SXM4, fp32,
+# M = N = 4096, about 1672 GB/s ("5.2 CUDA Online Softmax 实现优化" §6.3).  Another machine.
+PAGE_GBS = {"fp32_4096x4096": 1672.0}
+
+
+# ----------------------------------------------------------------------------------------------
+# helpers shared with the tests (no GPU needed)
+# ----------------------------------------------------------------------------------------------
+
+def dist_env() -> tuple[int, int, int]:
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def shard_row0(rank: int, rows_per_rank: int) -> int:
+    """First global row of a rank's shard: rank r owns rows [r * M, (r + 1) * M)."""
+    return rank * rows_per_rank
+
+
+def reduce_max(value: float, world: int) -> float:
+    """Max of a float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    backend = dist.get_backend()
+    dev = torch.device("cuda", torch.cuda.current_device()) if backend == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def measured_hbm_peak() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "row_wise_online_gb300", "csrc", "*"))):
+        with open(p, "rb") as fh:
+            h.update(os.path.basename(p).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str) -> float | None:
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current sources."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}__{workload}.md")
+    try:
+        text = open(path, encoding="utf-8").read()
+    except OSError:
+        return None
+    src = re.search(r"source_hash:\s*([0-9a-f]+)", text)
+    tb = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not src or not tb or src.group(1) != kernel_source_hash():
+        return None
+    return float(tb.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.proc = None
+        self.out = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", str(period_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm = [float(r[1]) for r in rows]
+        smax = max(float(r[2]) for r in rows)
+        power = [float(r[3]) for r in rows]
+        loaded = [s for s, p in zip(sm, power) if p >= 0.6 * max(power)] or sm
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.strip() == "Active"})
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(power)}
+
+
+# ----------------------------------------------------------------------------------------------
+# the CUDA arm
+# ----------------------------------------------------------------------------------------------
+
+def _pinned_workload(w: synth.Workload, row0: int):
+    import torch
+
+    tdt = torch.float32 if w.dtype == synth.F32 else torch.int16
+    host = torch.empty((w.M, w.N), dtype=tdt).pin_memory()
+    synth.fill(w, host.data_ptr(), row0, w.M)
+    if w.dtype == synth.BF16:
+        host = host.view(torch.bfloat16)
+    return host
+
+
+def _graph_time(run_step, nsteps: int, stream, graph_batch: int):
+    """Capture `graph_batch` steps in a CUDA graph, replay to cover exactly nsteps; return ms."""
+    import torch
+
+    full, rest = divmod(nsteps, graph_batch)
+    graphs = []
+    for count in ((graph_batch,) if full else ()) + ((rest,) if rest else ()):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(count):
+                run_step(i)
+        graphs.append((g, count))
+    return graphs, full, rest
+
+
+def bench_ours(args) -> dict | None:
+    import torch
+
+    import row_wise_online_gb300 as rwo
+    from row_wise_online_gb300 import _build
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    if rank == 0 or not _build.up_to_date():
+        _build.build()
+    barrier(world)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    w = synth.WORKLOADS[args.workload]
+    row0 = shard_row0(rank, w.M)
+    host_x = _pinned_workload(w, row0)
+    set_bytes = 2 * w.M * w.N * w.elem_bytes
+    nbuf = 1 if set_bytes >= 4 * L2_BYTES_NOMINAL else max(2, -(-4 * L2_BYTES_NOMINAL // set_bytes))
+    xs = [host_x.to(dev) for _ in range(nbuf)]
+    ys = [torch.empty_like(xs[0]) for _ in range(nbuf)]
+    stream = torch.cuda.Stream(device=dev)
+    variant = {"auto": rwo.VARIANT_AUTO, "reg": rwo.VARIANT_ONEREAD_REG, "smem": rwo.VARIANT_ONEREAD_SMEM,
+               "twopass": rwo.VARIANT_TWOPASS, "splitrow": rwo.VARIANT_SPLITROW}[args.variant]
+
+    def measure(var: int, nsteps: int, warm: int, clocks: bool = False):
+        def step(i):
+            rwo.softmax_rows_ex(xs[i % nbuf], ys[i % nbuf], variant=var, stream=stream)
+
+        with torch.cuda.stream(stream):
+            for i in range(warm):
+                step(i)
+        stream.synchronize()
+        used = rwo.last_variant()
+        graph_batch = max(nbuf, min(nsteps, 256) // nbuf * nbuf)
+        graphs, full, rest = _graph_time(step, nsteps, stream, graph_batch)
+        with torch.cuda.stream(stream):
+            graphs[0][0].replay()  # untimed: page in the graph
+        stream.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        sampler = ClockSampler(dev.index) if clocks else None
+        if sampler:
+            time.sleep(0.3)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(full):
+                graphs[0][0].replay()
+            if rest:
+                graphs[-1][0].replay()
+            ev1.record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        clk = sampler.stop() if sampler else None
+        ms = ev0.elapsed_time(ev1)
+        status = rwo.get_status(stream)
+        if status != rwo.OK:
+            raise rwo.SoftmaxError(status, "kernel status after timing")
+        return ms, used, clk
+
+    ms_local, used, clk = measure(variant, args.steps, args.warmup, clocks=True)
+    ms = reduce_max(ms_local, world)
+    per_step_ms = ms / args.steps
+    bytes_step = w.min_bytes
+    gbs = world * bytes_step * args.steps / (ms * 1e-3) / 1e9
+    rows_s = world * w.M * args.steps / (ms * 1e-3)
+
+    # Other variants on the same workload (fewer steps), for the record.
+    variants = {}
+    if world == 1 and not args.quick:
+        for name, var in (("oneread_reg", rwo.VARIANT_ONEREAD_REG), ("oneread_smem", rwo.VARIANT_ONEREAD_SMEM),
+                          ("twopass", rwo.VARIANT_TWOPASS), ("splitrow", rwo.VARIANT_SPLITROW)):
+            if var == used:
+                continue
+            try:
+                k = max(8, args.steps // 8)
+                vms, _, _ = measure(var, k, 3)
+                variants[name] = {"gbs": round(bytes_step * k / (vms * 1e-3) / 1e9, 1),
+                                  "us_per_step": round(vms * 1e3 / k, 2)}
+            except rwo.SoftmaxError as e:
+                variants[name] = {"unsupported": str(e)}
+
+    # End to end through the public host-buffer call: H2D of x, kernels, D2H of y, every step.
+    e2e = None
+    if not args.no_e2e:
+        y_host = torch.empty_like(host_x).pin_memory()
+        for _ in range(2):
+            rwo.softmax_rows_host(host_x, y_host)
+        k = max(3, min(args.steps, 20))
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(k):
+            rwo.softmax_rows_host(host_x, y_host)
+        torch.cuda.synchronize(dev)
+        t = reduce_max(time.perf_counter() - t0, world)
+        e2e = {"value": round(world * bytes_step * k / t / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": w.M * w.N * w.elem_bytes, "d2h_bytes_per_step": w.M * w.N * w.elem_bytes,
+               "steps": k, "ms_per_step": round(t * 1e3 / k, 4)}
+
+    if rank != 0:
+        return None
+    peak, peak_kind = measured_hbm_peak()
+    kernel = {rwo.VARIANT_ONEREAD_REG: "k_oneread_reg", rwo.VARIANT_ONEREAD_SMEM: "k_oneread_tma",
+              rwo.VARIANT_TWOPASS: "k_twopass", rwo.VARIANT_SPLITROW: "k_splitrow"}[used]
+    achieved = bytes_step / (per_step_ms * 1e-3) / 1e9
+    traffic = profiled_traffic(kernel, w.name)
+    result = {
+        "metric": METRIC,
+        "value": round(gbs, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(per_step_ms, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": round(gbs / world / PAGE_GBS[w.name], 3) if w.name in PAGE_GBS else None,
+        "vs_baseline_ref": ("pages' V3 register one-pass kernel, ~1672 GB/s on A100 80GB SXM4 "
+                            "(another machine: context, not the target)") if w.name in PAGE_GBS else None,
+        "dtype": "f32" if w.dtype == synth.F32 else "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "rows_total": w.M * world,
+                   "variant": rwo.VARIANT_NAMES[used], "parallelism": f"rows sharded over {world} GPU(s)",
+                   "l2": (f"{nbuf} rotating x/y buffer sets ({nbuf * set_bytes >> 20} MiB > L2)" if nbuf > 1
+                          else "inputs larger than L2"),
+                   "timing": "CUDA graph replays between CUDA events on the launching stream"},
+        "rows_per_s": round(rows_s, 1),
+        "pct_of_8tbs": round(100 * gbs / world / NOMINAL_HBM_GBS, 2),
+        "pct_of_measured_peak": round(100 * gbs / world / peak, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s", "kernel": kernel,
+                     "algorithmic_bytes_per_launch": bytes_step},
+        "gpu_launches": args.steps,
+        "e2e": e2e,
+        "clocks": clk,
+        "variants": variants,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w)
+    return result
+
+
+# ----------------------------------------------------------------------------------------------
+# the oracle (CPU) arms
+# ----------------------------------------------------------------------------------------------
+
+def cpu_baseline(w: synth.Workload, target_s: float = 1.5) -> dict:
+    """The fp64 oracle as it stands, on the host cores, on a bounded sample of the workload."""
+    import oracle
+
+    threads = oracle.default_threads()
+    probe = synth.generate(w, row0=0, nrows=min(w.M, 4 * threads))
+    t0 = time.perf_counter()
+    oracle.softmax_rows(probe, nthreads=threads)
+    per_row = (time.perf_counter() - t0) / probe.shape[0]
+    nrows = int(max(threads, min(w.M, target_s / max(per_row, 1e-9))))
+    x = synth.generate(w, row0=0, nrows=nrows)
+    t0 = time.perf_counter()
+    oracle.softmax_rows(x, nthreads=threads)
+    t = time.perf_counter() - t0
+    gbs = 2 * nrows * w.N * w.elem_bytes / t / 1e9
+    return {"value": round(gbs, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"rows 0..{nrows - 1} of {w.name} ({nrows} x {w.N}), fp64 three-pass, "
+                      f"{t:.2f} s wall on {threads} threads (~{t * threads:.0f} CPU-s)",
+            "rows_per_s": round(nrows / t, 1)}
+
+
+def bench_reference(args) -> dict | None:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+
+    w = synth.WORKLOADS[args.workload]
+    threads = oracle.default_threads()
+    probe = synth.generate(w, row0=0, nrows=min(w.M, 2 * threads))
+    t0 = time.perf_counter()
+    oracle.softmax_rows(probe, nthreads=threads)
+    per_row = (time.perf_counter() - t0) / probe.shape[0]
+    budget_s = 120.0  # the whole run, warm-up included
+    rows = int(max(1, min(w.M, budget_s / max(1, args.steps + args.warmup) / max(per_row, 1e-9))))
+    x = synth.generate(w, row0=0, nrows=rows)
+    for _ in range(args.warmup):
+        oracle.softmax_rows(x, nthreads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.softmax_rows(x, nthreads=threads)
+    t = time.perf_counter() - t0
+    gbs = 2 * rows * w.N * w.elem_bytes * args.steps / t / 1e9
+    sample = f"rows 0..{rows - 1} of {w.name} ({rows} x {w.N}) per step, fp64 three-pass oracle"
+    return {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3 / args.steps, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "M": w.M, "N": w.N, "rows_per_step": rows},
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--variant", default="auto", choices=["auto", "reg", "smem", "twopass", "splitrow"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--quick", action="store_true", help="skip the other-variant measurements")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    res = bench_reference(args) if args.impl == "reference" else bench_ours(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+    rank, world, _ = dist_env()
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,166 @@
+/*
+ * softmax_rows.h -- C ABI of the GB300 (sm_103a) row-wise online softmax library.
+ *
+ * Library: row_wise_online_gb300/lib/libsoftmax_rows.so.  Every compute call
+ * enqueues CUDA kernels on the caller's stream and returns at once; every step
+ * of the computation runs in the library's own kernels.
+ *
+ * The problem (as stated on "5.2 CUDA Online Softmax 实现优化", §1.1 and
+ * §2): for each row r of a row-major M x N matrix x,
+ *
+ *     m_r   = max_j x[r, j]
+ *     d_r   = sum_j exp(x[r, j] - m_r)
+ *     y[r,j]= exp(x[r, j] - m_r) / d_r
+ *     LSE_r = m_r + ln d_r      ("从原始Softmax到在线Softmax", log-sum-exp)
+ *
+ * computed with the online (m, d) recurrence (§2.1 of the same page): each
+ * thread folds its elements into a running max and a rescaled exp-sum, and
+ * partial states are merged with m = max(m1, m2),
+ * d = d1 e^(m1 - m) + d2 e^(m2 - m)  (§4.1; "Softmax 数值稳定性与 IO-Aware
+ * Attention" §4.1).  The empty state (-inf, 0) is the identity of that merge,
+ * so a fully masked (-inf) chunk, thread, warp or block contributes nothing
+ * and never produces NaN.  A row whose entries are all -inf gives y = 0,
+ * m = -inf, d = 0, LSE = -inf.
+ *
+ * Conventions shared by every call:
+ *  - Pointers are DEVICE pointers (except softmax_rows_host), owned by the
+ *    caller; the library keeps none of them after the call is enqueued.
+ *  - Matrices are row-major and contiguous: row r starts at element r * N.
+ *  - dtype is SOFTMAX_F32 (fp32 in / fp32 out) or SOFTMAX_BF16 (bf16 bit
+ *    patterns in / bf16 out, rounded to nearest even).  Arithmetic is fp32 in
+ *    both cases; exponentials use the hardware ex2 with a log2(e) prescale.
+ *  - State outputs m_out, d_out, lse_out are fp32 arrays of M entries; each
+ *    may be NULL.  m_out is the raw row maximum (bit-exact max of the inputs,
+ *    -0 and +0 equal).  d_out is relative to m_out, natural base.
+ *  - stream is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *  - M == 0 is a no-op returning SOFTMAX_OK.
+ *  - Return value: a softmax_status.  Argument errors are detected on the
+ *    host before anything is enqueued.  A CUDA launch error returns
+ *    SOFTMAX_ERR_CUDA (softmax_last_cuda_error() names it).  Errors found by a
+ *    kernel while it runs (a bounded wait that ran out) are recorded in a
+ *    per-device status word read by softmax_get_status().
+ */
+#ifndef ROW_WISE_ONLINE_SOFTMAX_ROWS_H
+#define ROW_WISE_ONLINE_SOFTMAX_ROWS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types. */
+enum softmax_dtype { SOFTMAX_F32 = 0, SOFTMAX_BF16 = 1 };
+
+/* Status codes. */
+enum softmax_status {
+  SOFTMAX_OK = 0,
+  SOFTMAX_ERR_INVALID_ARG = 1, /* NULL pointer, N < 1, M < 0, unknown dtype/variant, size overflow */
+  SOFTMAX_ERR_MISALIGNED = 2,  /* a forced vector/bulk-copy variant got a base or row pitch not 16-B aligned */
+  SOFTMAX_ERR_UNSUPPORTED = 3, /* a forced variant cannot take this shape (row too large, ...) */
+  SOFTMAX_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+  SOFTMAX_ERR_TIMEOUT = 5      /* a kernel's bounded wait ran out (reported by softmax_get_status) */
+};
+
+/* Kernel variants (softmax_rows_ex).  AUTO picks one from the shape. */
+enum softmax_variant {
+  SOFTMAX_VARIANT_AUTO = 0,
+  /* One read: the row is loaded once into registers with 128-bit loads (rows up to 8 KiB). */
+  SOFTMAX_VARIANT_ONEREAD_REG = 1,
+  /* One read: bulk copies (cp.async.bulk + mbarrier) stage whole rows in shared memory, a
+     warp-specialised persistent CTA normalises them and bulk-stores them (rows up to 64 KiB). */
+  SOFTMAX_VARIANT_ONEREAD_SMEM = 2,
+  /* Two passes over global memory: online fold with 128-bit loads, then re-read and normalise
+     (any N; the re-read is served from L2 while the row is still resident). */
+  SOFTMAX_VARIANT_TWOPASS = 3,
+  /* Split row: one row is spread over every CTA of the grid; CTAs of a thread-block cluster merge
+     (m, d) over distributed shared memory, clusters exchange 8-byte states through global memory
+     (for few, very long rows). */
+  SOFTMAX_VARIANT_SPLITROW = 4
+};
+
+/*
+ * softmax_rows -- y = softmax(x) along each row ("5.2 CUDA Online Softmax
+ * 实现优化", §2.2, the whole method).  x and y: device, M x N, dtype.  y may
+ * not overlap x unless y == x (in place).
+ */
+int softmax_rows(const void* x, void* y, int64_t M, int64_t N, int dtype, void* stream);
+
+/*
+ * softmax_rows_ex -- softmax_rows with optional per-row state outputs
+ * (m_out, d_out, lse_out: fp32[M] or NULL) and a forced variant.
+ * A forced variant that needs 16-byte alignment returns SOFTMAX_ERR_MISALIGNED
+ * when x, y or the row pitch N * sizeof(dtype) is not a multiple of 16;
+ * AUTO never does (it falls back to scalar-access kernels).
+ */
+int softmax_rows_ex(const void* x, void* y, float* m_out, float* d_out, float* lse_out, int64_t M,
+                    int64_t N, int dtype, int variant, void* stream);
+
+/*
+ * softmax_row_state -- only the per-row state (m, d) and LSE: the first pass
+ * of the online method ("5.2 CUDA Online Softmax 实现优化", §2.2, pass 1;
+ * "Softmax 数值稳定性与 IO-Aware Attention" §四, the mergeable state).  Reads x
+ * once; writes 12 bytes per row at most.  At least one of m_out, d_out,
+ * lse_out must be non-NULL.  With merge_states this lets a caller fold a row
+ * in pieces.
+ */
+int softmax_row_state(const void* x, float* m_out, float* d_out, float* lse_out, int64_t M,
+                      int64_t N, int dtype, void* stream);
+
+/*
+ * merge_states -- elementwise merge of two arrays of row states
+ * ("5.2 CUDA Online Softmax 实现优化", §4.1; "Softmax 数值稳定性与 IO-Aware
+ * Attention" §4.1):  m = max(m_a, m_b),  d = d_a e^(m_a - m) + d_b e^(m_b - m),
+ * with (-inf, 0) the identity.  Inputs: fp32[M] device arrays (all required).
+ * Outputs: fp32[M] device arrays, m_out and d_out required, lse_out optional.
+ * Outputs may alias the inputs of the same index (in place).
+ */
+int merge_states(const float* m_a, const float* d_a, const float* m_b, const float* d_b,
+                 float* m_out, float* d_out, float* lse_out, int64_t M, void* stream);
+
+/*
+ * softmax_rows_host -- softmax_rows on HOST buffers (x_host, y_host: M x N of
+ * dtype, ideally pinned).  Row blocks are copied host->device, normalised on
+ * the GPU and copied back, with copies and kernels of consecutive blocks
+ * overlapped on two internal streams.  Device staging memory is taken from
+ * the stream-ordered pool and released before return.  Returns when y_host
+ * holds the result (the call synchronises).  `stream` orders the work after
+ * earlier work on that stream.
+ */
+int softmax_rows_host(const void* x_host, void* y_host, int64_t M, int64_t N, int dtype,
+                      void* stream);
+
+/*
+ * softmax_get_status -- synchronises `stream`, then returns and clears the
+ * status word of the current device: SOFTMAX_OK, or the error a kernel
+ * recorded since the last call (SOFTMAX_ERR_TIMEOUT for a bounded wait that
+ * ran out).  SOFTMAX_ERR_CUDA if the synchronisation itself failed.
+ */
+int softmax_get_status(void* stream);
+
+/* A static, human-readable name for a status code. */
+const char* softmax_status_string(int status);
+
+/* The CUDA error string of the last SOFTMAX_ERR_CUDA on this host thread ("" if none). */
+const char* softmax_last_cuda_error(void);
+
+/* The variant (enum softmax_variant) the last successful compute call on this host thread ran. */
+int softmax_last_variant(void);
+
+/*
+ * softmax_debug_set_fault -- test hook.  fault = 1 makes the next
+ * split-row launches skip one cluster's state publication, so every other
+ * cluster's bounded wait runs out and the kernel records SOFTMAX_ERR_TIMEOUT
+ * instead of hanging; fault = 0 restores normal behaviour.  Returns the
+ * previous value.  Process-wide; not for production use.
+ */
+int softmax_debug_set_fault(int fault);
+
+/* The wait limit of the split-row exchange, in nanoseconds (default 200 ms).  Returns the old value. */
+int64_t softmax_debug_set_wait_limit_ns(int64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ROW_WISE_ONLINE_SOFTMAX_ROWS_H */

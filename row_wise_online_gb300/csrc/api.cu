@@ -1,0 +1,349 @@
+// api.cu -- the C ABI declared in include/softmax_rows.h.
+//
+// Host side only: argument validation, per-device properties, variant choice, the per-device
+// status word, and the host-buffer pipeline.  Every step of the computation runs in the
+// kernels of kernels_rowwise.cu, kernel_oneread_tma.cu and kernel_splitrow.cu.
+#include <mutex>
+#include <string>
+
+#include "../../include/softmax_rows.h"
+#include "launch.h"
+
+namespace rwo {
+
+__device__ unsigned g_status;  // per-device status word (kernels atomicOr status bits into it)
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[kMaxDevices];
+bool g_dev_ready[kMaxDevices];
+
+thread_local std::string t_last_cuda_error;
+thread_local int t_last_variant = SOFTMAX_VARIANT_AUTO;
+
+uint64_t g_exchange_wait_ns = 200ull * 1000 * 1000;  // 200 ms
+int g_debug_fault = 0;
+std::mutex g_debug_mutex;
+
+int cuda_fail(cudaError_t err) {
+  t_last_cuda_error = cudaGetErrorString(err);
+  return SOFTMAX_ERR_CUDA;
+}
+
+// Properties of the current device, queried once per device.
+int current_device_info(const DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return cuda_fail(err);
+  if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice);
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (!g_dev_ready[dev]) {
+    DeviceInfo info;
+    info.device = dev;
+    if ((err = cudaDeviceGetAttribute(&info.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (err = cudaDeviceGetAttribute(&info.max_smem_per_block_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                      dev)) != cudaSuccess ||
+        (err = cudaDeviceGetAttribute(&info.max_smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
+            cudaSuccess ||
+        (err = cudaDeviceGetAttribute(&info.max_threads_per_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev)) !=
+            cudaSuccess ||
+        (err = cudaDeviceGetAttribute(&info.l2_bytes, cudaDevAttrL2CacheSize, dev)) != cudaSuccess ||
+        (err = cudaDeviceGetAttribute(&info.cluster_launch, cudaDevAttrClusterLaunch, dev)) != cudaSuccess)
+      return cuda_fail(err);
+    void* status = nullptr;
+    if ((err = cudaGetSymbolAddress(&status, g_status)) != cudaSuccess) return cuda_fail(err);
+    info.status = static_cast<unsigned*>(status);
+    g_dev[dev] = info;
+    g_dev_ready[dev] = true;
+  }
+  *out = &g_dev[dev];
+  return SOFTMAX_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape and pointer checks shared by the row calls.  Returns a status; sets *noop for M == 0.
+int validate_rows(const void* x, int64_t M, int64_t N, int dtype, bool* noop) {
+  *noop = false;
+  if (!x) return SOFTMAX_ERR_INVALID_ARG;
+  if (dtype != SOFTMAX_F32 && dtype != SOFTMAX_BF16) return SOFTMAX_ERR_INVALID_ARG;
+  if (N < 1 || M < 0) return SOFTMAX_ERR_INVALID_ARG;
+  const int64_t s = elem_bytes(dtype);
+  if (N > INT64_MAX / s) return SOFTMAX_ERR_INVALID_ARG;
+  if (M > 0 && M > INT64_MAX / (N * s)) return SOFTMAX_ERR_INVALID_ARG;
+  if (M == 0) *noop = true;
+  return SOFTMAX_OK;
+}
+
+int run_variant(RowProblem& p, int variant, const DeviceInfo& dev) {
+  const bool aligned = aligned16(p.x) && (p.y == nullptr || aligned16(p.y)) &&
+                       (p.N * elem_bytes(p.dtype)) % 16 == 0;
+  const int64_t row_bytes = p.N * elem_bytes(p.dtype);
+  if (variant == SOFTMAX_VARIANT_AUTO) {
+    if (aligned) {
+      if (row_bytes <= 4096 && oneread_reg_fits(p, true))
+        variant = SOFTMAX_VARIANT_ONEREAD_REG;
+      else if (oneread_tma_fits(p, dev))
+        variant = SOFTMAX_VARIANT_ONEREAD_SMEM;
+      else if (p.M * 2 <= dev.sm_count && splitrow_fits(p, dev))
+        variant = SOFTMAX_VARIANT_SPLITROW;
+      else
+        variant = SOFTMAX_VARIANT_TWOPASS;
+    } else {
+      variant = (p.N <= 512 && oneread_reg_fits(p, false)) ? SOFTMAX_VARIANT_ONEREAD_REG
+                                                           : SOFTMAX_VARIANT_TWOPASS;
+    }
+  }
+  cudaError_t err;
+  switch (variant) {
+    case SOFTMAX_VARIANT_ONEREAD_REG:
+      if (!oneread_reg_fits(p, aligned)) return SOFTMAX_ERR_UNSUPPORTED;
+      err = launch_oneread_reg(p, aligned, dev);
+      break;
+    case SOFTMAX_VARIANT_ONEREAD_SMEM:
+      if (!aligned) return SOFTMAX_ERR_MISALIGNED;
+      if (!oneread_tma_fits(p, dev)) return SOFTMAX_ERR_UNSUPPORTED;
+      err = launch_oneread_tma(p, dev);
+      break;
+    case SOFTMAX_VARIANT_TWOPASS:
+      err = launch_twopass(p, aligned, dev);
+      break;
+    case SOFTMAX_VARIANT_SPLITROW:
+      if (!aligned) return SOFTMAX_ERR_MISALIGNED;
+      if (!splitrow_fits(p, dev)) return SOFTMAX_ERR_UNSUPPORTED;
+      err = launch_splitrow(p, dev);
+      break;
+    default:
+      return SOFTMAX_ERR_INVALID_ARG;
+  }
+  if (err != cudaSuccess) return cuda_fail(err);
+  t_last_variant = variant;
+  return SOFTMAX_OK;
+}
+
+}  // namespace
+
+uint64_t local_wait_limit_ns() { return 2000ull * 1000 * 1000; }  // 2 s: never reached normally
+
+uint64_t exchange_wait_limit_ns() {
+  std::lock_guard<std::mutex> lock(g_debug_mutex);
+  return g_exchange_wait_ns;
+}
+
+int debug_fault() {
+  std::lock_guard<std::mutex> lock(g_debug_mutex);
+  return g_debug_fault;
+}
+
+}  // namespace rwo
+
+using namespace rwo;
+
+extern "C" {
+
+int softmax_rows_ex(const void* x, void* y, float* m_out, float* d_out, float* lse_out, int64_t M,
+                    int64_t N, int dtype, int variant, void* stream) {
+  bool noop = false;
+  int st = validate_rows(x, M, N, dtype, &noop);
+  if (st != SOFTMAX_OK) return st;
+  if (!y) return SOFTMAX_ERR_INVALID_ARG;
+  if (variant < SOFTMAX_VARIANT_AUTO || variant > SOFTMAX_VARIANT_SPLITROW) return SOFTMAX_ERR_INVALID_ARG;
+  if (noop) return SOFTMAX_OK;
+  const DeviceInfo* dev = nullptr;
+  if ((st = current_device_info(&dev)) != SOFTMAX_OK) return st;
+  RowProblem p;
+  p.x = x;
+  p.y = y;
+  p.m_out = m_out;
+  p.d_out = d_out;
+  p.lse_out = lse_out;
+  p.M = M;
+  p.N = N;
+  p.dtype = dtype;
+  p.stream = static_cast<cudaStream_t>(stream);
+  return run_variant(p, variant, *dev);
+}
+
+int softmax_rows(const void* x, void* y, int64_t M, int64_t N, int dtype, void* stream) {
+  return softmax_rows_ex(x, y, nullptr, nullptr, nullptr, M, N, dtype, SOFTMAX_VARIANT_AUTO, stream);
+}
+
+int softmax_row_state(const void* x, float* m_out, float* d_out, float* lse_out, int64_t M, int64_t N,
+                      int dtype, void* stream) {
+  bool noop = false;
+  int st = validate_rows(x, M, N, dtype, &noop);
+  if (st != SOFTMAX_OK) return st;
+  if (!m_out && !d_out && !lse_out) return SOFTMAX_ERR_INVALID_ARG;
+  if (noop) return SOFTMAX_OK;
+  const DeviceInfo* dev = nullptr;
+  if ((st = current_device_info(&dev)) != SOFTMAX_OK) return st;
+  RowProblem p;
+  p.x = x;
+  p.m_out = m_out;
+  p.d_out = d_out;
+  p.lse_out = lse_out;
+  p.M = M;
+  p.N = N;
+  p.dtype = dtype;
+  p.stream = static_cast<cudaStream_t>(stream);
+  const bool aligned = aligned16(x) && (N * elem_bytes(dtype)) % 16 == 0;
+  cudaError_t err = launch_twopass(p, aligned, *dev);
+  if (err != cudaSuccess) return cuda_fail(err);
+  t_last_variant = SOFTMAX_VARIANT_TWOPASS;
+  return SOFTMAX_OK;
+}
+
+int merge_states(const float* m_a, const float* d_a, const float* m_b, const float* d_b, float* m_out,
+                 float* d_out, float* lse_out, int64_t M, void* stream) {
+  if (!m_a || !d_a || !m_b || !d_b || !m_out || !d_out || M < 0) return SOFTMAX_ERR_INVALID_ARG;
+  if (M == 0) return SOFTMAX_OK;
+  const DeviceInfo* dev = nullptr;
+  int st = current_device_info(&dev);
+  if (st != SOFTMAX_OK) return st;
+  cudaError_t err = launch_merge_states(m_a, d_a, m_b, d_b, m_out, d_out, lse_out, M,
+                                        static_cast<cudaStream_t>(stream), *dev);
+  if (err != cudaSuccess) return cuda_fail(err);
+  return SOFTMAX_OK;
+}
+
+int softmax_rows_host(const void* x_host, void* y_host, int64_t M, int64_t N, int dtype, void* stream) {
+  bool noop = false;
+  int st = validate_rows(x_host, M, N, dtype, &noop);
+  if (st != SOFTMAX_OK) return st;
+  if (!y_host) return SOFTMAX_ERR_INVALID_ARG;
+  if (noop) return SOFTMAX_OK;
+  const DeviceInfo* dev = nullptr;
+  if ((st = current_device_info(&dev)) != SOFTMAX_OK) return st;
+
+  const cudaStream_t user = static_cast<cudaStream_t>(stream);
+  const int64_t row_bytes = N * elem_bytes(dtype);
+  // Blocks of about 16 MiB: large enough for full-bandwidth copies, small enough to overlap.
+  int64_t block_rows = (int64_t(16) << 20) / row_bytes;
+  if (block_rows < 1) block_rows = 1;
+  if (block_rows > M) block_rows = M;
+  const int64_t nblocks = (M + block_rows - 1) / block_rows;
+  const int nbuf = nblocks > 1 ? 2 : 1;
+  const size_t buf_bytes = size_t(block_rows * row_bytes);
+
+  cudaStream_t lanes[2] = {nullptr, nullptr};
+  cudaEvent_t ev_start = nullptr, ev_done[2] = {nullptr, nullptr};
+  void* dbuf[2] = {nullptr, nullptr};
+  cudaError_t err = cudaSuccess;
+  int result = SOFTMAX_OK;
+
+  auto fail = [&](cudaError_t e) {
+    if (result == SOFTMAX_OK) result = cuda_fail(e);
+  };
+
+  for (int i = 0; i < nbuf && err == cudaSuccess; ++i) {
+    if ((err = cudaStreamCreateWithFlags(&lanes[i], cudaStreamNonBlocking)) != cudaSuccess) break;
+    if ((err = cudaEventCreateWithFlags(&ev_done[i], cudaEventDisableTiming)) != cudaSuccess) break;
+    // x and y of a block share one buffer: the kernels run in place.
+    if ((err = cudaMallocAsync(&dbuf[i], buf_bytes, user)) != cudaSuccess) break;
+  }
+  if (err == cudaSuccess) err = cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming);
+  if (err == cudaSuccess) err = cudaEventRecord(ev_start, user);
+  for (int i = 0; i < nbuf && err == cudaSuccess; ++i) err = cudaStreamWaitEvent(lanes[i], ev_start, 0);
+  if (err != cudaSuccess) fail(err);
+
+  for (int64_t b = 0; b < nblocks && result == SOFTMAX_OK; ++b) {
+    const int li = int(b % nbuf);
+    const int64_t r0 = b * block_rows;
+    const int64_t rows = (M - r0) < block_rows ? (M - r0) : block_rows;
+    const size_t bytes = size_t(rows * row_bytes);
+    const char* src = static_cast<const char*>(x_host) + r0 * row_bytes;
+    char* dst = static_cast<char*>(y_host) + r0 * row_bytes;
+    if ((err = cudaMemcpyAsync(dbuf[li], src, bytes, cudaMemcpyHostToDevice, lanes[li])) != cudaSuccess) {
+      fail(err);
+      break;
+    }
+    RowProblem p;
+    p.x = dbuf[li];
+    p.y = dbuf[li];
+    p.M = rows;
+    p.N = N;
+    p.dtype = dtype;
+    p.stream = lanes[li];
+    if ((st = run_variant(p, SOFTMAX_VARIANT_AUTO, *dev)) != SOFTMAX_OK) {
+      result = st;
+      break;
+    }
+    if ((err = cudaMemcpyAsync(dst, dbuf[li], bytes, cudaMemcpyDeviceToHost, lanes[li])) != cudaSuccess) {
+      fail(err);
+      break;
+    }
+  }
+  // Join the lanes back into the caller's stream, release staging memory, and wait.
+  for (int i = 0; i < nbuf; ++i) {
+    if (lanes[i] && ev_done[i]) {
+      if ((err = cudaEventRecord(ev_done[i], lanes[i])) != cudaSuccess) fail(err);
+      else if ((err = cudaStreamWaitEvent(user, ev_done[i], 0)) != cudaSuccess) fail(err);
+    }
+  }
+  for (int i = 0; i < nbuf; ++i)
+    if (dbuf[i] && (err = cudaFreeAsync(dbuf[i], user)) != cudaSuccess) fail(err);
+  if ((err = cudaStreamSynchronize(user)) != cudaSuccess) fail(err);
+  for (int i = 0; i < nbuf; ++i) {
+    if (ev_done[i]) cudaEventDestroy(ev_done[i]);
+    if (lanes[i]) cudaStreamDestroy(lanes[i]);
+  }
+  if (ev_start) cudaEventDestroy(ev_start);
+  return result;
+}
+
+int softmax_get_status(void* stream) {
+  const DeviceInfo* dev = nullptr;
+  int st = current_device_info(&dev);
+  if (st != SOFTMAX_OK) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned word = 0;
+  cudaError_t err = cudaStreamSynchronize(s);
+  if (err == cudaSuccess) err = cudaMemcpyAsync(&word, dev->status, sizeof word, cudaMemcpyDeviceToHost, s);
+  if (err == cudaSuccess) err = cudaMemsetAsync(dev->status, 0, sizeof word, s);
+  if (err == cudaSuccess) err = cudaStreamSynchronize(s);
+  if (err != cudaSuccess) return cuda_fail(err);
+  if (word & kStatusTimeout) return SOFTMAX_ERR_TIMEOUT;
+  return SOFTMAX_OK;
+}
+
+const char* softmax_status_string(int status) {
+  switch (status) {
+    case SOFTMAX_OK:
+      return "ok";
+    case SOFTMAX_ERR_INVALID_ARG:
+      return "invalid argument";
+    case SOFTMAX_ERR_MISALIGNED:
+      return "pointer or row pitch not 16-byte aligned for the forced variant";
+    case SOFTMAX_ERR_UNSUPPORTED:
+      return "the forced variant cannot take this shape";
+    case SOFTMAX_ERR_CUDA:
+      return "CUDA error";
+    case SOFTMAX_ERR_TIMEOUT:
+      return "a kernel's bounded wait ran out";
+    default:
+      return "unknown status";
+  }
+}
+
+const char* softmax_last_cuda_error(void) { return t_last_cuda_error.c_str(); }
+
+int softmax_last_variant(void) { return t_last_variant; }
+
+int softmax_debug_set_fault(int fault) {
+  std::lock_guard<std::mutex> lock(g_debug_mutex);
+  const int old = g_debug_fault;
+  g_debug_fault = fault;
+  return old;
+}
+
+int64_t softmax_debug_set_wait_limit_ns(int64_t ns) {
+  std::lock_guard<std::mutex> lock(g_debug_mutex);
+  const int64_t old = int64_t(g_exchange_wait_ns);
+  if (ns > 0) g_exchange_wait_ns = uint64_t(ns);
+  return old;
+}
+
+}  // extern "C"

@@ -1,0 +1,388 @@
+// device_common.cuh -- device primitives shared by the row-wise online softmax kernels.
+//
+// * State / merge: the online (m, d) state and its merge ("5.2 CUDA Online Softmax
+//   实现优化", §2.1 and §4.1; "Softmax 数值稳定性与 IO-Aware Attention", §4.1), with the
+//   empty state (-inf, 0) as identity: the exponent offset uses m_safe = 0 when m = -inf,
+//   so ex2(-inf - 0) = 0 replaces the NaN of -inf - (-inf).
+// * Exponentials are ex2.approx.ftz.f32 of (a - b) * log2(e): the difference is formed
+//   first so the rounding error scales with the spread of the row, not its magnitude.
+// * Warp (butterfly) and block (shared memory) merges ("5.2 ..." §4.2; "Softmax 数值稳定性
+//   ..." §4.2).  The merge is written to be bit-symmetric, so every lane of a butterfly and
+//   every warp of a block ends with the identical state.
+// * bf16 <-> fp32 conversion, 16-byte vector I/O.
+// * Inline-PTX wrappers for mbarrier, cp.async.bulk (global <-> shared), proxy fences,
+//   L2 cache policies, DSMEM and %globaltimer, used by the bulk-copy kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rwo {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------------------------------------
+// Arithmetic
+// ---------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// e^(a - b) for b finite (b is an m_safe); a = -inf gives 0.
+__device__ __forceinline__ float exp_diff(float a, float b) {
+  return ex2(__fmul_rn(__fsub_rn(a, b), kLog2e));
+}
+
+__device__ __forceinline__ float safe_max(float m) { return m == -INFINITY ? 0.f : m; }
+
+struct State {
+  float m;  // running maximum (raw input units)
+  float d;  // sum of e^(x - m) over the folded elements
+};
+
+__device__ __forceinline__ State empty_state() { return State{-INFINITY, 0.f}; }
+
+// Merge of two partial states.  Each product is rounded on its own before the add, so
+// merge(a, b) and merge(b, a) are bitwise equal.
+__device__ __forceinline__ State merge(State a, State b) {
+  const float m = fmaxf(a.m, b.m);
+  const float ms = safe_max(m);
+  const float sa = exp_diff(a.m, ms);
+  const float sb = exp_diff(b.m, ms);
+  return State{m, __fadd_rn(__fmul_rn(a.d, sa), __fmul_rn(b.d, sb))};
+}
+
+// Butterfly merge over the 32 lanes of a warp; every lane returns the same state.
+__device__ __forceinline__ State warp_merge(State s) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    State t;
+    t.m = __shfl_xor_sync(0xffffffffu, s.m, o);
+    t.d = __shfl_xor_sync(0xffffffffu, s.d, o);
+    s = merge(s, t);
+  }
+  return s;
+}
+
+__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Merge across the `nwarps` warps taking part (warp index `warp`, lane `lane`).  `slots`
+// points at nwarps State entries of shared memory reserved for this call (callers alternate
+// two buffers between consecutive rows, so one barrier per row suffices).  `sync()` is the
+// barrier over exactly those warps.  Every participating thread returns the same state.
+template <class Sync>
+__device__ __forceinline__ State group_merge(State s, State* slots, int nwarps, int warp, int lane,
+                                             Sync sync) {
+  s = warp_merge(s);
+  if (nwarps == 1) return s;
+  if (lane == 0) slots[warp] = s;
+  sync();
+  State t = lane < nwarps ? slots[lane] : empty_state();
+  return warp_merge(t);
+}
+
+// 1/d, with 0 for an empty row (d = 0) so that y = 0 there instead of 0 * inf.
+__device__ __forceinline__ float safe_inv(float d) { return d > 0.f ? __frcp_rn(d) : 0.f; }
+
+__device__ __forceinline__ float lse_of(State s) {
+  return s.m == -INFINITY ? -INFINITY : s.m + logf(s.d);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Element types
+// ---------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Two fp32 -> packed bf16x2 (lo in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint16_t to_bf16(float v) {
+  uint16_t r;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(v));
+  return r;
+}
+
+struct F32 {
+  static constexpr int kVec = 4;    // elements per 16-byte vector
+  static constexpr int kBytes = 4;  // bytes per element
+  static constexpr uint32_t kNegInfWord = 0xff800000u;
+  __device__ static __forceinline__ void unpack(const uint4& v, float (&f)[4]) {
+    f[0] = __uint_as_float(v.x);
+    f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z);
+    f[3] = __uint_as_float(v.w);
+  }
+  __device__ static __forceinline__ uint4 pack(const float (&f)[4]) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+  }
+  __device__ static __forceinline__ float load1(const void* p, int64_t i) {
+    return __ldg(static_cast<const float*>(p) + i);
+  }
+  __device__ static __forceinline__ void store1(void* p, int64_t i, float v) {
+    static_cast<float*>(p)[i] = v;
+  }
+};
+
+struct BF16 {
+  static constexpr int kVec = 8;
+  static constexpr int kBytes = 2;
+  static constexpr uint32_t kNegInfWord = 0xff80ff80u;
+  __device__ static __forceinline__ void unpack(const uint4& v, float (&f)[8]) {
+    f[0] = bf16_lo(v.x);
+    f[1] = bf16_hi(v.x);
+    f[2] = bf16_lo(v.y);
+    f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z);
+    f[5] = bf16_hi(v.z);
+    f[6] = bf16_lo(v.w);
+    f[7] = bf16_hi(v.w);
+  }
+  __device__ static __forceinline__ uint4 pack(const float (&f)[8]) {
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                      pack_bf16x2(f[6], f[7]));
+  }
+  __device__ static __forceinline__ float load1(const void* p, int64_t i) {
+    const unsigned short b = __ldg(static_cast<const unsigned short*>(p) + i);
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+  }
+  __device__ static __forceinline__ void store1(void* p, int64_t i, float v) {
+    static_cast<uint16_t*>(p)[i] = to_bf16(v);
+  }
+};
+
+// ---------------------------------------------------------------------------------------------
+// 16-byte global memory access
+// ---------------------------------------------------------------------------------------------
+
+// Read-only streaming load (input read once): no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Plain coherent 16-byte load (used where the same lines are read twice).
+__device__ __forceinline__ uint4 ld16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Streaming store (output written once, not re-read by this kernel).
+__device__ __forceinline__ void st_stream16(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// ---------------------------------------------------------------------------------------------
+// Shared memory, mbarrier and bulk copies (sm_90+ PTX; used on sm_103a)
+// ---------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint4 lds16(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void sts16(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Make barrier initialisation visible to the async proxy and to the cluster.
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase of parity `parity` of a local mbarrier to complete, for at most
+// `limit_ns` nanoseconds.  Returns false if the limit ran out (the caller records it).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// Bulk copy global -> shared (this CTA), completion signalled on mbarrier `bar` as
+// transaction bytes.  src, dst 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                        uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// Bulk copy shared (this CTA) -> global, tracked by the issuing thread's bulk groups.
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes, uint64_t policy) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst),
+               "r"(src), "r"(bytes), "l"(policy)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// All committed bulk stores of this thread have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// All committed bulk stores of this thread are complete (written to global memory).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------------------------
+// Thread-block clusters and distributed shared memory
+// ---------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_count_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+
+// The shared::cluster address of `local` in the CTA of rank `rank` of this cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float a, float b) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
+
+// Arrive on an mbarrier in another CTA of the cluster, releasing this thread's prior
+// (distributed) shared memory writes to the waiter.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait_cluster(bar, parity)) {
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+// ---------------------------------------------------------------------------------------------
+// Global-memory release/acquire (cross-cluster exchange)
+// ---------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+}  // namespace rwo

@@ -1,0 +1,253 @@
+// kernel_oneread_tma.cu -- one-read softmax with rows staged in shared memory by bulk copies.
+//
+// "5.2 CUDA Online Softmax 实现优化", §6 keeps the row on chip so that x is read from HBM once
+// and y written once; "Softmax 数值稳定性与 IO-Aware Attention" §三 names shared memory as the
+// place for rows that fit.  On sm_103a the copy engine does the moving:
+//
+//  * One producer warp (one elected lane) per CTA issues cp.async.bulk global -> shared for
+//    whole rows into a ring of S row slots, completion counted in bytes on an mbarrier per
+//    slot ("full"), and bulk-stores finished rows shared -> global.  It runs up to S - 1 rows
+//    ahead of the consumers, so HBM reads stay in flight while rows are being normalised.
+//  * NCW consumer warps wait on "full", read their part of the row (VPT 16-byte vectors per
+//    thread) into registers, fold it into the thread's (m, d) state with one exponential per
+//    element, merge states across the warp (butterfly) and across the consumer warps (shared
+//    memory, one named barrier per row), write y = e * 2^((m_t - m) log2 e) / d back into the
+//    same slot, fence the writes to the async proxy and arrive on the slot's "done" barrier.
+//  * The producer waits on "done", bulk-stores the row, and reuses the slot once the store has
+//    finished reading it.
+//
+// Persistent: the grid is (CTAs resident per SM) x (SM count); CTA b handles rows b, b + grid,
+// ...  Every wait is bounded (%globaltimer); a wait that runs out sets the status word and the
+// protocol continues, so the kernel always terminates.
+#include "device_common.cuh"
+#include "launch.h"
+
+namespace rwo {
+namespace {
+
+struct TmaArgs {
+  const unsigned char* x;
+  unsigned char* y;
+  float* m_out;
+  float* d_out;
+  float* lse_out;
+  int64_t M;
+  int64_t N;
+  uint32_t row_bytes;
+  uint32_t slot_bytes;
+  int stages;
+  unsigned* status;
+  uint64_t wait_ns;
+};
+
+constexpr int kSlotAlign = 128;
+
+template <class D, int VPT, int NCW>
+__global__ void __launch_bounds__((NCW + 1) * 32) k_oneread_tma(TmaArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int E = D::kVec;
+  constexpr int NCT = NCW * 32;
+  const int S = a.stages;
+  unsigned char* slots = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(S) * a.slot_bytes);
+  uint64_t* done = full + S;
+  State* wstate = reinterpret_cast<State*>(done + S);  // [2][NCW]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_addr(&full[s]), 1);
+      mbar_init(smem_addr(&done[s]), NCW);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const int64_t nrows = a.M > blockIdx.x ? (a.M - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  const int64_t nunits = a.N / E;
+
+  if (warp == NCW) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      bool timed_out = false;
+      int64_t stored = 0;
+      auto store_next = [&]() {
+        const int s = int(stored % S);
+        if (!mbar_wait(smem_addr(&done[s]), uint32_t((stored / S) & 1), a.wait_ns)) timed_out = true;
+        const int64_t row = blockIdx.x + stored * gridDim.x;
+        bulk_s2g(a.y + row * a.row_bytes, smem_addr(slots + size_t(s) * a.slot_bytes), a.row_bytes, pol);
+        bulk_commit();
+        ++stored;
+      };
+      for (int64_t j = 0; j < nrows; ++j) {
+        const int s = int(j % S);
+        if (j >= S) {
+          while (stored <= j - S) store_next();
+          bulk_wait_read_all();  // slot s has been read out by its store
+        }
+        const uint32_t bar = smem_addr(&full[s]);
+        mbar_arrive_expect_tx(bar, a.row_bytes);
+        const int64_t row = blockIdx.x + j * gridDim.x;
+        bulk_g2s(smem_addr(slots + size_t(s) * a.slot_bytes), a.x + row * a.row_bytes, a.row_bytes, bar, pol);
+      }
+      while (stored < nrows) store_next();
+      // Every load must have landed before the CTA may exit (the consumers normally saw them all).
+      for (int64_t j = nrows > S ? nrows - S : 0; j < nrows; ++j)
+        if (!mbar_wait(smem_addr(&full[j % S]), uint32_t((j / S) & 1), a.wait_ns)) timed_out = true;
+      bulk_wait_all();
+      if (timed_out) atomicOr(a.status, kStatusTimeout);
+    }
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  bool timed_out = false;
+  for (int64_t j = 0; j < nrows; ++j) {
+    const int s = int(j % S);
+    if (!mbar_wait(smem_addr(&full[s]), uint32_t((j / S) & 1), a.wait_ns)) timed_out = true;
+    const uint32_t slot = smem_addr(slots + size_t(s) * a.slot_bytes);
+
+    float v[VPT][E];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int u = tid + k * NCT;
+      if (u < nunits) {
+        D::unpack(lds16(slot + uint32_t(u) * 16u), v[k]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[k][e] = -INFINITY;
+      }
+    }
+    float mt = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k)
+#pragma unroll
+      for (int e = 0; e < E; ++e) mt = fmaxf(mt, v[k][e]);
+    const float mts = safe_max(mt);
+    float dt = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k)
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        v[k][e] = exp_diff(v[k][e], mts);
+        dt += v[k][e];
+      }
+    const State st = group_merge(State{mt, dt}, wstate + (j & 1) * NCW, NCW, warp, lane,
+                                 [] { named_barrier_sync(1, NCT); });
+    const float scale = __fmul_rn(exp_diff(mt, safe_max(st.m)), safe_inv(st.d));
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int u = tid + k * NCT;
+      if (u < nunits) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[k][e] = __fmul_rn(v[k][e], scale);
+        sts16(slot + uint32_t(u) * 16u, D::pack(v[k]));
+      }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&done[s]));
+    if (tid == 0) {
+      const int64_t row = blockIdx.x + j * gridDim.x;
+      if (a.m_out) a.m_out[row] = st.m;
+      if (a.d_out) a.d_out[row] = st.d;
+      if (a.lse_out) a.lse_out[row] = lse_of(st);
+    }
+  }
+  if (timed_out && lane == 0) atomicOr(a.status, kStatusTimeout);
+}
+
+using TmaKernel = void (*)(TmaArgs);
+
+struct TmaConfig {
+  int ncw, vpt;
+  TmaKernel f32, bf16;
+};
+
+template <int VPT, int NCW>
+constexpr TmaConfig tma_cfg() {
+  return TmaConfig{NCW, VPT, k_oneread_tma<F32, VPT, NCW>, k_oneread_tma<BF16, VPT, NCW>};
+}
+
+// Ordered by capacity (16-byte units per row = 32 * ncw * vpt).
+const TmaConfig kTma[] = {tma_cfg<2, 4>(), tma_cfg<4, 4>(), tma_cfg<4, 8>(), tma_cfg<8, 8>(),
+                          tma_cfg<8, 16>()};
+
+const TmaConfig* pick_tma(int64_t units) {
+  for (const TmaConfig& c : kTma)
+    if (units <= int64_t(32) * c.ncw * c.vpt) return &c;
+  return nullptr;
+}
+
+struct TmaPlan {
+  const TmaConfig* cfg = nullptr;
+  int stages = 0;
+  uint32_t slot_bytes = 0;
+  size_t smem = 0;
+  int ctas_per_sm = 0;
+};
+
+size_t tma_smem_bytes(int stages, uint32_t slot_bytes, int ncw) {
+  return size_t(stages) * slot_bytes + size_t(stages) * 2 * sizeof(uint64_t) +
+         size_t(2) * ncw * sizeof(State);
+}
+
+// Rows of up to 16 KiB get 4 slots, larger rows 3 (2 if 3 do not fit); then as many CTAs per
+// SM as shared memory and threads allow.
+TmaPlan plan_tma(const RowProblem& p, const DeviceInfo& dev) {
+  TmaPlan plan;
+  const int64_t row_bytes = p.N * elem_bytes(p.dtype);
+  if (row_bytes % 16 != 0 || row_bytes > (int64_t(1) << 20)) return plan;
+  const TmaConfig* cfg = pick_tma(row_bytes / 16);
+  if (!cfg) return plan;
+  const uint32_t slot = uint32_t((row_bytes + kSlotAlign - 1) / kSlotAlign * kSlotAlign);
+  const size_t per_cta_reserved = 1024;  // the runtime's per-block reservation
+  const int threads = (cfg->ncw + 1) * 32;
+  for (int stages = row_bytes <= 16384 ? 4 : 3; stages >= 2; --stages) {
+    const size_t smem = tma_smem_bytes(stages, slot, cfg->ncw);
+    if (smem > size_t(dev.max_smem_per_block_optin)) continue;
+    int by_smem = int(size_t(dev.max_smem_per_sm) / (smem + per_cta_reserved));
+    int by_threads = dev.max_threads_per_sm / threads;
+    int c = by_smem < by_threads ? by_smem : by_threads;
+    if (c > 8) c = 8;
+    if (c < 1) continue;
+    plan.cfg = cfg;
+    plan.stages = stages;
+    plan.slot_bytes = slot;
+    plan.smem = smem;
+    plan.ctas_per_sm = c;
+    return plan;
+  }
+  return plan;
+}
+
+}  // namespace
+
+bool oneread_tma_fits(const RowProblem& p, const DeviceInfo& dev) {
+  return plan_tma(p, dev).cfg != nullptr;
+}
+
+cudaError_t launch_oneread_tma(const RowProblem& p, const DeviceInfo& dev) {
+  const TmaPlan plan = plan_tma(p, dev);
+  if (!plan.cfg) return cudaErrorInvalidValue;
+  TmaKernel fn = p.dtype == 0 ? plan.cfg->f32 : plan.cfg->bf16;
+  cudaError_t err = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(plan.smem));
+  if (err != cudaSuccess) return err;
+  const int threads = (plan.cfg->ncw + 1) * 32;
+  int occ = 0;
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, (const void*)fn, threads, plan.smem);
+  if (err != cudaSuccess) return err;
+  if (occ < 1) return cudaErrorInvalidConfiguration;
+  int per_sm = plan.ctas_per_sm < occ ? plan.ctas_per_sm : occ;
+  const int64_t cap = int64_t(dev.sm_count) * per_sm;
+  const int grid = int(p.M < cap ? p.M : cap);
+  TmaArgs a{static_cast<const unsigned char*>(p.x), static_cast<unsigned char*>(p.y), p.m_out,
+            p.d_out, p.lse_out, p.M, p.N, uint32_t(p.N * elem_bytes(p.dtype)), plan.slot_bytes,
+            plan.stages, dev.status, local_wait_limit_ns()};
+  fn<<<grid, threads, plan.smem, p.stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace rwo

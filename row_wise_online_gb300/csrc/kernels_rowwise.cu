@@ -1,0 +1,319 @@
+// kernels_rowwise.cu -- register one-read kernel, two-pass streaming kernel, state merge kernel.
+//
+// Register one-read ("5.2 CUDA Online Softmax 实现优化", §6: keep the row on chip so x is
+// read once and y written once).  A group of WPR warps owns a row; each thread loads VPT
+// 16-byte vectors (or VPT scalars on the unaligned path) into registers, takes its local
+// max, forms e = 2^((x - m_t) log2 e) once per element and sums it: the thread's (m, d)
+// state.  States are merged across the warp by a butterfly and across the group's warps
+// through shared memory; then y = e * 2^((m_t - m) log2 e) / d is stored from the same
+// registers.  One exponential per element.  Persistent CTAs walk rows with a grid stride
+// (§7 of the same page).
+//
+// Two-pass ("5.2 ..." §2.2 and §5: the online recurrence with 128-bit loads).  A CTA owns a
+// row.  Pass 1 streams the row, four vectors per thread per step, folding each step into
+// the thread's (m, d) with one rescale (the online recurrence at step granularity) and a
+// compensated sum; the block merge gives the row state; pass 2 re-reads the row (from L2
+// while it is resident) and writes y.  Any N.  With WRITE_Y = false it is the state-only
+// kernel behind softmax_row_state.
+//
+// Merge kernel: the elementwise state merge ("5.2 ..." §4.1) behind merge_states.
+#include "device_common.cuh"
+#include "launch.h"
+
+namespace rwo {
+namespace {
+
+struct RowArgs {
+  const unsigned char* x;
+  unsigned char* y;
+  float* m_out;
+  float* d_out;
+  float* lse_out;
+  int64_t M;
+  int64_t N;
+};
+
+__device__ __forceinline__ void write_state(const RowArgs& a, int64_t row, State s) {
+  if (a.m_out) a.m_out[row] = s.m;
+  if (a.d_out) a.d_out[row] = s.d;
+  if (a.lse_out) a.lse_out[row] = lse_of(s);
+}
+
+// ------------------------------------------------------------------------------------------
+// Register one-read kernel
+// ------------------------------------------------------------------------------------------
+
+constexpr int kRegThreads = 256;
+
+template <class D, int VPT, int WPR, bool VEC>
+__global__ void __launch_bounds__(kRegThreads) k_oneread_reg(RowArgs a) {
+  constexpr int E = VEC ? D::kVec : 1;  // elements per unit (one 16-byte vector, or one element)
+  constexpr int G = (kRegThreads / 32) / WPR;  // row groups per CTA
+  constexpr int GT = WPR * 32;                 // threads per group
+  __shared__ State slots[2][kRegThreads / 32];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = warp / WPR, wig = warp % WPR;
+  const int gt = threadIdx.x - g * GT;
+  const int64_t nunits = a.N / E;
+  const int64_t row_bytes = a.N * D::kBytes;
+
+  int it = 0;
+  for (int64_t row = (int64_t)blockIdx.x * G + g; row < a.M; row += (int64_t)gridDim.x * G, ++it) {
+    const unsigned char* xr = a.x + row * row_bytes;
+    float v[VPT][E];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int64_t u = gt + (int64_t)k * GT;
+      if (u < nunits) {
+        if constexpr (VEC) {
+          D::unpack(ld_stream16(xr + u * 16), v[k]);
+        } else {
+          v[k][0] = D::load1(xr, u);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[k][e] = -INFINITY;
+      }
+    }
+    // thread state: local max first, then one exponential per element
+    float mt = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k)
+#pragma unroll
+      for (int e = 0; e < E; ++e) mt = fmaxf(mt, v[k][e]);
+    const float mts = safe_max(mt);
+    float dt = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k)
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        v[k][e] = exp_diff(v[k][e], mts);
+        dt += v[k][e];
+      }
+    const State s = group_merge(State{mt, dt}, &slots[it & 1][g * WPR], WPR, wig, lane,
+                                [&] { named_barrier_sync(1 + g, GT); });
+    const float scale = __fmul_rn(exp_diff(mt, safe_max(s.m)), safe_inv(s.d));
+    unsigned char* yr = a.y + row * row_bytes;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int64_t u = gt + (int64_t)k * GT;
+      if (u < nunits) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[k][e] = __fmul_rn(v[k][e], scale);
+        if constexpr (VEC) {
+          st_stream16(yr + u * 16, D::pack(v[k]));
+        } else {
+          D::store1(yr, u, v[k][0]);
+        }
+      }
+    }
+    if (gt == 0) write_state(a, row, s);
+  }
+}
+
+using RowKernel = void (*)(RowArgs);
+
+struct RegConfig {
+  int wpr, vpt;
+  RowKernel f32, bf16;
+};
+
+template <int VPT, int WPR, bool VEC>
+constexpr RegConfig reg_cfg() {
+  return RegConfig{WPR, VPT, k_oneread_reg<F32, VPT, WPR, VEC>, k_oneread_reg<BF16, VPT, WPR, VEC>};
+}
+
+// Ordered by capacity (units per row = 32 * wpr * vpt).
+const RegConfig kRegVec[] = {reg_cfg<2, 1, true>(), reg_cfg<4, 1, true>(), reg_cfg<8, 1, true>(),
+                             reg_cfg<8, 2, true>(), reg_cfg<8, 4, true>(), reg_cfg<8, 8, true>()};
+const RegConfig kRegScalar[] = {reg_cfg<4, 1, false>(), reg_cfg<16, 1, false>(),
+                                reg_cfg<8, 8, false>()};
+
+const RegConfig* pick_reg(int64_t units, bool vec) {
+  const RegConfig* tab = vec ? kRegVec : kRegScalar;
+  const int n = vec ? int(sizeof(kRegVec) / sizeof(kRegVec[0]))
+                    : int(sizeof(kRegScalar) / sizeof(kRegScalar[0]));
+  for (int i = 0; i < n; ++i)
+    if (units <= int64_t(32) * tab[i].wpr * tab[i].vpt) return &tab[i];
+  return nullptr;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int blocks_per_sm(const void* fn, int threads, size_t smem) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem) != cudaSuccess) {
+    cudaGetLastError();
+    n = 1;
+  }
+  return n < 1 ? 1 : n;
+}
+
+RowArgs row_args(const RowProblem& p) {
+  return RowArgs{static_cast<const unsigned char*>(p.x), static_cast<unsigned char*>(p.y),
+                 p.m_out, p.d_out, p.lse_out, p.M, p.N};
+}
+
+// ------------------------------------------------------------------------------------------
+// Two-pass streaming kernel
+// ------------------------------------------------------------------------------------------
+
+constexpr int kTwoPassMaxThreads = 1024;
+constexpr int kTwoPassUnroll = 4;
+
+template <class D, bool VEC>
+__device__ __forceinline__ void load_unit(const unsigned char* xr, int64_t u, int64_t nunits,
+                                          float (&v)[VEC ? D::kVec : 1]) {
+  constexpr int E = VEC ? D::kVec : 1;
+  if (u < nunits) {
+    if constexpr (VEC) {
+      D::unpack(ld16(xr + u * 16), v);
+    } else {
+      v[0] = D::load1(xr, u);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < E; ++e) v[e] = -INFINITY;
+  }
+}
+
+template <class D, bool VEC, bool WRITE_Y>
+__global__ void __launch_bounds__(kTwoPassMaxThreads) k_twopass(RowArgs a) {
+  constexpr int E = VEC ? D::kVec : 1;
+  constexpr int U = kTwoPassUnroll;
+  __shared__ State slots[2][kTwoPassMaxThreads / 32];
+  const int nt = blockDim.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t nunits = a.N / E;
+  const int64_t row_bytes = a.N * D::kBytes;
+
+  int it = 0;
+  for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x, ++it) {
+    const unsigned char* xr = a.x + row * row_bytes;
+    // pass 1: online fold, one rescale per step of U units; compensated (Kahan) sum of d
+    float m = -INFINITY, d = 0.f, c = 0.f;
+    for (int64_t base = threadIdx.x; base < nunits; base += (int64_t)nt * U) {
+      float v[U][E];
+#pragma unroll
+      for (int k = 0; k < U; ++k) load_unit<D, VEC>(xr, base + (int64_t)k * nt, nunits, v[k]);
+      float mu = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < U; ++k)
+#pragma unroll
+        for (int e = 0; e < E; ++e) mu = fmaxf(mu, v[k][e]);
+      const float m_new = fmaxf(m, mu);
+      const float ms = safe_max(m_new);
+      float acc = 0.f;
+#pragma unroll
+      for (int k = 0; k < U; ++k)
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc += exp_diff(v[k][e], ms);
+      const float r = exp_diff(m, ms);  // rescale of the running sum; 0 when m was -inf
+      const float ds = __fmul_rn(d, r);
+      c = __fmul_rn(c, r);
+      const float yk = __fsub_rn(acc, c);
+      const float t = __fadd_rn(ds, yk);
+      c = __fsub_rn(__fsub_rn(t, ds), yk);
+      d = t;
+      m = m_new;
+    }
+    const State s = group_merge(State{m, d}, slots[it & 1], nt >> 5, warp, lane,
+                                [] { __syncthreads(); });
+    if constexpr (WRITE_Y) {
+      // pass 2: re-read and normalise
+      const float ms = safe_max(s.m);
+      const float inv = safe_inv(s.d);
+      unsigned char* yr = a.y + row * row_bytes;
+      for (int64_t base = threadIdx.x; base < nunits; base += (int64_t)nt * U) {
+        float v[U][E];
+#pragma unroll
+        for (int k = 0; k < U; ++k) load_unit<D, VEC>(xr, base + (int64_t)k * nt, nunits, v[k]);
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+          const int64_t u = base + (int64_t)k * nt;
+          if (u < nunits) {
+#pragma unroll
+            for (int e = 0; e < E; ++e) v[k][e] = __fmul_rn(exp_diff(v[k][e], ms), inv);
+            if constexpr (VEC) {
+              st_stream16(yr + u * 16, D::pack(v[k]));
+            } else {
+              D::store1(yr, u, v[k][0]);
+            }
+          }
+        }
+      }
+    }
+    if (threadIdx.x == 0) write_state(a, row, s);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// Elementwise state merge
+// ------------------------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(256)
+    k_merge_states(const float* __restrict__ m_a, const float* __restrict__ d_a,
+                   const float* __restrict__ m_b, const float* __restrict__ d_b, float* m_out,
+                   float* d_out, float* lse_out, int64_t M) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < M;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const State s = merge(State{m_a[i], d_a[i]}, State{m_b[i], d_b[i]});
+    m_out[i] = s.m;
+    d_out[i] = s.d;
+    if (lse_out) lse_out[i] = lse_of(s);
+  }
+}
+
+}  // namespace
+
+bool oneread_reg_fits(const RowProblem& p, bool vec) {
+  const int64_t e = vec ? 16 / elem_bytes(p.dtype) : 1;
+  if (vec && p.N % e != 0) return false;
+  return pick_reg(p.N / e, vec) != nullptr;
+}
+
+cudaError_t launch_oneread_reg(const RowProblem& p, bool vec, const DeviceInfo& dev) {
+  const int64_t e = vec ? 16 / elem_bytes(p.dtype) : 1;
+  const RegConfig* cfg = pick_reg(p.N / e, vec);
+  if (!cfg) return cudaErrorInvalidValue;
+  RowKernel fn = p.dtype == 0 ? cfg->f32 : cfg->bf16;
+  const int groups = (kRegThreads / 32) / cfg->wpr;
+  const int64_t want = ceil_div(p.M, groups);
+  const int64_t cap = int64_t(dev.sm_count) * blocks_per_sm((const void*)fn, kRegThreads, 0);
+  const int grid = int(want < cap ? want : cap);
+  fn<<<grid, kRegThreads, 0, p.stream>>>(row_args(p));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_twopass(const RowProblem& p, bool vec, const DeviceInfo& dev) {
+  const int64_t e = vec ? 16 / elem_bytes(p.dtype) : 1;
+  if (vec && p.N % e != 0) return cudaErrorInvalidValue;
+  const int64_t units = p.N / e;
+  int nt = 128;
+  while (nt < kTwoPassMaxThreads && int64_t(nt) * kTwoPassUnroll < units) nt *= 2;
+  const bool write_y = p.y != nullptr;
+  RowKernel fn;
+  if (p.dtype == 0)
+    fn = vec ? (write_y ? k_twopass<F32, true, true> : k_twopass<F32, true, false>)
+             : (write_y ? k_twopass<F32, false, true> : k_twopass<F32, false, false>);
+  else
+    fn = vec ? (write_y ? k_twopass<BF16, true, true> : k_twopass<BF16, true, false>)
+             : (write_y ? k_twopass<BF16, false, true> : k_twopass<BF16, false, false>);
+  const int64_t cap = int64_t(dev.sm_count) * blocks_per_sm((const void*)fn, nt, 0);
+  const int grid = int(p.M < cap ? p.M : cap);
+  fn<<<grid, nt, 0, p.stream>>>(row_args(p));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge_states(const float* m_a, const float* d_a, const float* m_b,
+                                const float* d_b, float* m_out, float* d_out, float* lse_out,
+                                int64_t M, cudaStream_t stream, const DeviceInfo& dev) {
+  const int64_t want = ceil_div(M, 256);
+  const int64_t cap = int64_t(dev.sm_count) * 8;
+  const int grid = int(want < cap ? want : cap);
+  k_merge_states<<<grid, 256, 0, stream>>>(m_a, d_a, m_b, d_b, m_out, d_out, lse_out, M);
+  return cudaGetLastError();
+}
+
+}  // namespace rwo

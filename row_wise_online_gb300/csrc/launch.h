@@ -1,0 +1,61 @@
+// launch.h -- internal interface between the C ABI (api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rwo {
+
+struct DeviceInfo {
+  int device = -1;
+  int sm_count = 0;
+  int max_smem_per_block_optin = 0;  // bytes of dynamic + static shared memory a block may use
+  int max_smem_per_sm = 0;
+  int max_threads_per_sm = 0;
+  int l2_bytes = 0;
+  int cluster_launch = 0;
+  unsigned* status = nullptr;  // device address of this device's status word
+};
+
+// One softmax problem.  Pointers are device pointers; y may be null for state-only work.
+struct RowProblem {
+  const void* x = nullptr;
+  void* y = nullptr;
+  float* m_out = nullptr;
+  float* d_out = nullptr;
+  float* lse_out = nullptr;
+  int64_t M = 0;
+  int64_t N = 0;
+  int dtype = 0;  // 0 = fp32, 1 = bf16
+  cudaStream_t stream = nullptr;
+};
+
+// Status bits a kernel may set in the per-device status word.
+constexpr unsigned kStatusTimeout = 1u;
+
+inline int elem_bytes(int dtype) { return dtype == 0 ? 4 : 2; }
+
+// Host-side wait limits handed to kernels (nanoseconds).
+uint64_t local_wait_limit_ns();     // waits on this CTA's own copies and threads
+uint64_t exchange_wait_limit_ns();  // waits on other clusters (split row)
+int debug_fault();                  // test hook value (split row)
+
+// Each `*_fits` says whether the variant can take the problem (alignment already checked by
+// the caller where the variant needs it).  Each `launch_*` enqueues the work and returns a
+// cudaError_t from the launch.
+bool oneread_reg_fits(const RowProblem& p, bool vec);
+cudaError_t launch_oneread_reg(const RowProblem& p, bool vec, const DeviceInfo& dev);
+
+bool oneread_tma_fits(const RowProblem& p, const DeviceInfo& dev);
+cudaError_t launch_oneread_tma(const RowProblem& p, const DeviceInfo& dev);
+
+cudaError_t launch_twopass(const RowProblem& p, bool vec, const DeviceInfo& dev);
+
+bool splitrow_fits(const RowProblem& p, const DeviceInfo& dev);
+cudaError_t launch_splitrow(const RowProblem& p, const DeviceInfo& dev);
+
+cudaError_t launch_merge_states(const float* m_a, const float* d_a, const float* m_b,
+                                const float* d_b, float* m_out, float* d_out, float* lse_out,
+                                int64_t M, cudaStream_t stream, const DeviceInfo& dev);
+
+}  // namespace rwo

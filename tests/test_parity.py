@@ -1,0 +1,179 @@
+"""GPU parity: the CUDA path against the fp64 oracle on the seeded workloads.
+
+Small and medium cases are compared element by element in full (several tiles, grid-stride
+tails, ragged rows).  The full-size workloads run in the launch configuration the benchmark
+uses (AUTO) and are compared on sampled rows element by element, plus properties checked on
+every row (row sums, m = exact row max).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import row_wise_online_gb300 as rwo
+import synth
+from gpu_util import run_softmax, to_device, to_host
+from tolerances import check_rowsums, check_state, check_y
+
+pytestmark = pytest.mark.gpu
+
+V = rwo
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from row_wise_online_gb300 import _build
+
+    _build.build()
+    torch.cuda.set_device(0)
+
+
+def _full_check(x_host, dtype, variant, what):
+    x = to_device(x_host)
+    y, m, d, lse = run_softmax(x, variant)
+    y_ref, m_ref, d_ref, lse_ref = oracle.softmax_rows(x_host)
+    stats = check_y(to_host(y), y_ref, dtype, what)
+    masked = ~np.isfinite(m_ref)
+    check_rowsums(to_host(y), dtype, masked, what)
+    check_state(m.cpu().numpy(), d.cpu().numpy(), lse.cpu().numpy(), m_ref, d_ref, lse_ref, what)
+    return stats
+
+
+@pytest.mark.parametrize("variant", [V.VARIANT_AUTO, V.VARIANT_ONEREAD_REG, V.VARIANT_ONEREAD_SMEM,
+                                     V.VARIANT_TWOPASS])
+def test_fp32_64x1024(variant):
+    w = synth.WORKLOADS["fp32_64x1024"]
+    _full_check(synth.generate(w), w.dtype, variant, f"{w.name}/{V.VARIANT_NAMES[variant]}")
+
+
+@pytest.mark.parametrize("variant", [V.VARIANT_AUTO, V.VARIANT_ONEREAD_SMEM, V.VARIANT_TWOPASS])
+def test_fp32_4096x4096(variant):
+    w = synth.WORKLOADS["fp32_4096x4096"]
+    _full_check(synth.generate(w), w.dtype, variant, f"{w.name}/{V.VARIANT_NAMES[variant]}")
+
+
+# Medium shapes: many rows per CTA with a ragged grid-stride tail, rows spanning several vectors
+# per thread, and a row length that is not a power of two.
+MEDIUM = [
+    (synth.F32, 1000, 1000), (synth.F32, 777, 4100), (synth.F32, 300, 16384), (synth.F32, 129, 20000),
+    (synth.BF16, 1000, 1000), (synth.BF16, 517, 4104), (synth.BF16, 300, 32768), (synth.BF16, 65, 40000),
+]
+
+
+@pytest.mark.parametrize("dtype,M,N", MEDIUM)
+@pytest.mark.parametrize("variant", [V.VARIANT_AUTO, V.VARIANT_ONEREAD_REG, V.VARIANT_ONEREAD_SMEM,
+                                     V.VARIANT_TWOPASS])
+def test_medium_shapes(dtype, M, N, variant):
+    w = synth.custom("medium", dtype, M, N, seed=100 + N, p1=3.0)
+    x_host = synth.generate(w)
+    x = to_device(x_host)
+    try:
+        y, m, d, lse = run_softmax(x, variant)
+    except rwo.SoftmaxError as e:
+        assert variant != V.VARIANT_AUTO and e.status == rwo.ERR_UNSUPPORTED
+        return
+    y_ref, m_ref, d_ref, lse_ref = oracle.softmax_rows(x_host)
+    what = f"{M}x{N}/{V.VARIANT_NAMES[variant]}"
+    check_y(to_host(y), y_ref, dtype, what)
+    check_rowsums(to_host(y), dtype, None, what)
+    check_state(m.cpu().numpy(), d.cpu().numpy(), lse.cpu().numpy(), m_ref, d_ref, lse_ref, what)
+
+
+def _sampled_check(w, variant, sample_rows, chunk=None):
+    """Full-size run; every row checked for row sum and exact max; sampled rows against the oracle."""
+    x_host = synth.generate(w)
+    x = to_device(x_host)
+    y, m, d, lse = run_softmax(x, variant)
+    what = f"{w.name}/{V.VARIANT_NAMES[rwo.last_variant()]}"
+    # every row: m is the exact row max, rows sum to 1
+    assert torch.equal(m, x.amax(dim=1).float()), f"{what}: m != row max"
+    sums = torch.sum(y, dim=1, dtype=torch.float64)
+    tol = 1e-5 if w.dtype == synth.F32 else 4e-3
+    assert float((sums - 1).abs().max()) <= tol, f"{what}: row sums"
+    del sums
+    # sampled rows in full against the oracle
+    rows = np.unique(np.asarray(sample_rows, dtype=np.int64))
+    y_ref, m_ref, d_ref, lse_ref = oracle.softmax_rows(x_host, rows=rows)
+    idx = torch.from_numpy(rows).cuda()
+    ys = to_host(y.index_select(0, idx))
+    stats = check_y(ys, y_ref, w.dtype, what)
+    check_state(m[idx].cpu().numpy(), d[idx].cpu().numpy(), lse[idx].cpu().numpy(), m_ref, d_ref, lse_ref, what)
+    return stats
+
+
+def test_bf16_logits_16384x32768():
+    w = synth.WORKLOADS["bf16_logits_16384x32768"]
+    rng = np.random.default_rng(0)
+    rows = list(rng.integers(0, w.M, 40)) + [0, 100, 200, 16300, w.M - 1]  # stress rows r % 100 == 0
+    _sampled_check(w, V.VARIANT_AUTO, rows)
+
+
+def test_bf16_logits_twopass_sampled():
+    w = synth.WORKLOADS["bf16_logits_16384x32768"].with_rows(2048)
+    rng = np.random.default_rng(1)
+    _sampled_check(w, V.VARIANT_TWOPASS, list(rng.integers(0, w.M, 24)) + [0, 100, 2047])
+
+
+def test_bf16_causal_524288x4096():
+    w = synth.WORKLOADS["bf16_causal_4x32x4096x4096"]
+    rng = np.random.default_rng(2)
+    qs = [0, 1, 2, 127, 128, 129, 255, 256, 1000, 4095]
+    rows = list(rng.integers(0, w.M, 48)) + [h * 4096 + q for h in (0, 57, 127) for q in qs]
+    _sampled_check(w, V.VARIANT_AUTO, rows)
+
+
+@pytest.mark.parametrize("variant", [V.VARIANT_ONEREAD_REG, V.VARIANT_ONEREAD_SMEM, V.VARIANT_TWOPASS])
+def test_bf16_causal_variants_one_head(variant):
+    w = synth.WORKLOADS["bf16_causal_4x32x4096x4096"].with_rows(4096)
+    x_host = synth.generate(w)
+    _full_check(x_host, w.dtype, variant, f"causal-head/{V.VARIANT_NAMES[variant]}")
+
+
+@pytest.mark.parametrize("variant", [V.VARIANT_AUTO, V.VARIANT_TWOPASS])
+def test_fp32_longrow_32x4194304(variant):
+    w = synth.WORKLOADS["fp32_longrow_32x4194304"]
+    x_host = synth.generate(w)
+    x = to_device(x_host)
+    y, m, d, lse = run_softmax(x, variant)
+    what = f"{w.name}/{V.VARIANT_NAMES[rwo.last_variant()]}"
+    yh = to_host(y)
+    mh, dh, lh = m.cpu().numpy(), d.cpu().numpy(), lse.cpu().numpy()
+    for r0 in range(0, w.M, 4):  # four rows at a time keeps the fp64 reference at 128 MiB
+        sel = np.arange(r0, r0 + 4)
+        y_ref, m_ref, d_ref, lse_ref = oracle.softmax_rows(x_host, rows=sel)
+        check_y(yh[sel], y_ref, w.dtype, what)
+        check_rowsums(yh[sel], w.dtype, None, what)
+        check_state(mh[sel], dh[sel], lh[sel], m_ref, d_ref, lse_ref, what)
+    assert np.all(mh == 20.0)
+
+
+def test_in_place():
+    w = synth.custom("inplace", synth.BF16, 333, 4096, seed=9, p1=2.0)
+    x_host = synth.generate(w)
+    x = to_device(x_host)
+    rwo.softmax_rows(x, x)
+    y_ref, *_ = oracle.softmax_rows(x_host)
+    check_y(to_host(x), y_ref, w.dtype, "in place")
+
+
+def test_host_buffers_pipeline():
+    w = synth.custom("host", synth.F32, 5000, 4096, seed=10, p1=3.0)
+    x_host = synth.generate(w)
+    xt = torch.from_numpy(x_host).pin_memory()
+    yt = torch.empty_like(xt).pin_memory()
+    rwo.softmax_rows_host(xt, yt)
+    y_ref, *_ = oracle.softmax_rows(x_host)
+    check_y(yt.numpy(), y_ref, w.dtype, "host pipeline")
+
+
+def test_variant_choice():
+    cases = [
+        ("fp32_64x1024", V.VARIANT_ONEREAD_REG),
+        ("fp32_4096x4096", V.VARIANT_ONEREAD_SMEM),
+    ]
+    for name, want in cases:
+        w = synth.WORKLOADS[name].with_rows(8)
+        x = to_device(synth.generate(w))
+        rwo.softmax_rows(x)
+        torch.cuda.synchronize()
+        assert rwo.last_variant() == want, (name, rwo.last_variant())
