@@ -33,7 +33,8 @@
  *    may be NULL.  m_out is the raw row maximum (bit-exact max of the inputs,
  *    -0 and +0 equal).  d_out is relative to m_out, natural base.
  *  - stream is a cudaStream_t passed as void* (NULL = the legacy default stream).
- *  - M == 0 is a no-op returning SOFTMAX_OK.
+ *  - M == 0 is a no-op returning SOFTMAX_OK (the pointers may then be NULL,
+ *    as they are for an empty tensor); N, dtype and variant are still checked.
  *  - Return value: a softmax_status.  Argument errors are detected on the
  *    host before anything is enqueued.  A CUDA launch error returns
  *    SOFTMAX_ERR_CUDA (softmax_last_cuda_error() names it).  Errors found by a
@@ -65,7 +66,7 @@ enum softmax_status {
 /* Kernel variants (softmax_rows_ex).  AUTO picks one from the shape. */
 enum softmax_variant {
   SOFTMAX_VARIANT_AUTO = 0,
-  /* One read: the row is loaded once into registers with 128-bit loads (rows up to 8 KiB). */
+  /* One read: the row is loaded once into registers with 128-bit loads (rows up to 32 KiB). */
   SOFTMAX_VARIANT_ONEREAD_REG = 1,
   /* One read: bulk copies (cp.async.bulk + mbarrier) stage whole rows in shared memory, a
      warp-specialised persistent CTA normalises them and bulk-stores them (rows up to 64 KiB). */
@@ -75,7 +76,9 @@ enum softmax_variant {
   SOFTMAX_VARIANT_TWOPASS = 3,
   /* Split row: one row is spread over every CTA of the grid; CTAs of a thread-block cluster merge
      (m, d) over distributed shared memory, clusters exchange 8-byte states through global memory
-     (for few, very long rows). */
+     (for few, very long rows: each CTA's segment of a row must fit in its shared-memory ring,
+     about 200 KiB, so rows up to about 200 KiB x the number of SMs; 16-byte aligned).  It
+     needs every cluster resident at once, so it must not share the GPU with other kernels. */
   SOFTMAX_VARIANT_SPLITROW = 4
 };
 
@@ -120,12 +123,13 @@ int merge_states(const float* m_a, const float* d_a, const float* m_b, const flo
 
 /*
  * softmax_rows_host -- softmax_rows on HOST buffers (x_host, y_host: M x N of
- * dtype, ideally pinned).  Row blocks are copied host->device, normalised on
- * the GPU and copied back, with copies and kernels of consecutive blocks
- * overlapped on two internal streams.  Device staging memory is taken from
- * the stream-ordered pool and released before return.  Returns when y_host
- * holds the result (the call synchronises).  `stream` orders the work after
- * earlier work on that stream.
+ * dtype, ideally pinned).  Row blocks of about 8 MiB are copied host->device,
+ * normalised in place on the GPU and copied back, with the copies and kernels
+ * of consecutive blocks overlapped on three internal streams.  The streams and
+ * the device staging buffers (3 x one block) are created on the first call on
+ * a device and kept until the process exits; concurrent calls on one device
+ * are serialised.  Returns when y_host holds the result (the call
+ * synchronises).  `stream` orders the work after earlier work on that stream.
  */
 int softmax_rows_host(const void* x_host, void* y_host, int64_t M, int64_t N, int dtype,
                       void* stream);

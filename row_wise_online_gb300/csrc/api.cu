@@ -28,6 +28,46 @@ uint64_t g_exchange_wait_ns = 200ull * 1000 * 1000;  // 200 ms
 int g_debug_fault = 0;
 std::mutex g_debug_mutex;
 
+// Per-device resources of softmax_rows_host, created on first use and kept for the life of the
+// process: copy/compute lanes (non-blocking streams), events and grow-only staging buffers.
+struct HostPipe {
+  static constexpr int kLanes = 3;
+  std::mutex mu;
+  bool ready = false;
+  cudaStream_t lanes[kLanes] = {};
+  cudaEvent_t ev_start = nullptr;
+  cudaEvent_t ev_done[kLanes] = {};
+  void* buf[kLanes] = {};
+  size_t buf_bytes = 0;
+
+  cudaError_t prepare(size_t bytes) {
+    cudaError_t err;
+    if (!ready) {
+      for (int i = 0; i < kLanes; ++i) {
+        if ((err = cudaStreamCreateWithFlags(&lanes[i], cudaStreamNonBlocking)) != cudaSuccess) return err;
+        if ((err = cudaEventCreateWithFlags(&ev_done[i], cudaEventDisableTiming)) != cudaSuccess) return err;
+      }
+      if ((err = cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming)) != cudaSuccess) return err;
+      ready = true;
+    }
+    if (bytes > buf_bytes) {
+      for (int i = 0; i < kLanes; ++i) {
+        if (buf[i]) {
+          if ((err = cudaStreamSynchronize(lanes[i])) != cudaSuccess) return err;
+          if ((err = cudaFree(buf[i])) != cudaSuccess) return err;
+          buf[i] = nullptr;
+        }
+      }
+      buf_bytes = 0;
+      for (int i = 0; i < kLanes; ++i)
+        if ((err = cudaMalloc(&buf[i], bytes)) != cudaSuccess) return err;
+      buf_bytes = bytes;
+    }
+    return cudaSuccess;
+  }
+};
+HostPipe g_pipe[kMaxDevices];
+
 int cuda_fail(cudaError_t err) {
   t_last_cuda_error = cudaGetErrorString(err);
   return SOFTMAX_ERR_CUDA;
@@ -68,13 +108,16 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // Shape and pointer checks shared by the row calls.  Returns a status; sets *noop for M == 0.
 int validate_rows(const void* x, int64_t M, int64_t N, int dtype, bool* noop) {
   *noop = false;
-  if (!x) return SOFTMAX_ERR_INVALID_ARG;
   if (dtype != SOFTMAX_F32 && dtype != SOFTMAX_BF16) return SOFTMAX_ERR_INVALID_ARG;
   if (N < 1 || M < 0) return SOFTMAX_ERR_INVALID_ARG;
   const int64_t s = elem_bytes(dtype);
   if (N > INT64_MAX / s) return SOFTMAX_ERR_INVALID_ARG;
-  if (M > 0 && M > INT64_MAX / (N * s)) return SOFTMAX_ERR_INVALID_ARG;
-  if (M == 0) *noop = true;
+  if (M == 0) {  // nothing to do; pointers of an empty matrix may be NULL
+    *noop = true;
+    return SOFTMAX_OK;
+  }
+  if (M > INT64_MAX / (N * s)) return SOFTMAX_ERR_INVALID_ARG;
+  if (!x) return SOFTMAX_ERR_INVALID_ARG;
   return SOFTMAX_OK;
 }
 
@@ -84,7 +127,7 @@ int run_variant(RowProblem& p, int variant, const DeviceInfo& dev) {
   const int64_t row_bytes = p.N * elem_bytes(p.dtype);
   if (variant == SOFTMAX_VARIANT_AUTO) {
     if (aligned) {
-      if (row_bytes <= 4096 && oneread_reg_fits(p, true))
+      if (row_bytes <= 16384 && oneread_reg_fits(p, true))
         variant = SOFTMAX_VARIANT_ONEREAD_REG;
       else if (oneread_tma_fits(p, dev))
         variant = SOFTMAX_VARIANT_ONEREAD_SMEM;
@@ -149,9 +192,9 @@ int softmax_rows_ex(const void* x, void* y, float* m_out, float* d_out, float* l
   bool noop = false;
   int st = validate_rows(x, M, N, dtype, &noop);
   if (st != SOFTMAX_OK) return st;
-  if (!y) return SOFTMAX_ERR_INVALID_ARG;
   if (variant < SOFTMAX_VARIANT_AUTO || variant > SOFTMAX_VARIANT_SPLITROW) return SOFTMAX_ERR_INVALID_ARG;
   if (noop) return SOFTMAX_OK;
+  if (!y) return SOFTMAX_ERR_INVALID_ARG;
   const DeviceInfo* dev = nullptr;
   if ((st = current_device_info(&dev)) != SOFTMAX_OK) return st;
   RowProblem p;
@@ -176,8 +219,8 @@ int softmax_row_state(const void* x, float* m_out, float* d_out, float* lse_out,
   bool noop = false;
   int st = validate_rows(x, M, N, dtype, &noop);
   if (st != SOFTMAX_OK) return st;
-  if (!m_out && !d_out && !lse_out) return SOFTMAX_ERR_INVALID_ARG;
   if (noop) return SOFTMAX_OK;
+  if (!m_out && !d_out && !lse_out) return SOFTMAX_ERR_INVALID_ARG;
   const DeviceInfo* dev = nullptr;
   if ((st = current_device_info(&dev)) != SOFTMAX_OK) return st;
   RowProblem p;
@@ -198,8 +241,9 @@ int softmax_row_state(const void* x, float* m_out, float* d_out, float* lse_out,
 
 int merge_states(const float* m_a, const float* d_a, const float* m_b, const float* d_b, float* m_out,
                  float* d_out, float* lse_out, int64_t M, void* stream) {
-  if (!m_a || !d_a || !m_b || !d_b || !m_out || !d_out || M < 0) return SOFTMAX_ERR_INVALID_ARG;
+  if (M < 0) return SOFTMAX_ERR_INVALID_ARG;
   if (M == 0) return SOFTMAX_OK;
+  if (!m_a || !d_a || !m_b || !d_b || !m_out || !d_out) return SOFTMAX_ERR_INVALID_ARG;
   const DeviceInfo* dev = nullptr;
   int st = current_device_info(&dev);
   if (st != SOFTMAX_OK) return st;
@@ -213,84 +257,67 @@ int softmax_rows_host(const void* x_host, void* y_host, int64_t M, int64_t N, in
   bool noop = false;
   int st = validate_rows(x_host, M, N, dtype, &noop);
   if (st != SOFTMAX_OK) return st;
-  if (!y_host) return SOFTMAX_ERR_INVALID_ARG;
   if (noop) return SOFTMAX_OK;
+  if (!y_host) return SOFTMAX_ERR_INVALID_ARG;
   const DeviceInfo* dev = nullptr;
   if ((st = current_device_info(&dev)) != SOFTMAX_OK) return st;
 
   const cudaStream_t user = static_cast<cudaStream_t>(stream);
   const int64_t row_bytes = N * elem_bytes(dtype);
-  // Blocks of about 16 MiB: large enough for full-bandwidth copies, small enough to overlap.
-  int64_t block_rows = (int64_t(16) << 20) / row_bytes;
+  // Blocks of about 8 MiB: large enough for full-rate copies, small enough to overlap the
+  // host->device copy of one block with the kernel and device->host copy of the others.
+  int64_t block_rows = (int64_t(8) << 20) / row_bytes;
   if (block_rows < 1) block_rows = 1;
   if (block_rows > M) block_rows = M;
   const int64_t nblocks = (M + block_rows - 1) / block_rows;
-  const int nbuf = nblocks > 1 ? 2 : 1;
   const size_t buf_bytes = size_t(block_rows * row_bytes);
 
-  cudaStream_t lanes[2] = {nullptr, nullptr};
-  cudaEvent_t ev_start = nullptr, ev_done[2] = {nullptr, nullptr};
-  void* dbuf[2] = {nullptr, nullptr};
-  cudaError_t err = cudaSuccess;
-  int result = SOFTMAX_OK;
+  HostPipe& hp = g_pipe[dev->device];
+  std::lock_guard<std::mutex> lock(hp.mu);
+  cudaError_t err = hp.prepare(buf_bytes);
+  if (err != cudaSuccess) return cuda_fail(err);
 
+  int result = SOFTMAX_OK;
   auto fail = [&](cudaError_t e) {
     if (result == SOFTMAX_OK) result = cuda_fail(e);
   };
+  if ((err = cudaEventRecord(hp.ev_start, user)) != cudaSuccess) return cuda_fail(err);
+  for (int i = 0; i < HostPipe::kLanes; ++i)
+    if ((err = cudaStreamWaitEvent(hp.lanes[i], hp.ev_start, 0)) != cudaSuccess) return cuda_fail(err);
 
-  for (int i = 0; i < nbuf && err == cudaSuccess; ++i) {
-    if ((err = cudaStreamCreateWithFlags(&lanes[i], cudaStreamNonBlocking)) != cudaSuccess) break;
-    if ((err = cudaEventCreateWithFlags(&ev_done[i], cudaEventDisableTiming)) != cudaSuccess) break;
-    // x and y of a block share one buffer: the kernels run in place.
-    if ((err = cudaMallocAsync(&dbuf[i], buf_bytes, user)) != cudaSuccess) break;
-  }
-  if (err == cudaSuccess) err = cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming);
-  if (err == cudaSuccess) err = cudaEventRecord(ev_start, user);
-  for (int i = 0; i < nbuf && err == cudaSuccess; ++i) err = cudaStreamWaitEvent(lanes[i], ev_start, 0);
-  if (err != cudaSuccess) fail(err);
-
-  for (int64_t b = 0; b < nblocks && result == SOFTMAX_OK; ++b) {
-    const int li = int(b % nbuf);
+  for (int64_t b = 0; b < nblocks; ++b) {
+    const int li = int(b % HostPipe::kLanes);
     const int64_t r0 = b * block_rows;
     const int64_t rows = (M - r0) < block_rows ? (M - r0) : block_rows;
     const size_t bytes = size_t(rows * row_bytes);
     const char* src = static_cast<const char*>(x_host) + r0 * row_bytes;
     char* dst = static_cast<char*>(y_host) + r0 * row_bytes;
-    if ((err = cudaMemcpyAsync(dbuf[li], src, bytes, cudaMemcpyHostToDevice, lanes[li])) != cudaSuccess) {
+    if ((err = cudaMemcpyAsync(hp.buf[li], src, bytes, cudaMemcpyHostToDevice, hp.lanes[li])) != cudaSuccess) {
       fail(err);
       break;
     }
-    RowProblem p;
-    p.x = dbuf[li];
-    p.y = dbuf[li];
+    RowProblem p;  // in place on the staging buffer
+    p.x = hp.buf[li];
+    p.y = hp.buf[li];
     p.M = rows;
     p.N = N;
     p.dtype = dtype;
-    p.stream = lanes[li];
+    p.stream = hp.lanes[li];
     if ((st = run_variant(p, SOFTMAX_VARIANT_AUTO, *dev)) != SOFTMAX_OK) {
       result = st;
       break;
     }
-    if ((err = cudaMemcpyAsync(dst, dbuf[li], bytes, cudaMemcpyDeviceToHost, lanes[li])) != cudaSuccess) {
+    if ((err = cudaMemcpyAsync(dst, hp.buf[li], bytes, cudaMemcpyDeviceToHost, hp.lanes[li])) != cudaSuccess) {
       fail(err);
       break;
     }
   }
-  // Join the lanes back into the caller's stream, release staging memory, and wait.
-  for (int i = 0; i < nbuf; ++i) {
-    if (lanes[i] && ev_done[i]) {
-      if ((err = cudaEventRecord(ev_done[i], lanes[i])) != cudaSuccess) fail(err);
-      else if ((err = cudaStreamWaitEvent(user, ev_done[i], 0)) != cudaSuccess) fail(err);
-    }
+  // Join the lanes back into the caller's stream and wait for the result.
+  for (int i = 0; i < HostPipe::kLanes; ++i) {
+    if ((err = cudaEventRecord(hp.ev_done[i], hp.lanes[i])) != cudaSuccess) fail(err);
+    else if ((err = cudaStreamWaitEvent(user, hp.ev_done[i], 0)) != cudaSuccess) fail(err);
   }
-  for (int i = 0; i < nbuf; ++i)
-    if (dbuf[i] && (err = cudaFreeAsync(dbuf[i], user)) != cudaSuccess) fail(err);
   if ((err = cudaStreamSynchronize(user)) != cudaSuccess) fail(err);
-  for (int i = 0; i < nbuf; ++i) {
-    if (ev_done[i]) cudaEventDestroy(ev_done[i]);
-    if (lanes[i]) cudaStreamDestroy(lanes[i]);
-  }
-  if (ev_start) cudaEventDestroy(ev_start);
   return result;
 }
 

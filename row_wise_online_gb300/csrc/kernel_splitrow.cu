@@ -1,7 +1,450 @@
-// kernel_splitrow.cu -- split-row variant (not built yet: never selected).
+// kernel_splitrow.cu -- split-row softmax: few, very long rows spread over the whole GPU.
+//
+// "5.2 CUDA Online Softmax 实现优化" §7.1 names the case (small M, huge N: split one row over
+// several blocks and merge their partial results); the merge is the (m, d) merge of §4.1, which
+// is associative, so any partition of a row can be folded separately and combined.
+//
+// Layout: the grid is G persistent CTAs (one per SM), grouped in thread-block clusters of CS.
+// Every row is cut into G contiguous segments of 16-byte units, balanced to one unit; CTA c owns
+// segment c of every row.  A segment (up to ~200 KB) is staged in shared memory in pieces of
+// 16 KB by bulk copies (cp.async.bulk + mbarrier) issued by one producer lane, so x is read from
+// HBM once and y written once (bulk stores), as in the one-read kernel.
+//
+// Per row r, in every CTA:
+//   1. consumers fold the segment's pieces into per-thread (m, d) states (online recurrence);
+//   2. warp butterfly merge, then cross-warp merge through shared memory -> CTA state;
+//   3. cluster merge over distributed shared memory: each CTA writes its state into rank 0's
+//      shared memory (st.shared::cluster) and arrives on rank 0's mbarrier (release.cluster);
+//      rank 0 merges the CS states in rank order and publishes the cluster state to global
+//      memory, then bumps a release counter;
+//   4. while the exchange is in flight, the consumers fold the first pieces of row r + 1
+//      (already landing in free slots), so the HBM stream does not stop;
+//   5. one lane waits (acquire, bounded by %globaltimer) until every cluster has published row
+//      r, warp 0 merges all cluster states in a fixed order -- identical in every CTA, so every
+//      CTA normalises with bitwise the same (m, d) -- and the row is normalised in shared memory
+//      and bulk-stored.
+// All clusters must be resident at once; the host launches at most the number of clusters the
+// occupancy query reports.  Every wait is bounded; a wait that runs out records
+// SOFTMAX_ERR_TIMEOUT in the status word, skips the remaining exchange waits, and the kernel
+// still terminates.
+#include <mutex>
+
+#include "device_common.cuh"
 #include "launch.h"
 
 namespace rwo {
-bool splitrow_fits(const RowProblem&, const DeviceInfo&) { return false; }
-cudaError_t launch_splitrow(const RowProblem&, const DeviceInfo&) { return cudaErrorNotSupported; }
+namespace {
+
+constexpr int kPieceBytes = 16384;
+constexpr int kPieceUnits = kPieceBytes / 16;
+constexpr int kSplitNcw = 16;  // consumer warps
+constexpr int kMaxCluster = 8;
+
+struct SplitArgs {
+  const unsigned char* x;
+  unsigned char* y;
+  float* m_out;
+  float* d_out;
+  float* lse_out;
+  int64_t M;
+  int64_t units;      // 16-byte units per row
+  int64_t row_bytes;
+  int slots;          // ring slots of kPieceBytes
+  unsigned* counter;  // cluster publications so far (zeroed before launch)
+  float* gstate;      // [M][clusters][2]: published cluster states
+  unsigned* status;
+  uint64_t local_wait_ns;
+  uint64_t exchange_wait_ns;
+  int fault;  // test hook: cluster 0 never publishes
+};
+
+struct SplitSmem {
+  uint64_t* full;
+  uint64_t* done;
+  uint64_t* cbar;    // [2] cluster-merge barriers (used in rank 0)
+  State* cstate;     // [2][kMaxCluster] (written remotely into rank 0)
+  State* wstate;     // [2][kSplitNcw]
+  State* rowst;      // [2]
+  int* abort_flag;   // [1]
+};
+
+size_t split_tail_bytes(int slots) {
+  return size_t(slots) * 2 * sizeof(uint64_t) + 2 * sizeof(uint64_t) + 2 * kMaxCluster * sizeof(State) +
+         2 * kSplitNcw * sizeof(State) + 2 * sizeof(State) + 16;
+}
+
+__device__ __forceinline__ uint32_t piece_units(int64_t seg_units, int k) {
+  const int64_t rest = seg_units - int64_t(k) * kPieceUnits;
+  return uint32_t(rest < kPieceUnits ? rest : kPieceUnits);
+}
+
+// Online fold of `pu` units of a piece in shared memory into this thread's state.
+template <class D>
+__device__ __forceinline__ State fold_piece(State st, uint32_t slot, uint32_t pu, int tid) {
+  constexpr int E = D::kVec;
+  constexpr int NCT = kSplitNcw * 32;
+  for (uint32_t u = tid; u < pu; u += 2 * NCT) {
+    float v[2][E];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const uint32_t uu = u + k * NCT;
+      if (uu < pu) {
+        D::unpack(lds16(slot + uu * 16u), v[k]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[k][e] = -INFINITY;
+      }
+    }
+    float mu = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+#pragma unroll
+      for (int e = 0; e < E; ++e) mu = fmaxf(mu, v[k][e]);
+    const float m_new = fmaxf(st.m, mu);
+    const float ms = safe_max(m_new);
+    float acc = 0.f;
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc += exp_diff(v[k][e], ms);
+    st.d = __fadd_rn(__fmul_rn(st.d, exp_diff(st.m, ms)), acc);
+    st.m = m_new;
+  }
+  return st;
+}
+
+template <class D>
+__device__ __forceinline__ void normalise_piece(uint32_t slot, uint32_t pu, int tid, float ms, float inv) {
+  constexpr int E = D::kVec;
+  constexpr int NCT = kSplitNcw * 32;
+  for (uint32_t u = tid; u < pu; u += NCT) {
+    float v[E];
+    D::unpack(lds16(slot + u * 16u), v);
+#pragma unroll
+    for (int e = 0; e < E; ++e) v[e] = __fmul_rn(exp_diff(v[e], ms), inv);
+    sts16(slot + u * 16u, D::pack(v));
+  }
+}
+
+__device__ __forceinline__ float ld_relaxed_f32(const float* p) {
+  float v;
+  asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  // Non-aligned form: not every lane of every warp reaches it at the same instruction.
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+template <class D>
+__global__ void __launch_bounds__((kSplitNcw + 1) * 32, 1) k_splitrow(SplitArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int NCT = kSplitNcw * 32;
+  const int NS = a.slots;
+  SplitSmem sm;
+  {
+    unsigned char* p = smem + size_t(NS) * kPieceBytes;
+    sm.full = reinterpret_cast<uint64_t*>(p);
+    sm.done = sm.full + NS;
+    sm.cbar = sm.done + NS;
+    sm.cstate = reinterpret_cast<State*>(sm.cbar + 2);
+    sm.wstate = sm.cstate + 2 * kMaxCluster;
+    sm.rowst = sm.wstate + 2 * kSplitNcw;
+    sm.abort_flag = reinterpret_cast<int*>(sm.rowst + 2);
+  }
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t crank = cluster_ctarank();
+  const uint32_t csize = cluster_nctarank();
+  const uint32_t cid = cluster_id_x();
+  const uint32_t ncl = cluster_count_x();
+
+  // This CTA's segment of every row, in 16-byte units.
+  const int64_t G = gridDim.x, c = blockIdx.x;
+  const int64_t base = a.units / G, rem = a.units % G;
+  const int64_t seg_units = base + (c < rem ? 1 : 0);
+  const int64_t seg_start = c * base + (c < rem ? c : rem);
+  const int K = int((seg_units + kPieceUnits - 1) / kPieceUnits);
+  const int F = K < NS - K ? K : NS - K;  // pieces of row r + 1 folded during row r's exchange
+
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(smem_addr(&sm.full[s]), 1);
+      mbar_init(smem_addr(&sm.done[s]), kSplitNcw);
+    }
+    mbar_init(smem_addr(&sm.cbar[0]), csize);
+    mbar_init(smem_addr(&sm.cbar[1]), csize);
+    *sm.abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  cluster_sync_all();  // every CTA's barriers exist before any remote arrive
+
+  if (warp == kSplitNcw) {
+    // ---------------- producer ----------------
+    if (lane == 0 && K > 0) {
+      const uint64_t pol = policy_evict_first();
+      const int64_t total = a.M * K;
+      bool timed_out = false;
+      int64_t stored = 0;
+      auto piece_offset = [&](int64_t p) {
+        const int64_t r = p / K;
+        const int k = int(p % K);
+        return r * a.row_bytes + (seg_start + int64_t(k) * kPieceUnits) * 16;
+      };
+      auto store_next = [&]() {
+        const int s = int(stored % NS);
+        if (!mbar_wait(smem_addr(&sm.done[s]), uint32_t((stored / NS) & 1), a.local_wait_ns)) timed_out = true;
+        const uint32_t bytes = piece_units(seg_units, int(stored % K)) * 16u;
+        bulk_s2g(a.y + piece_offset(stored), smem_addr(smem + size_t(s) * kPieceBytes), bytes, pol);
+        bulk_commit();
+        ++stored;
+      };
+      for (int64_t p = 0; p < total; ++p) {
+        const int s = int(p % NS);
+        if (p >= NS) {
+          while (stored <= p - NS) store_next();
+          bulk_wait_read_all();
+        }
+        const uint32_t bytes = piece_units(seg_units, int(p % K)) * 16u;
+        const uint32_t bar = smem_addr(&sm.full[s]);
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_g2s(smem_addr(smem + size_t(s) * kPieceBytes), a.x + piece_offset(p), bytes, bar, pol);
+      }
+      while (stored < total) store_next();
+      for (int64_t p = total > NS ? total - NS : 0; p < total; ++p)
+        if (!mbar_wait(smem_addr(&sm.full[p % NS]), uint32_t((p / NS) & 1), a.local_wait_ns)) timed_out = true;
+      bulk_wait_all();
+      if (timed_out) atomicOr(a.status, kStatusTimeout);
+    }
+  } else {
+    // ---------------- consumers ----------------
+    bool timed_out = false;
+    State nxt = empty_state();
+    int pre = 0;
+    for (int64_t r = 0; r < a.M; ++r) {
+      const int b = int(r & 1);
+      State st = nxt;
+      for (int k = pre; k < K; ++k) {
+        const int64_t p = r * K + k;
+        const int s = int(p % NS);
+        if (!mbar_wait(smem_addr(&sm.full[s]), uint32_t((p / NS) & 1), a.local_wait_ns)) timed_out = true;
+        st = fold_piece<D>(st, smem_addr(smem + size_t(s) * kPieceBytes), piece_units(seg_units, k), tid);
+      }
+      st = group_merge(st, sm.wstate + b * kSplitNcw, kSplitNcw, warp, lane, [] { named_barrier_sync(1, NCT); });
+
+      // cluster merge over DSMEM; rank 0 publishes the cluster state
+      if (tid == 0) {
+        st_cluster_f32x2(map_to_rank(smem_addr(&sm.cstate[b * kMaxCluster + crank]), 0), st.m, st.d);
+        mbar_arrive_remote(map_to_rank(smem_addr(&sm.cbar[b]), 0));
+        if (crank == 0) {
+          if (!mbar_wait_cluster(smem_addr(&sm.cbar[b]), uint32_t((r >> 1) & 1), a.local_wait_ns)) timed_out = true;
+          State cs = empty_state();
+          for (uint32_t i = 0; i < csize; ++i) cs = merge(cs, sm.cstate[b * kMaxCluster + i]);
+          if (!(a.fault && cid == 0)) {
+            float* g = a.gstate + (r * ncl + cid) * 2;
+            g[0] = cs.m;
+            g[1] = cs.d;
+            red_release_add(a.counter, 1u);
+          }
+        }
+      }
+
+      // fold the first pieces of the next row while the exchange is in flight
+      nxt = empty_state();
+      pre = 0;
+      if (r + 1 < a.M) {
+        pre = F;
+        for (int k = 0; k < F; ++k) {
+          const int64_t p = (r + 1) * K + k;
+          const int s = int(p % NS);
+          if (!mbar_wait(smem_addr(&sm.full[s]), uint32_t((p / NS) & 1), a.local_wait_ns)) timed_out = true;
+          nxt = fold_piece<D>(nxt, smem_addr(smem + size_t(s) * kPieceBytes), piece_units(seg_units, k), tid);
+        }
+      }
+
+      // wait for every cluster's state of row r, then merge them in cluster order
+      if (warp == 0) {
+        if (lane == 0 && *sm.abort_flag == 0) {
+          const unsigned target = unsigned((r + 1) * ncl);
+          if (ld_acquire(a.counter) < target) {
+            const uint64_t t0 = global_timer_ns();
+            while (ld_acquire(a.counter) < target) {
+              if (global_timer_ns() - t0 > a.exchange_wait_ns) {
+                *sm.abort_flag = 1;
+                timed_out = true;
+                break;
+              }
+              __nanosleep(64);
+            }
+          }
+        }
+        __syncwarp();
+        State g = empty_state();
+        for (uint32_t i = lane; i < ncl; i += 32) {
+          const float* gp = a.gstate + (r * ncl + i) * 2;
+          g = merge(g, State{ld_relaxed_f32(gp), ld_relaxed_f32(gp + 1)});
+        }
+        g = warp_merge(g);
+        if (lane == 0) sm.rowst[b] = g;
+      }
+      named_barrier_sync(1, NCT);
+      const State row = sm.rowst[b];
+      const float ms = safe_max(row.m);
+      const float inv = safe_inv(row.d);
+      for (int k = 0; k < K; ++k) {
+        const int64_t p = r * K + k;
+        const int s = int(p % NS);
+        normalise_piece<D>(smem_addr(smem + size_t(s) * kPieceBytes), piece_units(seg_units, k), tid, ms, inv);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&sm.done[s]));
+      }
+      if (c == 0 && tid == 0) {
+        if (a.m_out) a.m_out[r] = row.m;
+        if (a.d_out) a.d_out[r] = row.d;
+        if (a.lse_out) a.lse_out[r] = lse_of(row);
+      }
+    }
+    if (timed_out && lane == 0) atomicOr(a.status, kStatusTimeout);
+  }
+  __syncwarp();
+  cluster_sync_all();  // no CTA leaves while a peer may still write into its shared memory
+}
+
+using SplitKernel = void (*)(SplitArgs);
+
+SplitKernel split_kernel(int dtype) { return dtype == 0 ? k_splitrow<F32> : k_splitrow<BF16>; }
+
+struct SplitPlan {
+  bool ok = false;
+  int cluster = 0;
+  int clusters = 0;
+  int slots = 0;
+  size_t smem = 0;
+};
+
+std::mutex g_plan_mutex;
+SplitPlan g_plan[64][2];
+bool g_plan_ready[64][2];
+
+// Cluster size and count giving the most resident CTAs (one per SM), and the ring size.
+SplitPlan plan_for(int dtype, const DeviceInfo& dev) {
+  std::lock_guard<std::mutex> lock(g_plan_mutex);
+  if (dev.device >= 0 && dev.device < 64 && g_plan_ready[dev.device][dtype]) return g_plan[dev.device][dtype];
+  SplitPlan best;
+  if (dev.cluster_launch) {
+    int slots = int((size_t(dev.max_smem_per_block_optin) - split_tail_bytes(16)) / kPieceBytes);
+    if (slots > 16) slots = 16;
+    const size_t smem = size_t(slots) * kPieceBytes + split_tail_bytes(slots);
+    SplitKernel fn = split_kernel(dtype);
+    if (slots >= 4 &&
+        cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) == cudaSuccess) {
+      for (int cs : {8, 4, 2}) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = cs;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(cs);
+        cfg.blockDim = dim3((kSplitNcw + 1) * 32);
+        cfg.dynamicSmemBytes = smem;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, (const void*)fn, &cfg) != cudaSuccess) {
+          cudaGetLastError();
+          continue;
+        }
+        if (n * cs > best.clusters * best.cluster) {
+          best.ok = n > 0;
+          best.cluster = cs;
+          best.clusters = n;
+          best.slots = slots;
+          best.smem = smem;
+        }
+      }
+    } else {
+      cudaGetLastError();
+    }
+  }
+  if (dev.device >= 0 && dev.device < 64) {
+    g_plan[dev.device][dtype] = best;
+    g_plan_ready[dev.device][dtype] = true;
+  }
+  return best;
+}
+
+}  // namespace
+
+bool splitrow_fits(const RowProblem& p, const DeviceInfo& dev) {
+  const int64_t row_bytes = p.N * elem_bytes(p.dtype);
+  if (row_bytes % 16 != 0) return false;
+  const SplitPlan plan = plan_for(p.dtype, dev);
+  if (!plan.ok) return false;
+  const int64_t G = int64_t(plan.cluster) * plan.clusters;
+  const int64_t units = row_bytes / 16;
+  if (units < G * 64) return false;  // rows this short belong to the one-read kernels
+  const int64_t seg = (units + G - 1) / G;
+  const int64_t K = (seg + kPieceUnits - 1) / kPieceUnits;
+  return K + 1 <= plan.slots;
+}
+
+cudaError_t launch_splitrow(const RowProblem& p, const DeviceInfo& dev) {
+  const SplitPlan plan = plan_for(p.dtype, dev);
+  if (!plan.ok) return cudaErrorInvalidConfiguration;
+  SplitKernel fn = split_kernel(p.dtype);
+  cudaError_t err =
+      cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(plan.smem));
+  if (err != cudaSuccess) return err;
+  const int G = plan.cluster * plan.clusters;
+  // Scratch: one publication counter and the published cluster states, stream-ordered.
+  const size_t state_bytes = size_t(p.M) * plan.clusters * 2 * sizeof(float);
+  void* scratch = nullptr;
+  if ((err = cudaMallocAsync(&scratch, 256 + state_bytes, p.stream)) != cudaSuccess) return err;
+  if ((err = cudaMemsetAsync(scratch, 0, 256, p.stream)) != cudaSuccess) {
+    cudaFreeAsync(scratch, p.stream);
+    return err;
+  }
+  SplitArgs a;
+  a.x = static_cast<const unsigned char*>(p.x);
+  a.y = static_cast<unsigned char*>(p.y);
+  a.m_out = p.m_out;
+  a.d_out = p.d_out;
+  a.lse_out = p.lse_out;
+  a.M = p.M;
+  a.row_bytes = p.N * elem_bytes(p.dtype);
+  a.units = a.row_bytes / 16;
+  a.slots = plan.slots;
+  a.counter = static_cast<unsigned*>(scratch);
+  a.gstate = reinterpret_cast<float*>(static_cast<unsigned char*>(scratch) + 256);
+  a.status = dev.status;
+  a.local_wait_ns = local_wait_limit_ns();
+  a.exchange_wait_ns = exchange_wait_limit_ns();
+  a.fault = debug_fault();
+
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = plan.cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(G);
+  cfg.blockDim = dim3((kSplitNcw + 1) * 32);
+  cfg.dynamicSmemBytes = plan.smem;
+  cfg.stream = p.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, fn, a);
+  cudaError_t ferr = cudaFreeAsync(scratch, p.stream);
+  return err != cudaSuccess ? err : ferr;
+}
+
 }  // namespace rwo

@@ -55,6 +55,8 @@ X = ctypes.c_void_p(0x1000)  # never dereferenced: every call below fails valida
     ((X, X, 4, 4, 7, NULL), rwo.ERR_INVALID_ARG),          # unknown dtype
     ((X, X, 2**62, 2**3, 0, NULL), rwo.ERR_INVALID_ARG),   # M*N*4 overflows int64
     ((X, X, 0, 4, 0, NULL), rwo.OK),                        # M = 0: no-op
+    ((NULL, NULL, 0, 4, 0, NULL), rwo.OK),                  # M = 0 with the NULL data of an empty tensor
+    ((NULL, NULL, 0, 0, 0, NULL), rwo.ERR_INVALID_ARG),     # ... but N is still checked
 ])
 def test_softmax_rows_argument_checks(lib, args, expect):
     assert lib.softmax_rows(*args) == expect

@@ -169,7 +169,8 @@ def test_host_buffers_pipeline():
 def test_variant_choice():
     cases = [
         ("fp32_64x1024", V.VARIANT_ONEREAD_REG),
-        ("fp32_4096x4096", V.VARIANT_ONEREAD_SMEM),
+        ("fp32_4096x4096", V.VARIANT_ONEREAD_REG),
+        ("bf16_logits_16384x32768", V.VARIANT_ONEREAD_SMEM),
     ]
     for name, want in cases:
         w = synth.WORKLOADS[name].with_rows(8)

@@ -1,0 +1,100 @@
+"""Split-row path: rows spread over every CTA, cluster (DSMEM) merge, bounded cross-cluster exchange.
+
+The failure test makes the exchange wait run out on purpose from the host side (a test hook
+keeps one cluster from publishing its state): the kernel must record SOFTMAX_ERR_TIMEOUT in the
+status word and terminate, and the next launch must work normally.  Nothing faults or hangs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import row_wise_online_gb300 as rwo
+import synth
+from gpu_util import run_softmax, to_device, to_host
+from tolerances import check_rowsums, check_state, check_y
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from row_wise_online_gb300 import _build
+
+    _build.build()
+    torch.cuda.set_device(0)
+
+
+@pytest.mark.parametrize("dtype,M,N", [
+    (synth.F32, 3, 1 << 21), (synth.F32, 5, 1_500_000), (synth.BF16, 2, 1 << 22), (synth.BF16, 7, 3_000_008),
+    (synth.F32, 1, 6_000_000),
+])
+def test_splitrow_against_oracle(dtype, M, N):
+    w = synth.custom("split", dtype, M, N, seed=N % 1000, dist=synth.UNIFORM, p0=-20.0, p1=20.0, late_max=20.0)
+    x_host = synth.generate(w)
+    x = to_device(x_host)
+    y, m, d, lse = run_softmax(x, rwo.VARIANT_SPLITROW)
+    assert rwo.last_variant() == rwo.VARIANT_SPLITROW
+    y_ref, m_ref, d_ref, lse_ref = oracle.softmax_rows(x_host)
+    yh = to_host(y)
+    check_y(yh, y_ref, dtype, f"split {M}x{N}")
+    check_rowsums(yh, dtype, None, "split")
+    check_state(m.cpu().numpy(), d.cpu().numpy(), lse.cpu().numpy(), m_ref, d_ref, lse_ref, "split")
+
+
+def test_splitrow_masked_segments_and_special_rows():
+    """Whole CTA segments and clusters that see only -inf must merge as the empty state."""
+    N = 1 << 21
+    rows = np.random.default_rng(0).standard_normal((4, N)).astype(np.float32) * 3
+    rows[0, : N - 1000] = -np.inf          # only the tail survives: most CTAs hold empty states
+    rows[1, 1000:] = -np.inf               # only the head survives
+    rows[2, :] = -np.inf                   # fully masked row
+    rows[3, N // 2] = 1e30                 # one huge value
+    x = to_device(rows)
+    y, m, d, lse = run_softmax(x, rwo.VARIANT_SPLITROW)
+    y_ref, m_ref, d_ref, lse_ref = oracle.softmax_rows(rows)
+    yh = to_host(y)
+    check_y(yh, y_ref, synth.F32, "split special")
+    check_rowsums(yh, synth.F32, ~np.isfinite(m_ref), "split special")
+    check_state(m.cpu().numpy(), d.cpu().numpy(), lse.cpu().numpy(), m_ref, d_ref, lse_ref, "split special")
+    assert not np.isnan(yh).any()
+
+
+def test_splitrow_in_place():
+    w = synth.custom("split-ip", synth.BF16, 3, 1 << 22, seed=5, p1=2.0)
+    x_host = synth.generate(w)
+    x = to_device(x_host)
+    rwo.softmax_rows_ex(x, x, variant=rwo.VARIANT_SPLITROW)
+    assert rwo.get_status() == rwo.OK
+    y_ref, *_ = oracle.softmax_rows(x_host)
+    check_y(to_host(x), y_ref, synth.BF16, "split in place")
+
+
+def test_auto_takes_splitrow_for_few_long_rows():
+    w = synth.WORKLOADS["fp32_longrow_32x4194304"].with_rows(4)
+    x = to_device(synth.generate(w))
+    rwo.softmax_rows(x)
+    torch.cuda.synchronize()
+    assert rwo.last_variant() == rwo.VARIANT_SPLITROW
+
+
+def test_exchange_wait_runs_out_and_reports_timeout():
+    w = synth.custom("fault", synth.F32, 3, 1 << 21, seed=1, p1=2.0)
+    x_host = synth.generate(w)
+    x = to_device(x_host)
+    y = torch.empty_like(x)
+    assert rwo.get_status() == rwo.OK
+    old_limit = rwo.debug_set_wait_limit_ns(20_000_000)  # 20 ms
+    old_fault = rwo.debug_set_fault(1)
+    try:
+        rwo.softmax_rows_ex(x, y, variant=rwo.VARIANT_SPLITROW)
+        assert rwo.get_status() == rwo.ERR_TIMEOUT
+    finally:
+        rwo.debug_set_fault(old_fault)
+        rwo.debug_set_wait_limit_ns(old_limit)
+    # the context is intact and the next launch is correct
+    assert rwo.get_status() == rwo.OK
+    rwo.softmax_rows_ex(x, y, variant=rwo.VARIANT_SPLITROW)
+    assert rwo.get_status() == rwo.OK
+    y_ref, *_ = oracle.softmax_rows(x_host)
+    check_y(to_host(y), y_ref, synth.F32, "after timeout")
