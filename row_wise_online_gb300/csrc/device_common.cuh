@@ -130,6 +130,11 @@ struct F32 {
   __device__ static __forceinline__ float load1(const void* p, int64_t i) {
     return __ldg(static_cast<const float*>(p) + i);
   }
+  // Largest of the vector's four values.
+  __device__ static __forceinline__ float vmax(const uint4& v) {
+    return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
+                 fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+  }
   __device__ static __forceinline__ void store1(void* p, int64_t i, float v) {
     static_cast<float*>(p)[i] = v;
   }
@@ -156,6 +161,14 @@ struct BF16 {
   __device__ static __forceinline__ float load1(const void* p, int64_t i) {
     const unsigned short b = __ldg(static_cast<const unsigned short*>(p) + i);
     return __uint_as_float(static_cast<uint32_t>(b) << 16);
+  }
+  // Largest of the vector's eight values: packed bf16x2 max (exact), then one widening.
+  __device__ static __forceinline__ float vmax(const uint4& v) {
+    uint32_t a, b, m;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(a) : "r"(v.x), "r"(v.y));
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(b) : "r"(v.z), "r"(v.w));
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(a), "r"(b));
+    return fmaxf(bf16_lo(m), bf16_hi(m));
   }
   __device__ static __forceinline__ void store1(void* p, int64_t i, float v) {
     static_cast<uint16_t*>(p)[i] = to_bf16(v);

@@ -2,19 +2,17 @@
 //
 // "5.2 CUDA Online Softmax 实现优化", §6 keeps the row on chip so that x is read from HBM once
 // and y written once; "Softmax 数值稳定性与 IO-Aware Attention" §三 names shared memory as the
-// place for rows that fit.  On sm_103a the copy engine does the moving:
+// place for rows that fit.  On sm_103a the copy engine does the loading:
 //
 //  * One producer warp (one elected lane) per CTA issues cp.async.bulk global -> shared for
 //    whole rows into a ring of S row slots, completion counted in bytes on an mbarrier per
-//    slot ("full"), and bulk-stores finished rows shared -> global.  It runs up to S - 1 rows
-//    ahead of the consumers, so HBM reads stay in flight while rows are being normalised.
-//  * NCW consumer warps wait on "full", read their part of the row (VPT 16-byte vectors per
-//    thread) into registers, fold it into the thread's (m, d) state with one exponential per
-//    element, merge states across the warp (butterfly) and across the consumer warps (shared
-//    memory, one named barrier per row), write y = e * 2^((m_t - m) log2 e) / d back into the
-//    same slot, fence the writes to the async proxy and arrive on the slot's "done" barrier.
-//  * The producer waits on "done", bulk-stores the row, and reuses the slot once the store has
-//    finished reading it.
+//    slot ("full").
+//  * NCW consumer warps wait on "full", copy their part of the row (VPT 16-byte vectors per
+//    thread) into registers and at once hand the slot back ("freed"), so all S slots carry HBM
+//    reads in flight while rows are being normalised.  Each thread folds its values into its
+//    (m, d) state with one exponential per element, states are merged across the warp
+//    (butterfly) and across the consumer warps (shared memory, one named barrier per row), and
+//    y = e * 2^((m_t - m) log2 e) / d leaves the registers in 16-byte streaming stores.
 //
 // Persistent: the grid is (CTAs resident per SM) x (SM count); CTA b handles rows b, b + grid,
 // ...  Every wait is bounded (%globaltimer); a wait that runs out sets the status word and the
@@ -50,14 +48,14 @@ __global__ void __launch_bounds__((NCW + 1) * 32) k_oneread_tma(TmaArgs a) {
   const int S = a.stages;
   unsigned char* slots = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(S) * a.slot_bytes);
-  uint64_t* done = full + S;
-  State* wstate = reinterpret_cast<State*>(done + S);  // [2][NCW]
+  uint64_t* freed = full + S;
+  State* wstate = reinterpret_cast<State*>(freed + S);  // [2][NCW]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_addr(&full[s]), 1);
-      mbar_init(smem_addr(&done[s]), NCW);
+      mbar_init(smem_addr(&freed[s]), NCW);
     }
     fence_mbar_init();
   }
@@ -67,35 +65,22 @@ __global__ void __launch_bounds__((NCW + 1) * 32) k_oneread_tma(TmaArgs a) {
   const int64_t nunits = a.N / E;
 
   if (warp == NCW) {
-    // ---------------- producer ----------------
+    // ---------------- producer: keep S row loads in flight ----------------
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       bool timed_out = false;
-      int64_t stored = 0;
-      auto store_next = [&]() {
-        const int s = int(stored % S);
-        if (!mbar_wait(smem_addr(&done[s]), uint32_t((stored / S) & 1), a.wait_ns)) timed_out = true;
-        const int64_t row = blockIdx.x + stored * gridDim.x;
-        bulk_s2g(a.y + row * a.row_bytes, smem_addr(slots + size_t(s) * a.slot_bytes), a.row_bytes, pol);
-        bulk_commit();
-        ++stored;
-      };
       for (int64_t j = 0; j < nrows; ++j) {
         const int s = int(j % S);
-        if (j >= S) {
-          while (stored <= j - S) store_next();
-          bulk_wait_read_all();  // slot s has been read out by its store
-        }
+        if (j >= S && !mbar_wait(smem_addr(&freed[s]), uint32_t(((j / S) - 1) & 1), a.wait_ns))
+          timed_out = true;
         const uint32_t bar = smem_addr(&full[s]);
         mbar_arrive_expect_tx(bar, a.row_bytes);
         const int64_t row = blockIdx.x + j * gridDim.x;
         bulk_g2s(smem_addr(slots + size_t(s) * a.slot_bytes), a.x + row * a.row_bytes, a.row_bytes, bar, pol);
       }
-      while (stored < nrows) store_next();
       // Every load must have landed before the CTA may exit (the consumers normally saw them all).
       for (int64_t j = nrows > S ? nrows - S : 0; j < nrows; ++j)
         if (!mbar_wait(smem_addr(&full[j % S]), uint32_t((j / S) & 1), a.wait_ns)) timed_out = true;
-      bulk_wait_all();
       if (timed_out) atomicOr(a.status, kStatusTimeout);
     }
     return;
@@ -108,6 +93,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32) k_oneread_tma(TmaArgs a) {
     if (!mbar_wait(smem_addr(&full[s]), uint32_t((j / S) & 1), a.wait_ns)) timed_out = true;
     const uint32_t slot = smem_addr(slots + size_t(s) * a.slot_bytes);
 
+    // copy this thread's part of the row into registers and hand the slot back at once
     float v[VPT][E];
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
@@ -119,6 +105,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32) k_oneread_tma(TmaArgs a) {
         for (int e = 0; e < E; ++e) v[k][e] = -INFINITY;
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&freed[s]));
+
     float mt = -INFINITY;
 #pragma unroll
     for (int k = 0; k < VPT; ++k)
@@ -136,20 +125,18 @@ __global__ void __launch_bounds__((NCW + 1) * 32) k_oneread_tma(TmaArgs a) {
     const State st = group_merge(State{mt, dt}, wstate + (j & 1) * NCW, NCW, warp, lane,
                                  [] { named_barrier_sync(1, NCT); });
     const float scale = __fmul_rn(exp_diff(mt, safe_max(st.m)), safe_inv(st.d));
+    const int64_t row = blockIdx.x + j * gridDim.x;
+    unsigned char* yr = a.y + row * a.row_bytes;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int u = tid + k * NCT;
       if (u < nunits) {
 #pragma unroll
         for (int e = 0; e < E; ++e) v[k][e] = __fmul_rn(v[k][e], scale);
-        sts16(slot + uint32_t(u) * 16u, D::pack(v[k]));
+        st_stream16(yr + int64_t(u) * 16, D::pack(v[k]));
       }
     }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&done[s]));
     if (tid == 0) {
-      const int64_t row = blockIdx.x + j * gridDim.x;
       if (a.m_out) a.m_out[row] = st.m;
       if (a.d_out) a.d_out[row] = st.d;
       if (a.lse_out) a.lse_out[row] = lse_of(st);

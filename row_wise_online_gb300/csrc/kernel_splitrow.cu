@@ -6,23 +6,25 @@
 //
 // Layout: the grid is G persistent CTAs (one per SM), grouped in thread-block clusters of CS.
 // Every row is cut into G contiguous segments of 16-byte units, balanced to one unit; CTA c owns
-// segment c of every row.  A segment (up to ~200 KB) is staged in shared memory in pieces of
-// 16 KB by bulk copies (cp.async.bulk + mbarrier) issued by one producer lane, so x is read from
-// HBM once and y written once (bulk stores), as in the one-read kernel.
+// segment c of every row.  One producer lane streams the segments of consecutive rows, in 15 KB
+// pieces, through a ring of shared-memory slots with bulk copies (cp.async.bulk + mbarrier).
+// Consumers copy each piece into registers as soon as it lands and free its slot, so the ring
+// only ever holds loads in flight and HBM reads keep streaming while a row waits for its
+// exchange.  x is read once; y is written once, straight from registers.
 //
 // Per row r, in every CTA:
-//   1. consumers fold the segment's pieces into per-thread (m, d) states (online recurrence);
+//   1. consumers gather the segment (up to 8 pieces, 2 vectors per thread per piece)
+//      into registers, take the thread max, then one exponential per element: the thread's
+//      (m, d) state;
 //   2. warp butterfly merge, then cross-warp merge through shared memory -> CTA state;
 //   3. cluster merge over distributed shared memory: each CTA writes its state into rank 0's
 //      shared memory (st.shared::cluster) and arrives on rank 0's mbarrier (release.cluster);
 //      rank 0 merges the CS states in rank order and publishes the cluster state to global
 //      memory, then bumps a release counter;
-//   4. while the exchange is in flight, the consumers fold the first pieces of row r + 1
-//      (already landing in free slots), so the HBM stream does not stop;
-//   5. one lane waits (acquire, bounded by %globaltimer) until every cluster has published row
-//      r, warp 0 merges all cluster states in a fixed order -- identical in every CTA, so every
-//      CTA normalises with bitwise the same (m, d) -- and the row is normalised in shared memory
-//      and bulk-stored.
+//   4. one lane waits (acquire, bounded by %globaltimer) until every cluster has published row
+//      r; warp 0 merges all cluster states in a fixed order -- identical in every CTA, so every
+//      CTA normalises with bitwise the same (m, d);
+//   5. y = e^(x - m) / d from registers, 16-byte stores.
 // All clusters must be resident at once; the host launches at most the number of clusters the
 // occupancy query reports.  Every wait is bounded; a wait that runs out records
 // SOFTMAX_ERR_TIMEOUT in the status word, skips the remaining exchange waits, and the kernel
@@ -35,10 +37,19 @@
 namespace rwo {
 namespace {
 
-constexpr int kPieceBytes = 16384;
-constexpr int kPieceUnits = kPieceBytes / 16;
-constexpr int kSplitNcw = 16;  // consumer warps
+// 15 consumer warps + 1 producer warp = 16 warps, 4 per SM sub-partition, so each thread may
+// use up to 128 registers (17 warps would cap it at 96 and spill the row).
+constexpr int kSplitNcw = 15;                                    // consumer warps
+constexpr int kSplitNct = kSplitNcw * 32;                        // consumer threads
+constexpr int kUnitsPerPiecePerThread = 2;
+constexpr int kPieceUnits = kSplitNct * kUnitsPerPiecePerThread;  // 960 units
+constexpr int kPieceBytes = kPieceUnits * 16;                    // 15 KB
+// Register capacity per CTA and row: 8 pieces (120 KB) for fp32; 6 for bf16, whose unpacking
+// needs more temporaries (7 or 8 would spill).
+template <class D>
+__host__ __device__ constexpr int max_pieces() { return D::kBytes == 4 ? 8 : 6; }
 constexpr int kMaxCluster = 8;
+static_assert(kPieceUnits % kSplitNct == 0, "a piece splits evenly over the consumer threads");
 
 struct SplitArgs {
   const unsigned char* x;
@@ -47,7 +58,7 @@ struct SplitArgs {
   float* d_out;
   float* lse_out;
   int64_t M;
-  int64_t units;      // 16-byte units per row
+  int64_t units;  // 16-byte units per row
   int64_t row_bytes;
   int slots;          // ring slots of kPieceBytes
   unsigned* counter;  // cluster publications so far (zeroed before launch)
@@ -58,72 +69,9 @@ struct SplitArgs {
   int fault;  // test hook: cluster 0 never publishes
 };
 
-struct SplitSmem {
-  uint64_t* full;
-  uint64_t* done;
-  uint64_t* cbar;    // [2] cluster-merge barriers (used in rank 0)
-  State* cstate;     // [2][kMaxCluster] (written remotely into rank 0)
-  State* wstate;     // [2][kSplitNcw]
-  State* rowst;      // [2]
-  int* abort_flag;   // [1]
-};
-
 size_t split_tail_bytes(int slots) {
   return size_t(slots) * 2 * sizeof(uint64_t) + 2 * sizeof(uint64_t) + 2 * kMaxCluster * sizeof(State) +
          2 * kSplitNcw * sizeof(State) + 2 * sizeof(State) + 16;
-}
-
-__device__ __forceinline__ uint32_t piece_units(int64_t seg_units, int k) {
-  const int64_t rest = seg_units - int64_t(k) * kPieceUnits;
-  return uint32_t(rest < kPieceUnits ? rest : kPieceUnits);
-}
-
-// Online fold of `pu` units of a piece in shared memory into this thread's state.
-template <class D>
-__device__ __forceinline__ State fold_piece(State st, uint32_t slot, uint32_t pu, int tid) {
-  constexpr int E = D::kVec;
-  constexpr int NCT = kSplitNcw * 32;
-  for (uint32_t u = tid; u < pu; u += 2 * NCT) {
-    float v[2][E];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const uint32_t uu = u + k * NCT;
-      if (uu < pu) {
-        D::unpack(lds16(slot + uu * 16u), v[k]);
-      } else {
-#pragma unroll
-        for (int e = 0; e < E; ++e) v[k][e] = -INFINITY;
-      }
-    }
-    float mu = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < 2; ++k)
-#pragma unroll
-      for (int e = 0; e < E; ++e) mu = fmaxf(mu, v[k][e]);
-    const float m_new = fmaxf(st.m, mu);
-    const float ms = safe_max(m_new);
-    float acc = 0.f;
-#pragma unroll
-    for (int k = 0; k < 2; ++k)
-#pragma unroll
-      for (int e = 0; e < E; ++e) acc += exp_diff(v[k][e], ms);
-    st.d = __fadd_rn(__fmul_rn(st.d, exp_diff(st.m, ms)), acc);
-    st.m = m_new;
-  }
-  return st;
-}
-
-template <class D>
-__device__ __forceinline__ void normalise_piece(uint32_t slot, uint32_t pu, int tid, float ms, float inv) {
-  constexpr int E = D::kVec;
-  constexpr int NCT = kSplitNcw * 32;
-  for (uint32_t u = tid; u < pu; u += NCT) {
-    float v[E];
-    D::unpack(lds16(slot + u * 16u), v);
-#pragma unroll
-    for (int e = 0; e < E; ++e) v[e] = __fmul_rn(exp_diff(v[e], ms), inv);
-    sts16(slot + u * 16u, D::pack(v));
-  }
 }
 
 __device__ __forceinline__ float ld_relaxed_f32(const float* p) {
@@ -139,26 +87,25 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
 }
 
 __device__ __forceinline__ void cluster_sync_all() {
-  // Non-aligned form: not every lane of every warp reaches it at the same instruction.
+  // Non-aligned form: the producer warp's lanes reach it from different paths.
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
 template <class D>
 __global__ void __launch_bounds__((kSplitNcw + 1) * 32, 1) k_splitrow(SplitArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
-  constexpr int NCT = kSplitNcw * 32;
+  constexpr int E = D::kVec;
+  constexpr int U = kUnitsPerPiecePerThread;
+  constexpr int KMAX = max_pieces<D>();
   const int NS = a.slots;
-  SplitSmem sm;
-  {
-    unsigned char* p = smem + size_t(NS) * kPieceBytes;
-    sm.full = reinterpret_cast<uint64_t*>(p);
-    sm.done = sm.full + NS;
-    sm.cbar = sm.done + NS;
-    sm.cstate = reinterpret_cast<State*>(sm.cbar + 2);
-    sm.wstate = sm.cstate + 2 * kMaxCluster;
-    sm.rowst = sm.wstate + 2 * kSplitNcw;
-    sm.abort_flag = reinterpret_cast<int*>(sm.rowst + 2);
-  }
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(NS) * kPieceBytes);
+  uint64_t* freed = full + NS;
+  uint64_t* cbar = freed + NS;                                // [2]
+  State* cstate = reinterpret_cast<State*>(cbar + 2);        // [2][kMaxCluster], written into rank 0
+  State* wstate = cstate + 2 * kMaxCluster;                  // [2][kSplitNcw]
+  State* rowst = wstate + 2 * kSplitNcw;                     // [2]
+  int* abort_flag = reinterpret_cast<int*>(rowst + 2);
+
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t crank = cluster_ctarank();
   const uint32_t csize = cluster_nctarank();
@@ -170,83 +117,100 @@ __global__ void __launch_bounds__((kSplitNcw + 1) * 32, 1) k_splitrow(SplitArgs 
   const int64_t base = a.units / G, rem = a.units % G;
   const int64_t seg_units = base + (c < rem ? 1 : 0);
   const int64_t seg_start = c * base + (c < rem ? c : rem);
-  const int K = int((seg_units + kPieceUnits - 1) / kPieceUnits);
-  const int F = K < NS - K ? K : NS - K;  // pieces of row r + 1 folded during row r's exchange
+  const int K = int((seg_units + kPieceUnits - 1) / kPieceUnits);  // <= KMAX (the host checks)
 
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
-      mbar_init(smem_addr(&sm.full[s]), 1);
-      mbar_init(smem_addr(&sm.done[s]), kSplitNcw);
+      mbar_init(smem_addr(&full[s]), 1);
+      mbar_init(smem_addr(&freed[s]), kSplitNcw);
     }
-    mbar_init(smem_addr(&sm.cbar[0]), csize);
-    mbar_init(smem_addr(&sm.cbar[1]), csize);
-    *sm.abort_flag = 0;
+    mbar_init(smem_addr(&cbar[0]), csize);
+    mbar_init(smem_addr(&cbar[1]), csize);
+    *abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
   cluster_sync_all();  // every CTA's barriers exist before any remote arrive
 
   if (warp == kSplitNcw) {
-    // ---------------- producer ----------------
+    // ---------------- producer: stream pieces of consecutive rows through the ring ----------------
     if (lane == 0 && K > 0) {
       const uint64_t pol = policy_evict_first();
       const int64_t total = a.M * K;
       bool timed_out = false;
-      int64_t stored = 0;
-      auto piece_offset = [&](int64_t p) {
-        const int64_t r = p / K;
-        const int k = int(p % K);
-        return r * a.row_bytes + (seg_start + int64_t(k) * kPieceUnits) * 16;
-      };
-      auto store_next = [&]() {
-        const int s = int(stored % NS);
-        if (!mbar_wait(smem_addr(&sm.done[s]), uint32_t((stored / NS) & 1), a.local_wait_ns)) timed_out = true;
-        const uint32_t bytes = piece_units(seg_units, int(stored % K)) * 16u;
-        bulk_s2g(a.y + piece_offset(stored), smem_addr(smem + size_t(s) * kPieceBytes), bytes, pol);
-        bulk_commit();
-        ++stored;
-      };
       for (int64_t p = 0; p < total; ++p) {
         const int s = int(p % NS);
-        if (p >= NS) {
-          while (stored <= p - NS) store_next();
-          bulk_wait_read_all();
-        }
-        const uint32_t bytes = piece_units(seg_units, int(p % K)) * 16u;
-        const uint32_t bar = smem_addr(&sm.full[s]);
+        if (p >= NS &&
+            !mbar_wait(smem_addr(&freed[s]), uint32_t(((p / NS) - 1) & 1), a.local_wait_ns))
+          timed_out = true;
+        const int64_t r = p / K;
+        const int k = int(p % K);
+        const int64_t rest = seg_units - int64_t(k) * kPieceUnits;
+        const uint32_t bytes = uint32_t(rest < kPieceUnits ? rest : kPieceUnits) * 16u;
+        const uint32_t bar = smem_addr(&full[s]);
         mbar_arrive_expect_tx(bar, bytes);
-        bulk_g2s(smem_addr(smem + size_t(s) * kPieceBytes), a.x + piece_offset(p), bytes, bar, pol);
+        bulk_g2s(smem_addr(smem + size_t(s) * kPieceBytes),
+                 a.x + r * a.row_bytes + (seg_start + int64_t(k) * kPieceUnits) * 16, bytes, bar, pol);
       }
-      while (stored < total) store_next();
+      // every load has landed before the CTA may exit (the consumers normally saw them all)
       for (int64_t p = total > NS ? total - NS : 0; p < total; ++p)
-        if (!mbar_wait(smem_addr(&sm.full[p % NS]), uint32_t((p / NS) & 1), a.local_wait_ns)) timed_out = true;
-      bulk_wait_all();
+        if (!mbar_wait(smem_addr(&full[p % NS]), uint32_t((p / NS) & 1), a.local_wait_ns)) timed_out = true;
       if (timed_out) atomicOr(a.status, kStatusTimeout);
     }
   } else {
     // ---------------- consumers ----------------
     bool timed_out = false;
-    State nxt = empty_state();
-    int pre = 0;
     for (int64_t r = 0; r < a.M; ++r) {
       const int b = int(r & 1);
-      State st = nxt;
-      for (int k = pre; k < K; ++k) {
-        const int64_t p = r * K + k;
-        const int s = int(p % NS);
-        if (!mbar_wait(smem_addr(&sm.full[s]), uint32_t((p / NS) & 1), a.local_wait_ns)) timed_out = true;
-        st = fold_piece<D>(st, smem_addr(smem + size_t(s) * kPieceBytes), piece_units(seg_units, k), tid);
+      // 1. gather the segment into registers, freeing each slot at once
+      uint4 v[KMAX][U];
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) {
+#pragma unroll
+        for (int i = 0; i < U; ++i) v[k][i] = make_uint4(D::kNegInfWord, D::kNegInfWord, D::kNegInfWord, D::kNegInfWord);
+        if (k < K) {
+          const int64_t p = r * K + k;
+          const int s = int(p % NS);
+          if (!mbar_wait(smem_addr(&full[s]), uint32_t((p / NS) & 1), a.local_wait_ns)) timed_out = true;
+          const uint32_t slot = smem_addr(smem + size_t(s) * kPieceBytes);
+          const int64_t rest = seg_units - int64_t(k) * kPieceUnits;
+#pragma unroll
+          for (int i = 0; i < U; ++i) {
+            const int u = tid + i * kSplitNct;
+            if (u < rest) v[k][i] = lds16(slot + uint32_t(u) * 16u);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&freed[s]));
+        }
       }
-      st = group_merge(st, sm.wstate + b * kSplitNcw, kSplitNcw, warp, lane, [] { named_barrier_sync(1, NCT); });
-
-      // cluster merge over DSMEM; rank 0 publishes the cluster state
+      // thread state: max first, then one exponential per element
+      float mt = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k)
+#pragma unroll
+        for (int i = 0; i < U; ++i) mt = fmaxf(mt, D::vmax(v[k][i]));
+      const float mts = safe_max(mt);
+      float dt = 0.f;
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k)
+#pragma unroll
+        for (int i = 0; i < U; ++i) {
+          float f[E];
+          D::unpack(v[k][i], f);
+#pragma unroll
+          for (int e = 0; e < E; ++e) dt += exp_diff(f[e], mts);
+        }
+      // 2. CTA merge
+      const State st = group_merge(State{mt, dt}, wstate + b * kSplitNcw, kSplitNcw, warp, lane,
+                                   [] { named_barrier_sync(1, kSplitNct); });
+      // 3. cluster merge over DSMEM; rank 0 publishes the cluster state
       if (tid == 0) {
-        st_cluster_f32x2(map_to_rank(smem_addr(&sm.cstate[b * kMaxCluster + crank]), 0), st.m, st.d);
-        mbar_arrive_remote(map_to_rank(smem_addr(&sm.cbar[b]), 0));
+        st_cluster_f32x2(map_to_rank(smem_addr(&cstate[b * kMaxCluster + crank]), 0), st.m, st.d);
+        mbar_arrive_remote(map_to_rank(smem_addr(&cbar[b]), 0));
         if (crank == 0) {
-          if (!mbar_wait_cluster(smem_addr(&sm.cbar[b]), uint32_t((r >> 1) & 1), a.local_wait_ns)) timed_out = true;
+          if (!mbar_wait_cluster(smem_addr(&cbar[b]), uint32_t((r >> 1) & 1), a.local_wait_ns)) timed_out = true;
           State cs = empty_state();
-          for (uint32_t i = 0; i < csize; ++i) cs = merge(cs, sm.cstate[b * kMaxCluster + i]);
+          for (uint32_t i = 0; i < csize; ++i) cs = merge(cs, cstate[b * kMaxCluster + i]);
           if (!(a.fault && cid == 0)) {
             float* g = a.gstate + (r * ncl + cid) * 2;
             g[0] = cs.m;
@@ -255,33 +219,19 @@ __global__ void __launch_bounds__((kSplitNcw + 1) * 32, 1) k_splitrow(SplitArgs 
           }
         }
       }
-
-      // fold the first pieces of the next row while the exchange is in flight
-      nxt = empty_state();
-      pre = 0;
-      if (r + 1 < a.M) {
-        pre = F;
-        for (int k = 0; k < F; ++k) {
-          const int64_t p = (r + 1) * K + k;
-          const int s = int(p % NS);
-          if (!mbar_wait(smem_addr(&sm.full[s]), uint32_t((p / NS) & 1), a.local_wait_ns)) timed_out = true;
-          nxt = fold_piece<D>(nxt, smem_addr(smem + size_t(s) * kPieceBytes), piece_units(seg_units, k), tid);
-        }
-      }
-
-      // wait for every cluster's state of row r, then merge them in cluster order
+      // 4. wait for every cluster's state of row r, then merge them in cluster order
       if (warp == 0) {
-        if (lane == 0 && *sm.abort_flag == 0) {
+        if (lane == 0 && *abort_flag == 0) {
           const unsigned target = unsigned((r + 1) * ncl);
           if (ld_acquire(a.counter) < target) {
             const uint64_t t0 = global_timer_ns();
             while (ld_acquire(a.counter) < target) {
               if (global_timer_ns() - t0 > a.exchange_wait_ns) {
-                *sm.abort_flag = 1;
+                *abort_flag = 1;
                 timed_out = true;
                 break;
               }
-              __nanosleep(64);
+              __nanosleep(32);
             }
           }
         }
@@ -292,19 +242,30 @@ __global__ void __launch_bounds__((kSplitNcw + 1) * 32, 1) k_splitrow(SplitArgs 
           g = merge(g, State{ld_relaxed_f32(gp), ld_relaxed_f32(gp + 1)});
         }
         g = warp_merge(g);
-        if (lane == 0) sm.rowst[b] = g;
+        if (lane == 0) rowst[b] = g;
       }
-      named_barrier_sync(1, NCT);
-      const State row = sm.rowst[b];
+      named_barrier_sync(1, kSplitNct);
+      const State row = rowst[b];
+      // 5. normalise from registers and store
       const float ms = safe_max(row.m);
       const float inv = safe_inv(row.d);
-      for (int k = 0; k < K; ++k) {
-        const int64_t p = r * K + k;
-        const int s = int(p % NS);
-        normalise_piece<D>(smem_addr(smem + size_t(s) * kPieceBytes), piece_units(seg_units, k), tid, ms, inv);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&sm.done[s]));
+      unsigned char* yseg = a.y + r * a.row_bytes + seg_start * 16;
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) {
+        if (k < K) {
+          const int64_t rest = seg_units - int64_t(k) * kPieceUnits;
+#pragma unroll
+          for (int i = 0; i < U; ++i) {
+            const int u = tid + i * kSplitNct;
+            if (u < rest) {
+              float f[E];
+              D::unpack(v[k][i], f);
+#pragma unroll
+              for (int e = 0; e < E; ++e) f[e] = __fmul_rn(exp_diff(f[e], ms), inv);
+              st_stream16(yseg + (int64_t(k) * kPieceUnits + u) * 16, D::pack(f));
+            }
+          }
+        }
       }
       if (c == 0 && tid == 0) {
         if (a.m_out) a.m_out[r] = row.m;
@@ -393,8 +354,7 @@ bool splitrow_fits(const RowProblem& p, const DeviceInfo& dev) {
   const int64_t units = row_bytes / 16;
   if (units < G * 64) return false;  // rows this short belong to the one-read kernels
   const int64_t seg = (units + G - 1) / G;
-  const int64_t K = (seg + kPieceUnits - 1) / kPieceUnits;
-  return K + 1 <= plan.slots;
+  return (seg + kPieceUnits - 1) / kPieceUnits <= (p.dtype == 0 ? max_pieces<F32>() : max_pieces<BF16>());
 }
 
 cudaError_t launch_splitrow(const RowProblem& p, const DeviceInfo& dev) {

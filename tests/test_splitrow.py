@@ -27,7 +27,7 @@ def _built():
 
 @pytest.mark.parametrize("dtype,M,N", [
     (synth.F32, 3, 1 << 21), (synth.F32, 5, 1_500_000), (synth.BF16, 2, 1 << 22), (synth.BF16, 7, 3_000_008),
-    (synth.F32, 1, 6_000_000),
+    (synth.F32, 1, 4_000_000),
 ])
 def test_splitrow_against_oracle(dtype, M, N):
     w = synth.custom("split", dtype, M, N, seed=N % 1000, dist=synth.UNIFORM, p0=-20.0, p1=20.0, late_max=20.0)
@@ -98,3 +98,18 @@ def test_exchange_wait_runs_out_and_reports_timeout():
     assert rwo.get_status() == rwo.OK
     y_ref, *_ = oracle.softmax_rows(x_host)
     check_y(to_host(y), y_ref, synth.F32, "after timeout")
+
+
+def test_rows_beyond_split_capacity_take_twopass():
+    """A single 32 Mi-element fp32 row (128 MiB) exceeds the split kernel's register capacity;
+    AUTO runs it with the two-pass kernel and a forced split reports UNSUPPORTED."""
+    N = 1 << 25
+    x = torch.randn((1, N), device="cuda") * 3
+    with pytest.raises(rwo.SoftmaxError) as ei:
+        rwo.softmax_rows_ex(x, variant=rwo.VARIANT_SPLITROW)
+    assert ei.value.status == rwo.ERR_UNSUPPORTED
+    m = torch.empty(1, device="cuda")
+    y = rwo.softmax_rows_ex(x, m_out=m)
+    assert rwo.get_status() == rwo.OK and rwo.last_variant() == rwo.VARIANT_TWOPASS
+    assert float(m) == float(x.max())
+    assert abs(float(torch.sum(y, dtype=torch.float64)) - 1.0) <= 1e-5
