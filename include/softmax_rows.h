@@ -76,9 +76,10 @@ enum softmax_variant {
   SOFTMAX_VARIANT_TWOPASS = 3,
   /* Split row: one row is spread over every CTA of the grid; CTAs of a thread-block cluster merge
      (m, d) over distributed shared memory, clusters exchange 8-byte states through global memory
-     (for few, very long rows: each CTA's segment of a row must fit in its shared-memory ring,
-     about 200 KiB, so rows up to about 200 KiB x the number of SMs; 16-byte aligned).  It
-     needs every cluster resident at once, so it must not share the GPU with other kernels. */
+     (for few, very long rows, 16-byte aligned).  Each CTA holds its segment of the row waiting
+     for its exchange in registers (up to 112 KiB fp32 / 84 KiB bf16 per SM, so rows up to about
+     that times the SM count) while it folds the next row from shared memory.  It needs every
+     cluster resident at once, so it must not share the GPU with other kernels. */
   SOFTMAX_VARIANT_SPLITROW = 4
 };
 

@@ -82,8 +82,19 @@ __device__ __forceinline__ State group_merge(State s, State* slots, int nwarps, 
   if (nwarps == 1) return s;
   if (lane == 0) slots[warp] = s;
   sync();
-  State t = lane < nwarps ? slots[lane] : empty_state();
-  return warp_merge(t);
+  // Lanes hold the warp states replicated modulo p (the power of two >= nwarps), so a butterfly
+  // over offsets p/2 .. 1 leaves the full merge in every lane: log2(p) rounds instead of 5.
+  int p = 1;
+  while (p < nwarps) p <<= 1;
+  const int i = lane & (p - 1);
+  State t = i < nwarps ? slots[i] : empty_state();
+  for (int o = p >> 1; o > 0; o >>= 1) {
+    State u;
+    u.m = __shfl_xor_sync(0xffffffffu, t.m, o);
+    u.d = __shfl_xor_sync(0xffffffffu, t.d, o);
+    t = merge(t, u);
+  }
+  return t;
 }
 
 // 1/d, with 0 for an empty row (d = 0) so that y = 0 there instead of 0 * inf.
