@@ -136,6 +136,29 @@ int softmax_rows_host(const void* x_host, void* y_host, int64_t M, int64_t N, in
                       void* stream);
 
 /*
+ * softmax_rows_splitrow_noalloc -- the split-row softmax (SOFTMAX_VARIANT_SPLITROW) for callers
+ * that cannot allocate device memory.  The pages describe no such call; it exists for callers
+ * such as code held to a device-memory budget fixed in advance, code whose framework allocator
+ * owns the device memory, or host threads that must not make a call that may block or
+ * synchronise the device.  It allocates nothing (no cudaMalloc, cudaMallocAsync, cudaFree or
+ * library allocator): the exchange scratch lives in a fixed 320 KiB device array inside the
+ * library (40960 slots of 8 bytes), present on every device that loads the library until the
+ * process exits.
+ *  - Arguments as softmax_rows_ex (device pointers; x, y 16-byte aligned with N * sizeof(dtype)
+ *    a multiple of 16, else SOFTMAX_ERR_MISALIGNED).
+ *  - Capacity: M x (number of clusters) <= 40960 slots; with the 19 clusters of 8 CTAs used on a
+ *    152-SM GB300 that is M <= 2155 rows (at least 512 rows with up to 80 clusters).  Larger M,
+ *    or rows the split kernel cannot take, return SOFTMAX_ERR_UNSUPPORTED without launching.
+ *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress, with
+ *    that device current) and keeps it; make that first call before any stream capture.
+ *  - Every call shares the one array and resets the part it uses (a cudaMemsetAsync on `stream`
+ *    before the kernel); calls whose executions overlap on the GPU -- on different streams, or
+ *    from different threads -- race on it and must be serialised by the caller.
+ */
+int softmax_rows_splitrow_noalloc(const void* x, void* y, float* m_out, float* d_out, float* lse_out,
+                                  int64_t M, int64_t N, int dtype, void* stream);
+
+/*
  * softmax_get_status -- synchronises `stream`, then returns and clears the
  * status word of the current device: SOFTMAX_OK, or the error a kernel
  * recorded since the last call (SOFTMAX_ERR_TIMEOUT for a bounded wait that

@@ -20,6 +20,7 @@ __all__ = [
     "VARIANT_SPLITROW", "VARIANT_NAMES", "SoftmaxError", "softmax_rows", "softmax_rows_ex",
     "softmax_row_state", "merge_states", "softmax_rows_host", "get_status", "status_string",
     "last_variant", "debug_set_fault", "debug_set_wait_limit_ns", "capi", "library_path",
+    "softmax_rows_splitrow_noalloc",
 ]
 
 F32, BF16 = 0, 1
@@ -37,7 +38,7 @@ _lib = None
 EXPORTED = (
     "softmax_rows", "softmax_rows_ex", "softmax_row_state", "merge_states", "softmax_rows_host",
     "softmax_get_status", "softmax_status_string", "softmax_last_cuda_error", "softmax_last_variant",
-    "softmax_debug_set_fault", "softmax_debug_set_wait_limit_ns",
+    "softmax_debug_set_fault", "softmax_debug_set_wait_limit_ns", "softmax_rows_splitrow_noalloc",
 )
 
 
@@ -77,10 +78,11 @@ def capi() -> ctypes.CDLL:
         lib.softmax_last_variant.argtypes = []
         lib.softmax_debug_set_fault.argtypes = [ci]
         lib.softmax_debug_set_wait_limit_ns.argtypes = [i64]
+        lib.softmax_rows_splitrow_noalloc.argtypes = [vp, vp, fp, fp, fp, i64, i64, ci, vp]
         lib.softmax_debug_set_wait_limit_ns.restype = i64
         for name in ("softmax_rows", "softmax_rows_ex", "softmax_row_state", "merge_states",
                      "softmax_rows_host", "softmax_get_status", "softmax_last_variant",
-                     "softmax_debug_set_fault"):
+                     "softmax_debug_set_fault", "softmax_rows_splitrow_noalloc"):
             getattr(lib, name).restype = ci
         _lib = lib
     return _lib
@@ -215,6 +217,27 @@ def softmax_rows_host(x_host, y_host, stream=None):
     _check(capi().softmax_rows_host(_ptr(x_host), _ptr(y_host), M, N, _dtype_code(x_host), _stream(stream)),
            "softmax_rows_host")
     return y_host
+
+
+def softmax_rows_splitrow_noalloc(x, y=None, m_out=None, d_out=None, lse_out=None, stream=None):
+    """Split-row softmax that allocates no device memory inside the library, for callers that
+    cannot let a library allocate (see the C header: M x clusters <= 40960 slots; calls that
+    overlap on the GPU race on the shared scratch)."""
+    import torch
+
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor")
+    M, N = _rows(x)
+    if y is None:
+        y = torch.empty_like(x)
+    if y.shape != x.shape or y.dtype != x.dtype or not y.is_cuda or not y.is_contiguous():
+        raise ValueError("y must be a contiguous CUDA tensor with x's shape and dtype")
+    st = capi().softmax_rows_splitrow_noalloc(_ptr(x), _ptr(y), _ptr(_state_out(m_out, M, "m_out")),
+                                              _ptr(_state_out(d_out, M, "d_out")),
+                                              _ptr(_state_out(lse_out, M, "lse_out")), M, N, _dtype_code(x),
+                                              _stream(stream))
+    _check(st, "softmax_rows_splitrow_noalloc")
+    return y
 
 
 def get_status(stream=None) -> int:

@@ -169,6 +169,10 @@ int run_variant(RowProblem& p, int variant, const DeviceInfo& dev) {
 
 }  // namespace
 
+int current_device(const DeviceInfo** out) { return current_device_info(out); }
+
+int cuda_failure(cudaError_t err) { return cuda_fail(err); }
+
 uint64_t local_wait_limit_ns() { return 2000ull * 1000 * 1000; }  // 2 s: never reached normally
 
 uint64_t exchange_wait_limit_ns() {

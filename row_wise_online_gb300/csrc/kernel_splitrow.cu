@@ -560,4 +560,50 @@ cudaError_t launch_splitrow(const RowProblem& p, const DeviceInfo& dev) {
   return err != cudaSuccess ? err : ferr;
 }
 
+cudaError_t launch_splitrow_scratch(const RowProblem& p, const DeviceInfo& dev, unsigned long long* pub,
+                                    size_t pub_slots, bool* too_big) {
+  *too_big = false;
+  const SplitPlan plan = plan_for(p.dtype, dev);
+  if (!plan.ok) return cudaErrorInvalidConfiguration;
+  const size_t need = size_t(p.M) * plan.clusters;
+  if (need > pub_slots) {
+    *too_big = true;
+    return cudaErrorInvalidValue;
+  }
+  SplitKernel fn = split_kernel(p.dtype);
+  cudaError_t err =
+      cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(plan.smem));
+  if (err != cudaSuccess) return err;
+  // The slots must read as "not published" (all ones) when the kernel starts.
+  if ((err = cudaMemsetAsync(pub, 0xFF, need * sizeof(unsigned long long), p.stream)) != cudaSuccess) return err;
+  SplitArgs a;
+  a.x = static_cast<const unsigned char*>(p.x);
+  a.y = static_cast<unsigned char*>(p.y);
+  a.m_out = p.m_out;
+  a.d_out = p.d_out;
+  a.lse_out = p.lse_out;
+  a.M = p.M;
+  a.row_bytes = p.N * elem_bytes(p.dtype);
+  a.units = a.row_bytes / 16;
+  a.slots = plan.slots;
+  a.pub = pub;
+  a.status = dev.status;
+  a.local_wait_ns = local_wait_limit_ns();
+  a.exchange_wait_ns = exchange_wait_limit_ns();
+  a.fault = debug_fault();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = plan.cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(plan.cluster * plan.clusters);
+  cfg.blockDim = dim3(kSplitThreads);
+  cfg.dynamicSmemBytes = plan.smem;
+  cfg.stream = p.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, a);
+}
+
 }  // namespace rwo

@@ -54,6 +54,17 @@ cudaError_t launch_twopass(const RowProblem& p, bool vec, const DeviceInfo& dev)
 bool splitrow_fits(const RowProblem& p, const DeviceInfo& dev);
 cudaError_t launch_splitrow(const RowProblem& p, const DeviceInfo& dev);
 
+// Split row with caller-provided scratch: `pub` holds `pub_slots` 64-bit publication slots
+// (device memory).  Nothing is allocated.  Returns cudaErrorInvalidValue when the problem
+// needs more slots than given (*too_big is then set).
+cudaError_t launch_splitrow_scratch(const RowProblem& p, const DeviceInfo& dev, unsigned long long* pub,
+                                    size_t pub_slots, bool* too_big);
+
+// The current device's properties (softmax_status code), for entry points outside api.cu.
+int current_device(const DeviceInfo** out);
+// Records err as the thread's last CUDA error and returns SOFTMAX_ERR_CUDA.
+int cuda_failure(cudaError_t err);
+
 cudaError_t launch_merge_states(const float* m_a, const float* d_a, const float* m_b,
                                 const float* d_b, float* m_out, float* d_out, float* lse_out,
                                 int64_t M, cudaStream_t stream, const DeviceInfo& dev);
