@@ -299,6 +299,8 @@ def bench_ours(args) -> dict | None:
     peak, peak_kind = measured_hbm_peak()
     kernel = {rwo.VARIANT_ONEREAD_REG: "k_oneread_reg", rwo.VARIANT_ONEREAD_SMEM: "k_oneread_tma",
               rwo.VARIANT_TWOPASS: "k_twopass", rwo.VARIANT_SPLITROW: "k_splitrow"}[used]
+    if used == rwo.VARIANT_ONEREAD_SMEM and w.N * w.elem_bytes <= 16384:
+        kernel = "k_oneread_warp"  # rows up to 16 KiB: one warp per row
     achieved = bytes_step / (per_step_ms * 1e-3) / 1e9
     traffic = profiled_traffic(kernel, w.name)
     result = {

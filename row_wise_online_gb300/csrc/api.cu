@@ -127,7 +127,13 @@ int run_variant(RowProblem& p, int variant, const DeviceInfo& dev) {
   const int64_t row_bytes = p.N * elem_bytes(p.dtype);
   if (variant == SOFTMAX_VARIANT_AUTO) {
     if (aligned) {
-      if (row_bytes <= 16384 && oneread_reg_fits(p, true))
+      // Measured on GB300: warp-per-row bulk-copy kernel for many rows of 2-8 KiB, register
+      // kernel for shorter rows, for few rows and for 8-16 KiB rows, CTA bulk-copy kernel for
+      // 16-64 KiB rows.
+      if (row_bytes > 2048 && row_bytes <= 8192 && p.M >= 4 * int64_t(dev.sm_count) &&
+          oneread_warp_fits(p, dev))
+        variant = SOFTMAX_VARIANT_ONEREAD_SMEM;
+      else if (row_bytes <= 16384 && oneread_reg_fits(p, true))
         variant = SOFTMAX_VARIANT_ONEREAD_REG;
       else if (oneread_tma_fits(p, dev))
         variant = SOFTMAX_VARIANT_ONEREAD_SMEM;
@@ -148,8 +154,12 @@ int run_variant(RowProblem& p, int variant, const DeviceInfo& dev) {
       break;
     case SOFTMAX_VARIANT_ONEREAD_SMEM:
       if (!aligned) return SOFTMAX_ERR_MISALIGNED;
-      if (!oneread_tma_fits(p, dev)) return SOFTMAX_ERR_UNSUPPORTED;
-      err = launch_oneread_tma(p, dev);
+      if (oneread_warp_fits(p, dev))  // rows up to 16 KiB: one warp per row
+        err = launch_oneread_warp(p, dev);
+      else if (oneread_tma_fits(p, dev))
+        err = launch_oneread_tma(p, dev);
+      else
+        return SOFTMAX_ERR_UNSUPPORTED;
       break;
     case SOFTMAX_VARIANT_TWOPASS:
       err = launch_twopass(p, aligned, dev);

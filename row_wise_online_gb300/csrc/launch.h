@@ -46,6 +46,9 @@ int debug_fault();                  // test hook value (split row)
 bool oneread_reg_fits(const RowProblem& p, bool vec);
 cudaError_t launch_oneread_reg(const RowProblem& p, bool vec, const DeviceInfo& dev);
 
+bool oneread_warp_fits(const RowProblem& p, const DeviceInfo& dev);
+cudaError_t launch_oneread_warp(const RowProblem& p, const DeviceInfo& dev);
+
 bool oneread_tma_fits(const RowProblem& p, const DeviceInfo& dev);
 cudaError_t launch_oneread_tma(const RowProblem& p, const DeviceInfo& dev);
 

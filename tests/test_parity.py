@@ -167,13 +167,15 @@ def test_host_buffers_pipeline():
 
 
 def test_variant_choice():
-    cases = [
-        ("fp32_64x1024", V.VARIANT_ONEREAD_REG),
-        ("fp32_4096x4096", V.VARIANT_ONEREAD_REG),
-        ("bf16_logits_16384x32768", V.VARIANT_ONEREAD_SMEM),
+    cases = [  # (workload, rows, variant AUTO must pick)
+        ("fp32_64x1024", 64, V.VARIANT_ONEREAD_REG),
+        ("fp32_4096x4096", 8, V.VARIANT_ONEREAD_REG),
+        ("bf16_logits_16384x32768", 8, V.VARIANT_ONEREAD_SMEM),
+        ("bf16_causal_4x32x4096x4096", 8, V.VARIANT_ONEREAD_REG),      # few rows: launch-bound
+        ("bf16_causal_4x32x4096x4096", 4096, V.VARIANT_ONEREAD_SMEM),  # many rows: warp per row
     ]
-    for name, want in cases:
-        w = synth.WORKLOADS[name].with_rows(8)
+    for name, rows, want in cases:
+        w = synth.WORKLOADS[name].with_rows(rows)
         x = to_device(synth.generate(w))
         rwo.softmax_rows(x)
         torch.cuda.synchronize()
