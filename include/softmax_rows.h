@@ -126,12 +126,15 @@ int merge_states(const float* m_a, const float* d_a, const float* m_b, const flo
 
 /*
  * softmax_rows_host -- softmax_rows on HOST buffers (x_host, y_host: M x N of
- * dtype, ideally pinned).  Row blocks of about 8 MiB are copied host->device,
+ * dtype).  When both buffers are page-locked (cudaHostAlloc / cudaHostRegister,
+ * e.g. torch pin_memory) and rows are at most 32 KiB, the register one-read
+ * kernel reads x and writes y in host memory directly over the host link
+ * (zero-copy).  Otherwise row blocks of about 8 MiB are copied host->device,
  * normalised in place on the GPU and copied back, with the copies and kernels
- * of consecutive blocks overlapped on three internal streams.  The streams and
+ * of consecutive blocks overlapped on three internal streams; those streams and
  * the device staging buffers (3 x one block) are created on the first call on
- * a device and kept until the process exits; concurrent calls on one device
- * are serialised.  Returns when y_host holds the result (the call
+ * a device and kept until the process exits, and concurrent calls on one
+ * device are serialised.  Returns when y_host holds the result (the call
  * synchronises).  `stream` orders the work after earlier work on that stream.
  */
 int softmax_rows_host(const void* x_host, void* y_host, int64_t M, int64_t N, int dtype,

@@ -278,6 +278,36 @@ int softmax_rows_host(const void* x_host, void* y_host, int64_t M, int64_t N, in
 
   const cudaStream_t user = static_cast<cudaStream_t>(stream);
   const int64_t row_bytes = N * elem_bytes(dtype);
+
+  // Page-locked host buffers are directly addressable by the GPU (over NVLink-C2C on a
+  // Grace-Blackwell node).  When both are, and the register kernel takes the rows, that kernel
+  // reads x and writes y in host memory itself: no staging copies, one pass over the link each
+  // way.  It uses plain loads and stores only.
+  {
+    void* dx = nullptr;
+    void* dy = nullptr;
+    if (cudaHostGetDevicePointer(&dx, const_cast<void*>(x_host), 0) == cudaSuccess &&
+        cudaHostGetDevicePointer(&dy, y_host, 0) == cudaSuccess) {
+      RowProblem p;
+      p.x = dx;
+      p.y = dy;
+      p.M = M;
+      p.N = N;
+      p.dtype = dtype;
+      p.stream = user;
+      const bool aligned = aligned16(dx) && aligned16(dy) && row_bytes % 16 == 0;
+      if (oneread_reg_fits(p, aligned)) {
+        cudaError_t err = launch_oneread_reg(p, aligned, *dev);
+        if (err == cudaSuccess) err = cudaStreamSynchronize(user);
+        if (err != cudaSuccess) return cuda_fail(err);
+        t_last_variant = SOFTMAX_VARIANT_ONEREAD_REG;
+        return SOFTMAX_OK;
+      }
+    } else {
+      cudaGetLastError();  // pageable memory: not an error, take the staged path
+    }
+  }
+
   // Blocks of about 8 MiB: large enough for full-rate copies, small enough to overlap the
   // host->device copy of one block with the kernel and device->host copy of the others.
   int64_t block_rows = (int64_t(8) << 20) / row_bytes;

@@ -156,12 +156,32 @@ def test_in_place():
     check_y(to_host(x), y_ref, w.dtype, "in place")
 
 
+def test_host_buffers_staged_pipeline():
+    """Pageable host memory, and pinned rows too long for the direct path, go through staging."""
+    w = synth.custom("host-pageable", synth.F32, 3000, 4096, seed=11, p1=3.0)
+    x_host = synth.generate(w)
+    xt = torch.from_numpy(x_host)
+    yt = torch.empty_like(xt)
+    rwo.softmax_rows_host(xt, yt)
+    y_ref, *_ = oracle.softmax_rows(x_host)
+    check_y(yt.numpy(), y_ref, w.dtype, "host pipeline, pageable")
+    w = synth.custom("host-long", synth.BF16, 700, 32768, seed=12, p1=2.0)
+    x_host = synth.generate(w)
+    xt = torch.from_numpy(x_host.view(np.int16)).pin_memory()
+    yt = torch.empty_like(xt).pin_memory()
+    rwo.softmax_rows_host(xt.view(torch.bfloat16), yt.view(torch.bfloat16))
+    assert rwo.last_variant() == rwo.VARIANT_ONEREAD_SMEM
+    y_ref, *_ = oracle.softmax_rows(x_host)
+    check_y(yt.numpy().view(np.uint16), y_ref, w.dtype, "host pipeline, long rows")
+
+
 def test_host_buffers_pipeline():
     w = synth.custom("host", synth.F32, 5000, 4096, seed=10, p1=3.0)
     x_host = synth.generate(w)
     xt = torch.from_numpy(x_host).pin_memory()
     yt = torch.empty_like(xt).pin_memory()
     rwo.softmax_rows_host(xt, yt)
+    assert rwo.last_variant() == rwo.VARIANT_ONEREAD_REG  # pinned: read and written in place
     y_ref, *_ = oracle.softmax_rows(x_host)
     check_y(yt.numpy(), y_ref, w.dtype, "host pipeline")
 
