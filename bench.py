@@ -214,12 +214,19 @@ def bench_ours(args) -> dict | None:
     xs = [host_x.to(dev) for _ in range(nbuf)]
     ys = [torch.empty_like(xs[0]) for _ in range(nbuf)]
     stream = torch.cuda.Stream(device=dev)
+    causal = args.variant == "causal"
+    if causal and not w.causal_q:
+        raise SystemExit("--variant causal needs a workload with a causal mask")
     variant = {"auto": rwo.VARIANT_AUTO, "reg": rwo.VARIANT_ONEREAD_REG, "smem": rwo.VARIANT_ONEREAD_SMEM,
-               "twopass": rwo.VARIANT_TWOPASS, "splitrow": rwo.VARIANT_SPLITROW}[args.variant]
+               "twopass": rwo.VARIANT_TWOPASS, "splitrow": rwo.VARIANT_SPLITROW,
+               "causal": rwo.VARIANT_AUTO}[args.variant]
 
     def measure(var: int, nsteps: int, warm: int, clocks: bool = False):
         def step(i):
-            rwo.softmax_rows_ex(xs[i % nbuf], ys[i % nbuf], variant=var, stream=stream)
+            if causal:  # masked keys are not read: the causal rule replaces the -inf entries
+                rwo.softmax_rows_causal(xs[i % nbuf], w.causal_q, 0, ys[i % nbuf], stream=stream)
+            else:
+                rwo.softmax_rows_ex(xs[i % nbuf], ys[i % nbuf], variant=var, stream=stream)
 
         with torch.cuda.stream(stream):
             for i in range(warm):
@@ -263,7 +270,7 @@ def bench_ours(args) -> dict | None:
 
     # Other variants on the same workload (fewer steps), for the record.
     variants = {}
-    if world == 1 and not args.quick:
+    if world == 1 and not args.quick and not causal:
         for name, var in (("oneread_reg", rwo.VARIANT_ONEREAD_REG), ("oneread_smem", rwo.VARIANT_ONEREAD_SMEM),
                           ("twopass", rwo.VARIANT_TWOPASS), ("splitrow", rwo.VARIANT_SPLITROW)):
             if var == used:
@@ -300,8 +307,14 @@ def bench_ours(args) -> dict | None:
     kernel = {rwo.VARIANT_ONEREAD_REG: "k_oneread_reg", rwo.VARIANT_ONEREAD_SMEM: "k_oneread_tma",
               rwo.VARIANT_TWOPASS: "k_twopass", rwo.VARIANT_SPLITROW: "k_splitrow"}[used]
     if used == rwo.VARIANT_ONEREAD_SMEM and w.N * w.elem_bytes <= 16384:
-        kernel = "k_oneread_warp"  # rows up to 16 KiB: one warp per row
-    achieved = bytes_step / (per_step_ms * 1e-3) / 1e9
+        kernel = "k_causal_warp" if causal else "k_oneread_warp"  # rows up to 16 KiB: one warp per row
+    alg_bytes = bytes_step
+    if causal:  # bytes the kernel needs: the live prefix of every row (whole 16-byte vectors) + all of y
+        vec = 16 // w.elem_bytes
+        r = np.arange(row0, row0 + w.M, dtype=np.int64)
+        live = np.clip(r % w.causal_q + 1, 0, w.N)
+        alg_bytes = int(((live + vec - 1) // vec).sum()) * 16 + w.M * w.N * w.elem_bytes
+    achieved = alg_bytes / (per_step_ms * 1e-3) / 1e9
     traffic = profiled_traffic(kernel, w.name)
     result = {
         "metric": METRIC,
@@ -320,7 +333,7 @@ def bench_ours(args) -> dict | None:
         "data": "synthetic",
         "config": {"workload": w.name if not args.rows else f"{w.name}[rows={w.M}]", "M": w.M, "N": w.N,
                    "rows_total": w.M * world,
-                   "variant": rwo.VARIANT_NAMES[used], "parallelism": f"rows sharded over {world} GPU(s)",
+                   "variant": rwo.VARIANT_NAMES[used] + ("+causal_skip" if causal else ""), "parallelism": f"rows sharded over {world} GPU(s)",
                    "l2": (f"{nbuf} rotating x/y buffer sets ({nbuf * set_bytes >> 20} MiB > L2)" if nbuf > 1
                           else "inputs larger than L2"),
                    "timing": "CUDA graph replays between CUDA events on the launching stream"},
@@ -331,7 +344,7 @@ def bench_ours(args) -> dict | None:
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s", "kernel": kernel,
-                     "algorithmic_bytes_per_launch": bytes_step},
+                     "algorithmic_bytes_per_launch": alg_bytes},
         "gpu_launches": args.steps,
         "e2e": e2e,
         "clocks": clk,
@@ -410,7 +423,8 @@ def main(argv=None) -> int:
     ap.add_argument("--steps", type=int, default=50000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--variant", default="auto", choices=["auto", "reg", "smem", "twopass", "splitrow"])
+    ap.add_argument("--variant", default="auto", choices=["auto", "reg", "smem", "twopass", "splitrow", "causal"],
+                    help="causal: softmax_rows_causal on a causal workload (masked keys not read)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--rows", type=int, default=0, help="use only the first ROWS rows (profiling small cases)")
     ap.add_argument("--quick", action="store_true", help="skip the other-variant measurements")

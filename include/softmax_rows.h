@@ -103,6 +103,22 @@ int softmax_rows_ex(const void* x, void* y, float* m_out, float* d_out, float* l
                     int64_t N, int dtype, int variant, void* stream);
 
 /*
+ * softmax_rows_causal -- softmax_rows_ex for rows masked by position, as in causal attention
+ * scores: row r keeps its first
+ *     L_r = clamp(r % q_period + 1 + key_offset, 0, N)
+ * entries (query q = r % q_period sees keys 0 .. q + key_offset; key_offset = 0 when queries and
+ * keys have the same length), and entries j >= L_r count as -inf.  Masked entries are never read
+ * -- their bytes may hold anything -- and y is 0 there, so each row reads L_r elements instead of
+ * N: the block skipping of FlashAttention-2 ("Softmax 数值稳定性与 IO-Aware Attention" §八,
+ * skipping the causal mask's invalid blocks) applied to the plain softmax.  A row with L_r = 0
+ * gives y = 0, m = -inf, d = 0, LSE = -inf.  q_period >= 1 (else SOFTMAX_ERR_INVALID_ARG); other
+ * arguments as softmax_rows_ex.  Rows of at most 16 KiB (16-byte aligned) run one warp per row
+ * loading only the live prefix; other rows run the two-pass kernel over the live prefix.
+ */
+int softmax_rows_causal(const void* x, void* y, float* m_out, float* d_out, float* lse_out, int64_t M,
+                        int64_t N, int64_t q_period, int64_t key_offset, int dtype, void* stream);
+
+/*
  * softmax_row_state -- only the per-row state (m, d) and LSE: the first pass
  * of the online method ("5.2 CUDA Online Softmax 实现优化", §2.2, pass 1;
  * "Softmax 数值稳定性与 IO-Aware Attention" §四, the mergeable state).  Reads x

@@ -20,7 +20,7 @@ __all__ = [
     "VARIANT_SPLITROW", "VARIANT_NAMES", "SoftmaxError", "softmax_rows", "softmax_rows_ex",
     "softmax_row_state", "merge_states", "softmax_rows_host", "get_status", "status_string",
     "last_variant", "debug_set_fault", "debug_set_wait_limit_ns", "capi", "library_path",
-    "softmax_rows_splitrow_noalloc",
+    "softmax_rows_splitrow_noalloc", "softmax_rows_causal",
 ]
 
 F32, BF16 = 0, 1
@@ -39,6 +39,7 @@ EXPORTED = (
     "softmax_rows", "softmax_rows_ex", "softmax_row_state", "merge_states", "softmax_rows_host",
     "softmax_get_status", "softmax_status_string", "softmax_last_cuda_error", "softmax_last_variant",
     "softmax_debug_set_fault", "softmax_debug_set_wait_limit_ns", "softmax_rows_splitrow_noalloc",
+    "softmax_rows_causal",
 )
 
 
@@ -79,10 +80,11 @@ def capi() -> ctypes.CDLL:
         lib.softmax_debug_set_fault.argtypes = [ci]
         lib.softmax_debug_set_wait_limit_ns.argtypes = [i64]
         lib.softmax_rows_splitrow_noalloc.argtypes = [vp, vp, fp, fp, fp, i64, i64, ci, vp]
+        lib.softmax_rows_causal.argtypes = [vp, vp, fp, fp, fp, i64, i64, i64, i64, ci, vp]
         lib.softmax_debug_set_wait_limit_ns.restype = i64
         for name in ("softmax_rows", "softmax_rows_ex", "softmax_row_state", "merge_states",
                      "softmax_rows_host", "softmax_get_status", "softmax_last_variant",
-                     "softmax_debug_set_fault", "softmax_rows_splitrow_noalloc"):
+                     "softmax_debug_set_fault", "softmax_rows_splitrow_noalloc", "softmax_rows_causal"):
             getattr(lib, name).restype = ci
         _lib = lib
     return _lib
@@ -171,6 +173,26 @@ def softmax_rows(x, y=None, stream=None):
     if y.shape != x.shape or y.dtype != x.dtype or not y.is_cuda or not y.is_contiguous():
         raise ValueError("y must be a contiguous CUDA tensor with x's shape and dtype")
     _check(capi().softmax_rows(_ptr(x), _ptr(y), M, N, _dtype_code(x), _stream(stream)), "softmax_rows")
+    return y
+
+
+def softmax_rows_causal(x, q_period: int, key_offset: int = 0, y=None, m_out=None, d_out=None, lse_out=None,
+                        stream=None):
+    """Softmax of rows masked by position: row r keeps its first clamp(r % q_period + 1 + key_offset, 0, N)
+    entries; the rest count as -inf, are never read, and give y = 0."""
+    import torch
+
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor")
+    M, N = _rows(x)
+    if y is None:
+        y = torch.empty_like(x)
+    if y.shape != x.shape or y.dtype != x.dtype or not y.is_cuda or not y.is_contiguous():
+        raise ValueError("y must be a contiguous CUDA tensor with x's shape and dtype")
+    st = capi().softmax_rows_causal(_ptr(x), _ptr(y), _ptr(_state_out(m_out, M, "m_out")),
+                                    _ptr(_state_out(d_out, M, "d_out")), _ptr(_state_out(lse_out, M, "lse_out")),
+                                    M, N, int(q_period), int(key_offset), _dtype_code(x), _stream(stream))
+    _check(st, "softmax_rows_causal")
     return y
 
 

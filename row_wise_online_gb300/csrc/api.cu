@@ -228,6 +228,46 @@ int softmax_rows(const void* x, void* y, int64_t M, int64_t N, int dtype, void* 
   return softmax_rows_ex(x, y, nullptr, nullptr, nullptr, M, N, dtype, SOFTMAX_VARIANT_AUTO, stream);
 }
 
+int softmax_rows_causal(const void* x, void* y, float* m_out, float* d_out, float* lse_out, int64_t M, int64_t N,
+                        int64_t q_period, int64_t key_offset, int dtype, void* stream) {
+  bool noop = false;
+  int st = validate_rows(x, M, N, dtype, &noop);
+  if (st != SOFTMAX_OK) return st;
+  if (q_period < 1) return SOFTMAX_ERR_INVALID_ARG;
+  if (noop) return SOFTMAX_OK;
+  if (!y) return SOFTMAX_ERR_INVALID_ARG;
+  // Offsets beyond these bounds give the same lengths (all N, or all 0) and cannot overflow; a
+  // period beyond M gives r % q_period = r for every row, as q_period = M does.
+  if (q_period > M) q_period = M;
+  if (key_offset > N) key_offset = N;
+  if (key_offset < -q_period - 1) key_offset = -q_period - 1;
+  const DeviceInfo* dev = nullptr;
+  if ((st = current_device_info(&dev)) != SOFTMAX_OK) return st;
+  RowProblem p;
+  p.x = x;
+  p.y = y;
+  p.m_out = m_out;
+  p.d_out = d_out;
+  p.lse_out = lse_out;
+  p.M = M;
+  p.N = N;
+  p.dtype = dtype;
+  p.stream = static_cast<cudaStream_t>(stream);
+  const bool aligned = aligned16(x) && aligned16(y) && (N * elem_bytes(dtype)) % 16 == 0;
+  cudaError_t err;
+  int variant;
+  if (aligned && causal_warp_fits(p, *dev)) {  // rows up to 16 KiB: warp per row, live prefix only
+    err = launch_causal_warp(p, *dev, q_period, key_offset);
+    variant = SOFTMAX_VARIANT_ONEREAD_SMEM;
+  } else {
+    err = launch_twopass(p, aligned, *dev, q_period, key_offset);
+    variant = SOFTMAX_VARIANT_TWOPASS;
+  }
+  if (err != cudaSuccess) return cuda_fail(err);
+  t_last_variant = variant;
+  return SOFTMAX_OK;
+}
+
 int softmax_row_state(const void* x, float* m_out, float* d_out, float* lse_out, int64_t M, int64_t N,
                       int dtype, void* stream) {
   bool noop = false;

@@ -36,6 +36,14 @@ __device__ __forceinline__ float exp_diff(float a, float b) {
   return ex2(__fmul_rn(__fsub_rn(a, b), kLog2e));
 }
 
+// The same for a pair of values, with the shift passed negated.  The packed f32x2 add and
+// multiply of sm_100 and later round each half exactly as the scalar instructions do, so this
+// gives bit for bit the two exp_diff values in half the add/multiply issue slots.
+__device__ __forceinline__ float2 exp_diff2(float2 a, float2 neg_b) {
+  const float2 t = __fmul2_rn(__fadd2_rn(a, neg_b), make_float2(kLog2e, kLog2e));
+  return make_float2(ex2(t.x), ex2(t.y));
+}
+
 __device__ __forceinline__ float safe_max(float m) { return m == -INFINITY ? 0.f : m; }
 
 struct State {
@@ -138,6 +146,14 @@ struct F32 {
     return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
                       __float_as_uint(f[3]));
   }
+  __device__ static __forceinline__ void unpack2(const uint4& v, float2 (&f)[2]) {
+    f[0] = make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
+    f[1] = make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
+  }
+  __device__ static __forceinline__ uint4 pack2(const float2 (&f)[2]) {
+    return make_uint4(__float_as_uint(f[0].x), __float_as_uint(f[0].y), __float_as_uint(f[1].x),
+                      __float_as_uint(f[1].y));
+  }
   __device__ static __forceinline__ float load1(const void* p, int64_t i) {
     return __ldg(static_cast<const float*>(p) + i);
   }
@@ -169,6 +185,16 @@ struct BF16 {
     return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
                       pack_bf16x2(f[6], f[7]));
   }
+  __device__ static __forceinline__ void unpack2(const uint4& v, float2 (&f)[4]) {
+    f[0] = make_float2(bf16_lo(v.x), bf16_hi(v.x));
+    f[1] = make_float2(bf16_lo(v.y), bf16_hi(v.y));
+    f[2] = make_float2(bf16_lo(v.z), bf16_hi(v.z));
+    f[3] = make_float2(bf16_lo(v.w), bf16_hi(v.w));
+  }
+  __device__ static __forceinline__ uint4 pack2(const float2 (&f)[4]) {
+    return make_uint4(pack_bf16x2(f[0].x, f[0].y), pack_bf16x2(f[1].x, f[1].y), pack_bf16x2(f[2].x, f[2].y),
+                      pack_bf16x2(f[3].x, f[3].y));
+  }
   __device__ static __forceinline__ float load1(const void* p, int64_t i) {
     const unsigned short b = __ldg(static_cast<const unsigned short*>(p) + i);
     return __uint_as_float(static_cast<uint32_t>(b) << 16);
@@ -185,6 +211,23 @@ struct BF16 {
     static_cast<uint16_t*>(p)[i] = to_bf16(v);
   }
 };
+
+// Keep the first `keep` (0 < keep < kVec) elements of a packed vector and set the rest to -inf.
+template <class D>
+__device__ __forceinline__ uint4 mask_tail(uint4 v, int keep) {
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  constexpr int per_word = 4 / D::kBytes;  // elements per 32-bit word
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (per_word == 1) {
+      if (i >= keep) w[i] = 0xff800000u;
+    } else {
+      if (2 * i >= keep) w[i] = 0xff80ff80u;
+      else if (2 * i + 1 >= keep) w[i] = (w[i] & 0x0000ffffu) | 0xff800000u;  // high half is element 2i+1
+    }
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
 
 // ---------------------------------------------------------------------------------------------
 // 16-byte global memory access

@@ -31,6 +31,8 @@ struct RowArgs {
   float* lse_out;
   int64_t M;
   int64_t N;
+  int64_t q_period;    // causal rule (two-pass CAUSAL only): row r keeps its first
+  int64_t key_offset;  // clamp(r % q_period + 1 + key_offset, 0, N) entries
 };
 
 __device__ __forceinline__ void write_state(const RowArgs& a, int64_t row, State s) {
@@ -152,7 +154,7 @@ int blocks_per_sm(const void* fn, int threads, size_t smem) {
 
 RowArgs row_args(const RowProblem& p) {
   return RowArgs{static_cast<const unsigned char*>(p.x), static_cast<unsigned char*>(p.y),
-                 p.m_out, p.d_out, p.lse_out, p.M, p.N};
+                 p.m_out, p.d_out, p.lse_out, p.M, p.N, 1, 0};
 }
 
 // ------------------------------------------------------------------------------------------
@@ -178,7 +180,7 @@ __device__ __forceinline__ void load_unit(const unsigned char* xr, int64_t u, in
   }
 }
 
-template <class D, bool VEC, bool WRITE_Y>
+template <class D, bool VEC, bool WRITE_Y, bool CAUSAL>
 __global__ void __launch_bounds__(kTwoPassMaxThreads) k_twopass(RowArgs a) {
   constexpr int E = VEC ? D::kVec : 1;
   constexpr int U = kTwoPassUnroll;
@@ -191,12 +193,29 @@ __global__ void __launch_bounds__(kTwoPassMaxThreads) k_twopass(RowArgs a) {
   int it = 0;
   for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x, ++it) {
     const unsigned char* xr = a.x + row * row_bytes;
+    // live elements and units: all of them, or the causal prefix (the rest is never read)
+    int64_t L = a.N;
+    if constexpr (CAUSAL) {
+      L = row % a.q_period + 1 + a.key_offset;
+      L = L < 0 ? 0 : (L > a.N ? a.N : L);
+    }
+    const int64_t lunits = CAUSAL ? (L + E - 1) / E : nunits;
     // pass 1: online fold, one rescale per step of U units; compensated (Kahan) sum of d
     float m = -INFINITY, d = 0.f, c = 0.f;
-    for (int64_t base = threadIdx.x; base < nunits; base += (int64_t)nt * U) {
+    for (int64_t base = threadIdx.x; base < lunits; base += (int64_t)nt * U) {
       float v[U][E];
 #pragma unroll
-      for (int k = 0; k < U; ++k) load_unit<D, VEC>(xr, base + (int64_t)k * nt, nunits, v[k]);
+      for (int k = 0; k < U; ++k) {
+        load_unit<D, VEC>(xr, base + (int64_t)k * nt, lunits, v[k]);
+        if constexpr (CAUSAL && E > 1) {  // the vector straddling the live length
+          const int64_t keep = L - (base + (int64_t)k * nt) * E;
+          if (keep > 0 && keep < E) {
+#pragma unroll
+            for (int e = 0; e < E; ++e)
+              if (e >= keep) v[k][e] = -INFINITY;
+          }
+        }
+      }
       float mu = -INFINITY;
 #pragma unroll
       for (int k = 0; k < U; ++k)
@@ -228,11 +247,19 @@ __global__ void __launch_bounds__(kTwoPassMaxThreads) k_twopass(RowArgs a) {
       for (int64_t base = threadIdx.x; base < nunits; base += (int64_t)nt * U) {
         float v[U][E];
 #pragma unroll
-        for (int k = 0; k < U; ++k) load_unit<D, VEC>(xr, base + (int64_t)k * nt, nunits, v[k]);
+        for (int k = 0; k < U; ++k) load_unit<D, VEC>(xr, base + (int64_t)k * nt, lunits, v[k]);
 #pragma unroll
         for (int k = 0; k < U; ++k) {
           const int64_t u = base + (int64_t)k * nt;
           if (u < nunits) {
+            if constexpr (CAUSAL && E > 1) {  // entries past L count as -inf: y = 0 there
+              const int64_t keep = L - u * E;
+              if (keep > 0 && keep < E) {
+#pragma unroll
+                for (int e = 0; e < E; ++e)
+                  if (e >= keep) v[k][e] = -INFINITY;
+              }
+            }
 #pragma unroll
             for (int e = 0; e < E; ++e) v[k][e] = __fmul_rn(exp_diff(v[k][e], ms), inv);
             if constexpr (VEC) {
@@ -286,23 +313,32 @@ cudaError_t launch_oneread_reg(const RowProblem& p, bool vec, const DeviceInfo& 
   return cudaGetLastError();
 }
 
-cudaError_t launch_twopass(const RowProblem& p, bool vec, const DeviceInfo& dev) {
+cudaError_t launch_twopass(const RowProblem& p, bool vec, const DeviceInfo& dev, int64_t q_period,
+                           int64_t key_offset) {
   const int64_t e = vec ? 16 / elem_bytes(p.dtype) : 1;
   if (vec && p.N % e != 0) return cudaErrorInvalidValue;
   const int64_t units = p.N / e;
   int nt = 128;
   while (nt < kTwoPassMaxThreads && int64_t(nt) * kTwoPassUnroll < units) nt *= 2;
   const bool write_y = p.y != nullptr;
-  RowKernel fn;
-  if (p.dtype == 0)
-    fn = vec ? (write_y ? k_twopass<F32, true, true> : k_twopass<F32, true, false>)
-             : (write_y ? k_twopass<F32, false, true> : k_twopass<F32, false, false>);
-  else
-    fn = vec ? (write_y ? k_twopass<BF16, true, true> : k_twopass<BF16, true, false>)
-             : (write_y ? k_twopass<BF16, false, true> : k_twopass<BF16, false, false>);
+  const bool causal = q_period > 0;
+  // [dtype][vec][write_y][causal]
+  static const RowKernel table[2][2][2][2] = {
+      {{{k_twopass<F32, false, false, false>, k_twopass<F32, false, false, true>},
+        {k_twopass<F32, false, true, false>, k_twopass<F32, false, true, true>}},
+       {{k_twopass<F32, true, false, false>, k_twopass<F32, true, false, true>},
+        {k_twopass<F32, true, true, false>, k_twopass<F32, true, true, true>}}},
+      {{{k_twopass<BF16, false, false, false>, k_twopass<BF16, false, false, true>},
+        {k_twopass<BF16, false, true, false>, k_twopass<BF16, false, true, true>}},
+       {{k_twopass<BF16, true, false, false>, k_twopass<BF16, true, false, true>},
+        {k_twopass<BF16, true, true, false>, k_twopass<BF16, true, true, true>}}}};
+  RowKernel fn = table[p.dtype == 0 ? 0 : 1][vec ? 1 : 0][write_y ? 1 : 0][causal ? 1 : 0];
   const int64_t cap = int64_t(dev.sm_count) * blocks_per_sm((const void*)fn, nt, 0);
   const int grid = int(p.M < cap ? p.M : cap);
-  fn<<<grid, nt, 0, p.stream>>>(row_args(p));
+  RowArgs a = row_args(p);
+  a.q_period = causal ? q_period : 1;
+  a.key_offset = key_offset;
+  fn<<<grid, nt, 0, p.stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -49,10 +49,17 @@ cudaError_t launch_oneread_reg(const RowProblem& p, bool vec, const DeviceInfo& 
 bool oneread_warp_fits(const RowProblem& p, const DeviceInfo& dev);
 cudaError_t launch_oneread_warp(const RowProblem& p, const DeviceInfo& dev);
 
+// Causal rows (q_period >= 1): row r keeps its first clamp(r % q_period + 1 + key_offset, 0, N)
+// entries; the rest are not read and give y = 0.
+bool causal_warp_fits(const RowProblem& p, const DeviceInfo& dev);
+cudaError_t launch_causal_warp(const RowProblem& p, const DeviceInfo& dev, int64_t q_period, int64_t key_offset);
+
 bool oneread_tma_fits(const RowProblem& p, const DeviceInfo& dev);
 cudaError_t launch_oneread_tma(const RowProblem& p, const DeviceInfo& dev);
 
-cudaError_t launch_twopass(const RowProblem& p, bool vec, const DeviceInfo& dev);
+// q_period >= 1 applies the causal rule above; 0 processes whole rows.
+cudaError_t launch_twopass(const RowProblem& p, bool vec, const DeviceInfo& dev, int64_t q_period = 0,
+                           int64_t key_offset = 0);
 
 bool splitrow_fits(const RowProblem& p, const DeviceInfo& dev);
 cudaError_t launch_splitrow(const RowProblem& p, const DeviceInfo& dev);

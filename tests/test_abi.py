@@ -71,6 +71,9 @@ def test_other_calls_argument_checks(lib):
     assert lib.merge_states(X, X, X, X, X, None, None, 4, None) == rwo.ERR_INVALID_ARG
     assert lib.merge_states(X, X, X, X, X, X, None, 0, None) == rwo.OK
     assert lib.softmax_rows_host(X, NULL, 4, 4, 0, None) == rwo.ERR_INVALID_ARG
+    assert lib.softmax_rows_causal(X, X, None, None, None, 4, 4, 0, 0, 0, None) == rwo.ERR_INVALID_ARG  # period 0
+    assert lib.softmax_rows_causal(X, NULL, None, None, None, 4, 4, 4, 0, 0, None) == rwo.ERR_INVALID_ARG
+    assert lib.softmax_rows_causal(NULL, NULL, None, None, None, 0, 4, 4, 0, 0, None) == rwo.OK  # M = 0
 
 
 def test_status_strings(lib):
