@@ -10,6 +10,9 @@ The arithmetic lives in ``oracle.c`` (plain C, double precision):
   in "5.2 CUDA Online Softmax 实现优化" §1.1 and "Softmax 数值稳定性与
   IO-Aware Attention" §三, plus LSE = m + log d ("从原始Softmax到在线Softmax",
   section "softmax形式推导").
+* ``log_softmax_rows`` -- log_probs = x - max - log(sum exp(x - max)), and
+  ``cross_entropy_rows`` -- the per-row loss -log_probs[r, label_r]
+  ("从原始Softmax到在线Softmax", section "softmax实际代码实现").
 * ``online_state`` -- the element-by-element (m, d) recurrence,
   "5.2 CUDA Online Softmax 实现优化" §2.1.
 * ``merge_state`` -- the merge of two partial states,
@@ -64,6 +67,10 @@ def _load():
             lib.oracle_online_state.restype = None
             lib.oracle_merge_state.argtypes = [ctypes.c_double] * 4 + [dp, dp]
             lib.oracle_merge_state.restype = None
+            lib.oracle_log_softmax_rows.argtypes = [vp, ctypes.c_int, i64, vp, i64, vp, ctypes.c_int]
+            lib.oracle_log_softmax_rows.restype = ctypes.c_int
+            lib.oracle_cross_entropy_rows.argtypes = [vp, ctypes.c_int, i64, vp, i64, vp, ctypes.c_int]
+            lib.oracle_cross_entropy_rows.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -111,6 +118,50 @@ def softmax_rows(x: np.ndarray, dtype: int | None = None, rows=None, *, want_y: 
     if rc != 0:
         raise RuntimeError("oracle_softmax_rows rejected its arguments")
     return y, m, d, lse
+
+
+def _matrix(x, dtype):
+    x = np.ascontiguousarray(x)
+    if x.ndim != 2:
+        raise ValueError("x must be 2-D")
+    if dtype is None:
+        dtype = F32 if x.dtype == np.float32 else BF16 if x.dtype == np.uint16 else None
+    if dtype is None or (dtype == F32 and x.dtype != np.float32) or (dtype == BF16 and x.dtype != np.uint16):
+        raise TypeError("x must be float32 (F32) or uint16 bf16 bits (BF16)")
+    return x, dtype
+
+
+def log_softmax_rows(x: np.ndarray, dtype: int | None = None, rows=None, *, nthreads: int | None = None):
+    """fp64 log softmax of rows of a row-major matrix (all -inf row: -inf).  Returns (nrows, N) float64."""
+    x, dtype = _matrix(x, dtype)
+    M, N = x.shape
+    idx = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    if idx is not None and idx.size and (idx.min() < 0 or idx.max() >= M):
+        raise IndexError("row index out of range")
+    nrows = M if idx is None else idx.size
+    ly = np.empty((nrows, N), np.float64)
+    if nrows == 0:
+        return ly
+    rc = _load().oracle_log_softmax_rows(_ptr(x), dtype, N, _ptr(idx), nrows, _ptr(ly), nthreads or default_threads())
+    if rc != 0:
+        raise RuntimeError("oracle_log_softmax_rows rejected its arguments")
+    return ly
+
+
+def cross_entropy_rows(x: np.ndarray, labels, dtype: int | None = None, *, nthreads: int | None = None):
+    """fp64 per-row cross-entropy loss against int labels (negative: 0; >= N: NaN).  Returns (M,) float64."""
+    x, dtype = _matrix(x, dtype)
+    M, N = x.shape
+    lab = np.ascontiguousarray(np.asarray(labels, dtype=np.int64).reshape(-1))
+    if lab.size != M:
+        raise ValueError("one label per row")
+    loss = np.empty(M, np.float64)
+    if M == 0:
+        return loss
+    rc = _load().oracle_cross_entropy_rows(_ptr(x), dtype, N, _ptr(lab), M, _ptr(loss), nthreads or default_threads())
+    if rc != 0:
+        raise RuntimeError("oracle_cross_entropy_rows rejected its arguments")
+    return loss
 
 
 def online_state(xs) -> tuple[float, float]:

@@ -17,6 +17,14 @@
  *      and the log-sum-exp  LSE = m + log(d)
  *      ("从原始Softmax到在线Softmax", section "softmax形式推导").
  *
+ *  oracle_log_softmax_rows -- the log of the softmax, as the page's
+ *      log_probs = x - max - log(sum_j exp(x_j - max))
+ *      ("从原始Softmax到在线Softmax", section "softmax实际代码实现").
+ *
+ *  oracle_cross_entropy_rows -- the per-row cross-entropy loss of the same
+ *      section's cross_entropy_loss, -log_probs[r, label_r], before its mean
+ *      over rows (worked example "交叉熵损失计算": 0.4170).
+ *
  *  oracle_online_state -- the element-by-element (m, d) recurrence
  *      ("5.2 CUDA Online Softmax 实现优化", §2.1):
  *          m_{k+1} = max(m_k, x_k)
@@ -36,6 +44,10 @@
  *    is ever evaluated.
  *  - A row whose entries are all -inf has y = 0, m = -inf, d = 0, LSE = -inf.
  *  - bf16 inputs are widened exactly (bf16 -> fp32 -> fp64).
+ *  - log softmax of an all -inf row is -inf everywhere (log 0).
+ *  - Cross entropy: a negative label marks a row to ignore (loss 0); a label
+ *    >= N gives NaN.  A row whose labelled entry is -inf has loss +inf
+ *    (-log 0); an all -inf row gives -inf - (-inf) = NaN.
  *
  * Rows are independent, so they are spread over POSIX threads; inside a row
  * the three passes run in plain index order.
@@ -153,6 +165,113 @@ int oracle_softmax_rows(const void* x, int dtype, int64_t N,
   free(tids);
   free(jobs);
   return 0;
+}
+
+/* The row's m and d (passes 1 and 2 of the three-pass softmax above). */
+static void row_max_and_sum(const void* x, int dtype, int64_t N, int64_t row, double* m_out, double* d_out) {
+  const int64_t base = row * N;
+  double m = -INFINITY;
+  for (int64_t j = 0; j < N; ++j) {
+    double v = load_elem(x, dtype, base + j);
+    if (v > m) m = v;
+  }
+  double d = 0.0;
+  for (int64_t j = 0; j < N; ++j) d += scaled_exp(load_elem(x, dtype, base + j), m);
+  *m_out = m;
+  *d_out = d;
+}
+
+typedef struct {
+  const void* x;
+  int dtype;
+  int64_t N;
+  const int64_t* rows;   /* log softmax: selected rows, or NULL */
+  const int64_t* labels; /* cross entropy: one label per row */
+  double* out;           /* log softmax: nrows x N; cross entropy: nrows */
+  int64_t begin, end;
+} oracle_log_job;
+
+static void* oracle_log_worker(void* arg) {
+  oracle_log_job* job = (oracle_log_job*)arg;
+  for (int64_t i = job->begin; i < job->end; ++i) {
+    int64_t row = job->rows ? job->rows[i] : i;
+    double m, d;
+    row_max_and_sum(job->x, job->dtype, job->N, row, &m, &d);
+    /* log_probs = x - max - log(sum_exp); all -inf row: -inf */
+    double log_d = (m == -INFINITY) ? INFINITY : log(d);
+    double shift = (m == -INFINITY) ? 0.0 : m;
+    if (!job->labels) {
+      double* ly = job->out + i * job->N;
+      for (int64_t j = 0; j < job->N; ++j) ly[j] = load_elem(job->x, job->dtype, row * job->N + j) - shift - log_d;
+    } else {
+      int64_t label = job->labels[i];
+      double loss;
+      if (label < 0) {
+        loss = 0.0;
+      } else if (label >= job->N) {
+        loss = NAN;
+      } else {
+        double xl = load_elem(job->x, job->dtype, row * job->N + label);
+        loss = (m == -INFINITY) ? NAN : -(xl - m - log(d));
+      }
+      job->out[i] = loss;
+    }
+  }
+  return NULL;
+}
+
+static int run_log_jobs(oracle_log_job proto, int64_t nrows, int nthreads) {
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > nrows) nthreads = (int)nrows;
+  pthread_t* tids = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+  oracle_log_job* jobs = (oracle_log_job*)calloc((size_t)nthreads, sizeof(oracle_log_job));
+  if (!tids || !jobs) {
+    free(tids);
+    free(jobs);
+    return -1;
+  }
+  for (int t = 0; t < nthreads; ++t) {
+    jobs[t] = proto;
+    jobs[t].begin = nrows * t / nthreads;
+    jobs[t].end = nrows * (t + 1) / nthreads;
+    if (t == 0) continue;
+    if (pthread_create(&tids[t], NULL, oracle_log_worker, &jobs[t]) != 0) {
+      oracle_log_worker(&jobs[t]);
+      tids[t] = (pthread_t)0;
+    }
+  }
+  oracle_log_worker(&jobs[0]);
+  for (int t = 1; t < nthreads; ++t)
+    if (tids[t] != (pthread_t)0) pthread_join(tids[t], NULL);
+  free(tids);
+  free(jobs);
+  return 0;
+}
+
+/*
+ * Log softmax of selected rows (rows == NULL: rows 0..nrows-1) into ly
+ * (nrows x N).  Returns 0, or -1 on a bad argument.
+ */
+int oracle_log_softmax_rows(const void* x, int dtype, int64_t N, const int64_t* rows, int64_t nrows,
+                            double* ly, int nthreads) {
+  if (!x || !ly || N < 1 || nrows < 0) return -1;
+  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return -1;
+  if (nrows == 0) return 0;
+  oracle_log_job proto = {x, dtype, N, rows, NULL, ly, 0, 0};
+  return run_log_jobs(proto, nrows, nthreads);
+}
+
+/*
+ * Cross-entropy loss of rows 0..M-1 against labels[0..M) into loss[0..M).
+ * Returns 0, or -1 on a bad argument.
+ */
+int oracle_cross_entropy_rows(const void* x, int dtype, int64_t N, const int64_t* labels, int64_t M,
+                              double* loss, int nthreads) {
+  if (!x || !labels || !loss || N < 1 || M < 0) return -1;
+  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return -1;
+  if (M == 0) return 0;
+  oracle_log_job proto = {x, dtype, N, NULL, labels, loss, 0, 0};
+  return run_log_jobs(proto, M, nthreads);
 }
 
 /*

@@ -64,6 +64,9 @@ def test_golden_worked_examples():
             xl = float(np.float32(x[label]))
             assert abs((lse[0] - xl) - float(kv["loss"])) <= tol
             assert abs(-math.log(y[0][label]) - float(kv["loss"])) <= tol
+            # the oracle's own cross-entropy and log-softmax functions
+            assert abs(oracle.cross_entropy_rows(_f32([x]), [label])[0] - float(kv["loss"])) <= tol
+            assert abs(-oracle.log_softmax_rows(_f32([x]))[0, label] - float(kv["loss"])) <= tol
         elif kind == "state":
             x = _vec(kv["x"])
             m, d = oracle.online_state(x)
@@ -328,3 +331,74 @@ def test_bad_arguments_are_rejected():
         oracle.softmax_rows(np.zeros((2, 2), np.float64))
     with pytest.raises(IndexError):
         oracle.softmax_rows(np.zeros((2, 2), np.float32), rows=[2])
+
+
+# ---------------------------------------------------------------------------------------------
+# log softmax and cross entropy ("从原始Softmax到在线Softmax", section "softmax实际代码实现")
+# ---------------------------------------------------------------------------------------------
+
+
+def _mp_log_softmax(row):
+    """50-digit log softmax with no max subtraction: x_j - log(sum_k exp(x_k))."""
+    with mpmath.workdps(50):
+        xs = [mpmath.mpf(float(v)) for v in row]
+        lse = mpmath.log(mpmath.fsum(mpmath.exp(v) for v in xs))
+        return np.array([float(v - lse) for v in xs])
+
+
+def test_log_softmax_mpmath_brute_force():
+    rng = np.random.default_rng(11)
+    for M, N in [(3, 5), (5, 3), (4, 33), (1, 1), (2, 64)]:
+        x = (rng.standard_normal((M, N)) * 6).astype(np.float32)
+        ly = oracle.log_softmax_rows(x)
+        assert ly.shape == (M, N)
+        for r in range(M):
+            ref = _mp_log_softmax(x[r])
+            np.testing.assert_allclose(ly[r], ref, rtol=1e-14, atol=1e-14)
+
+
+def test_log_softmax_closed_forms():
+    # uniform row of 2^k entries: -ln(2^k) everywhere
+    for k in (0, 3, 10):
+        ly = oracle.log_softmax_rows(np.full((1, 1 << k), 1.25, np.float32))
+        np.testing.assert_allclose(ly, -k * math.log(2.0), rtol=0, atol=1e-15)
+    # two elements: log y_0 = -log1p(exp(x_1 - x_0)) (softplus)
+    for a, b in [(0.0, 0.0), (3.0, -1.5), (-2.0, 7.0), (40.0, -40.0)]:
+        ly = oracle.log_softmax_rows(np.array([[a, b]], np.float32))
+        assert abs(ly[0, 0] + math.log1p(math.exp(b - a))) <= 1e-15 * max(1.0, abs(b - a))
+        assert abs(ly[0, 1] + math.log1p(math.exp(a - b))) <= 1e-15 * max(1.0, abs(b - a))
+    # shift invariance, with values on a 1/64 grid so that x + c is exact in fp32
+    x = (np.round(np.random.default_rng(2).standard_normal((3, 50)) * 3 * 64) / 64).astype(np.float32)
+    for c in (1024.0, -1024.0):
+        np.testing.assert_allclose(oracle.log_softmax_rows(x + np.float32(c)), oracle.log_softmax_rows(x),
+                                   rtol=0, atol=1e-12)
+
+
+def test_log_softmax_masked_rows_and_selection():
+    x = np.array([[1.0, -np.inf, 2.0, -np.inf], [-np.inf] * 4, [0.5, 0.5, -np.inf, 3.0]], np.float32)
+    ly = oracle.log_softmax_rows(x)
+    assert np.all(np.isneginf(ly[1]))                       # all -inf row: log 0
+    assert np.isneginf(ly[0, 1]) and np.isneginf(ly[0, 3])  # masked entries: log 0
+    np.testing.assert_allclose(ly[0, [0, 2]], _mp_log_softmax([1.0, 2.0]), rtol=1e-15)
+    np.testing.assert_allclose(oracle.log_softmax_rows(x, rows=[2, 0]), ly[[2, 0]], rtol=0, atol=0)
+    # bf16 bits are widened exactly
+    xb = synth.f32_to_bf16(x)
+    np.testing.assert_array_equal(oracle.log_softmax_rows(xb), ly)
+
+
+def test_cross_entropy_against_brute_force_and_label_rules():
+    rng = np.random.default_rng(4)
+    x = (rng.standard_normal((6, 19)) * 5).astype(np.float32)
+    labels = np.array([0, 18, 7, -1, 19, -100])
+    loss = oracle.cross_entropy_rows(x, labels)
+    for r in (0, 1, 2):
+        assert abs(loss[r] + _mp_log_softmax(x[r])[labels[r]]) <= 1e-14 * max(1.0, abs(loss[r]))
+    assert loss[3] == 0.0 and loss[5] == 0.0   # negative label: ignored row
+    assert math.isnan(loss[4])                  # label >= N
+    # loss >= 0, and equals the page's -log p of the labelled class
+    y, *_ = oracle.softmax_rows(x[:3])
+    np.testing.assert_allclose(loss[:3], -np.log(y[np.arange(3), labels[:3]]), rtol=1e-13)
+    # masked labelled entry: -log 0 = +inf; all -inf row: NaN
+    xm = np.array([[1.0, -np.inf], [-np.inf, -np.inf]], np.float32)
+    lm = oracle.cross_entropy_rows(xm, [1, 0])
+    assert np.isposinf(lm[0]) and math.isnan(lm[1])
