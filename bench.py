@@ -217,14 +217,24 @@ def bench_ours(args) -> dict | None:
     causal = args.variant == "causal"
     if causal and not w.causal_q:
         raise SystemExit("--variant causal needs a workload with a causal mask")
+    log_mode = args.variant == "log"
+    ce_mode = args.variant == "ce"
+    special = causal or log_mode or ce_mode  # another entry point than softmax_rows_ex
+    if ce_mode:  # synthetic labels, uniform over the classes
+        labels = torch.from_numpy(np.random.default_rng(5).integers(0, w.N, w.M)).to(dev)
+        loss = torch.empty(w.M, dtype=torch.float32, device=dev)
     variant = {"auto": rwo.VARIANT_AUTO, "reg": rwo.VARIANT_ONEREAD_REG, "smem": rwo.VARIANT_ONEREAD_SMEM,
                "twopass": rwo.VARIANT_TWOPASS, "splitrow": rwo.VARIANT_SPLITROW,
-               "causal": rwo.VARIANT_AUTO}[args.variant]
+               "causal": rwo.VARIANT_AUTO, "log": rwo.VARIANT_AUTO, "ce": rwo.VARIANT_AUTO}[args.variant]
 
     def measure(var: int, nsteps: int, warm: int, clocks: bool = False):
         def step(i):
             if causal:  # masked keys are not read: the causal rule replaces the -inf entries
                 rwo.softmax_rows_causal(xs[i % nbuf], w.causal_q, 0, ys[i % nbuf], stream=stream)
+            elif log_mode:
+                rwo.log_softmax_rows(xs[i % nbuf], ys[i % nbuf], stream=stream)
+            elif ce_mode:
+                rwo.cross_entropy_rows(xs[i % nbuf], labels, loss, stream=stream)
             else:
                 rwo.softmax_rows_ex(xs[i % nbuf], ys[i % nbuf], variant=var, stream=stream)
 
@@ -265,12 +275,14 @@ def bench_ours(args) -> dict | None:
     ms = reduce_max(ms_local, world)
     per_step_ms = ms / args.steps
     bytes_step = w.min_bytes
+    if ce_mode:  # x read once, labels read, losses written: no y
+        bytes_step = w.M * w.N * w.elem_bytes + 12 * w.M
     gbs = world * bytes_step * args.steps / (ms * 1e-3) / 1e9
     rows_s = world * w.M * args.steps / (ms * 1e-3)
 
     # Other variants on the same workload (fewer steps), for the record.
     variants = {}
-    if world == 1 and not args.quick and not causal:
+    if world == 1 and not args.quick and not special:
         for name, var in (("oneread_reg", rwo.VARIANT_ONEREAD_REG), ("oneread_smem", rwo.VARIANT_ONEREAD_SMEM),
                           ("twopass", rwo.VARIANT_TWOPASS), ("splitrow", rwo.VARIANT_SPLITROW)):
             if var == used:
@@ -285,7 +297,7 @@ def bench_ours(args) -> dict | None:
 
     # End to end through the public host-buffer call: H2D of x, kernels, D2H of y, every step.
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not special:
         y_host = torch.empty_like(host_x).pin_memory()
         for _ in range(2):
             rwo.softmax_rows_host(host_x, y_host)
@@ -306,8 +318,10 @@ def bench_ours(args) -> dict | None:
     peak, peak_kind = measured_hbm_peak()
     kernel = {rwo.VARIANT_ONEREAD_REG: "k_oneread_reg", rwo.VARIANT_ONEREAD_SMEM: "k_oneread_tma",
               rwo.VARIANT_TWOPASS: "k_twopass", rwo.VARIANT_SPLITROW: "k_splitrow"}[used]
-    if used == rwo.VARIANT_ONEREAD_SMEM and w.N * w.elem_bytes <= 16384:
+    if used == rwo.VARIANT_ONEREAD_SMEM and w.N * w.elem_bytes <= 16384 and not log_mode:
         kernel = "k_causal_warp" if causal else "k_oneread_warp"  # rows up to 16 KiB: one warp per row
+    # profile summaries are per kernel, output mode and workload
+    profile_key = kernel + ("-log" if log_mode else "-ce" if ce_mode else "")
     alg_bytes = bytes_step
     if causal:  # bytes the kernel needs: the live prefix of every row (whole 16-byte vectors) + all of y
         vec = 16 // w.elem_bytes
@@ -315,7 +329,7 @@ def bench_ours(args) -> dict | None:
         live = np.clip(r % w.causal_q + 1, 0, w.N)
         alg_bytes = int(((live + vec - 1) // vec).sum()) * 16 + w.M * w.N * w.elem_bytes
     achieved = alg_bytes / (per_step_ms * 1e-3) / 1e9
-    traffic = profiled_traffic(kernel, w.name)
+    traffic = profiled_traffic(profile_key, w.name)
     result = {
         "metric": METRIC,
         "value": round(gbs, 1),
@@ -333,7 +347,9 @@ def bench_ours(args) -> dict | None:
         "data": "synthetic",
         "config": {"workload": w.name if not args.rows else f"{w.name}[rows={w.M}]", "M": w.M, "N": w.N,
                    "rows_total": w.M * world,
-                   "variant": rwo.VARIANT_NAMES[used] + ("+causal_skip" if causal else ""), "parallelism": f"rows sharded over {world} GPU(s)",
+                   "variant": rwo.VARIANT_NAMES[used] + ("+causal_skip" if causal else "+log_softmax" if log_mode
+                                                         else "+cross_entropy" if ce_mode else ""),
+                   "parallelism": f"rows sharded over {world} GPU(s)",
                    "l2": (f"{nbuf} rotating x/y buffer sets ({nbuf * set_bytes >> 20} MiB > L2)" if nbuf > 1
                           else "inputs larger than L2"),
                    "timing": "CUDA graph replays between CUDA events on the launching stream"},
@@ -423,8 +439,10 @@ def main(argv=None) -> int:
     ap.add_argument("--steps", type=int, default=50000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--variant", default="auto", choices=["auto", "reg", "smem", "twopass", "splitrow", "causal"],
-                    help="causal: softmax_rows_causal on a causal workload (masked keys not read)")
+    ap.add_argument("--variant", default="auto",
+                    choices=["auto", "reg", "smem", "twopass", "splitrow", "causal", "log", "ce"],
+                    help="causal: softmax_rows_causal on a causal workload (masked keys not read); "
+                         "log: log_softmax_rows; ce: cross_entropy_rows with uniform synthetic labels")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--rows", type=int, default=0, help="use only the first ROWS rows (profiling small cases)")
     ap.add_argument("--quick", action="store_true", help="skip the other-variant measurements")

@@ -119,6 +119,37 @@ int softmax_rows_causal(const void* x, void* y, float* m_out, float* d_out, floa
                         int64_t N, int64_t q_period, int64_t key_offset, int dtype, void* stream);
 
 /*
+ * log_softmax_rows -- y = log softmax(x) row by row: y_j = x_j - LSE with LSE = m + ln d
+ * ("从原始Softmax到在线Softmax", section "softmax实际代码实现": log_probs = logits - max -
+ * log(sum_exp), the step before the cross-entropy loss).  Computed as (x_j - m) - ln d from the
+ * online state, so x is read once as for softmax.  An all -inf row gives y = -inf everywhere
+ * (log 0).  Arguments, layout, outputs and errors as softmax_rows_ex; `variant` may be AUTO,
+ * ONEREAD_REG, ONEREAD_SMEM (the CTA bulk-copy kernel) or TWOPASS.  SPLITROW gives
+ * SOFTMAX_ERR_UNSUPPORTED; AUTO never picks it (a single very long row runs TWOPASS).
+ */
+int log_softmax_rows(const void* x, void* y, float* m_out, float* d_out, float* lse_out, int64_t M,
+                     int64_t N, int dtype, int variant, void* stream);
+
+/*
+ * cross_entropy_rows -- per-row cross-entropy loss against integer labels:
+ *     loss[r] = LSE_r - x[r, labels[r]]  ( = -log softmax(x_r)[labels[r]] )
+ * ("从原始Softmax到在线Softmax", section "softmax实际代码实现", cross_entropy_loss, and the
+ * worked example "交叉熵损失计算": logits [2.0, 1.0, 0.1], label 0 -> 0.4170), evaluated as
+ * (m - x_label) + ln d in the page's order (no cancellation for large |m|).  The page
+ * returns the mean over rows; this call returns each row's loss (the mean is the caller's sum
+ * over loss / M).  Only x is read (no y is written): one pass over each row for the online
+ * state, plus the labelled element.
+ *   labels  -- device, int64, M entries.  A negative label marks a row to ignore: loss = 0.
+ *              A label >= N gives loss = NaN, x is not read there, and the next
+ *              softmax_get_status() returns SOFTMAX_ERR_INVALID_ARG.
+ *   loss    -- device, fp32, M entries (required).
+ *   lse_out -- device, fp32, M entries, or NULL.
+ * Other arguments and errors as softmax_row_state.
+ */
+int cross_entropy_rows(const void* x, const int64_t* labels, float* loss, float* lse_out, int64_t M, int64_t N,
+                       int dtype, void* stream);
+
+/*
  * softmax_row_state -- only the per-row state (m, d) and LSE: the first pass
  * of the online method ("5.2 CUDA Online Softmax 实现优化", §2.2, pass 1;
  * "Softmax 数值稳定性与 IO-Aware Attention" §四, the mergeable state).  Reads x
@@ -183,7 +214,8 @@ int softmax_rows_splitrow_noalloc(const void* x, void* y, float* m_out, float* d
  * softmax_get_status -- synchronises `stream`, then returns and clears the
  * status word of the current device: SOFTMAX_OK, or the error a kernel
  * recorded since the last call (SOFTMAX_ERR_TIMEOUT for a bounded wait that
- * ran out).  SOFTMAX_ERR_CUDA if the synchronisation itself failed.
+ * ran out, which takes precedence; SOFTMAX_ERR_INVALID_ARG for a cross-entropy
+ * label >= N).  SOFTMAX_ERR_CUDA if the synchronisation itself failed.
  */
 int softmax_get_status(void* stream);
 

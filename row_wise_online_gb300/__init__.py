@@ -39,7 +39,7 @@ EXPORTED = (
     "softmax_rows", "softmax_rows_ex", "softmax_row_state", "merge_states", "softmax_rows_host",
     "softmax_get_status", "softmax_status_string", "softmax_last_cuda_error", "softmax_last_variant",
     "softmax_debug_set_fault", "softmax_debug_set_wait_limit_ns", "softmax_rows_splitrow_noalloc",
-    "softmax_rows_causal",
+    "softmax_rows_causal", "log_softmax_rows", "cross_entropy_rows",
 )
 
 
@@ -81,10 +81,13 @@ def capi() -> ctypes.CDLL:
         lib.softmax_debug_set_wait_limit_ns.argtypes = [i64]
         lib.softmax_rows_splitrow_noalloc.argtypes = [vp, vp, fp, fp, fp, i64, i64, ci, vp]
         lib.softmax_rows_causal.argtypes = [vp, vp, fp, fp, fp, i64, i64, i64, i64, ci, vp]
+        lib.log_softmax_rows.argtypes = [vp, vp, fp, fp, fp, i64, i64, ci, ci, vp]
+        lib.cross_entropy_rows.argtypes = [vp, vp, fp, fp, i64, i64, ci, vp]
         lib.softmax_debug_set_wait_limit_ns.restype = i64
         for name in ("softmax_rows", "softmax_rows_ex", "softmax_row_state", "merge_states",
                      "softmax_rows_host", "softmax_get_status", "softmax_last_variant",
-                     "softmax_debug_set_fault", "softmax_rows_splitrow_noalloc", "softmax_rows_causal"):
+                     "softmax_debug_set_fault", "softmax_rows_splitrow_noalloc", "softmax_rows_causal",
+                     "log_softmax_rows", "cross_entropy_rows"):
             getattr(lib, name).restype = ci
         _lib = lib
     return _lib
@@ -194,6 +197,41 @@ def softmax_rows_causal(x, q_period: int, key_offset: int = 0, y=None, m_out=Non
                                     M, N, int(q_period), int(key_offset), _dtype_code(x), _stream(stream))
     _check(st, "softmax_rows_causal")
     return y
+
+
+def log_softmax_rows(x, y=None, m_out=None, d_out=None, lse_out=None, variant: int = VARIANT_AUTO, stream=None):
+    """y = log softmax(x) = x - LSE along the last dimension, optionally with per-row m, d, LSE (fp32)."""
+    import torch
+
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor")
+    M, N = _rows(x)
+    if y is None:
+        y = torch.empty_like(x)
+    if y.shape != x.shape or y.dtype != x.dtype or not y.is_cuda or not y.is_contiguous():
+        raise ValueError("y must be a contiguous CUDA tensor with x's shape and dtype")
+    st = capi().log_softmax_rows(_ptr(x), _ptr(y), _ptr(_state_out(m_out, M, "m_out")),
+                                 _ptr(_state_out(d_out, M, "d_out")), _ptr(_state_out(lse_out, M, "lse_out")),
+                                 M, N, _dtype_code(x), int(variant), _stream(stream))
+    _check(st, "log_softmax_rows")
+    return y
+
+
+def cross_entropy_rows(x, labels, loss=None, lse_out=None, stream=None):
+    """Per-row cross-entropy loss LSE_r - x[r, labels[r]] (fp32); labels int64, negative = ignored row (loss 0)."""
+    import torch
+
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor")
+    M, N = _rows(x)
+    if labels.dtype != torch.int64 or labels.numel() != M or not labels.is_contiguous() or not labels.is_cuda:
+        raise ValueError(f"labels must be a contiguous CUDA int64 tensor of {M} entries")
+    if loss is None:
+        loss = torch.empty(M, dtype=torch.float32, device=x.device)
+    st = capi().cross_entropy_rows(_ptr(x), _ptr(labels), _ptr(_state_out(loss, M, "loss")),
+                                   _ptr(_state_out(lse_out, M, "lse_out")), M, N, _dtype_code(x), _stream(stream))
+    _check(st, "cross_entropy_rows")
+    return loss
 
 
 def softmax_row_state(x, m_out=None, d_out=None, lse_out=None, stream=None):

@@ -177,6 +177,25 @@ int run_variant(RowProblem& p, int variant, const DeviceInfo& dev) {
   return SOFTMAX_OK;
 }
 
+// Row state only (optionally with the cross-entropy loss): the CTA bulk-copy kernel, whose copy
+// ring keeps the next rows' reads in flight while a row is reduced, for aligned rows it holds;
+// the two-pass kernel's first pass otherwise.
+int run_state_only(RowProblem& p, const DeviceInfo& dev) {
+  const bool aligned = aligned16(p.x) && (p.N * elem_bytes(p.dtype)) % 16 == 0;
+  cudaError_t err;
+  int variant;
+  if (aligned && oneread_tma_fits(p, dev)) {
+    err = launch_oneread_tma(p, dev);
+    variant = SOFTMAX_VARIANT_ONEREAD_SMEM;
+  } else {
+    err = launch_twopass(p, aligned, dev);
+    variant = SOFTMAX_VARIANT_TWOPASS;
+  }
+  if (err != cudaSuccess) return cuda_fail(err);
+  t_last_variant = variant;
+  return SOFTMAX_OK;
+}
+
 }  // namespace
 
 int current_device(const DeviceInfo** out) { return current_device_info(out); }
@@ -268,6 +287,80 @@ int softmax_rows_causal(const void* x, void* y, float* m_out, float* d_out, floa
   return SOFTMAX_OK;
 }
 
+int log_softmax_rows(const void* x, void* y, float* m_out, float* d_out, float* lse_out, int64_t M, int64_t N,
+                     int dtype, int variant, void* stream) {
+  bool noop = false;
+  int st = validate_rows(x, M, N, dtype, &noop);
+  if (st != SOFTMAX_OK) return st;
+  if (variant < SOFTMAX_VARIANT_AUTO || variant > SOFTMAX_VARIANT_SPLITROW) return SOFTMAX_ERR_INVALID_ARG;
+  if (noop) return SOFTMAX_OK;
+  if (!y) return SOFTMAX_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  if ((st = current_device_info(&dev)) != SOFTMAX_OK) return st;
+  RowProblem p;
+  p.x = x;
+  p.y = y;
+  p.m_out = m_out;
+  p.d_out = d_out;
+  p.lse_out = lse_out;
+  p.M = M;
+  p.N = N;
+  p.dtype = dtype;
+  p.log_out = true;
+  p.stream = static_cast<cudaStream_t>(stream);
+  const bool aligned = aligned16(x) && aligned16(y) && (N * elem_bytes(dtype)) % 16 == 0;
+  const int64_t row_bytes = N * elem_bytes(dtype);
+  if (variant == SOFTMAX_VARIANT_AUTO) {  // the softmax choice, without the warp and split kernels
+    if (aligned)
+      variant = row_bytes <= 16384 && oneread_reg_fits(p, true) ? SOFTMAX_VARIANT_ONEREAD_REG
+                : oneread_tma_fits(p, *dev)                     ? SOFTMAX_VARIANT_ONEREAD_SMEM
+                                                                : SOFTMAX_VARIANT_TWOPASS;
+    else
+      variant = (N <= 512 && oneread_reg_fits(p, false)) ? SOFTMAX_VARIANT_ONEREAD_REG : SOFTMAX_VARIANT_TWOPASS;
+  }
+  cudaError_t err;
+  switch (variant) {
+    case SOFTMAX_VARIANT_ONEREAD_REG:
+      if (!oneread_reg_fits(p, aligned)) return SOFTMAX_ERR_UNSUPPORTED;
+      err = launch_oneread_reg(p, aligned, *dev);
+      break;
+    case SOFTMAX_VARIANT_ONEREAD_SMEM:
+      if (!aligned) return SOFTMAX_ERR_MISALIGNED;
+      if (!oneread_tma_fits(p, *dev)) return SOFTMAX_ERR_UNSUPPORTED;
+      err = launch_oneread_tma(p, *dev);
+      break;
+    case SOFTMAX_VARIANT_TWOPASS:
+      err = launch_twopass(p, aligned, *dev);
+      break;
+    default:  // SOFTMAX_VARIANT_SPLITROW
+      return SOFTMAX_ERR_UNSUPPORTED;
+  }
+  if (err != cudaSuccess) return cuda_fail(err);
+  t_last_variant = variant;
+  return SOFTMAX_OK;
+}
+
+int cross_entropy_rows(const void* x, const int64_t* labels, float* loss, float* lse_out, int64_t M, int64_t N,
+                       int dtype, void* stream) {
+  bool noop = false;
+  int st = validate_rows(x, M, N, dtype, &noop);
+  if (st != SOFTMAX_OK) return st;
+  if (noop) return SOFTMAX_OK;
+  if (!labels || !loss) return SOFTMAX_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  if ((st = current_device_info(&dev)) != SOFTMAX_OK) return st;
+  RowProblem p;
+  p.x = x;
+  p.lse_out = lse_out;
+  p.M = M;
+  p.N = N;
+  p.dtype = dtype;
+  p.labels = labels;
+  p.loss = loss;
+  p.stream = static_cast<cudaStream_t>(stream);
+  return run_state_only(p, *dev);
+}
+
 int softmax_row_state(const void* x, float* m_out, float* d_out, float* lse_out, int64_t M, int64_t N,
                       int dtype, void* stream) {
   bool noop = false;
@@ -286,11 +379,7 @@ int softmax_row_state(const void* x, float* m_out, float* d_out, float* lse_out,
   p.N = N;
   p.dtype = dtype;
   p.stream = static_cast<cudaStream_t>(stream);
-  const bool aligned = aligned16(x) && (N * elem_bytes(dtype)) % 16 == 0;
-  cudaError_t err = launch_twopass(p, aligned, *dev);
-  if (err != cudaSuccess) return cuda_fail(err);
-  t_last_variant = SOFTMAX_VARIANT_TWOPASS;
-  return SOFTMAX_OK;
+  return run_state_only(p, *dev);
 }
 
 int merge_states(const float* m_a, const float* d_a, const float* m_b, const float* d_b, float* m_out,
@@ -417,6 +506,7 @@ int softmax_get_status(void* stream) {
   if (err == cudaSuccess) err = cudaStreamSynchronize(s);
   if (err != cudaSuccess) return cuda_fail(err);
   if (word & kStatusTimeout) return SOFTMAX_ERR_TIMEOUT;
+  if (word & kStatusBadLabel) return SOFTMAX_ERR_INVALID_ARG;
   return SOFTMAX_OK;
 }
 

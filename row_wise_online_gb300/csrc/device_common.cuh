@@ -46,6 +46,27 @@ __device__ __forceinline__ float2 exp_diff2(float2 a, float2 neg_b) {
 
 __device__ __forceinline__ float safe_max(float m) { return m == -INFINITY ? 0.f : m; }
 
+// Sum of e^(x - m) over pairs, with one packed fused multiply-add per pair for the exponent:
+// fma(x, log2 e, -mc) where mc = m log2 e rounded.  The exact value of that fma is
+// (x - m) log2 e + delta with delta = m log2 e - mc, the same for every term, so the sum comes
+// out scaled by 2^delta; delta is exact (fma(m, log2 e, -mc)) and the scale is removed at the
+// end.  Only for |m| < 2^20, where |delta| <= 1/16 and 2^-delta is accurate; the caller uses
+// the difference form (exp_diff2) otherwise.  m must be an m_safe (finite).
+struct ExpShift {
+  float2 log2e2, neg_mc2;
+  float unscale;  // 2^-delta
+};
+__device__ __forceinline__ ExpShift exp_shift(float m) {
+  const float mc = __fmul_rn(m, kLog2e);
+  const float delta = __fmaf_rn(m, kLog2e, -mc);
+  return ExpShift{make_float2(kLog2e, kLog2e), make_float2(-mc, -mc), ex2(-delta)};
+}
+__device__ __forceinline__ float2 exp_shifted2(float2 x, const ExpShift& s) {
+  const float2 t = __ffma2_rn(x, s.log2e2, s.neg_mc2);
+  return make_float2(ex2(t.x), ex2(t.y));
+}
+__device__ __forceinline__ bool exp_shift_ok(float m) { return fabsf(m) < 0x1p20f; }
+
 struct State {
   float m;  // running maximum (raw input units)
   float d;  // sum of e^(x - m) over the folded elements
@@ -105,11 +126,63 @@ __device__ __forceinline__ State group_merge(State s, State* slots, int nwarps, 
   return t;
 }
 
+// The same merges taken n-ary instead of pairwise: m = max_i m_i first (a max butterfly), then
+// d = sum_i d_i e^(m_i - m) (one rescale per lane, a sum butterfly).  This is the merge formula
+// applied to all parts at once -- equal to the pairwise tree up to the order of the additions --
+// at one exponential per lane instead of two per round.
+__device__ __forceinline__ State warp_merge_nary(State s) {
+  float m = s.m;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float d = __fmul_rn(s.d, exp_diff(s.m, safe_max(m)));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) d = __fadd_rn(d, __shfl_xor_sync(0xffffffffu, d, o));
+  return State{m, d};
+}
+
+template <class Sync>
+__device__ __forceinline__ State group_merge_nary(State s, State* slots, int nwarps, int warp, int lane,
+                                                  Sync sync) {
+  s = warp_merge_nary(s);
+  if (nwarps == 1) return s;
+  if (lane == 0) slots[warp] = s;
+  sync();
+  int p = 1;
+  while (p < nwarps) p <<= 1;
+  const int i = lane & (p - 1);
+  const State t = i < nwarps ? slots[i] : empty_state();
+  float m = t.m;
+  for (int o = p >> 1; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float d = __fmul_rn(t.d, exp_diff(t.m, safe_max(m)));
+  for (int o = p >> 1; o > 0; o >>= 1) d = __fadd_rn(d, __shfl_xor_sync(0xffffffffu, d, o));
+  return State{m, d};
+}
+
 // 1/d, with 0 for an empty row (d = 0) so that y = 0 there instead of 0 * inf.
 __device__ __forceinline__ float safe_inv(float d) { return d > 0.f ? __frcp_rn(d) : 0.f; }
 
 __device__ __forceinline__ float lse_of(State s) {
   return s.m == -INFINITY ? -INFINITY : s.m + logf(s.d);
+}
+
+// log y_j = x_j - LSE, evaluated as (x_j - m) - ln d: the difference x_j - m is exact for the
+// entries near the maximum (the ones that matter), so only ln d and the last subtraction round.
+// An empty row (d = 0) gives ln d = +inf, so every entry becomes -inf (log 0).
+struct LogNorm {
+  float ms;   // m_safe
+  float lnd;  // ln d
+};
+__device__ __forceinline__ LogNorm log_norm(State s) {
+  return LogNorm{safe_max(s.m), s.d > 0.f ? logf(s.d) : INFINITY};
+}
+__device__ __forceinline__ float log_prob(float x, LogNorm n) { return __fsub_rn(__fsub_rn(x, n.ms), n.lnd); }
+
+// Cross-entropy loss -log p_label = (m - x_label) + ln d, in the order the page's
+// cross_entropy_loss takes it (logits - max first): m - x_label is exact when the two are close,
+// so a large |m| costs no cancellation, as LSE - x_label would.  An all -inf row gives NaN.
+__device__ __forceinline__ float ce_loss(State s, float x_label) {
+  if (s.m == -INFINITY) return __int_as_float(0x7fc00000);
+  return __fadd_rn(__fsub_rn(s.m, x_label), logf(s.d));
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -157,10 +230,24 @@ struct F32 {
   __device__ static __forceinline__ float load1(const void* p, int64_t i) {
     return __ldg(static_cast<const float*>(p) + i);
   }
+  // Element i of a row staged in shared memory at address `slot`.
+  __device__ static __forceinline__ float lds1(uint32_t slot, int64_t i) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(slot + uint32_t(i) * 4u) : "memory");
+    return v;
+  }
   // Largest of the vector's four values.
   __device__ static __forceinline__ float vmax(const uint4& v) {
     return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
                  fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+  }
+  // Largest value of n vectors.
+  template <int n>
+  __device__ static __forceinline__ float vmax_all(const uint4 (&q)[n]) {
+    float m = vmax(q[0]);
+#pragma unroll
+    for (int k = 1; k < n; ++k) m = fmaxf(m, vmax(q[k]));
+    return m;
   }
   __device__ static __forceinline__ void store1(void* p, int64_t i, float v) {
     static_cast<float*>(p)[i] = v;
@@ -199,6 +286,11 @@ struct BF16 {
     const unsigned short b = __ldg(static_cast<const unsigned short*>(p) + i);
     return __uint_as_float(static_cast<uint32_t>(b) << 16);
   }
+  __device__ static __forceinline__ float lds1(uint32_t slot, int64_t i) {
+    unsigned short b;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(b) : "r"(slot + uint32_t(i) * 2u) : "memory");
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+  }
   // Largest of the vector's eight values: packed bf16x2 max (exact), then one widening.
   __device__ static __forceinline__ float vmax(const uint4& v) {
     uint32_t a, b, m;
@@ -206,6 +298,19 @@ struct BF16 {
     asm("max.bf16x2 %0, %1, %2;" : "=r"(b) : "r"(v.z), "r"(v.w));
     asm("max.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(a), "r"(b));
     return fmaxf(bf16_lo(m), bf16_hi(m));
+  }
+  // Largest value of n vectors: a packed bf16x2 max over all their words, then one widening.
+  template <int n>
+  __device__ static __forceinline__ float vmax_all(const uint4 (&q)[n]) {
+    uint32_t w[4] = {q[0].x, q[0].y, q[0].z, q[0].w};
+#pragma unroll
+    for (int k = 1; k < n; ++k) {
+      asm("max.bf16x2 %0, %0, %1;" : "+r"(w[0]) : "r"(q[k].x));
+      asm("max.bf16x2 %0, %0, %1;" : "+r"(w[1]) : "r"(q[k].y));
+      asm("max.bf16x2 %0, %0, %1;" : "+r"(w[2]) : "r"(q[k].z));
+      asm("max.bf16x2 %0, %0, %1;" : "+r"(w[3]) : "r"(q[k].w));
+    }
+    return vmax(make_uint4(w[0], w[1], w[2], w[3]));
   }
   __device__ static __forceinline__ void store1(void* p, int64_t i, float v) {
     static_cast<uint16_t*>(p)[i] = to_bf16(v);

@@ -36,12 +36,20 @@ struct TmaArgs {
   int stages;
   unsigned* status;
   uint64_t wait_ns;
+  const int64_t* labels;  // state-only mode: cross-entropy labels, or null
+  float* loss;
 };
 
 constexpr int kSlotAlign = 128;
 
-template <class D, int VPT, int NCW>
+// What the kernel writes besides the row state: y = softmax, y = log softmax, or nothing (the
+// row state alone, optionally the cross-entropy loss).
+enum TmaOut { kTmaProb = 0, kTmaLog = 1, kTmaState = 2 };
+
+template <class D, int VPT, int NCW, int OUT>
 __global__ void __launch_bounds__((NCW + 1) * 32) k_oneread_tma(TmaArgs a) {
+  constexpr bool LOG = OUT == kTmaLog;
+  constexpr bool WRITE_Y = OUT != kTmaState;
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int E = D::kVec;
   constexpr int NCT = NCW * 32;
@@ -90,56 +98,129 @@ __global__ void __launch_bounds__((NCW + 1) * 32) k_oneread_tma(TmaArgs a) {
   bool timed_out = false;
   for (int64_t j = 0; j < nrows; ++j) {
     const int s = int(j % S);
+    // cross entropy: thread 0 fetches the label before the row arrives
+    int64_t label = -1;
+    if constexpr (OUT == kTmaState) {
+      if (a.loss && tid == 0) label = a.labels[blockIdx.x + j * gridDim.x];
+    }
     if (!mbar_wait(smem_addr(&full[s]), uint32_t((j / S) & 1), a.wait_ns)) timed_out = true;
     const uint32_t slot = smem_addr(slots + size_t(s) * a.slot_bytes);
+    float x_label = 0.f;  // the labelled entry, read from the staged row before the slot is freed
+    if constexpr (OUT == kTmaState) {
+      if (a.loss && tid == 0 && label >= 0 && label < a.N) x_label = D::lds1(slot, label);
+    }
 
     // copy this thread's part of the row into registers and hand the slot back at once
-    float v[VPT][E];
+    float mt = -INFINITY, dt = 0.f;
+    float v[WRITE_Y ? VPT : 1][E];  // values kept for the normalisation (not in state-only mode)
+    if constexpr (WRITE_Y) {
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      const int u = tid + k * NCT;
-      if (u < nunits) {
-        D::unpack(lds16(slot + uint32_t(u) * 16u), v[k]);
+      for (int k = 0; k < VPT; ++k) {
+        const int u = tid + k * NCT;
+        if (u < nunits) {
+          D::unpack(lds16(slot + uint32_t(u) * 16u), v[k]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < E; ++e) v[k][e] = -INFINITY;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&freed[s]));
+
+#pragma unroll
+      for (int k = 0; k < VPT; ++k)
+#pragma unroll
+        for (int e = 0; e < E; ++e) mt = fmaxf(mt, v[k][e]);
+      const float mts = safe_max(mt);
+#pragma unroll
+      for (int k = 0; k < VPT; ++k)
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          if constexpr (LOG) {  // x stays in registers for y = (x - m) - ln d
+            dt += exp_diff(v[k][e], mts);
+          } else {
+            v[k][e] = exp_diff(v[k][e], mts);
+            dt += v[k][e];
+          }
+        }
+    } else {
+      // state only: keep the packed vectors, take the max on them (packed bf16 max), then the
+      // exponentials in pairs (packed f32x2 add and multiply)
+      uint4 q[VPT];
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int u = tid + k * NCT;
+        q[k] = u < nunits ? lds16(slot + uint32_t(u) * 16u)
+                          : make_uint4(D::kNegInfWord, D::kNegInfWord, D::kNegInfWord, D::kNegInfWord);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&freed[s]));
+      mt = D::vmax_all(q);
+      const float mts = safe_max(mt);
+      float2 acc = make_float2(0.f, 0.f);
+      if (exp_shift_ok(mts)) {
+        const ExpShift sh = exp_shift(mts);
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+          float2 f[E / 2];
+          D::unpack2(q[k], f);
+#pragma unroll
+          for (int e = 0; e < E / 2; ++e) acc = __fadd2_rn(acc, exp_shifted2(f[e], sh));
+        }
+        dt = __fmul_rn(__fadd_rn(acc.x, acc.y), sh.unscale);
       } else {
+        const float2 nms = make_float2(-mts, -mts);
 #pragma unroll
-        for (int e = 0; e < E; ++e) v[k][e] = -INFINITY;
+        for (int k = 0; k < VPT; ++k) {
+          float2 f[E / 2];
+          D::unpack2(q[k], f);
+#pragma unroll
+          for (int e = 0; e < E / 2; ++e) acc = __fadd2_rn(acc, exp_diff2(f[e], nms));
+        }
+        dt = __fadd_rn(acc.x, acc.y);
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&freed[s]));
-
-    float mt = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < VPT; ++k)
-#pragma unroll
-      for (int e = 0; e < E; ++e) mt = fmaxf(mt, v[k][e]);
-    const float mts = safe_max(mt);
-    float dt = 0.f;
-#pragma unroll
-    for (int k = 0; k < VPT; ++k)
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        v[k][e] = exp_diff(v[k][e], mts);
-        dt += v[k][e];
-      }
-    const State st = group_merge(State{mt, dt}, wstate + (j & 1) * NCW, NCW, warp, lane,
-                                 [] { named_barrier_sync(1, NCT); });
-    const float scale = __fmul_rn(exp_diff(mt, safe_max(st.m)), safe_inv(st.d));
+    State st;
+    if constexpr (WRITE_Y)
+      st = group_merge(State{mt, dt}, wstate + (j & 1) * NCW, NCW, warp, lane, [] { named_barrier_sync(1, NCT); });
+    else
+      st = group_merge_nary(State{mt, dt}, wstate + (j & 1) * NCW, NCW, warp, lane,
+                            [] { named_barrier_sync(1, NCT); });
     const int64_t row = blockIdx.x + j * gridDim.x;
-    unsigned char* yr = a.y + row * a.row_bytes;
+    if constexpr (WRITE_Y) {
+      float scale = 0.f;
+      LogNorm ln{};
+      if constexpr (LOG) ln = log_norm(st);
+      else scale = __fmul_rn(exp_diff(mt, safe_max(st.m)), safe_inv(st.d));
+      unsigned char* yr = a.y + row * a.row_bytes;
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      const int u = tid + k * NCT;
-      if (u < nunits) {
+      for (int k = 0; k < VPT; ++k) {
+        const int u = tid + k * NCT;
+        if (u < nunits) {
 #pragma unroll
-        for (int e = 0; e < E; ++e) v[k][e] = __fmul_rn(v[k][e], scale);
-        st_stream16(yr + int64_t(u) * 16, D::pack(v[k]));
+          for (int e = 0; e < E; ++e) v[k][e] = LOG ? log_prob(v[k][e], ln) : __fmul_rn(v[k][e], scale);
+          st_stream16(yr + int64_t(u) * 16, D::pack(v[k]));
+        }
       }
     }
     if (tid == 0) {
       if (a.m_out) a.m_out[row] = st.m;
       if (a.d_out) a.d_out[row] = st.d;
       if (a.lse_out) a.lse_out[row] = lse_of(st);
+      if constexpr (OUT == kTmaState) {
+        // cross entropy ("从原始Softmax到在线Softmax", "交叉熵损失计算"); negative label: ignored
+        // row (0); label >= N: NaN and a status bit, x not read
+        if (a.loss) {
+          float l = 0.f;
+          if (label >= a.N) {
+            l = __int_as_float(0x7fc00000);
+            atomicOr(a.status, kStatusBadLabel);
+          } else if (label >= 0) {
+            l = ce_loss(st, x_label);
+          }
+          a.loss[row] = l;
+        }
+      }
     }
   }
   if (timed_out && lane == 0) atomicOr(a.status, kStatusTimeout);
@@ -149,12 +230,15 @@ using TmaKernel = void (*)(TmaArgs);
 
 struct TmaConfig {
   int ncw, vpt;
-  TmaKernel f32, bf16;
+  TmaKernel fn[3][2];  // [output mode][dtype]
 };
 
 template <int VPT, int NCW>
 constexpr TmaConfig tma_cfg() {
-  return TmaConfig{NCW, VPT, k_oneread_tma<F32, VPT, NCW>, k_oneread_tma<BF16, VPT, NCW>};
+  return TmaConfig{NCW, VPT,
+                   {{k_oneread_tma<F32, VPT, NCW, kTmaProb>, k_oneread_tma<BF16, VPT, NCW, kTmaProb>},
+                    {k_oneread_tma<F32, VPT, NCW, kTmaLog>, k_oneread_tma<BF16, VPT, NCW, kTmaLog>},
+                    {k_oneread_tma<F32, VPT, NCW, kTmaState>, k_oneread_tma<BF16, VPT, NCW, kTmaState>}}};
 }
 
 // Ordered by capacity (16-byte units per row = 32 * ncw * vpt).
@@ -218,7 +302,9 @@ bool oneread_tma_fits(const RowProblem& p, const DeviceInfo& dev) {
 cudaError_t launch_oneread_tma(const RowProblem& p, const DeviceInfo& dev) {
   const TmaPlan plan = plan_tma(p, dev);
   if (!plan.cfg) return cudaErrorInvalidValue;
-  TmaKernel fn = p.dtype == 0 ? plan.cfg->f32 : plan.cfg->bf16;
+  const int out = p.y == nullptr ? kTmaState : p.log_out ? kTmaLog : kTmaProb;
+  if (p.loss && out != kTmaState) return cudaErrorInvalidValue;
+  TmaKernel fn = plan.cfg->fn[out][p.dtype == 0 ? 0 : 1];
   cudaError_t err = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(plan.smem));
   if (err != cudaSuccess) return err;
@@ -232,7 +318,7 @@ cudaError_t launch_oneread_tma(const RowProblem& p, const DeviceInfo& dev) {
   const int grid = int(p.M < cap ? p.M : cap);
   TmaArgs a{static_cast<const unsigned char*>(p.x), static_cast<unsigned char*>(p.y), p.m_out,
             p.d_out, p.lse_out, p.M, p.N, uint32_t(p.N * elem_bytes(p.dtype)), plan.slot_bytes,
-            plan.stages, dev.status, local_wait_limit_ns()};
+            plan.stages, dev.status, local_wait_limit_ns(), p.labels, p.loss};
   fn<<<grid, threads, plan.smem, p.stream>>>(a);
   return cudaGetLastError();
 }

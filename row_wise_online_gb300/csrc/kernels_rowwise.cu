@@ -31,8 +31,11 @@ struct RowArgs {
   float* lse_out;
   int64_t M;
   int64_t N;
-  int64_t q_period;    // causal rule (two-pass CAUSAL only): row r keeps its first
+  int64_t q_period;    // causal rule (two-pass causal mode only): row r keeps its first
   int64_t key_offset;  // clamp(r % q_period + 1 + key_offset, 0, N) entries
+  const int64_t* labels;  // cross entropy (two-pass state mode only), else null
+  float* loss;
+  unsigned* status;
 };
 
 __device__ __forceinline__ void write_state(const RowArgs& a, int64_t row, State s) {
@@ -41,13 +44,31 @@ __device__ __forceinline__ void write_state(const RowArgs& a, int64_t row, State
   if (a.lse_out) a.lse_out[row] = lse_of(s);
 }
 
+// Cross entropy of row `row` against its label ("从原始Softmax到在线Softmax", section
+// "交叉熵损失计算": loss = -log p_label).  A negative label marks a row to
+// ignore (loss 0); a label >= N gives NaN and sets kStatusBadLabel, without reading x there.
+template <class D>
+__device__ __forceinline__ void write_loss(const RowArgs& a, int64_t row, const unsigned char* xr, State s) {
+  const int64_t label = a.labels[row];
+  float l;
+  if (label < 0) {
+    l = 0.f;
+  } else if (label >= a.N) {
+    l = __int_as_float(0x7fc00000);
+    atomicOr(a.status, kStatusBadLabel);
+  } else {
+    l = ce_loss(s, D::load1(xr, label));
+  }
+  a.loss[row] = l;
+}
+
 // ------------------------------------------------------------------------------------------
 // Register one-read kernel
 // ------------------------------------------------------------------------------------------
 
 constexpr int kRegThreads = 256;
 
-template <class D, int VPT, int WPR, bool VEC>
+template <class D, int VPT, int WPR, bool VEC, bool LOG>
 __global__ void __launch_bounds__(kRegThreads) k_oneread_reg(RowArgs a) {
   constexpr int E = VEC ? D::kVec : 1;  // elements per unit (one 16-byte vector, or one element)
   constexpr int G = (kRegThreads / 32) / WPR;  // row groups per CTA
@@ -90,19 +111,26 @@ __global__ void __launch_bounds__(kRegThreads) k_oneread_reg(RowArgs a) {
     for (int k = 0; k < VPT; ++k)
 #pragma unroll
       for (int e = 0; e < E; ++e) {
-        v[k][e] = exp_diff(v[k][e], mts);
-        dt += v[k][e];
+        if constexpr (LOG) {  // x stays in registers for y = (x - m) - ln d
+          dt += exp_diff(v[k][e], mts);
+        } else {
+          v[k][e] = exp_diff(v[k][e], mts);
+          dt += v[k][e];
+        }
       }
     const State s = group_merge(State{mt, dt}, &slots[it & 1][g * WPR], WPR, wig, lane,
                                 [&] { named_barrier_sync(1 + g, GT); });
-    const float scale = __fmul_rn(exp_diff(mt, safe_max(s.m)), safe_inv(s.d));
+    float scale = 0.f;
+    LogNorm ln{};
+    if constexpr (LOG) ln = log_norm(s);
+    else scale = __fmul_rn(exp_diff(mt, safe_max(s.m)), safe_inv(s.d));
     unsigned char* yr = a.y + row * row_bytes;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int64_t u = gt + (int64_t)k * GT;
       if (u < nunits) {
 #pragma unroll
-        for (int e = 0; e < E; ++e) v[k][e] = __fmul_rn(v[k][e], scale);
+        for (int e = 0; e < E; ++e) v[k][e] = LOG ? log_prob(v[k][e], ln) : __fmul_rn(v[k][e], scale);
         if constexpr (VEC) {
           st_stream16(yr + u * 16, D::pack(v[k]));
         } else {
@@ -118,12 +146,13 @@ using RowKernel = void (*)(RowArgs);
 
 struct RegConfig {
   int wpr, vpt;
-  RowKernel f32, bf16;
+  RowKernel f32, bf16, f32_log, bf16_log;
 };
 
 template <int VPT, int WPR, bool VEC>
 constexpr RegConfig reg_cfg() {
-  return RegConfig{WPR, VPT, k_oneread_reg<F32, VPT, WPR, VEC>, k_oneread_reg<BF16, VPT, WPR, VEC>};
+  return RegConfig{WPR, VPT, k_oneread_reg<F32, VPT, WPR, VEC, false>, k_oneread_reg<BF16, VPT, WPR, VEC, false>,
+                   k_oneread_reg<F32, VPT, WPR, VEC, true>, k_oneread_reg<BF16, VPT, WPR, VEC, true>};
 }
 
 // Ordered by capacity (units per row = 32 * wpr * vpt).
@@ -152,9 +181,9 @@ int blocks_per_sm(const void* fn, int threads, size_t smem) {
   return n < 1 ? 1 : n;
 }
 
-RowArgs row_args(const RowProblem& p) {
+RowArgs row_args(const RowProblem& p, const DeviceInfo& dev) {
   return RowArgs{static_cast<const unsigned char*>(p.x), static_cast<unsigned char*>(p.y),
-                 p.m_out, p.d_out, p.lse_out, p.M, p.N, 1, 0};
+                 p.m_out, p.d_out, p.lse_out, p.M, p.N, 1, 0, p.labels, p.loss, dev.status};
 }
 
 // ------------------------------------------------------------------------------------------
@@ -180,8 +209,14 @@ __device__ __forceinline__ void load_unit(const unsigned char* xr, int64_t u, in
   }
 }
 
-template <class D, bool VEC, bool WRITE_Y, bool CAUSAL>
+// What the two-pass kernel writes.
+enum TwoPassMode { kProb = 0, kProbCausal = 1, kLogProb = 2, kStateOnly = 3 };
+
+template <class D, bool VEC, int MODE>
 __global__ void __launch_bounds__(kTwoPassMaxThreads) k_twopass(RowArgs a) {
+  constexpr bool WRITE_Y = MODE != kStateOnly;
+  constexpr bool CAUSAL = MODE == kProbCausal;
+  constexpr bool LOG = MODE == kLogProb;
   constexpr int E = VEC ? D::kVec : 1;
   constexpr int U = kTwoPassUnroll;
   __shared__ State slots[2][kTwoPassMaxThreads / 32];
@@ -243,6 +278,7 @@ __global__ void __launch_bounds__(kTwoPassMaxThreads) k_twopass(RowArgs a) {
       // pass 2: re-read and normalise
       const float ms = safe_max(s.m);
       const float inv = safe_inv(s.d);
+      const LogNorm ln = log_norm(s);
       unsigned char* yr = a.y + row * row_bytes;
       for (int64_t base = threadIdx.x; base < nunits; base += (int64_t)nt * U) {
         float v[U][E];
@@ -261,7 +297,7 @@ __global__ void __launch_bounds__(kTwoPassMaxThreads) k_twopass(RowArgs a) {
               }
             }
 #pragma unroll
-            for (int e = 0; e < E; ++e) v[k][e] = __fmul_rn(exp_diff(v[k][e], ms), inv);
+            for (int e = 0; e < E; ++e) v[k][e] = LOG ? log_prob(v[k][e], ln) : __fmul_rn(exp_diff(v[k][e], ms), inv);
             if constexpr (VEC) {
               st_stream16(yr + u * 16, D::pack(v[k]));
             } else {
@@ -271,7 +307,12 @@ __global__ void __launch_bounds__(kTwoPassMaxThreads) k_twopass(RowArgs a) {
         }
       }
     }
-    if (threadIdx.x == 0) write_state(a, row, s);
+    if (threadIdx.x == 0) {
+      write_state(a, row, s);
+      if constexpr (MODE == kStateOnly) {
+        if (a.loss) write_loss<D>(a, row, xr, s);
+      }
+    }
   }
 }
 
@@ -304,12 +345,12 @@ cudaError_t launch_oneread_reg(const RowProblem& p, bool vec, const DeviceInfo& 
   const int64_t e = vec ? 16 / elem_bytes(p.dtype) : 1;
   const RegConfig* cfg = pick_reg(p.N / e, vec);
   if (!cfg) return cudaErrorInvalidValue;
-  RowKernel fn = p.dtype == 0 ? cfg->f32 : cfg->bf16;
+  RowKernel fn = p.dtype == 0 ? (p.log_out ? cfg->f32_log : cfg->f32) : (p.log_out ? cfg->bf16_log : cfg->bf16);
   const int groups = (kRegThreads / 32) / cfg->wpr;
   const int64_t want = ceil_div(p.M, groups);
   const int64_t cap = int64_t(dev.sm_count) * blocks_per_sm((const void*)fn, kRegThreads, 0);
   const int grid = int(want < cap ? want : cap);
-  fn<<<grid, kRegThreads, 0, p.stream>>>(row_args(p));
+  fn<<<grid, kRegThreads, 0, p.stream>>>(row_args(p, dev));
   return cudaGetLastError();
 }
 
@@ -320,22 +361,23 @@ cudaError_t launch_twopass(const RowProblem& p, bool vec, const DeviceInfo& dev,
   const int64_t units = p.N / e;
   int nt = 128;
   while (nt < kTwoPassMaxThreads && int64_t(nt) * kTwoPassUnroll < units) nt *= 2;
-  const bool write_y = p.y != nullptr;
   const bool causal = q_period > 0;
-  // [dtype][vec][write_y][causal]
-  static const RowKernel table[2][2][2][2] = {
-      {{{k_twopass<F32, false, false, false>, k_twopass<F32, false, false, true>},
-        {k_twopass<F32, false, true, false>, k_twopass<F32, false, true, true>}},
-       {{k_twopass<F32, true, false, false>, k_twopass<F32, true, false, true>},
-        {k_twopass<F32, true, true, false>, k_twopass<F32, true, true, true>}}},
-      {{{k_twopass<BF16, false, false, false>, k_twopass<BF16, false, false, true>},
-        {k_twopass<BF16, false, true, false>, k_twopass<BF16, false, true, true>}},
-       {{k_twopass<BF16, true, false, false>, k_twopass<BF16, true, false, true>},
-        {k_twopass<BF16, true, true, false>, k_twopass<BF16, true, true, true>}}}};
-  RowKernel fn = table[p.dtype == 0 ? 0 : 1][vec ? 1 : 0][write_y ? 1 : 0][causal ? 1 : 0];
+  const int mode = p.y == nullptr ? kStateOnly : causal ? kProbCausal : p.log_out ? kLogProb : kProb;
+  if ((causal && p.log_out) || (p.loss && mode != kStateOnly)) return cudaErrorInvalidValue;
+  // [dtype][vec][mode]
+  static const RowKernel table[2][2][4] = {
+      {{k_twopass<F32, false, kProb>, k_twopass<F32, false, kProbCausal>, k_twopass<F32, false, kLogProb>,
+        k_twopass<F32, false, kStateOnly>},
+       {k_twopass<F32, true, kProb>, k_twopass<F32, true, kProbCausal>, k_twopass<F32, true, kLogProb>,
+        k_twopass<F32, true, kStateOnly>}},
+      {{k_twopass<BF16, false, kProb>, k_twopass<BF16, false, kProbCausal>, k_twopass<BF16, false, kLogProb>,
+        k_twopass<BF16, false, kStateOnly>},
+       {k_twopass<BF16, true, kProb>, k_twopass<BF16, true, kProbCausal>, k_twopass<BF16, true, kLogProb>,
+        k_twopass<BF16, true, kStateOnly>}}};
+  RowKernel fn = table[p.dtype == 0 ? 0 : 1][vec ? 1 : 0][mode];
   const int64_t cap = int64_t(dev.sm_count) * blocks_per_sm((const void*)fn, nt, 0);
   const int grid = int(p.M < cap ? p.M : cap);
-  RowArgs a = row_args(p);
+  RowArgs a = row_args(p, dev);
   a.q_period = causal ? q_period : 1;
   a.key_offset = key_offset;
   fn<<<grid, nt, 0, p.stream>>>(a);

@@ -27,11 +27,15 @@ struct RowProblem {
   int64_t M = 0;
   int64_t N = 0;
   int dtype = 0;  // 0 = fp32, 1 = bf16
+  bool log_out = false;  // y = log-softmax instead of softmax (register, CTA bulk-copy, two-pass)
+  const int64_t* labels = nullptr;  // cross entropy (two-pass, no y): loss[r] = LSE_r - x_r[labels[r]]
+  float* loss = nullptr;
   cudaStream_t stream = nullptr;
 };
 
 // Status bits a kernel may set in the per-device status word.
 constexpr unsigned kStatusTimeout = 1u;
+constexpr unsigned kStatusBadLabel = 2u;  // a cross-entropy label >= N
 
 inline int elem_bytes(int dtype) { return dtype == 0 ? 4 : 2; }
 

@@ -74,6 +74,13 @@ def test_other_calls_argument_checks(lib):
     assert lib.softmax_rows_causal(X, X, None, None, None, 4, 4, 0, 0, 0, None) == rwo.ERR_INVALID_ARG  # period 0
     assert lib.softmax_rows_causal(X, NULL, None, None, None, 4, 4, 4, 0, 0, None) == rwo.ERR_INVALID_ARG
     assert lib.softmax_rows_causal(NULL, NULL, None, None, None, 0, 4, 4, 0, 0, None) == rwo.OK  # M = 0
+    assert lib.log_softmax_rows(X, NULL, None, None, None, 4, 4, 0, 0, None) == rwo.ERR_INVALID_ARG  # no y
+    assert lib.log_softmax_rows(X, X, None, None, None, 4, 4, 0, 5, None) == rwo.ERR_INVALID_ARG  # variant
+    assert lib.log_softmax_rows(NULL, NULL, None, None, None, 0, 4, 1, 0, None) == rwo.OK  # M = 0
+    assert lib.cross_entropy_rows(X, NULL, X, None, 4, 4, 0, None) == rwo.ERR_INVALID_ARG  # no labels
+    assert lib.cross_entropy_rows(X, X, None, None, 4, 4, 0, None) == rwo.ERR_INVALID_ARG  # no loss
+    assert lib.cross_entropy_rows(X, X, X, None, 4, 0, 0, None) == rwo.ERR_INVALID_ARG  # N = 0
+    assert lib.cross_entropy_rows(NULL, NULL, NULL, None, 0, 4, 0, None) == rwo.OK  # M = 0
 
 
 def test_status_strings(lib):

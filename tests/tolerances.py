@@ -10,6 +10,12 @@ Tolerances (per element, against the oracle's exact fp64 result y_ref):
   * LSE:         |LSE - LSE_ref| <= 1e-5 * max(1, |LSE_ref|)
 The 2^-126 floor admits results below the smallest normal fp32, which the hardware exponential
 flushes to zero.  Fully masked rows (all -inf) must give y = 0, m = -inf, d = 0, LSE = -inf.
+
+Log softmax and cross-entropy loss (values x_j - LSE and LSE - x_label; same arithmetic as LSE):
+  * fp32 log y:  |v - v_ref| <= 1e-5 * max(1, |v_ref|)
+  * bf16 log y:  |v - v_ref| <= ulp_bf16(v_ref) + 1e-5 * max(1, |v_ref|)
+  * loss (fp32): |l - l_ref| <= 1e-5 * max(1, |l_ref|)
+  -inf references (masked entries, log 0) must be -inf exactly; NaN references must be NaN.
 """
 from __future__ import annotations
 
@@ -86,3 +92,27 @@ def check_state(m, d, lse, m_ref, d_ref, lse_ref, what: str = "") -> None:
         assert np.all(np.isneginf(lse[~fin])), f"{what}: LSE of fully masked rows must be -inf"
         ok = np.abs(lse[fin] - lse_ref[fin]) <= LSE_REL * np.maximum(1.0, np.abs(lse_ref[fin]))
         assert np.all(ok), f"{what}: LSE off"
+
+
+def check_log_values(v: np.ndarray, v_ref: np.ndarray, dtype: int, what: str = "") -> float:
+    """Log-softmax values (dtype output) or losses (fp32) against fp64 references; returns max abs error."""
+    vg = output_as_f64(v, dtype)
+    assert vg.shape == v_ref.shape, (vg.shape, v_ref.shape)
+    ninf = np.isneginf(v_ref)
+    pinf = np.isposinf(v_ref)
+    nan = np.isnan(v_ref)
+    assert np.all(np.isneginf(vg[ninf])), f"{what}: -inf references must give -inf"
+    assert np.all(np.isposinf(vg[pinf])), f"{what}: +inf references must give +inf"
+    assert np.all(np.isnan(vg[nan])), f"{what}: NaN references must give NaN"
+    fin = ~(ninf | pinf | nan)
+    err = np.abs(vg[fin] - v_ref[fin])
+    bound = LSE_REL * np.maximum(1.0, np.abs(v_ref[fin]))
+    if dtype == synth.BF16:
+        bound = bound + bf16_ulp(v_ref[fin])
+    bad = ~(err <= bound)
+    if bad.any():
+        k = int(np.argmax(bad))
+        idx = tuple(np.argwhere(fin)[k])
+        raise AssertionError(f"{what}: {bad.sum()} values out of tolerance; first at {idx}: "
+                             f"v={vg[idx]!r} v_ref={v_ref[idx]!r}")
+    return float(err.max()) if err.size else 0.0
