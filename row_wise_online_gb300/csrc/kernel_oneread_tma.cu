@@ -77,14 +77,18 @@ __global__ void __launch_bounds__((NCW + 1) * 32) k_oneread_tma(TmaArgs a) {
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       bool timed_out = false;
+      int s = 0;         // slot of row j and the parity of its lap, kept incrementally (a 64-bit
+      uint32_t ph = 0;   // division per row would cost ~0.1 us of this lane's time)
       for (int64_t j = 0; j < nrows; ++j) {
-        const int s = int(j % S);
-        if (j >= S && !mbar_wait(smem_addr(&freed[s]), uint32_t(((j / S) - 1) & 1), a.wait_ns))
-          timed_out = true;
+        if (j >= S && !mbar_wait(smem_addr(&freed[s]), ph ^ 1u, a.wait_ns)) timed_out = true;
         const uint32_t bar = smem_addr(&full[s]);
         mbar_arrive_expect_tx(bar, a.row_bytes);
         const int64_t row = blockIdx.x + j * gridDim.x;
         bulk_g2s(smem_addr(slots + size_t(s) * a.slot_bytes), a.x + row * a.row_bytes, a.row_bytes, bar, pol);
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
       // Every load must have landed before the CTA may exit (the consumers normally saw them all).
       for (int64_t j = nrows > S ? nrows - S : 0; j < nrows; ++j)
@@ -96,14 +100,30 @@ __global__ void __launch_bounds__((NCW + 1) * 32) k_oneread_tma(TmaArgs a) {
 
   // ---------------- consumers ----------------
   bool timed_out = false;
+  int cs = 0;  // slot of row j and the parity of its lap (state-only mode)
+  uint32_t cph = 0;
   for (int64_t j = 0; j < nrows; ++j) {
-    const int s = int(j % S);
+    // Kept incrementally in the state-only mode, whose consumers set the pace (measured 7% faster
+    // on 64 KiB rows); the modes that write y measured 3% faster with the division here.
+    int s;
+    uint32_t par;
+    if constexpr (WRITE_Y) {
+      s = int(j % S);
+      par = uint32_t((j / S) & 1);
+    } else {
+      s = cs;
+      par = cph;
+      if (++cs == S) {
+        cs = 0;
+        cph ^= 1u;
+      }
+    }
     // cross entropy: thread 0 fetches the label before the row arrives
     int64_t label = -1;
     if constexpr (OUT == kTmaState) {
       if (a.loss && tid == 0) label = a.labels[blockIdx.x + j * gridDim.x];
     }
-    if (!mbar_wait(smem_addr(&full[s]), uint32_t((j / S) & 1), a.wait_ns)) timed_out = true;
+    if (!mbar_wait(smem_addr(&full[s]), par, a.wait_ns)) timed_out = true;
     const uint32_t slot = smem_addr(slots + size_t(s) * a.slot_bytes);
     float x_label = 0.f;  // the labelled entry, read from the staged row before the slot is freed
     if constexpr (OUT == kTmaState) {

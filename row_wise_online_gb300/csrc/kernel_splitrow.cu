@@ -6,31 +6,35 @@
 //
 // Layout: the grid is G persistent CTAs (one per SM), grouped in thread-block clusters of CS.
 // Every row is cut into G contiguous segments of 16-byte units, balanced to one unit; CTA c owns
-// segment c of every row.  One producer lane streams the segments of consecutive rows, in 14 KB
-// pieces, through a ring of shared-memory slots with bulk copies (cp.async.bulk + mbarrier).
-// Consumers keep row r's segment in registers (up to 8 pieces, 2 vectors per thread per piece)
-// while its exchange is in flight, fold row r + 1 straight from its staged slots, and then,
-// piece by piece, normalise row r from registers and gather row r + 1 into the registers just
-// freed, handing each slot back to the producer.  x is read once; y is written once, straight
-// from registers.
+// segment c of every row.  One producer lane streams the segments through a ring of shared-memory
+// slots in 28 KB pieces with bulk copies (cp.async.bulk + mbarrier), each row's segment twice:
+//
+//   P1 -- the fold pass: loads marked L2::evict_last, so the lines stay in L2;
+//   P2 -- the normalisation pass, issued once the row's exchange has completed: loads marked
+//         evict_first, served from L2 (measured: DRAM reads stay at one read of x for 16 MiB rows).
+//
+// The producer picks each next piece: a P2 piece of the oldest row whose exchange is done, else a
+// P1 piece of a row at most kL2Lag rows ahead of the oldest row still waiting for its P2, else it
+// waits.  Each slot carries a tag (row, piece, pass); the consumers follow the ring in order, so
+// they never wait for an exchange and HBM reads keep flowing while rows wait for theirs.  Nothing
+// of a row is held on chip, so the row length is not bounded by registers or shared memory (a row
+// larger than L2 is still correct; its P2 then also reads HBM).
 //
 // Per row r, in every CTA:
-//   1. the thread's (m, d) state: online fold over its units (one rescale per 16-byte unit, one
-//      exponential per element);
-//   2. warp butterfly merge, then cross-warp merge through shared memory -> CTA state;
+//   1. P1 pieces: the thread's (m, d) state, folded a piece at a time (its values' maximum first,
+//      one exponential per element, one rescale of the running sum per piece);
+//   2. after the last P1 piece: warp butterfly merge, then cross-warp merge through shared memory
+//      -> CTA state;
 //   3. cluster merge over distributed shared memory: each CTA pushes its state into rank 0's
-//      shared memory with st.async, which completes on rank 0's mbarrier as transaction bytes
-//      (no fence, so it never waits behind the row's output stores); rank 0's producer lane,
-//      which polls that barrier while it waits for free slots, merges the CS states in rank
-//      order and publishes the cluster state with one 64-bit release store into a
+//      shared memory with st.async, which completes on rank 0's mbarrier as transaction bytes;
+//      rank 0's producer lane, which polls that barrier while it waits, merges the CS states in
+//      rank order and publishes the cluster state with one 64-bit release store into a
 //      per-(row, cluster) slot;
 //   4. the exchange warp (it issues no other global stores) polls the row's slots (acquire,
 //      bounded by %globaltimer), merges all cluster states in a fixed order -- identical in
 //      every CTA, so every CTA normalises with bitwise the same (m, d) -- and hands the row
-//      state to the consumers through an mbarrier;
-//   5. y = e^(x - m) / d from registers, 16-byte stores.
-// Row r + 1 is published before row r is awaited, so the exchange of one row overlaps the work
-// of the next.
+//      state to the producer (and through the ring to the consumers) with an mbarrier;
+//   5. P2 pieces: y = e^(x - m) / d, 16-byte stores.
 // All clusters must be resident at once; the host launches at most the number of clusters the
 // occupancy query reports.  Every wait is bounded; a wait that runs out records
 // SOFTMAX_ERR_TIMEOUT in the status word, skips the remaining exchange waits, and the kernel
@@ -43,22 +47,17 @@
 namespace rwo {
 namespace {
 
-// Warp roles: 14 consumer warps, 1 exchange warp, 1 producer warp = 16 warps, 4 per SM
-// sub-partition, so each thread may use up to 128 registers (17 warps would cap it at 96 and
-// spill the row).  The exchange warp issues no global stores of its own, so its release
-// operations never wait behind the row's output stores.
+// Warp roles: 14 consumer warps, 1 exchange warp, 1 producer warp = 16 warps (measured: faster
+// than 30 consumer warps).  The exchange warp issues no global stores of its own, so its
+// release operations never wait behind the row's output stores.
 constexpr int kSplitNcw = 14;                                    // consumer warps
 constexpr int kSplitNct = kSplitNcw * 32;                        // consumer threads
 constexpr int kExchangeWarp = kSplitNcw;
 constexpr int kProducerWarp = kSplitNcw + 1;
 constexpr int kSplitThreads = (kSplitNcw + 2) * 32;
-constexpr int kUnitsPerPiecePerThread = 2;
-constexpr int kPieceUnits = kSplitNct * kUnitsPerPiecePerThread;  // 896 units
-constexpr int kPieceBytes = kPieceUnits * 16;                    // 14 KB
-// Register capacity per CTA and row: 8 pieces (112 KB) for fp32; 6 for bf16, whose unpacking
-// needs more temporaries (7 or 8 would spill).
-template <class D>
-__host__ __device__ constexpr int max_pieces() { return D::kBytes == 4 ? 8 : 6; }
+constexpr int kUnitsPerPiecePerThread = 4;
+constexpr int kPieceUnits = kSplitNct * kUnitsPerPiecePerThread;  // 1792 units
+constexpr int kPieceBytes = kPieceUnits * 16;                    // 28 KB
 constexpr int kMaxCluster = 8;
 static_assert(kPieceUnits % kSplitNct == 0, "a piece splits evenly over the consumer threads");
 
@@ -79,13 +78,6 @@ struct SplitArgs {
   uint64_t exchange_wait_ns;
   int fault;  // test hook: cluster 0 never publishes
 };
-
-// Shared memory after the slots: full[S], freed[S], cbar[2], cta_ready[2], row_ready[2],
-// cstate[2][kMaxCluster], wstate[2][kSplitNcw], rowst[2].
-size_t split_tail_bytes(int slots) {
-  return size_t(slots) * 2 * sizeof(uint64_t) + 6 * sizeof(uint64_t) + 2 * kMaxCluster * sizeof(State) +
-         2 * kSplitNcw * sizeof(State) + 2 * sizeof(State);
-}
 
 __device__ __forceinline__ uint32_t cluster_nctarank() {
   uint32_t r;
@@ -144,27 +136,46 @@ __device__ __forceinline__ State unpack_state(unsigned long long v) {
   return State{__uint_as_float(uint32_t(v)), __uint_as_float(uint32_t(v >> 32))};
 }
 
-// Online fold of the units this thread owns in one staged piece: per 16-byte unit, one
-// rescale of the running sum and one exponential per element (the recurrence, unit-wise).
-template <class D>
-__device__ __forceinline__ State fold_piece_smem(State st, uint32_t slot, int64_t rest, int tid) {
+// Online fold of one staged piece at piece granularity: the thread's values of the piece are
+// loaded, their maximum taken first (packed for bf16), then one exponential per element with the
+// packed f32x2 arithmetic, and one rescale of the running sum per piece.
+template <class D, int UPT>
+__device__ __forceinline__ State fold_piece(State st, uint32_t slot, int64_t rest, int tid) {
   constexpr int E = D::kVec;
+  uint4 q[UPT];
 #pragma unroll
-  for (int i = 0; i < kUnitsPerPiecePerThread; ++i) {
+  for (int i = 0; i < UPT; ++i) {
     const int u = tid + i * kSplitNct;
-    if (u < rest) {
-      const uint4 q = lds16(slot + uint32_t(u) * 16u);
-      float f[E];
-      D::unpack(q, f);
-      const float m_new = fmaxf(st.m, D::vmax(q));
-      const float ms = safe_max(m_new);
-      float acc = 0.f;
-#pragma unroll
-      for (int e = 0; e < E; ++e) acc += exp_diff(f[e], ms);
-      st.d = __fadd_rn(__fmul_rn(st.d, exp_diff(st.m, ms)), acc);
-      st.m = m_new;
-    }
+    q[i] = u < rest ? lds16(slot + uint32_t(u) * 16u)
+                    : make_uint4(D::kNegInfWord, D::kNegInfWord, D::kNegInfWord, D::kNegInfWord);
   }
+  const float m_new = fmaxf(st.m, D::vmax_all(q));
+  const float ms = safe_max(m_new);
+  float2 acc = make_float2(0.f, 0.f);
+  float sum;
+  if (exp_shift_ok(ms)) {
+    const ExpShift sh = exp_shift(ms);
+#pragma unroll
+    for (int i = 0; i < UPT; ++i) {
+      float2 f[E / 2];
+      D::unpack2(q[i], f);
+#pragma unroll
+      for (int e = 0; e < E / 2; ++e) acc = __fadd2_rn(acc, exp_shifted2(f[e], sh));
+    }
+    sum = __fmul_rn(__fadd_rn(acc.x, acc.y), sh.unscale);
+  } else {
+    const float2 nms = make_float2(-ms, -ms);
+#pragma unroll
+    for (int i = 0; i < UPT; ++i) {
+      float2 f[E / 2];
+      D::unpack2(q[i], f);
+#pragma unroll
+      for (int e = 0; e < E / 2; ++e) acc = __fadd2_rn(acc, exp_diff2(f[e], nms));
+    }
+    sum = __fadd_rn(acc.x, acc.y);
+  }
+  st.d = __fadd_rn(__fmul_rn(st.d, exp_diff(st.m, ms)), sum);
+  st.m = m_new;
   return st;
 }
 
@@ -173,21 +184,33 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
+constexpr int kL2Lag = 2;    // P1 may run this many rows ahead of the oldest pending P2
+constexpr int kRowBufs = 4;  // per-row buffers (states, barriers) in flight: kL2Lag + 2 <= 4
+static_assert(kL2Lag + 2 <= kRowBufs, "row buffers must cover the rows in flight");
+
+// Shared memory after the slots: full[S], freed[S], tag[S], cbar[4], cta_ready[4], row_ready[4],
+// cstate[4][kMaxCluster], wstate[2][kSplitNcw], rowst[4].
+size_t split_tail_bytes(int slots) {
+  return size_t(slots) * 3 * sizeof(uint64_t) + 3 * kRowBufs * sizeof(uint64_t) +
+         size_t(kRowBufs) * kMaxCluster * sizeof(State) + 2 * kSplitNcw * sizeof(State) + kRowBufs * sizeof(State);
+}
+
 template <class D>
 __global__ void __launch_bounds__(kSplitThreads, 1) k_splitrow(SplitArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int E = D::kVec;
   constexpr int U = kUnitsPerPiecePerThread;
-  constexpr int KMAX = max_pieces<D>();
+  constexpr int RB = kRowBufs;
   const int NS = a.slots;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(NS) * kPieceBytes);
   uint64_t* freed = full + NS;
-  uint64_t* cbar = freed + NS;          // [2] cluster merge (used in rank 0), count = cluster size
-  uint64_t* cta_ready = cbar + 2;       // [2] consumers -> exchange warp: row's CTA state sent
-  uint64_t* row_ready = cta_ready + 2;  // [2] exchange warp -> consumers: row state is in rowst
-  State* cstate = reinterpret_cast<State*>(row_ready + 2);  // [2][kMaxCluster], written into rank 0
-  State* wstate = cstate + 2 * kMaxCluster;                 // [2][kSplitNcw]
-  State* rowst = wstate + 2 * kSplitNcw;                    // [2]
+  uint64_t* tag = freed + NS;            // [NS] (row << 32) | (piece << 1) | second
+  uint64_t* cbar = tag + NS;             // [RB] cluster merge (rank 0)
+  uint64_t* cta_ready = cbar + RB;       // [RB] consumers -> exchange warp
+  uint64_t* row_ready = cta_ready + RB;  // [RB] exchange warp -> producer
+  State* cstate = reinterpret_cast<State*>(row_ready + RB);  // [RB][kMaxCluster]
+  State* wstate = cstate + RB * kMaxCluster;                 // [2][kSplitNcw]
+  State* rowst = wstate + 2 * kSplitNcw;                     // [RB]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t crank = cluster_ctarank();
@@ -195,76 +218,107 @@ __global__ void __launch_bounds__(kSplitThreads, 1) k_splitrow(SplitArgs a) {
   const uint32_t cid = cluster_id_x();
   const uint32_t ncl = cluster_count_x();
 
-  // This CTA's segment of every row, in 16-byte units.
   const int64_t G = gridDim.x, c = blockIdx.x;
   const int64_t base = a.units / G, rem = a.units % G;
   const int64_t seg_units = base + (c < rem ? 1 : 0);
   const int64_t seg_start = c * base + (c < rem ? c : rem);
-  const int K = int((seg_units + kPieceUnits - 1) / kPieceUnits);  // <= KMAX, 2K <= NS (the host checks)
+  const int64_t K = (seg_units + kPieceUnits - 1) / kPieceUnits;  // >= 1 (the host checks)
+  const int64_t total = 2 * a.M * K;
 
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(smem_addr(&full[s]), 1);
       mbar_init(smem_addr(&freed[s]), kSplitNcw);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < RB; ++i) {
       mbar_init(smem_addr(&cbar[i]), 1);
       mbar_init(smem_addr(&cta_ready[i]), 1);
       mbar_init(smem_addr(&row_ready[i]), 1);
     }
     fence_mbar_init();
-    // rank 0 expects csize states of 8 bytes for each of rows 0 and 1 (re-armed per row)
     if (crank == 0)
-      for (int i = 0; i < 2 && i < a.M; ++i) mbar_arrive_expect_tx(smem_addr(&cbar[i]), csize * 8u);
+      for (int i = 0; i < RB && i < a.M; ++i) mbar_arrive_expect_tx(smem_addr(&cbar[i]), csize * 8u);
   }
   __syncthreads();
-  cluster_sync_all();  // every CTA's barriers exist before any remote arrive
+  cluster_sync_all();
 
   bool timed_out = false;
   if (warp == kProducerWarp) {
-    // ---------------- producer: stream pieces of consecutive rows through the ring ----------------
-    // In rank 0 the same lane also merges and publishes the cluster's state of each row as soon
-    // as all of the cluster's states have landed: it polls that barrier while it waits for free
-    // slots, and it issues no generic global stores, so its release store is not held up.
     if (lane == 0) {
       int64_t pubd = 0;
       auto service = [&]() {
         if (crank != 0) return;
-        while (pubd < a.M && mbar_test_cluster(smem_addr(&cbar[pubd & 1]), uint32_t((pubd >> 1) & 1))) {
+        while (pubd < a.M && mbar_test(smem_addr(&cbar[pubd % RB]), uint32_t((pubd / RB) & 1)) &&
+               mbar_test_cluster(smem_addr(&cbar[pubd % RB]), uint32_t((pubd / RB) & 1))) {
           State cs = empty_state();
-          for (uint32_t i = 0; i < csize; ++i) cs = merge(cs, cstate[(pubd & 1) * kMaxCluster + i]);
+          for (uint32_t i = 0; i < csize; ++i) cs = merge(cs, cstate[(pubd % RB) * kMaxCluster + i]);
           if (!(a.fault && cid == 0)) st_release_u64(a.pub + pubd * ncl + cid, pack_state(cs));
-          if (pubd + 2 < a.M) mbar_arrive_expect_tx(smem_addr(&cbar[pubd & 1]), csize * 8u);  // row pubd + 2
+          if (pubd + RB < a.M) mbar_arrive_expect_tx(smem_addr(&cbar[pubd % RB]), csize * 8u);
           ++pubd;
         }
       };
-      const uint64_t pol = policy_evict_first();
-      const int64_t total = K > 0 ? a.M * K : 0;
-      for (int64_t p = 0; p < total; ++p) {
-        const int s = int(p % NS);
-        if (p >= NS) {
+      const uint64_t keep = policy_evict_last(), drop = policy_evict_first();
+      int64_t r1 = 0, k1 = 0;  // next P1 piece
+      int64_t r2 = 0, k2 = 0;  // next P2 piece
+      bool ready2 = false;     // row r2's exchange is done
+      int ps = 0;              // ring slot of piece n, and the parity of its lap (kept
+      uint32_t pph = 0;        // incrementally: a 64-bit division per piece costs ~0.1 us)
+      for (int64_t n = 0; n < total; ++n) {
+        // choose the next piece (bounded: a missing exchange signal ends the wait)
+        bool second = false;
+        const uint64_t t0 = global_timer_ns();
+        while (true) {
+          if (!ready2) ready2 = mbar_test(smem_addr(&row_ready[r2 % RB]), uint32_t((r2 / RB) & 1));
+          if (ready2) {
+            second = true;
+            break;
+          }
+          if (r1 < a.M && r1 <= r2 + kL2Lag) break;
+          service();
+          if (global_timer_ns() - t0 > a.local_wait_ns) {
+            timed_out = true;
+            second = r1 >= a.M || r1 > r2 + kL2Lag;  // keep the stream going either way
+            break;
+          }
+        }
+        const int s = ps;
+        if (n >= NS) {
           const uint32_t bar = smem_addr(&freed[s]);
-          const uint32_t par = uint32_t(((p / NS) - 1) & 1);
-          const uint64_t t0 = global_timer_ns();
+          const uint32_t par = pph ^ 1u;  // the previous lap's release of this slot
+          const uint64_t t1 = global_timer_ns();
           while (!mbar_test(bar, par)) {
             service();
-            if (global_timer_ns() - t0 > a.local_wait_ns) {
+            if (global_timer_ns() - t1 > a.local_wait_ns) {
               timed_out = true;
               break;
             }
           }
         }
-        const int64_t r = p / K;
-        const int k = int(p % K);
-        const int64_t rest = seg_units - int64_t(k) * kPieceUnits;
+        const int64_t r = second ? r2 : r1;
+        const int64_t k = second ? k2 : k1;
+        tag[s] = (uint64_t(r) << 32) | (uint64_t(k) << 1) | (second ? 1u : 0u);
+        const int64_t rest = seg_units - k * kPieceUnits;
         const uint32_t bytes = uint32_t(rest < kPieceUnits ? rest : kPieceUnits) * 16u;
         const uint32_t bar = smem_addr(&full[s]);
         mbar_arrive_expect_tx(bar, bytes);
-        bulk_g2s(smem_addr(smem + size_t(s) * kPieceBytes),
-                 a.x + r * a.row_bytes + (seg_start + int64_t(k) * kPieceUnits) * 16, bytes, bar, pol);
+        bulk_g2s(smem_addr(smem + size_t(s) * kPieceBytes), a.x + r * a.row_bytes + (seg_start + k * kPieceUnits) * 16,
+                 bytes, bar, second ? drop : keep);
+        if (second) {
+          if (++k2 == K) {
+            k2 = 0;
+            ++r2;
+            ready2 = false;
+          }
+        } else if (++k1 == K) {
+          k1 = 0;
+          ++r1;
+        }
+        if (++ps == NS) {
+          ps = 0;
+          pph ^= 1u;
+        }
         service();
       }
-      // rank 0: publish the remaining rows (bounded: a peer that timed out may never send)
       const uint64_t t0 = global_timer_ns();
       while (crank == 0 && pubd < a.M) {
         service();
@@ -273,14 +327,10 @@ __global__ void __launch_bounds__(kSplitThreads, 1) k_splitrow(SplitArgs a) {
           break;
         }
       }
-      // every load has landed before the CTA may exit (the consumers normally saw them all)
-      for (int64_t p = total > NS ? total - NS : 0; p < total; ++p)
-        if (!mbar_wait(smem_addr(&full[p % NS]), uint32_t((p / NS) & 1), a.local_wait_ns)) timed_out = true;
+      for (int64_t n = total > NS ? total - NS : 0; n < total; ++n)  // once per launch
+        if (!mbar_wait(smem_addr(&full[n % NS]), uint32_t((n / NS) & 1), a.local_wait_ns)) timed_out = true;
     }
   } else if (warp == kExchangeWarp) {
-    // ---------------- exchange: wait across clusters ----------------
-    // All lanes poll the published cluster states of the row being awaited (the consumers
-    // push CTA states into rank 0 with st.async; rank 0's producer lane publishes).
     bool abort = false;
     for (int64_t r = 0; r < a.M; ++r) {
       const uint64_t t0 = global_timer_ns();
@@ -297,11 +347,11 @@ __global__ void __launch_bounds__(kSplitThreads, 1) k_splitrow(SplitArgs a) {
           }
         }
         if (__all_sync(0xffffffffu, ready)) {
-          g = warp_merge(gg);  // every CTA merges the same states in the same order
+          g = warp_merge(gg);  // the same states in the same order in every CTA
           break;
         }
         if (global_timer_ns() - t0 > a.exchange_wait_ns) {
-          abort = true;  // later rows do not wait again
+          abort = true;
           timed_out = true;
           g = warp_merge(gg);
           break;
@@ -309,127 +359,83 @@ __global__ void __launch_bounds__(kSplitThreads, 1) k_splitrow(SplitArgs a) {
         __nanosleep(20);
       }
       if (lane == 0) {
-        // Signal row r only once the consumers have handed over row r's state: they do that after
-        // consuming row r - 2's signal, so one buffer never completes two phases ahead of its
-        // waiters (this already holds when the exchange did not run out).
-        if (!mbar_wait(smem_addr(&cta_ready[r & 1]), uint32_t((r >> 1) & 1), a.local_wait_ns)) timed_out = true;
-        rowst[r & 1] = g;
-        mbar_arrive(smem_addr(&row_ready[r & 1]));
+        // row r's buffer is free once this CTA handed over row r's state (it does so only after
+        // the producer has issued every P2 piece of row r - RB + kL2Lag + 1 or later)
+        if (!mbar_wait(smem_addr(&cta_ready[r % RB]), uint32_t((r / RB) & 1), a.local_wait_ns)) timed_out = true;
+        rowst[r % RB] = g;
+        mbar_arrive(smem_addr(&row_ready[r % RB]));
       }
     }
   } else {
-    // ---------------- consumers ----------------
-    // Registers hold row r while it waits for its exchange; row r + 1 is folded straight from
-    // its staged slots and handed to the exchange warp first, so exchanges overlap a row of work.
-    uint4 v[KMAX][U];
-    auto publish = [&](int64_t r, State st) {
-      st = group_merge(st, wstate + (r & 1) * kSplitNcw, kSplitNcw, warp, lane,
-                       [] { named_barrier_sync(1, kSplitNct); });
-      if (tid == 0) {
-        st_async_cluster_f32x2(map_to_rank(smem_addr(&cstate[(r & 1) * kMaxCluster + crank]), 0), st.m, st.d,
-                               map_to_rank(smem_addr(&cbar[r & 1]), 0));
-        mbar_arrive(smem_addr(&cta_ready[r & 1]));
+    // ---------------- consumers: follow the ring ----------------
+    State st = empty_state();  // fold of the P1 row in progress
+    int cs = 0;                // ring slot of piece n and its lap parity
+    uint32_t cph = 0;
+    for (int64_t n = 0; n < total; ++n) {
+      const int s = cs;
+      const uint32_t par = cph;
+      if (++cs == NS) {
+        cs = 0;
+        cph ^= 1u;
       }
-    };
-    // prologue: row 0 into registers, then its state
-    if (a.M > 0) {
-#pragma unroll
-      for (int k = 0; k < KMAX; ++k) {
-#pragma unroll
-        for (int i = 0; i < U; ++i) v[k][i] = make_uint4(D::kNegInfWord, D::kNegInfWord, D::kNegInfWord, D::kNegInfWord);
-        if (k < K) {
-          const int s = k % NS;
-          if (!mbar_wait(smem_addr(&full[s]), 0u, a.local_wait_ns)) timed_out = true;
-          const uint32_t slot = smem_addr(smem + size_t(s) * kPieceBytes);
-          const int64_t rest = seg_units - int64_t(k) * kPieceUnits;
-#pragma unroll
-          for (int i = 0; i < U; ++i) {
-            const int u = tid + i * kSplitNct;
-            if (u < rest) v[k][i] = lds16(slot + uint32_t(u) * 16u);
+      if (!mbar_wait(smem_addr(&full[s]), par, a.local_wait_ns)) timed_out = true;
+      const uint64_t tg = tag[s];
+      const int64_t r = int64_t(tg >> 32);
+      const int64_t k = int64_t((tg & 0xffffffffu) >> 1);
+      const uint32_t slot = smem_addr(smem + size_t(s) * kPieceBytes);
+      const int64_t rest = seg_units - k * kPieceUnits;
+      if (!(tg & 1u)) {
+        // P1: fold the piece; after the row's last piece, the CTA state to the cluster
+        st = fold_piece<D, kUnitsPerPiecePerThread>(st, slot, rest, tid);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&freed[s]));
+        if (k == K - 1) {
+          const State cs = group_merge(st, wstate + (r & 1) * kSplitNcw, kSplitNcw, warp, lane,
+                                       [] { named_barrier_sync(1, kSplitNct); });
+          if (tid == 0) {
+            st_async_cluster_f32x2(map_to_rank(smem_addr(&cstate[(r % RB) * kMaxCluster + crank]), 0), cs.m, cs.d,
+                                   map_to_rank(smem_addr(&cbar[r % RB]), 0));
+            mbar_arrive(smem_addr(&cta_ready[r % RB]));
           }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_addr(&freed[s]));
+          st = empty_state();
         }
-      }
-      float mt = -INFINITY;
-#pragma unroll
-      for (int k = 0; k < KMAX; ++k)
-#pragma unroll
-        for (int i = 0; i < U; ++i) mt = fmaxf(mt, D::vmax(v[k][i]));
-      const float mts = safe_max(mt);
-      float dt = 0.f;
-#pragma unroll
-      for (int k = 0; k < KMAX; ++k)
+      } else {
+        // P2: normalise the re-read piece with the row's state and store y
+        const State row = rowst[r % RB];
+        const float ms = safe_max(row.m);
+        const float inv = safe_inv(row.d);
+        const float2 nms = make_float2(-ms, -ms), inv2 = make_float2(inv, inv);
+        uint4 q[U];
 #pragma unroll
         for (int i = 0; i < U; ++i) {
-          float f[E];
-          D::unpack(v[k][i], f);
-#pragma unroll
-          for (int e = 0; e < E; ++e) dt += exp_diff(f[e], mts);
+          const int u = tid + i * kSplitNct;
+          if (u < rest) q[i] = lds16(slot + uint32_t(u) * 16u);
         }
-      publish(0, State{mt, dt});
-    }
-    for (int64_t r = 0; r < a.M; ++r) {
-      const bool more = r + 1 < a.M;
-      // 1. fold row r + 1 from its slots and hand its state over
-      if (more) {
-        State st = empty_state();
-        for (int k = 0; k < K; ++k) {
-          const int64_t p = (r + 1) * K + k;
-          const int s = int(p % NS);
-          if (!mbar_wait(smem_addr(&full[s]), uint32_t((p / NS) & 1), a.local_wait_ns)) timed_out = true;
-          st = fold_piece_smem<D>(st, smem_addr(smem + size_t(s) * kPieceBytes),
-                                  seg_units - int64_t(k) * kPieceUnits, tid);
-        }
-        publish(r + 1, st);
-      }
-      // 2. row r's state
-      if (!mbar_wait(smem_addr(&row_ready[r & 1]), uint32_t((r >> 1) & 1), a.local_wait_ns)) timed_out = true;
-      const State row = rowst[r & 1];
-      const float ms = safe_max(row.m);
-      const float inv = safe_inv(row.d);
-      // 3. piece by piece: normalise row r from registers and store, then gather row r + 1's
-      //    piece into the registers just freed and hand its slot back
-      unsigned char* yseg = a.y + r * a.row_bytes + seg_start * 16;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&freed[s]));
+        unsigned char* yseg = a.y + r * a.row_bytes + (seg_start + k * kPieceUnits) * 16;
 #pragma unroll
-      for (int k = 0; k < KMAX; ++k) {
-        if (k < K) {
-          const int64_t rest = seg_units - int64_t(k) * kPieceUnits;
+        for (int i = 0; i < U; ++i) {
+          const int u = tid + i * kSplitNct;
+          if (u < rest) {
+            float2 f[E / 2];
+            D::unpack2(q[i], f);
 #pragma unroll
-          for (int i = 0; i < U; ++i) {
-            const int u = tid + i * kSplitNct;
-            if (u < rest) {
-              float f[E];
-              D::unpack(v[k][i], f);
-#pragma unroll
-              for (int e = 0; e < E; ++e) f[e] = __fmul_rn(exp_diff(f[e], ms), inv);
-              st_stream16(yseg + (int64_t(k) * kPieceUnits + u) * 16, D::pack(f));
-            }
-          }
-          if (more) {
-            const int64_t p = (r + 1) * K + k;
-            const int s = int(p % NS);
-            const uint32_t slot = smem_addr(smem + size_t(s) * kPieceBytes);
-#pragma unroll
-            for (int i = 0; i < U; ++i) {
-              const int u = tid + i * kSplitNct;
-              if (u < rest) v[k][i] = lds16(slot + uint32_t(u) * 16u);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&freed[s]));
+            for (int e = 0; e < E / 2; ++e) f[e] = __fmul2_rn(exp_diff2(f[e], nms), inv2);
+            st_stream16(yseg + int64_t(u) * 16, D::pack2(f));
           }
         }
-      }
-      if (c == 0 && tid == 0) {
-        if (a.m_out) a.m_out[r] = row.m;
-        if (a.d_out) a.d_out[r] = row.d;
-        if (a.lse_out) a.lse_out[r] = lse_of(row);
+        if (k == 0 && c == 0 && tid == 0) {
+          if (a.m_out) a.m_out[r] = row.m;
+          if (a.d_out) a.d_out[r] = row.d;
+          if (a.lse_out) a.lse_out[r] = lse_of(row);
+        }
       }
     }
   }
   if (timed_out) atomicOr(a.status, kStatusTimeout);
   __syncwarp();
-  cluster_sync_all();  // no CTA leaves while a peer may still write into its shared memory
+  cluster_sync_all();
 }
 
 using SplitKernel = void (*)(SplitArgs);
@@ -506,9 +512,7 @@ bool splitrow_fits(const RowProblem& p, const DeviceInfo& dev) {
   const int64_t G = int64_t(plan.cluster) * plan.clusters;
   const int64_t units = row_bytes / 16;
   if (units < G * 64) return false;  // rows this short belong to the one-read kernels
-  const int64_t seg = (units + G - 1) / G;
-  const int64_t K = (seg + kPieceUnits - 1) / kPieceUnits;
-  return K <= (p.dtype == 0 ? max_pieces<F32>() : max_pieces<BF16>()) && 2 * K <= plan.slots;
+  return true;  // nothing of a row is held on chip: any length
 }
 
 cudaError_t launch_splitrow(const RowProblem& p, const DeviceInfo& dev) {

@@ -100,16 +100,21 @@ def test_exchange_wait_runs_out_and_reports_timeout():
     check_y(to_host(y), y_ref, synth.F32, "after timeout")
 
 
-def test_rows_beyond_split_capacity_take_twopass():
-    """A single 32 Mi-element fp32 row (128 MiB) exceeds the split kernel's register capacity;
-    AUTO runs it with the two-pass kernel and a forced split reports UNSUPPORTED."""
+def test_rows_larger_than_l2():
+    """A single 32 Mi-element fp32 row (128 MiB, larger than L2): nothing of a row is held on chip,
+    so the split kernel takes it (its second pass then reads HBM again); AUTO picks it too."""
     N = 1 << 25
-    x = torch.randn((1, N), device="cuda") * 3
-    with pytest.raises(rwo.SoftmaxError) as ei:
-        rwo.softmax_rows_ex(x, variant=rwo.VARIANT_SPLITROW)
-    assert ei.value.status == rwo.ERR_UNSUPPORTED
-    m = torch.empty(1, device="cuda")
-    y = rwo.softmax_rows_ex(x, m_out=m)
-    assert rwo.get_status() == rwo.OK and rwo.last_variant() == rwo.VARIANT_TWOPASS
-    assert float(m) == float(x.max())
-    assert abs(float(torch.sum(y, dtype=torch.float64)) - 1.0) <= 1e-5
+    w = synth.custom("split-huge", synth.F32, 1, N, seed=77, dist=synth.UNIFORM, p0=-20.0, p1=20.0, late_max=20.0)
+    x_host = synth.generate(w)
+    x = to_device(x_host)
+    y, m, d, lse = run_softmax(x, rwo.VARIANT_SPLITROW)
+    assert rwo.last_variant() == rwo.VARIANT_SPLITROW
+    y_ref, m_ref, d_ref, lse_ref = oracle.softmax_rows(x_host)
+    yh = to_host(y)
+    check_y(yh, y_ref, synth.F32, "split 1 x 32Mi")
+    check_rowsums(yh, synth.F32, None, "split 1 x 32Mi")
+    check_state(m.cpu().numpy(), d.cpu().numpy(), lse.cpu().numpy(), m_ref, d_ref, lse_ref, "split 1 x 32Mi")
+    del y_ref
+    rwo.softmax_rows(x)
+    torch.cuda.synchronize()
+    assert rwo.last_variant() == rwo.VARIANT_SPLITROW
