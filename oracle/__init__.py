@@ -42,6 +42,7 @@ _lib = None
 
 F32 = 0
 BF16 = 1
+F16 = 2
 
 
 def build(force: bool = False) -> str:
@@ -96,8 +97,8 @@ def softmax_rows(x: np.ndarray, dtype: int | None = None, rows=None, *, want_y: 
         raise ValueError("x must be 2-D")
     if dtype is None:
         dtype = F32 if x.dtype == np.float32 else BF16 if x.dtype == np.uint16 else None
-    if dtype is None or (dtype == F32 and x.dtype != np.float32) or (dtype == BF16 and x.dtype != np.uint16):
-        raise TypeError("x must be float32 (F32) or uint16 bf16 bits (BF16)")
+    if dtype is None or (dtype == F32 and x.dtype != np.float32) or (dtype in (BF16, F16) and x.dtype != np.uint16):
+        raise TypeError("x must be float32 (F32) or uint16 bf16 / fp16 bits (BF16 / F16, dtype given)")
     M, N = x.shape
     if rows is None:
         idx = None
@@ -126,8 +127,8 @@ def _matrix(x, dtype):
         raise ValueError("x must be 2-D")
     if dtype is None:
         dtype = F32 if x.dtype == np.float32 else BF16 if x.dtype == np.uint16 else None
-    if dtype is None or (dtype == F32 and x.dtype != np.float32) or (dtype == BF16 and x.dtype != np.uint16):
-        raise TypeError("x must be float32 (F32) or uint16 bf16 bits (BF16)")
+    if dtype is None or (dtype == F32 and x.dtype != np.float32) or (dtype in (BF16, F16) and x.dtype != np.uint16):
+        raise TypeError("x must be float32 (F32) or uint16 bf16 / fp16 bits (BF16 / F16, dtype given)")
     return x, dtype
 
 

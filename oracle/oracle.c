@@ -43,7 +43,7 @@
  *    first merge uses scale_old = 0 for m_old = -inf), and no -inf - (-inf)
  *    is ever evaluated.
  *  - A row whose entries are all -inf has y = 0, m = -inf, d = 0, LSE = -inf.
- *  - bf16 inputs are widened exactly (bf16 -> fp32 -> fp64).
+ *  - bf16 and fp16 inputs are widened exactly (bf16 -> fp32 -> fp64; fp16 -> fp64).
  *  - log softmax of an all -inf row is -inf everywhere (log 0).
  *  - Cross entropy: a negative label marks a row to ignore (loss 0); a label
  *    >= N gives NaN.  A row whose labelled entry is -inf has loss +inf
@@ -60,10 +60,17 @@
 
 #define ORACLE_F32 0
 #define ORACLE_BF16 1
+#define ORACLE_F16 2
 
-/* Element i of a row-major matrix of the given dtype, widened exactly. */
+/* Element i of a row-major matrix of the given dtype, widened exactly (the C compiler's
+ * IEEE binary16 type for fp16). */
 static double load_elem(const void* x, int dtype, int64_t i) {
   if (dtype == ORACLE_F32) return (double)((const float*)x)[i];
+  if (dtype == ORACLE_F16) {
+    _Float16 h;
+    memcpy(&h, (const uint16_t*)x + i, sizeof h);
+    return (double)h;
+  }
   uint32_t bits = (uint32_t)((const uint16_t*)x)[i] << 16;
   float f;
   memcpy(&f, &bits, sizeof f);
@@ -137,7 +144,7 @@ int oracle_softmax_rows(const void* x, int dtype, int64_t N,
                         const int64_t* rows, int64_t nrows, double* y,
                         double* m, double* d, double* lse, int nthreads) {
   if (!x || N < 1 || nrows < 0) return -1;
-  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return -1;
+  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F16) return -1;
   if (nrows == 0) return 0;
   if (nthreads < 1) nthreads = 1;
   if (nthreads > nrows) nthreads = (int)nrows;
@@ -255,7 +262,7 @@ static int run_log_jobs(oracle_log_job proto, int64_t nrows, int nthreads) {
 int oracle_log_softmax_rows(const void* x, int dtype, int64_t N, const int64_t* rows, int64_t nrows,
                             double* ly, int nthreads) {
   if (!x || !ly || N < 1 || nrows < 0) return -1;
-  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return -1;
+  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F16) return -1;
   if (nrows == 0) return 0;
   oracle_log_job proto = {x, dtype, N, rows, NULL, ly, 0, 0};
   return run_log_jobs(proto, nrows, nthreads);
@@ -268,7 +275,7 @@ int oracle_log_softmax_rows(const void* x, int dtype, int64_t N, const int64_t* 
 int oracle_cross_entropy_rows(const void* x, int dtype, int64_t N, const int64_t* labels, int64_t M,
                               double* loss, int nthreads) {
   if (!x || !labels || !loss || N < 1 || M < 0) return -1;
-  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return -1;
+  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F16) return -1;
   if (M == 0) return 0;
   oracle_log_job proto = {x, dtype, N, NULL, labels, loss, 0, 0};
   return run_log_jobs(proto, M, nthreads);

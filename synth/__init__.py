@@ -44,6 +44,7 @@ _lib = None
 
 F32 = 0
 BF16 = 1
+F16 = 2
 NORMAL = 0
 UNIFORM = 1
 
@@ -89,7 +90,7 @@ def np_dtype(dtype: int):
 @dataclasses.dataclass(frozen=True)
 class Workload:
     name: str
-    dtype: int  # F32 or BF16
+    dtype: int  # F32, BF16 or F16
     M: int
     N: int
     seed: int
@@ -171,6 +172,16 @@ def generate_rows(w: Workload, rows, nthreads: int | None = None) -> np.ndarray:
     for i, r in enumerate(rows):
         fill(w, out[i:i + 1].ctypes.data, r, 1, nthreads=1)
     return out
+
+
+def f16_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Widen fp16 bit patterns (uint16) to float32 exactly."""
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float32)
+
+
+def f32_to_f16(a: np.ndarray) -> np.ndarray:
+    """Round float32 to fp16 bit patterns, round-to-nearest-even (input encoding only)."""
+    return np.ascontiguousarray(a, dtype=np.float32).astype(np.float16).view(np.uint16)
 
 
 def bf16_to_f32(bits: np.ndarray) -> np.ndarray:

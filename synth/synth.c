@@ -25,6 +25,7 @@
 
 #define SYNTH_F32 0
 #define SYNTH_BF16 1
+#define SYNTH_F16 2
 #define SYNTH_NORMAL 0
 #define SYNTH_UNIFORM 1
 
@@ -63,10 +64,14 @@ static uint16_t f32_to_bf16_rne(float f) {
 
 static void store_value(void* out, int dtype, int64_t i, double v) {
   float f = (float)v;
-  if (dtype == SYNTH_F32)
+  if (dtype == SYNTH_F32) {
     ((float*)out)[i] = f;
-  else
+  } else if (dtype == SYNTH_F16) {
+    _Float16 h = (_Float16)f; /* IEEE binary16, round to nearest even */
+    memcpy((uint16_t*)out + i, &h, sizeof h);
+  } else {
     ((uint16_t*)out)[i] = f32_to_bf16_rne(f);
+  }
 }
 
 static double draw(int dist, double p0, double p1, uint64_t s, int64_t j) {
@@ -105,7 +110,7 @@ static void* fill_worker(void* arg) {
 int synth_fill(void* out, int dtype, int64_t N, int64_t row0, int64_t nrows, int dist,
                double p0, double p1, uint64_t seed, int nthreads) {
   if (!out || N < 1 || nrows < 0 || row0 < 0) return -1;
-  if (dtype != SYNTH_F32 && dtype != SYNTH_BF16) return -1;
+  if (dtype != SYNTH_F32 && dtype != SYNTH_BF16 && dtype != SYNTH_F16) return -1;
   if (dist != SYNTH_NORMAL && dist != SYNTH_UNIFORM) return -1;
   if (nrows == 0) return 0;
   if (nthreads < 1) nthreads = 1;

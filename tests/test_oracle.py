@@ -402,3 +402,24 @@ def test_cross_entropy_against_brute_force_and_label_rules():
     xm = np.array([[1.0, -np.inf], [-np.inf, -np.inf]], np.float32)
     lm = oracle.cross_entropy_rows(xm, [1, 0])
     assert np.isposinf(lm[0]) and math.isnan(lm[1])
+
+
+def test_f16_input_is_widened_exactly():
+    """Every finite fp16 bit pattern: the oracle's widening equals numpy's float16 -> float64 (a
+    one-element row's m is the value itself); and a softmax of fp16 data equals the softmax of
+    the same values given as fp32."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = bits.view(np.float16)
+    fin = np.isfinite(vals)
+    rows = bits[fin].reshape(-1, 1)
+    _, m, d, lse = oracle.softmax_rows(rows, dtype=oracle.F16, want_y=False)
+    np.testing.assert_array_equal(m, vals[fin].astype(np.float64))
+    assert np.all(d == 1.0)
+    rng = np.random.default_rng(5)
+    x16 = (rng.standard_normal((6, 77)) * 6).astype(np.float16)
+    y16, m16, d16, l16 = oracle.softmax_rows(x16.view(np.uint16), dtype=oracle.F16)
+    y32, m32, d32, l32 = oracle.softmax_rows(x16.astype(np.float32))
+    for a, b in ((y16, y32), (m16, m32), (d16, d32), (l16, l32)):
+        np.testing.assert_array_equal(a, b)
+    np.testing.assert_array_equal(oracle.log_softmax_rows(x16.view(np.uint16), dtype=oracle.F16),
+                                  oracle.log_softmax_rows(x16.astype(np.float32)))

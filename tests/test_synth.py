@@ -66,3 +66,15 @@ def test_causal_mask():
         q = r % 4096
         assert np.all(np.isneginf(x[i, q + 1:]))
         assert np.all(np.isfinite(x[i, : q + 1]))
+
+
+def test_generated_f16_matches_rounded_fp32():
+    """fp16 workloads hold the fp32 draw rounded to nearest even (numpy's float16 conversion)."""
+    w32 = synth.custom("g", synth.F32, 7, 333, seed=9, p1=5.0)
+    w16 = synth.custom("g", synth.F16, 7, 333, seed=9, p1=5.0)
+    a = synth.generate(w32)
+    b = synth.generate(w16)
+    assert b.dtype == np.uint16
+    np.testing.assert_array_equal(b, a.astype(np.float16).view(np.uint16))
+    np.testing.assert_array_equal(synth.f16_to_f32(b), a.astype(np.float16).astype(np.float32))
+    assert w16.elem_bytes == 2
