@@ -26,9 +26,14 @@
  *  - Pointers are DEVICE pointers (except softmax_rows_host), owned by the
  *    caller; the library keeps none of them after the call is enqueued.
  *  - Matrices are row-major and contiguous: row r starts at element r * N.
- *  - dtype is SOFTMAX_F32 (fp32 in / fp32 out) or SOFTMAX_BF16 (bf16 bit
- *    patterns in / bf16 out, rounded to nearest even).  Arithmetic is fp32 in
- *    both cases; exponentials use the hardware ex2 with a log2(e) prescale.
+ *  - dtype is SOFTMAX_F32 (fp32 in / fp32 out), SOFTMAX_BF16 (bf16 bit
+ *    patterns in / bf16 out) or SOFTMAX_F16 (IEEE binary16 in / out); 16-bit
+ *    outputs are rounded to nearest even (fp16 keeps subnormals).  Arithmetic
+ *    is fp32 in every case; exponentials use the hardware ex2 with a log2(e)
+ *    prescale.  fp16's range ends at 65504 ("Softmax 数值稳定性与 IO-Aware
+ *    Attention" §一, precision and range of the floating-point formats):
+ *    inputs cannot exceed it, softmax outputs (in [0, 1]) always fit, and
+ *    log-softmax outputs below -65504 round to -inf.
  *  - State outputs m_out, d_out, lse_out are fp32 arrays of M entries; each
  *    may be NULL.  m_out is the raw row maximum (bit-exact max of the inputs,
  *    -0 and +0 equal).  d_out is relative to m_out, natural base.
@@ -51,7 +56,7 @@ extern "C" {
 #endif
 
 /* Element types. */
-enum softmax_dtype { SOFTMAX_F32 = 0, SOFTMAX_BF16 = 1 };
+enum softmax_dtype { SOFTMAX_F32 = 0, SOFTMAX_BF16 = 1, SOFTMAX_F16 = 2 };
 
 /* Status codes. */
 enum softmax_status {

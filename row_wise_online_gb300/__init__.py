@@ -23,7 +23,7 @@ __all__ = [
     "softmax_rows_splitrow_noalloc", "softmax_rows_causal",
 ]
 
-F32, BF16 = 0, 1
+F32, BF16, F16 = 0, 1, 2
 VARIANT_AUTO, VARIANT_ONEREAD_REG, VARIANT_ONEREAD_SMEM, VARIANT_TWOPASS, VARIANT_SPLITROW = range(5)
 VARIANT_NAMES = {VARIANT_AUTO: "auto", VARIANT_ONEREAD_REG: "oneread_reg",
                  VARIANT_ONEREAD_SMEM: "oneread_smem", VARIANT_TWOPASS: "twopass",
@@ -117,7 +117,9 @@ def _dtype_code(t) -> int:
         return F32
     if t.dtype == torch.bfloat16:
         return BF16
-    raise TypeError(f"unsupported dtype {t.dtype}: float32 or bfloat16")
+    if t.dtype == torch.float16:
+        return F16
+    raise TypeError(f"unsupported dtype {t.dtype}: float32, bfloat16 or float16")
 
 
 def _rows(t):

@@ -108,7 +108,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // Shape and pointer checks shared by the row calls.  Returns a status; sets *noop for M == 0.
 int validate_rows(const void* x, int64_t M, int64_t N, int dtype, bool* noop) {
   *noop = false;
-  if (dtype != SOFTMAX_F32 && dtype != SOFTMAX_BF16) return SOFTMAX_ERR_INVALID_ARG;
+  if (dtype != SOFTMAX_F32 && dtype != SOFTMAX_BF16 && dtype != SOFTMAX_F16) return SOFTMAX_ERR_INVALID_ARG;
   if (N < 1 || M < 0) return SOFTMAX_ERR_INVALID_ARG;
   const int64_t s = elem_bytes(dtype);
   if (N > INT64_MAX / s) return SOFTMAX_ERR_INVALID_ARG;

@@ -317,6 +317,87 @@ struct BF16 {
   }
 };
 
+// IEEE binary16: conversions by cvt (exact widening, round-to-nearest-even narrowing, subnormals
+// kept), packed max.f16x2 for the maximum.
+__device__ __forceinline__ float f16_lo(uint32_t w) {
+  float f;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, l;\n\t}" : "=f"(f) : "r"(w));
+  return f;
+}
+__device__ __forceinline__ float f16_hi(uint32_t w) {
+  float f;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, h;\n\t}" : "=f"(f) : "r"(w));
+  return f;
+}
+// Two fp32 -> packed f16x2 (lo in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+struct F16 {
+  static constexpr int kVec = 8;
+  static constexpr int kBytes = 2;
+  static constexpr uint32_t kNegInfWord = 0xfc00fc00u;
+  __device__ static __forceinline__ void unpack(const uint4& v, float (&f)[8]) {
+    f[0] = f16_lo(v.x);
+    f[1] = f16_hi(v.x);
+    f[2] = f16_lo(v.y);
+    f[3] = f16_hi(v.y);
+    f[4] = f16_lo(v.z);
+    f[5] = f16_hi(v.z);
+    f[6] = f16_lo(v.w);
+    f[7] = f16_hi(v.w);
+  }
+  __device__ static __forceinline__ uint4 pack(const float (&f)[8]) {
+    return make_uint4(pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]),
+                      pack_f16x2(f[6], f[7]));
+  }
+  __device__ static __forceinline__ void unpack2(const uint4& v, float2 (&f)[4]) {
+    f[0] = make_float2(f16_lo(v.x), f16_hi(v.x));
+    f[1] = make_float2(f16_lo(v.y), f16_hi(v.y));
+    f[2] = make_float2(f16_lo(v.z), f16_hi(v.z));
+    f[3] = make_float2(f16_lo(v.w), f16_hi(v.w));
+  }
+  __device__ static __forceinline__ uint4 pack2(const float2 (&f)[4]) {
+    return make_uint4(pack_f16x2(f[0].x, f[0].y), pack_f16x2(f[1].x, f[1].y), pack_f16x2(f[2].x, f[2].y),
+                      pack_f16x2(f[3].x, f[3].y));
+  }
+  __device__ static __forceinline__ float load1(const void* p, int64_t i) {
+    const unsigned short b = __ldg(static_cast<const unsigned short*>(p) + i);
+    return f16_lo(b);
+  }
+  __device__ static __forceinline__ float lds1(uint32_t slot, int64_t i) {
+    unsigned short b;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(b) : "r"(slot + uint32_t(i) * 2u) : "memory");
+    return f16_lo(b);
+  }
+  // Largest of the vector's eight values: packed f16x2 max (exact), then one widening.
+  __device__ static __forceinline__ float vmax(const uint4& v) {
+    uint32_t a, b, m;
+    asm("max.f16x2 %0, %1, %2;" : "=r"(a) : "r"(v.x), "r"(v.y));
+    asm("max.f16x2 %0, %1, %2;" : "=r"(b) : "r"(v.z), "r"(v.w));
+    asm("max.f16x2 %0, %1, %2;" : "=r"(m) : "r"(a), "r"(b));
+    return fmaxf(f16_lo(m), f16_hi(m));
+  }
+  template <int n>
+  __device__ static __forceinline__ float vmax_all(const uint4 (&q)[n]) {
+    uint32_t w[4] = {q[0].x, q[0].y, q[0].z, q[0].w};
+#pragma unroll
+    for (int k = 1; k < n; ++k) {
+      asm("max.f16x2 %0, %0, %1;" : "+r"(w[0]) : "r"(q[k].x));
+      asm("max.f16x2 %0, %0, %1;" : "+r"(w[1]) : "r"(q[k].y));
+      asm("max.f16x2 %0, %0, %1;" : "+r"(w[2]) : "r"(q[k].z));
+      asm("max.f16x2 %0, %0, %1;" : "+r"(w[3]) : "r"(q[k].w));
+    }
+    return vmax(make_uint4(w[0], w[1], w[2], w[3]));
+  }
+  __device__ static __forceinline__ void store1(void* p, int64_t i, float v) {
+    static_cast<uint16_t*>(p)[i] = uint16_t(pack_f16x2(v, 0.f) & 0xffffu);
+  }
+};
+
 // Keep the first `keep` (0 < keep < kVec) elements of a packed vector and set the rest to -inf.
 template <class D>
 __device__ __forceinline__ uint4 mask_tail(uint4 v, int keep) {
@@ -327,8 +408,8 @@ __device__ __forceinline__ uint4 mask_tail(uint4 v, int keep) {
     if constexpr (per_word == 1) {
       if (i >= keep) w[i] = 0xff800000u;
     } else {
-      if (2 * i >= keep) w[i] = 0xff80ff80u;
-      else if (2 * i + 1 >= keep) w[i] = (w[i] & 0x0000ffffu) | 0xff800000u;  // high half is element 2i+1
+      if (2 * i >= keep) w[i] = D::kNegInfWord;
+      else if (2 * i + 1 >= keep) w[i] = (w[i] & 0x0000ffffu) | (D::kNegInfWord & 0xffff0000u);  // high half: 2i+1
     }
   }
   return make_uint4(w[0], w[1], w[2], w[3]);

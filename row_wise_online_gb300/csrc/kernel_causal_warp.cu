@@ -1,9 +1,10 @@
 // kernel_causal_warp.cu -- softmax of causally masked rows that never reads the masked entries.
 //
 // In causal attention a query at position q only sees keys 0..q; the scores of the later keys
-// are -inf, their exponentials 0, so they change neither m nor d ("Online normalizer
-// calculation for softmax", §3, the recurrence with e^(-inf) = 0).  Row r of the score matrix
-// therefore only has a live prefix of L_r = clamp(r % q_period + 1 + key_offset, 0, N) entries.
+// are -inf, their exponentials 0, so they change neither m nor d (the recurrence of
+// "5.2 CUDA Online Softmax 实现优化" §2.1 with e^(-inf) = 0), and "Softmax 数值稳定性与
+// IO-Aware Attention" §八 skips such fully masked blocks.  Row r of the score matrix therefore
+// only has a live prefix of L_r = clamp(r % q_period + 1 + key_offset, 0, N) entries.
 // This kernel folds and normalises that prefix and writes y = 0 for the rest without reading it:
 // on a square causal mask it reads about half of x.
 //
@@ -236,12 +237,12 @@ using CausalKernel = void (*)(CausalArgs);
 
 struct CausalConfig {
   int vpl;  // 16-byte vectors per lane (row capacity 32 * vpl vectors)
-  CausalKernel f32, bf16;
+  CausalKernel fn[3];  // [dtype]
 };
 
 template <int VPL>
 constexpr CausalConfig causal_cfg() {
-  return CausalConfig{VPL, k_causal_warp<F32, VPL>, k_causal_warp<BF16, VPL>};
+  return CausalConfig{VPL, {k_causal_warp<F32, VPL>, k_causal_warp<BF16, VPL>, k_causal_warp<F16, VPL>}};
 }
 
 const CausalConfig kCausalCfg[] = {causal_cfg<4>(), causal_cfg<8>(), causal_cfg<16>(), causal_cfg<32>()};
@@ -296,7 +297,7 @@ bool causal_warp_fits(const RowProblem& p, const DeviceInfo& dev) { return plan_
 cudaError_t launch_causal_warp(const RowProblem& p, const DeviceInfo& dev, int64_t q_period, int64_t key_offset) {
   const CausalPlan plan = plan_causal(p, dev);
   if (!plan.cfg || q_period < 1) return cudaErrorInvalidValue;
-  CausalKernel fn = p.dtype == 0 ? plan.cfg->f32 : plan.cfg->bf16;
+  CausalKernel fn = plan.cfg->fn[p.dtype];
   cudaError_t err = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(plan.smem));
   if (err != cudaSuccess) return err;

@@ -250,15 +250,18 @@ using TmaKernel = void (*)(TmaArgs);
 
 struct TmaConfig {
   int ncw, vpt;
-  TmaKernel fn[3][2];  // [output mode][dtype]
+  TmaKernel fn[3][3];  // [output mode][dtype]
 };
 
 template <int VPT, int NCW>
 constexpr TmaConfig tma_cfg() {
   return TmaConfig{NCW, VPT,
-                   {{k_oneread_tma<F32, VPT, NCW, kTmaProb>, k_oneread_tma<BF16, VPT, NCW, kTmaProb>},
-                    {k_oneread_tma<F32, VPT, NCW, kTmaLog>, k_oneread_tma<BF16, VPT, NCW, kTmaLog>},
-                    {k_oneread_tma<F32, VPT, NCW, kTmaState>, k_oneread_tma<BF16, VPT, NCW, kTmaState>}}};
+                   {{k_oneread_tma<F32, VPT, NCW, kTmaProb>, k_oneread_tma<BF16, VPT, NCW, kTmaProb>,
+                     k_oneread_tma<F16, VPT, NCW, kTmaProb>},
+                    {k_oneread_tma<F32, VPT, NCW, kTmaLog>, k_oneread_tma<BF16, VPT, NCW, kTmaLog>,
+                     k_oneread_tma<F16, VPT, NCW, kTmaLog>},
+                    {k_oneread_tma<F32, VPT, NCW, kTmaState>, k_oneread_tma<BF16, VPT, NCW, kTmaState>,
+                     k_oneread_tma<F16, VPT, NCW, kTmaState>}}};
 }
 
 // Ordered by capacity (16-byte units per row = 32 * ncw * vpt).
@@ -324,7 +327,7 @@ cudaError_t launch_oneread_tma(const RowProblem& p, const DeviceInfo& dev) {
   if (!plan.cfg) return cudaErrorInvalidValue;
   const int out = p.y == nullptr ? kTmaState : p.log_out ? kTmaLog : kTmaProb;
   if (p.loss && out != kTmaState) return cudaErrorInvalidValue;
-  TmaKernel fn = plan.cfg->fn[out][p.dtype == 0 ? 0 : 1];
+  TmaKernel fn = plan.cfg->fn[out][p.dtype];
   cudaError_t err = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(plan.smem));
   if (err != cudaSuccess) return err;

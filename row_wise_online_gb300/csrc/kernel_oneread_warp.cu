@@ -148,12 +148,12 @@ using WarpKernel = void (*)(WarpArgs);
 
 struct WarpConfig {
   int vpl;  // 16-byte vectors per lane (row capacity 32 * vpl vectors)
-  WarpKernel f32, bf16;
+  WarpKernel fn[3];  // [dtype]
 };
 
 template <int VPL>
 constexpr WarpConfig warp_cfg() {
-  return WarpConfig{VPL, k_oneread_warp<F32, VPL>, k_oneread_warp<BF16, VPL>};
+  return WarpConfig{VPL, {k_oneread_warp<F32, VPL>, k_oneread_warp<BF16, VPL>, k_oneread_warp<F16, VPL>}};
 }
 
 const WarpConfig kWarpCfg[] = {warp_cfg<4>(), warp_cfg<8>(), warp_cfg<16>(), warp_cfg<32>()};
@@ -208,7 +208,7 @@ bool oneread_warp_fits(const RowProblem& p, const DeviceInfo& dev) { return plan
 cudaError_t launch_oneread_warp(const RowProblem& p, const DeviceInfo& dev) {
   const WarpPlan plan = plan_warp(p, dev);
   if (!plan.cfg) return cudaErrorInvalidValue;
-  WarpKernel fn = p.dtype == 0 ? plan.cfg->f32 : plan.cfg->bf16;
+  WarpKernel fn = plan.cfg->fn[p.dtype];
   cudaError_t err = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(plan.smem));
   if (err != cudaSuccess) return err;

@@ -440,7 +440,9 @@ __global__ void __launch_bounds__(kSplitThreads, 1) k_splitrow(SplitArgs a) {
 
 using SplitKernel = void (*)(SplitArgs);
 
-SplitKernel split_kernel(int dtype) { return dtype == 0 ? k_splitrow<F32> : k_splitrow<BF16>; }
+SplitKernel split_kernel(int dtype) {
+  return dtype == 0 ? k_splitrow<F32> : dtype == 1 ? k_splitrow<BF16> : k_splitrow<F16>;
+}
 
 struct SplitPlan {
   bool ok = false;
@@ -451,8 +453,8 @@ struct SplitPlan {
 };
 
 std::mutex g_plan_mutex;
-SplitPlan g_plan[64][2];
-bool g_plan_ready[64][2];
+SplitPlan g_plan[64][3];
+bool g_plan_ready[64][3];
 
 // Cluster size and count giving the most resident CTAs (one per SM), and the ring size.
 SplitPlan plan_for(int dtype, const DeviceInfo& dev) {

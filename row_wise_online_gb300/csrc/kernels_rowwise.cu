@@ -146,13 +146,16 @@ using RowKernel = void (*)(RowArgs);
 
 struct RegConfig {
   int wpr, vpt;
-  RowKernel f32, bf16, f32_log, bf16_log;
+  RowKernel fn[2][3];  // [log output][dtype]
 };
 
 template <int VPT, int WPR, bool VEC>
 constexpr RegConfig reg_cfg() {
-  return RegConfig{WPR, VPT, k_oneread_reg<F32, VPT, WPR, VEC, false>, k_oneread_reg<BF16, VPT, WPR, VEC, false>,
-                   k_oneread_reg<F32, VPT, WPR, VEC, true>, k_oneread_reg<BF16, VPT, WPR, VEC, true>};
+  return RegConfig{WPR, VPT,
+                   {{k_oneread_reg<F32, VPT, WPR, VEC, false>, k_oneread_reg<BF16, VPT, WPR, VEC, false>,
+                     k_oneread_reg<F16, VPT, WPR, VEC, false>},
+                    {k_oneread_reg<F32, VPT, WPR, VEC, true>, k_oneread_reg<BF16, VPT, WPR, VEC, true>,
+                     k_oneread_reg<F16, VPT, WPR, VEC, true>}}};
 }
 
 // Ordered by capacity (units per row = 32 * wpr * vpt).
@@ -345,7 +348,7 @@ cudaError_t launch_oneread_reg(const RowProblem& p, bool vec, const DeviceInfo& 
   const int64_t e = vec ? 16 / elem_bytes(p.dtype) : 1;
   const RegConfig* cfg = pick_reg(p.N / e, vec);
   if (!cfg) return cudaErrorInvalidValue;
-  RowKernel fn = p.dtype == 0 ? (p.log_out ? cfg->f32_log : cfg->f32) : (p.log_out ? cfg->bf16_log : cfg->bf16);
+  RowKernel fn = cfg->fn[p.log_out ? 1 : 0][p.dtype];
   const int groups = (kRegThreads / 32) / cfg->wpr;
   const int64_t want = ceil_div(p.M, groups);
   const int64_t cap = int64_t(dev.sm_count) * blocks_per_sm((const void*)fn, kRegThreads, 0);
@@ -365,7 +368,7 @@ cudaError_t launch_twopass(const RowProblem& p, bool vec, const DeviceInfo& dev,
   const int mode = p.y == nullptr ? kStateOnly : causal ? kProbCausal : p.log_out ? kLogProb : kProb;
   if ((causal && p.log_out) || (p.loss && mode != kStateOnly)) return cudaErrorInvalidValue;
   // [dtype][vec][mode]
-  static const RowKernel table[2][2][4] = {
+  static const RowKernel table[3][2][4] = {
       {{k_twopass<F32, false, kProb>, k_twopass<F32, false, kProbCausal>, k_twopass<F32, false, kLogProb>,
         k_twopass<F32, false, kStateOnly>},
        {k_twopass<F32, true, kProb>, k_twopass<F32, true, kProbCausal>, k_twopass<F32, true, kLogProb>,
@@ -373,8 +376,12 @@ cudaError_t launch_twopass(const RowProblem& p, bool vec, const DeviceInfo& dev,
       {{k_twopass<BF16, false, kProb>, k_twopass<BF16, false, kProbCausal>, k_twopass<BF16, false, kLogProb>,
         k_twopass<BF16, false, kStateOnly>},
        {k_twopass<BF16, true, kProb>, k_twopass<BF16, true, kProbCausal>, k_twopass<BF16, true, kLogProb>,
-        k_twopass<BF16, true, kStateOnly>}}};
-  RowKernel fn = table[p.dtype == 0 ? 0 : 1][vec ? 1 : 0][mode];
+        k_twopass<BF16, true, kStateOnly>}},
+      {{k_twopass<F16, false, kProb>, k_twopass<F16, false, kProbCausal>, k_twopass<F16, false, kLogProb>,
+        k_twopass<F16, false, kStateOnly>},
+       {k_twopass<F16, true, kProb>, k_twopass<F16, true, kProbCausal>, k_twopass<F16, true, kLogProb>,
+        k_twopass<F16, true, kStateOnly>}}};
+  RowKernel fn = table[p.dtype][vec ? 1 : 0][mode];
   const int64_t cap = int64_t(dev.sm_count) * blocks_per_sm((const void*)fn, nt, 0);
   const int grid = int(p.M < cap ? p.M : cap);
   RowArgs a = row_args(p, dev);

@@ -46,7 +46,7 @@ using namespace rwo;
 
 extern "C" int softmax_rows_splitrow_noalloc(const void* x, void* y, float* m_out, float* d_out, float* lse_out,
                                              int64_t M, int64_t N, int dtype, void* stream) {
-  if (dtype != SOFTMAX_F32 && dtype != SOFTMAX_BF16) return SOFTMAX_ERR_INVALID_ARG;
+  if (dtype != SOFTMAX_F32 && dtype != SOFTMAX_BF16 && dtype != SOFTMAX_F16) return SOFTMAX_ERR_INVALID_ARG;
   if (N < 1 || M < 0) return SOFTMAX_ERR_INVALID_ARG;
   const int64_t s = elem_bytes(dtype);
   if (N > INT64_MAX / s) return SOFTMAX_ERR_INVALID_ARG;

@@ -8,14 +8,16 @@ import row_wise_online_gb300 as rwo
 import synth
 
 
-def to_device(x_host: np.ndarray) -> torch.Tensor:
+def to_device(x_host: np.ndarray, dtype: int | None = None) -> torch.Tensor:
+    """uint16 host arrays are bf16 bit patterns unless dtype is synth.F16."""
     if x_host.dtype == np.uint16:
-        return torch.from_numpy(np.ascontiguousarray(x_host).view(np.int16)).cuda().view(torch.bfloat16)
+        t = torch.from_numpy(np.ascontiguousarray(x_host).view(np.int16)).cuda()
+        return t.view(torch.float16 if dtype == synth.F16 else torch.bfloat16)
     return torch.from_numpy(np.ascontiguousarray(x_host)).cuda()
 
 
 def to_host(y: torch.Tensor) -> np.ndarray:
-    if y.dtype == torch.bfloat16:
+    if y.dtype in (torch.bfloat16, torch.float16):
         return y.view(torch.int16).cpu().numpy().view(np.uint16)
     return y.cpu().numpy()
 

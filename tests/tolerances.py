@@ -4,7 +4,9 @@ Tolerances (per element, against the oracle's exact fp64 result y_ref):
   * fp32 output: |y - y_ref| <= 1e-5 * |y_ref| + 2^-126
   * bf16 output: |y - y_ref| <= ulp_bf16(y_ref) + 2^-126, ulp_bf16(v) = 2^(floor(log2|v|) - 7)
     (one unit in the last place of bf16's 8-bit significand)
-  * row sums:    |sum_j y_j - 1| <= 1e-5 (fp32) / 4e-3 (bf16), for rows that are not fully masked
+  * fp16 output: |y - y_ref| <= ulp_f16(y_ref) + 2^-126, ulp_f16(v) = 2^(max(floor(log2|v|), -14) - 10)
+    (one unit in the last place of fp16's 11-bit significand; subnormal spacing below 2^-14)
+  * row sums:    |sum_j y_j - 1| <= 1e-5 (fp32) / 4e-3 (bf16) / 1e-3 (fp16), rows not fully masked
   * m:           bit-exact (as fp32; -0 == +0)
   * d:           |d - d_ref| <= 1e-5 * d_ref
   * LSE:         |LSE - LSE_ref| <= 1e-5 * max(1, |LSE_ref|)
@@ -27,6 +29,7 @@ TINY = 2.0 ** -126
 Y_REL_F32 = 1e-5
 ROWSUM_F32 = 1e-5
 ROWSUM_BF16 = 4e-3
+ROWSUM_F16 = 1e-3
 D_REL = 1e-5
 LSE_REL = 1e-5
 
@@ -38,8 +41,20 @@ def bf16_ulp(v: np.ndarray) -> np.ndarray:
     return np.where(a > 0, np.exp2(e - 7), 0.0)
 
 
+def f16_ulp(v: np.ndarray) -> np.ndarray:
+    """Spacing of fp16 at |v|: 2^(floor(log2|v|) - 10), 2^-24 in the subnormal range."""
+    a = np.abs(v)
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.exp2(np.maximum(e, -14.0) - 10)
+
+
 def output_as_f64(y: np.ndarray, dtype: int) -> np.ndarray:
-    return (synth.bf16_to_f32(y) if dtype == synth.BF16 else y).astype(np.float64)
+    if dtype == synth.BF16:
+        return synth.bf16_to_f32(y).astype(np.float64)
+    if dtype == synth.F16:
+        return synth.f16_to_f32(y).astype(np.float64)
+    return y.astype(np.float64)
 
 
 def check_y(y: np.ndarray, y_ref: np.ndarray, dtype: int, what: str = "") -> dict:
@@ -49,6 +64,8 @@ def check_y(y: np.ndarray, y_ref: np.ndarray, dtype: int, what: str = "") -> dic
     err = np.abs(yg - y_ref)
     if dtype == synth.F32:
         bound = Y_REL_F32 * np.abs(y_ref) + TINY
+    elif dtype == synth.F16:
+        bound = f16_ulp(y_ref) + TINY
     else:
         bound = bf16_ulp(y_ref) + TINY
     bad = ~(err <= bound)
@@ -68,7 +85,7 @@ def check_rowsums(y: np.ndarray, dtype: int, masked_rows=None, what: str = "") -
     yg = output_as_f64(y, dtype)
     s = yg.sum(axis=1)
     keep = np.ones(len(s), bool) if masked_rows is None else ~np.asarray(masked_rows, bool)
-    tol = ROWSUM_F32 if dtype == synth.F32 else ROWSUM_BF16
+    tol = ROWSUM_F32 if dtype == synth.F32 else ROWSUM_F16 if dtype == synth.F16 else ROWSUM_BF16
     dev = np.abs(s[keep] - 1.0)
     assert np.all(dev <= tol), f"{what}: row sum off by {dev.max()}"
     if masked_rows is not None:
@@ -109,6 +126,8 @@ def check_log_values(v: np.ndarray, v_ref: np.ndarray, dtype: int, what: str = "
     bound = LSE_REL * np.maximum(1.0, np.abs(v_ref[fin]))
     if dtype == synth.BF16:
         bound = bound + bf16_ulp(v_ref[fin])
+    elif dtype == synth.F16:
+        bound = bound + f16_ulp(v_ref[fin])
     bad = ~(err <= bound)
     if bad.any():
         k = int(np.argmax(bad))
