@@ -62,13 +62,14 @@ def _load():
         if _lib is None:
             lib = ctypes.CDLL(build())
             i64, dp, vp = ctypes.c_int64, ctypes.POINTER(ctypes.c_double), ctypes.c_void_p
-            lib.oracle_softmax_rows.argtypes = [vp, ctypes.c_int, i64, vp, i64, vp, vp, vp, vp, ctypes.c_int]
-            lib.oracle_softmax_rows.restype = ctypes.c_int
+            lib.oracle_softmax_rows_scaled.argtypes = [vp, ctypes.c_int, i64, vp, i64, ctypes.c_double, vp, vp, vp,
+                                                       vp, ctypes.c_int]
+            lib.oracle_softmax_rows_scaled.restype = ctypes.c_int
             lib.oracle_online_state.argtypes = [vp, i64, dp, dp]
             lib.oracle_online_state.restype = None
             lib.oracle_merge_state.argtypes = [ctypes.c_double] * 4 + [dp, dp]
             lib.oracle_merge_state.restype = None
-            lib.oracle_log_softmax_rows.argtypes = [vp, ctypes.c_int, i64, vp, i64, vp, ctypes.c_int]
+            lib.oracle_log_softmax_rows.argtypes = [vp, ctypes.c_int, i64, vp, i64, ctypes.c_double, vp, ctypes.c_int]
             lib.oracle_log_softmax_rows.restype = ctypes.c_int
             lib.oracle_cross_entropy_rows.argtypes = [vp, ctypes.c_int, i64, vp, i64, vp, ctypes.c_int]
             lib.oracle_cross_entropy_rows.restype = ctypes.c_int
@@ -85,8 +86,8 @@ def default_threads() -> int:
 
 
 def softmax_rows(x: np.ndarray, dtype: int | None = None, rows=None, *, want_y: bool = True,
-                 nthreads: int | None = None):
-    """Three-pass fp64 softmax of rows of a row-major matrix.
+                 nthreads: int | None = None, scale: float = 1.0):
+    """Three-pass fp64 softmax of rows of a row-major matrix (of scale * x; exact in fp64).
 
     ``x`` is a 2-D float32 array, or a 2-D uint16 array of bf16 bit patterns.
     ``rows`` selects rows (default: all).  Returns ``(y, m, d, lse)`` as
@@ -114,8 +115,10 @@ def softmax_rows(x: np.ndarray, dtype: int | None = None, rows=None, *, want_y: 
     lse = np.empty(nrows, np.float64)
     if nrows == 0:
         return y, m, d, lse
-    rc = _load().oracle_softmax_rows(_ptr(x), dtype, N, _ptr(idx), nrows, _ptr(y), _ptr(m), _ptr(d),
-                                     _ptr(lse), nthreads or default_threads())
+    if not scale > 0:
+        raise ValueError("scale must be > 0")
+    rc = _load().oracle_softmax_rows_scaled(_ptr(x), dtype, N, _ptr(idx), nrows, float(scale), _ptr(y), _ptr(m),
+                                            _ptr(d), _ptr(lse), nthreads or default_threads())
     if rc != 0:
         raise RuntimeError("oracle_softmax_rows rejected its arguments")
     return y, m, d, lse
@@ -132,7 +135,8 @@ def _matrix(x, dtype):
     return x, dtype
 
 
-def log_softmax_rows(x: np.ndarray, dtype: int | None = None, rows=None, *, nthreads: int | None = None):
+def log_softmax_rows(x: np.ndarray, dtype: int | None = None, rows=None, *, nthreads: int | None = None,
+                     scale: float = 1.0):
     """fp64 log softmax of rows of a row-major matrix (all -inf row: -inf).  Returns (nrows, N) float64."""
     x, dtype = _matrix(x, dtype)
     M, N = x.shape
@@ -143,7 +147,8 @@ def log_softmax_rows(x: np.ndarray, dtype: int | None = None, rows=None, *, nthr
     ly = np.empty((nrows, N), np.float64)
     if nrows == 0:
         return ly
-    rc = _load().oracle_log_softmax_rows(_ptr(x), dtype, N, _ptr(idx), nrows, _ptr(ly), nthreads or default_threads())
+    rc = _load().oracle_log_softmax_rows(_ptr(x), dtype, N, _ptr(idx), nrows, float(scale), _ptr(ly),
+                                         nthreads or default_threads())
     if rc != 0:
         raise RuntimeError("oracle_log_softmax_rows rejected its arguments")
     return ly

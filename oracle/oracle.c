@@ -17,6 +17,9 @@
  *      and the log-sum-exp  LSE = m + log(d)
  *      ("从原始Softmax到在线Softmax", section "softmax形式推导").
  *
+ *  Every row function takes the softmax of z = scale * x (scale > 0; z is exact
+ *  in double), which is x itself for scale 1.
+ *
  *  oracle_log_softmax_rows -- the log of the softmax, as the page's
  *      log_probs = x - max - log(sum_j exp(x_j - max))
  *      ("从原始Softmax到在线Softmax", section "softmax实际代码实现").
@@ -83,8 +86,14 @@ static double scaled_exp(double a, double b) {
   return exp(a - b);
 }
 
-/* Three-pass safe softmax of row `row`; y may be NULL (state only). */
-static void softmax_one_row(const void* x, int dtype, int64_t N, int64_t row,
+/* The softmax input z = scale * x (exact in double: a 24-bit scale times a value of at most 24
+ * significant bits). */
+static double load_z(const void* x, int dtype, int64_t i, double scale) {
+  return scale * load_elem(x, dtype, i);
+}
+
+/* Three-pass safe softmax of row `row` of z = scale * x; y may be NULL (state only). */
+static void softmax_one_row(const void* x, int dtype, int64_t N, int64_t row, double scale,
                             double* y, double* m_out, double* d_out,
                             double* lse_out) {
   const int64_t base = row * N;
@@ -92,18 +101,18 @@ static void softmax_one_row(const void* x, int dtype, int64_t N, int64_t row,
   /* pass 1: the row maximum */
   double m = -INFINITY;
   for (int64_t j = 0; j < N; ++j) {
-    double v = load_elem(x, dtype, base + j);
+    double v = load_z(x, dtype, base + j, scale);
     if (v > m) m = v;
   }
 
   /* pass 2: the denominator */
   double d = 0.0;
-  for (int64_t j = 0; j < N; ++j) d += scaled_exp(load_elem(x, dtype, base + j), m);
+  for (int64_t j = 0; j < N; ++j) d += scaled_exp(load_z(x, dtype, base + j, scale), m);
 
   /* pass 3: normalise */
   if (y) {
     for (int64_t j = 0; j < N; ++j) {
-      y[j] = (m == -INFINITY) ? 0.0 : scaled_exp(load_elem(x, dtype, base + j), m) / d;
+      y[j] = (m == -INFINITY) ? 0.0 : scaled_exp(load_z(x, dtype, base + j, scale), m) / d;
     }
   }
   if (m_out) *m_out = m;
@@ -119,13 +128,14 @@ typedef struct {
   int64_t nrows;
   double *y, *m, *d, *lse;
   int64_t begin, end; /* slice of [0, nrows) handled by this thread */
+  double scale;
 } oracle_job;
 
 static void* oracle_worker(void* arg) {
   oracle_job* job = (oracle_job*)arg;
   for (int64_t i = job->begin; i < job->end; ++i) {
     int64_t row = job->rows ? job->rows[i] : i;
-    softmax_one_row(job->x, job->dtype, job->N, row,
+    softmax_one_row(job->x, job->dtype, job->N, row, job->scale,
                     job->y ? job->y + i * job->N : NULL,
                     job->m ? job->m + i : NULL, job->d ? job->d + i : NULL,
                     job->lse ? job->lse + i : NULL);
@@ -134,15 +144,16 @@ static void* oracle_worker(void* arg) {
 }
 
 /*
- * Softmax of selected rows of a row-major matrix x (dtype ORACLE_F32 or
- * ORACLE_BF16, N columns).  rows[i] is the i-th row to compute, or rows ==
+ * Softmax of z = scale * x for selected rows of a row-major matrix x (dtype
+ * ORACLE_F32, ORACLE_BF16 or ORACLE_F16, N columns); scale > 0.  rows[i] is the i-th row to compute, or rows ==
  * NULL for rows 0..nrows-1.  Outputs are indexed by i: y is nrows x N,
  * m / d / lse have nrows entries; each output may be NULL.  Returns 0, or -1
  * on a bad argument.
  */
-int oracle_softmax_rows(const void* x, int dtype, int64_t N,
-                        const int64_t* rows, int64_t nrows, double* y,
-                        double* m, double* d, double* lse, int nthreads) {
+int oracle_softmax_rows_scaled(const void* x, int dtype, int64_t N,
+                               const int64_t* rows, int64_t nrows, double scale,
+                               double* y, double* m, double* d, double* lse,
+                               int nthreads) {
   if (!x || N < 1 || nrows < 0) return -1;
   if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F16) return -1;
   if (nrows == 0) return 0;
@@ -158,7 +169,7 @@ int oracle_softmax_rows(const void* x, int dtype, int64_t N,
   }
   for (int t = 0; t < nthreads; ++t) {
     oracle_job job = {x, dtype, N, rows, nrows, y, m, d, lse,
-                      nrows * t / nthreads, nrows * (t + 1) / nthreads};
+                      nrows * t / nthreads, nrows * (t + 1) / nthreads, scale};
     jobs[t] = job;
     if (t == 0) continue; /* the calling thread takes slice 0 */
     if (pthread_create(&tids[t], NULL, oracle_worker, &jobs[t]) != 0) {
@@ -174,16 +185,23 @@ int oracle_softmax_rows(const void* x, int dtype, int64_t N,
   return 0;
 }
 
+/* The softmax of x itself (scale 1). */
+int oracle_softmax_rows(const void* x, int dtype, int64_t N, const int64_t* rows, int64_t nrows,
+                        double* y, double* m, double* d, double* lse, int nthreads) {
+  return oracle_softmax_rows_scaled(x, dtype, N, rows, nrows, 1.0, y, m, d, lse, nthreads);
+}
+
 /* The row's m and d (passes 1 and 2 of the three-pass softmax above). */
-static void row_max_and_sum(const void* x, int dtype, int64_t N, int64_t row, double* m_out, double* d_out) {
+static void row_max_and_sum(const void* x, int dtype, int64_t N, int64_t row, double scale, double* m_out,
+                            double* d_out) {
   const int64_t base = row * N;
   double m = -INFINITY;
   for (int64_t j = 0; j < N; ++j) {
-    double v = load_elem(x, dtype, base + j);
+    double v = load_z(x, dtype, base + j, scale);
     if (v > m) m = v;
   }
   double d = 0.0;
-  for (int64_t j = 0; j < N; ++j) d += scaled_exp(load_elem(x, dtype, base + j), m);
+  for (int64_t j = 0; j < N; ++j) d += scaled_exp(load_z(x, dtype, base + j, scale), m);
   *m_out = m;
   *d_out = d;
 }
@@ -196,6 +214,7 @@ typedef struct {
   const int64_t* labels; /* cross entropy: one label per row */
   double* out;           /* log softmax: nrows x N; cross entropy: nrows */
   int64_t begin, end;
+  double scale;
 } oracle_log_job;
 
 static void* oracle_log_worker(void* arg) {
@@ -203,13 +222,13 @@ static void* oracle_log_worker(void* arg) {
   for (int64_t i = job->begin; i < job->end; ++i) {
     int64_t row = job->rows ? job->rows[i] : i;
     double m, d;
-    row_max_and_sum(job->x, job->dtype, job->N, row, &m, &d);
+    row_max_and_sum(job->x, job->dtype, job->N, row, job->scale, &m, &d);
     /* log_probs = x - max - log(sum_exp); all -inf row: -inf */
     double log_d = (m == -INFINITY) ? INFINITY : log(d);
     double shift = (m == -INFINITY) ? 0.0 : m;
     if (!job->labels) {
       double* ly = job->out + i * job->N;
-      for (int64_t j = 0; j < job->N; ++j) ly[j] = load_elem(job->x, job->dtype, row * job->N + j) - shift - log_d;
+      for (int64_t j = 0; j < job->N; ++j) ly[j] = load_z(job->x, job->dtype, row * job->N + j, job->scale) - shift - log_d;
     } else {
       int64_t label = job->labels[i];
       double loss;
@@ -218,7 +237,7 @@ static void* oracle_log_worker(void* arg) {
       } else if (label >= job->N) {
         loss = NAN;
       } else {
-        double xl = load_elem(job->x, job->dtype, row * job->N + label);
+        double xl = load_z(job->x, job->dtype, row * job->N + label, job->scale);
         loss = (m == -INFINITY) ? NAN : -(xl - m - log(d));
       }
       job->out[i] = loss;
@@ -256,15 +275,15 @@ static int run_log_jobs(oracle_log_job proto, int64_t nrows, int nthreads) {
 }
 
 /*
- * Log softmax of selected rows (rows == NULL: rows 0..nrows-1) into ly
- * (nrows x N).  Returns 0, or -1 on a bad argument.
+ * Log softmax of z = scale * x for selected rows (rows == NULL: rows
+ * 0..nrows-1) into ly (nrows x N).  Returns 0, or -1 on a bad argument.
  */
 int oracle_log_softmax_rows(const void* x, int dtype, int64_t N, const int64_t* rows, int64_t nrows,
-                            double* ly, int nthreads) {
-  if (!x || !ly || N < 1 || nrows < 0) return -1;
+                            double scale, double* ly, int nthreads) {
+  if (!x || !ly || N < 1 || nrows < 0 || !(scale > 0.0)) return -1;
   if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F16) return -1;
   if (nrows == 0) return 0;
-  oracle_log_job proto = {x, dtype, N, rows, NULL, ly, 0, 0};
+  oracle_log_job proto = {x, dtype, N, rows, NULL, ly, 0, 0, scale};
   return run_log_jobs(proto, nrows, nthreads);
 }
 
@@ -277,7 +296,7 @@ int oracle_cross_entropy_rows(const void* x, int dtype, int64_t N, const int64_t
   if (!x || !labels || !loss || N < 1 || M < 0) return -1;
   if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F16) return -1;
   if (M == 0) return 0;
-  oracle_log_job proto = {x, dtype, N, NULL, labels, loss, 0, 0};
+  oracle_log_job proto = {x, dtype, N, NULL, labels, loss, 0, 0, 1.0};
   return run_log_jobs(proto, M, nthreads);
 }
 

@@ -423,3 +423,32 @@ def test_f16_input_is_widened_exactly():
         np.testing.assert_array_equal(a, b)
     np.testing.assert_array_equal(oracle.log_softmax_rows(x16.view(np.uint16), dtype=oracle.F16),
                                   oracle.log_softmax_rows(x16.astype(np.float32)))
+
+
+def test_scaled_softmax_pins():
+    """softmax(scale * x): a power-of-two scale equals the pre-multiplied input exactly; any other
+    scale (here fp32(1/sqrt(128)), attention's 1/sqrt(d)) against a 50-digit brute force."""
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal((5, 40)) * 4).astype(np.float32)
+    for k in (-3, 1, 4):
+        a = oracle.softmax_rows(x, scale=2.0 ** k)
+        b = oracle.softmax_rows((x * np.float32(2.0 ** k)).astype(np.float32))
+        for u, v in zip(a, b):
+            np.testing.assert_array_equal(u, v)
+        np.testing.assert_array_equal(oracle.log_softmax_rows(x, scale=2.0 ** k),
+                                      oracle.log_softmax_rows((x * np.float32(2.0 ** k)).astype(np.float32)))
+    s = float(np.float32(1.0 / np.sqrt(128.0)))
+    y, m, d, lse = oracle.softmax_rows(x, scale=s)
+    ly = oracle.log_softmax_rows(x, scale=s)
+    for r in range(x.shape[0]):
+        with mpmath.workdps(50):
+            z = [mpmath.mpf(s) * mpmath.mpf(float(v)) for v in x[r]]
+            mz = max(z)
+            dz = mpmath.fsum(mpmath.exp(t - mz) for t in z)
+            for j in range(x.shape[1]):
+                assert abs(y[r, j] - float(mpmath.exp(z[j] - mz) / dz)) <= 1e-15 * y[r, j] + 1e-300
+                assert abs(ly[r, j] - float(z[j] - mz - mpmath.log(dz))) <= 1e-14 * max(1.0, abs(ly[r, j]))
+            assert m[r] == float(mz)
+            assert abs(d[r] - float(dz)) <= 1e-14 * float(dz)
+    with pytest.raises(ValueError):
+        oracle.softmax_rows(x, scale=0.0)
