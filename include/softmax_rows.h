@@ -123,6 +123,32 @@ int softmax_rows_ex(const void* x, void* y, float* m_out, float* d_out, float* l
 int softmax_rows_causal(const void* x, void* y, float* m_out, float* d_out, float* lse_out, int64_t M,
                         int64_t N, int64_t q_period, int64_t key_offset, int dtype, void* stream);
 
+/* Flags of softmax_rows_strided. */
+enum softmax_flags { SOFTMAX_FLAG_LOG = 1 /* y = log softmax instead of softmax */ };
+
+/*
+ * softmax_rows_strided -- softmax_rows_ex with a row pitch, a scale and an output choice:
+ *     y[r, j] = softmax(scale * x[r, :])_j        (flags = 0)
+ *     y[r, j] = log softmax(scale * x[r, :])_j    (flags = SOFTMAX_FLAG_LOG)
+ * for r < M, j < N, where row r of x starts at element r * ldx and row r of y at r * ldy (a
+ * column block of a wider matrix, or rows with padding).  The scale folds into the exponent slope
+ * (scale * log2 e), as attention's 1/sqrt(d) does, at no cost per element; the state outputs
+ * describe scale * x: m_out = scale * max_j x[r, j] (rounded once, the maximum of the rounded
+ * products), d_out relative to it, LSE = m_out + ln d.
+ *   ldx, ldy -- row pitches in ELEMENTS, >= N (0 means N).
+ *   scale    -- finite and > 0 (else SOFTMAX_ERR_INVALID_ARG); 1 gives softmax_rows_ex's result.
+ *   flags    -- 0 or SOFTMAX_FLAG_LOG.
+ *   variant  -- AUTO, ONEREAD_REG, ONEREAD_SMEM (the CTA bulk-copy kernel) or TWOPASS; SPLITROW
+ *               gives SOFTMAX_ERR_UNSUPPORTED.  The vector and bulk-copy paths also need ldx * s and
+ *               ldy * s to be multiples of 16 bytes (a forced ONEREAD_SMEM otherwise returns
+ *               SOFTMAX_ERR_MISALIGNED; AUTO takes the scalar paths).
+ * x and y may be the same matrix (x == y, ldx == ldy); other overlaps are undefined.  Other
+ * arguments and errors as softmax_rows_ex.
+ */
+int softmax_rows_strided(const void* x, int64_t ldx, void* y, int64_t ldy, float* m_out, float* d_out,
+                         float* lse_out, int64_t M, int64_t N, int dtype, float scale, int flags, int variant,
+                         void* stream);
+
 /*
  * log_softmax_rows -- y = log softmax(x) row by row: y_j = x_j - LSE with LSE = m + ln d
  * ("从原始Softmax到在线Softmax", section "softmax实际代码实现": log_probs = logits - max -

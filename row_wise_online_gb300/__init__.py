@@ -39,7 +39,7 @@ EXPORTED = (
     "softmax_rows", "softmax_rows_ex", "softmax_row_state", "merge_states", "softmax_rows_host",
     "softmax_get_status", "softmax_status_string", "softmax_last_cuda_error", "softmax_last_variant",
     "softmax_debug_set_fault", "softmax_debug_set_wait_limit_ns", "softmax_rows_splitrow_noalloc",
-    "softmax_rows_causal", "log_softmax_rows", "cross_entropy_rows",
+    "softmax_rows_causal", "log_softmax_rows", "cross_entropy_rows", "softmax_rows_strided",
 )
 
 
@@ -83,11 +83,12 @@ def capi() -> ctypes.CDLL:
         lib.softmax_rows_causal.argtypes = [vp, vp, fp, fp, fp, i64, i64, i64, i64, ci, vp]
         lib.log_softmax_rows.argtypes = [vp, vp, fp, fp, fp, i64, i64, ci, ci, vp]
         lib.cross_entropy_rows.argtypes = [vp, vp, fp, fp, i64, i64, ci, vp]
+        lib.softmax_rows_strided.argtypes = [vp, i64, vp, i64, fp, fp, fp, i64, i64, ci, ctypes.c_float, ci, ci, vp]
         lib.softmax_debug_set_wait_limit_ns.restype = i64
         for name in ("softmax_rows", "softmax_rows_ex", "softmax_row_state", "merge_states",
                      "softmax_rows_host", "softmax_get_status", "softmax_last_variant",
                      "softmax_debug_set_fault", "softmax_rows_splitrow_noalloc", "softmax_rows_causal",
-                     "log_softmax_rows", "cross_entropy_rows"):
+                     "log_softmax_rows", "cross_entropy_rows", "softmax_rows_strided"):
             getattr(lib, name).restype = ci
         _lib = lib
     return _lib
@@ -198,6 +199,38 @@ def softmax_rows_causal(x, q_period: int, key_offset: int = 0, y=None, m_out=Non
                                     _ptr(_state_out(d_out, M, "d_out")), _ptr(_state_out(lse_out, M, "lse_out")),
                                     M, N, int(q_period), int(key_offset), _dtype_code(x), _stream(stream))
     _check(st, "softmax_rows_causal")
+    return y
+
+
+FLAG_LOG = 1
+
+
+def _rows_strided(t):
+    """(M, N, row pitch) of a 2-D tensor whose rows are contiguous (stride(1) == 1)."""
+    if t.dim() != 2 or t.stride(1) != 1 or (t.shape[0] > 1 and t.stride(0) < t.shape[1]):
+        raise ValueError("expected a 2-D tensor with contiguous rows (stride(1) == 1, stride(0) >= N)")
+    return int(t.shape[0]), int(t.shape[1]), int(t.stride(0)) if t.shape[0] > 1 else int(t.shape[1])
+
+
+def softmax_rows_strided(x, y=None, m_out=None, d_out=None, lse_out=None, scale: float = 1.0, log: bool = False,
+                         variant: int = VARIANT_AUTO, stream=None):
+    """softmax(scale * x) (or its log) along the last dimension of a 2-D tensor whose rows may be
+    pitched (e.g. x[:, a:b] of a wider matrix).  y defaults to a new contiguous tensor."""
+    import torch
+
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor")
+    M, N, ldx = _rows_strided(x)
+    if y is None:
+        y = torch.empty((M, N), dtype=x.dtype, device=x.device)
+    if tuple(y.shape) != (M, N) or y.dtype != x.dtype or not y.is_cuda:
+        raise ValueError("y must be a CUDA tensor with x's shape and dtype")
+    _, _, ldy = _rows_strided(y)
+    st = capi().softmax_rows_strided(_ptr(x), ldx, _ptr(y), ldy, _ptr(_state_out(m_out, M, "m_out")),
+                                     _ptr(_state_out(d_out, M, "d_out")), _ptr(_state_out(lse_out, M, "lse_out")),
+                                     M, N, _dtype_code(x), float(scale), FLAG_LOG if log else 0, int(variant),
+                                     _stream(stream))
+    _check(st, "softmax_rows_strided")
     return y
 
 

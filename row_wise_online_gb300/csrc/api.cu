@@ -287,12 +287,20 @@ int softmax_rows_causal(const void* x, void* y, float* m_out, float* d_out, floa
   return SOFTMAX_OK;
 }
 
-int log_softmax_rows(const void* x, void* y, float* m_out, float* d_out, float* lse_out, int64_t M, int64_t N,
-                     int dtype, int variant, void* stream) {
+int softmax_rows_strided(const void* x, int64_t ldx, void* y, int64_t ldy, float* m_out, float* d_out,
+                         float* lse_out, int64_t M, int64_t N, int dtype, float scale, int flags, int variant,
+                         void* stream) {
   bool noop = false;
   int st = validate_rows(x, M, N, dtype, &noop);
   if (st != SOFTMAX_OK) return st;
   if (variant < SOFTMAX_VARIANT_AUTO || variant > SOFTMAX_VARIANT_SPLITROW) return SOFTMAX_ERR_INVALID_ARG;
+  if (flags & ~SOFTMAX_FLAG_LOG) return SOFTMAX_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !(scale <= 3.4028234663852886e38f)) return SOFTMAX_ERR_INVALID_ARG;  // finite, > 0
+  if (ldx == 0) ldx = N;
+  if (ldy == 0) ldy = N;
+  if (ldx < N || ldy < N) return SOFTMAX_ERR_INVALID_ARG;
+  const int64_t s = elem_bytes(dtype);
+  if (M > 0 && (ldx > INT64_MAX / s / M || ldy > INT64_MAX / s / M)) return SOFTMAX_ERR_INVALID_ARG;
   if (noop) return SOFTMAX_OK;
   if (!y) return SOFTMAX_ERR_INVALID_ARG;
   const DeviceInfo* dev = nullptr;
@@ -306,11 +314,15 @@ int log_softmax_rows(const void* x, void* y, float* m_out, float* d_out, float* 
   p.M = M;
   p.N = N;
   p.dtype = dtype;
-  p.log_out = true;
+  p.log_out = (flags & SOFTMAX_FLAG_LOG) != 0;
+  p.x_pitch = ldx * s;
+  p.y_pitch = ldy * s;
+  p.scale = scale;
   p.stream = static_cast<cudaStream_t>(stream);
-  const bool aligned = aligned16(x) && aligned16(y) && (N * elem_bytes(dtype)) % 16 == 0;
-  const int64_t row_bytes = N * elem_bytes(dtype);
-  if (variant == SOFTMAX_VARIANT_AUTO) {  // the softmax choice, without the warp and split kernels
+  const int64_t row_bytes = N * s;
+  const bool aligned = aligned16(x) && aligned16(y) && row_bytes % 16 == 0 && p.x_pitch % 16 == 0 &&
+                       p.y_pitch % 16 == 0;
+  if (variant == SOFTMAX_VARIANT_AUTO) {  // the kernels that take a pitch and a scale
     if (aligned)
       variant = row_bytes <= 16384 && oneread_reg_fits(p, true) ? SOFTMAX_VARIANT_ONEREAD_REG
                 : oneread_tma_fits(p, *dev)                     ? SOFTMAX_VARIANT_ONEREAD_SMEM
@@ -338,6 +350,12 @@ int log_softmax_rows(const void* x, void* y, float* m_out, float* d_out, float* 
   if (err != cudaSuccess) return cuda_fail(err);
   t_last_variant = variant;
   return SOFTMAX_OK;
+}
+
+int log_softmax_rows(const void* x, void* y, float* m_out, float* d_out, float* lse_out, int64_t M, int64_t N,
+                     int dtype, int variant, void* stream) {
+  return softmax_rows_strided(x, N, y, N, m_out, d_out, lse_out, M, N, dtype, 1.f, SOFTMAX_FLAG_LOG, variant,
+                              stream);
 }
 
 int cross_entropy_rows(const void* x, const int64_t* labels, float* loss, float* lse_out, int64_t M, int64_t N,

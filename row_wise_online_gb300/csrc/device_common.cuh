@@ -31,16 +31,17 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// e^(a - b) for b finite (b is an m_safe); a = -inf gives 0.
-__device__ __forceinline__ float exp_diff(float a, float b) {
-  return ex2(__fmul_rn(__fsub_rn(a, b), kLog2e));
+// e^(c (a - b) / log2 e) for b finite (b is an m_safe); a = -inf gives 0.  c = log2 e gives
+// e^(a - b); c = scale * log2 e gives e^(scale (a - b)), the softmax of scale * x.
+__device__ __forceinline__ float exp_diff(float a, float b, float c = kLog2e) {
+  return ex2(__fmul_rn(__fsub_rn(a, b), c));
 }
 
 // The same for a pair of values, with the shift passed negated.  The packed f32x2 add and
 // multiply of sm_100 and later round each half exactly as the scalar instructions do, so this
 // gives bit for bit the two exp_diff values in half the add/multiply issue slots.
-__device__ __forceinline__ float2 exp_diff2(float2 a, float2 neg_b) {
-  const float2 t = __fmul2_rn(__fadd2_rn(a, neg_b), make_float2(kLog2e, kLog2e));
+__device__ __forceinline__ float2 exp_diff2(float2 a, float2 neg_b, float c = kLog2e) {
+  const float2 t = __fmul2_rn(__fadd2_rn(a, neg_b), make_float2(c, c));
   return make_float2(ex2(t.x), ex2(t.y));
 }
 
@@ -56,10 +57,10 @@ struct ExpShift {
   float2 log2e2, neg_mc2;
   float unscale;  // 2^-delta
 };
-__device__ __forceinline__ ExpShift exp_shift(float m) {
-  const float mc = __fmul_rn(m, kLog2e);
-  const float delta = __fmaf_rn(m, kLog2e, -mc);
-  return ExpShift{make_float2(kLog2e, kLog2e), make_float2(-mc, -mc), ex2(-delta)};
+__device__ __forceinline__ ExpShift exp_shift(float m, float c = kLog2e) {
+  const float mc = __fmul_rn(m, c);
+  const float delta = __fmaf_rn(m, c, -mc);
+  return ExpShift{make_float2(c, c), make_float2(-mc, -mc), ex2(-delta)};
 }
 __device__ __forceinline__ float2 exp_shifted2(float2 x, const ExpShift& s) {
   const float2 t = __ffma2_rn(x, s.log2e2, s.neg_mc2);
@@ -76,22 +77,22 @@ __device__ __forceinline__ State empty_state() { return State{-INFINITY, 0.f}; }
 
 // Merge of two partial states.  Each product is rounded on its own before the add, so
 // merge(a, b) and merge(b, a) are bitwise equal.
-__device__ __forceinline__ State merge(State a, State b) {
+__device__ __forceinline__ State merge(State a, State b, float c = kLog2e) {
   const float m = fmaxf(a.m, b.m);
   const float ms = safe_max(m);
-  const float sa = exp_diff(a.m, ms);
-  const float sb = exp_diff(b.m, ms);
+  const float sa = exp_diff(a.m, ms, c);
+  const float sb = exp_diff(b.m, ms, c);
   return State{m, __fadd_rn(__fmul_rn(a.d, sa), __fmul_rn(b.d, sb))};
 }
 
 // Butterfly merge over the 32 lanes of a warp; every lane returns the same state.
-__device__ __forceinline__ State warp_merge(State s) {
+__device__ __forceinline__ State warp_merge(State s, float c = kLog2e) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     State t;
     t.m = __shfl_xor_sync(0xffffffffu, s.m, o);
     t.d = __shfl_xor_sync(0xffffffffu, s.d, o);
-    s = merge(s, t);
+    s = merge(s, t, c);
   }
   return s;
 }
@@ -106,8 +107,8 @@ __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
 // barrier over exactly those warps.  Every participating thread returns the same state.
 template <class Sync>
 __device__ __forceinline__ State group_merge(State s, State* slots, int nwarps, int warp, int lane,
-                                             Sync sync) {
-  s = warp_merge(s);
+                                             Sync sync, float c = kLog2e) {
+  s = warp_merge(s, c);
   if (nwarps == 1) return s;
   if (lane == 0) slots[warp] = s;
   sync();
@@ -121,7 +122,7 @@ __device__ __forceinline__ State group_merge(State s, State* slots, int nwarps, 
     State u;
     u.m = __shfl_xor_sync(0xffffffffu, t.m, o);
     u.d = __shfl_xor_sync(0xffffffffu, t.d, o);
-    t = merge(t, u);
+    t = merge(t, u, c);
   }
   return t;
 }
@@ -130,11 +131,11 @@ __device__ __forceinline__ State group_merge(State s, State* slots, int nwarps, 
 // d = sum_i d_i e^(m_i - m) (one rescale per lane, a sum butterfly).  This is the merge formula
 // applied to all parts at once -- equal to the pairwise tree up to the order of the additions --
 // at one exponential per lane instead of two per round.
-__device__ __forceinline__ State warp_merge_nary(State s) {
+__device__ __forceinline__ State warp_merge_nary(State s, float c = kLog2e) {
   float m = s.m;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  float d = __fmul_rn(s.d, exp_diff(s.m, safe_max(m)));
+  float d = __fmul_rn(s.d, exp_diff(s.m, safe_max(m), c));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) d = __fadd_rn(d, __shfl_xor_sync(0xffffffffu, d, o));
   return State{m, d};
@@ -142,8 +143,8 @@ __device__ __forceinline__ State warp_merge_nary(State s) {
 
 template <class Sync>
 __device__ __forceinline__ State group_merge_nary(State s, State* slots, int nwarps, int warp, int lane,
-                                                  Sync sync) {
-  s = warp_merge_nary(s);
+                                                  Sync sync, float c = kLog2e) {
+  s = warp_merge_nary(s, c);
   if (nwarps == 1) return s;
   if (lane == 0) slots[warp] = s;
   sync();
@@ -153,7 +154,7 @@ __device__ __forceinline__ State group_merge_nary(State s, State* slots, int nwa
   const State t = i < nwarps ? slots[i] : empty_state();
   float m = t.m;
   for (int o = p >> 1; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  float d = __fmul_rn(t.d, exp_diff(t.m, safe_max(m)));
+  float d = __fmul_rn(t.d, exp_diff(t.m, safe_max(m), c));
   for (int o = p >> 1; o > 0; o >>= 1) d = __fadd_rn(d, __shfl_xor_sync(0xffffffffu, d, o));
   return State{m, d};
 }
@@ -175,14 +176,22 @@ struct LogNorm {
 __device__ __forceinline__ LogNorm log_norm(State s) {
   return LogNorm{safe_max(s.m), s.d > 0.f ? logf(s.d) : INFINITY};
 }
-__device__ __forceinline__ float log_prob(float x, LogNorm n) { return __fsub_rn(__fsub_rn(x, n.ms), n.lnd); }
+// With a scale (the softmax of scale * x, m the raw maximum): scale (x - m) - ln d, one rounding
+// for the product and the subtraction (identical to the unscaled form when scale = 1).
+__device__ __forceinline__ float log_prob(float x, LogNorm n, float scale = 1.f) {
+  return __fmaf_rn(__fsub_rn(x, n.ms), scale, -n.lnd);
+}
+
+// The state reported for the softmax of scale * x: m scaled (monotone rounding keeps it the
+// maximum of the rounded scale * x_j), d unchanged (already relative to it).
+__device__ __forceinline__ State scaled_state(State s, float scale) { return State{__fmul_rn(s.m, scale), s.d}; }
 
 // Cross-entropy loss -log p_label = (m - x_label) + ln d, in the order the page's
 // cross_entropy_loss takes it (logits - max first): m - x_label is exact when the two are close,
 // so a large |m| costs no cancellation, as LSE - x_label would.  An all -inf row gives NaN.
-__device__ __forceinline__ float ce_loss(State s, float x_label) {
+__device__ __forceinline__ float ce_loss(State s, float x_label, float scale = 1.f) {
   if (s.m == -INFINITY) return __int_as_float(0x7fc00000);
-  return __fadd_rn(__fsub_rn(s.m, x_label), logf(s.d));
+  return __fmaf_rn(__fsub_rn(s.m, x_label), scale, logf(s.d));
 }
 
 // ---------------------------------------------------------------------------------------------

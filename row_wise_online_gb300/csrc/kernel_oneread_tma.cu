@@ -38,6 +38,9 @@ struct TmaArgs {
   uint64_t wait_ns;
   const int64_t* labels;  // state-only mode: cross-entropy labels, or null
   float* loss;
+  int64_t x_pitch, y_pitch;  // bytes between rows
+  float scale;               // softmax of scale * x
+  float c;                   // scale * log2 e
 };
 
 constexpr int kSlotAlign = 128;
@@ -84,7 +87,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32) k_oneread_tma(TmaArgs a) {
         const uint32_t bar = smem_addr(&full[s]);
         mbar_arrive_expect_tx(bar, a.row_bytes);
         const int64_t row = blockIdx.x + j * gridDim.x;
-        bulk_g2s(smem_addr(slots + size_t(s) * a.slot_bytes), a.x + row * a.row_bytes, a.row_bytes, bar, pol);
+        bulk_g2s(smem_addr(slots + size_t(s) * a.slot_bytes), a.x + row * a.x_pitch, a.row_bytes, bar, pol);
         if (++s == S) {
           s = 0;
           ph ^= 1u;
@@ -156,10 +159,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32) k_oneread_tma(TmaArgs a) {
       for (int k = 0; k < VPT; ++k)
 #pragma unroll
         for (int e = 0; e < E; ++e) {
-          if constexpr (LOG) {  // x stays in registers for y = (x - m) - ln d
-            dt += exp_diff(v[k][e], mts);
+          if constexpr (LOG) {  // x stays in registers for y = scale (x - m) - ln d
+            dt += exp_diff(v[k][e], mts, a.c);
           } else {
-            v[k][e] = exp_diff(v[k][e], mts);
+            v[k][e] = exp_diff(v[k][e], mts, a.c);
             dt += v[k][e];
           }
         }
@@ -179,7 +182,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32) k_oneread_tma(TmaArgs a) {
       const float mts = safe_max(mt);
       float2 acc = make_float2(0.f, 0.f);
       if (exp_shift_ok(mts)) {
-        const ExpShift sh = exp_shift(mts);
+        const ExpShift sh = exp_shift(mts, a.c);
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
           float2 f[E / 2];
@@ -195,38 +198,40 @@ __global__ void __launch_bounds__((NCW + 1) * 32) k_oneread_tma(TmaArgs a) {
           float2 f[E / 2];
           D::unpack2(q[k], f);
 #pragma unroll
-          for (int e = 0; e < E / 2; ++e) acc = __fadd2_rn(acc, exp_diff2(f[e], nms));
+          for (int e = 0; e < E / 2; ++e) acc = __fadd2_rn(acc, exp_diff2(f[e], nms, a.c));
         }
         dt = __fadd_rn(acc.x, acc.y);
       }
     }
     State st;
     if constexpr (WRITE_Y)
-      st = group_merge(State{mt, dt}, wstate + (j & 1) * NCW, NCW, warp, lane, [] { named_barrier_sync(1, NCT); });
+      st = group_merge(
+          State{mt, dt}, wstate + (j & 1) * NCW, NCW, warp, lane, [] { named_barrier_sync(1, NCT); }, a.c);
     else
-      st = group_merge_nary(State{mt, dt}, wstate + (j & 1) * NCW, NCW, warp, lane,
-                            [] { named_barrier_sync(1, NCT); });
+      st = group_merge_nary(
+          State{mt, dt}, wstate + (j & 1) * NCW, NCW, warp, lane, [] { named_barrier_sync(1, NCT); }, a.c);
     const int64_t row = blockIdx.x + j * gridDim.x;
     if constexpr (WRITE_Y) {
       float scale = 0.f;
       LogNorm ln{};
       if constexpr (LOG) ln = log_norm(st);
-      else scale = __fmul_rn(exp_diff(mt, safe_max(st.m)), safe_inv(st.d));
-      unsigned char* yr = a.y + row * a.row_bytes;
+      else scale = __fmul_rn(exp_diff(mt, safe_max(st.m), a.c), safe_inv(st.d));
+      unsigned char* yr = a.y + row * a.y_pitch;
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
         const int u = tid + k * NCT;
         if (u < nunits) {
 #pragma unroll
-          for (int e = 0; e < E; ++e) v[k][e] = LOG ? log_prob(v[k][e], ln) : __fmul_rn(v[k][e], scale);
+          for (int e = 0; e < E; ++e) v[k][e] = LOG ? log_prob(v[k][e], ln, a.scale) : __fmul_rn(v[k][e], scale);
           st_stream16(yr + int64_t(u) * 16, D::pack(v[k]));
         }
       }
     }
     if (tid == 0) {
-      if (a.m_out) a.m_out[row] = st.m;
-      if (a.d_out) a.d_out[row] = st.d;
-      if (a.lse_out) a.lse_out[row] = lse_of(st);
+      const State o = scaled_state(st, a.scale);
+      if (a.m_out) a.m_out[row] = o.m;
+      if (a.d_out) a.d_out[row] = o.d;
+      if (a.lse_out) a.lse_out[row] = lse_of(o);
       if constexpr (OUT == kTmaState) {
         // cross entropy ("从原始Softmax到在线Softmax", "交叉熵损失计算"); negative label: ignored
         // row (0); label >= N: NaN and a status bit, x not read
@@ -236,7 +241,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32) k_oneread_tma(TmaArgs a) {
             l = __int_as_float(0x7fc00000);
             atomicOr(a.status, kStatusBadLabel);
           } else if (label >= 0) {
-            l = ce_loss(st, x_label);
+            l = ce_loss(st, x_label, a.scale);
           }
           a.loss[row] = l;
         }
@@ -341,7 +346,9 @@ cudaError_t launch_oneread_tma(const RowProblem& p, const DeviceInfo& dev) {
   const int grid = int(p.M < cap ? p.M : cap);
   TmaArgs a{static_cast<const unsigned char*>(p.x), static_cast<unsigned char*>(p.y), p.m_out,
             p.d_out, p.lse_out, p.M, p.N, uint32_t(p.N * elem_bytes(p.dtype)), plan.slot_bytes,
-            plan.stages, dev.status, local_wait_limit_ns(), p.labels, p.loss};
+            plan.stages, dev.status, local_wait_limit_ns(), p.labels, p.loss,
+            p.x_pitch ? p.x_pitch : int64_t(p.N) * elem_bytes(p.dtype),
+            p.y_pitch ? p.y_pitch : int64_t(p.N) * elem_bytes(p.dtype), p.scale, p.scale * kLog2e};
   fn<<<grid, threads, plan.smem, p.stream>>>(a);
   return cudaGetLastError();
 }

@@ -36,12 +36,17 @@ struct RowArgs {
   const int64_t* labels;  // cross entropy (two-pass state mode only), else null
   float* loss;
   unsigned* status;
+  int64_t x_pitch, y_pitch;  // bytes between rows
+  float scale;               // softmax of scale * x
+  float c;                   // scale * log2 e: the exponent slope
 };
 
+// Row outputs for the softmax of scale * x (s holds the raw maximum).
 __device__ __forceinline__ void write_state(const RowArgs& a, int64_t row, State s) {
-  if (a.m_out) a.m_out[row] = s.m;
-  if (a.d_out) a.d_out[row] = s.d;
-  if (a.lse_out) a.lse_out[row] = lse_of(s);
+  const State o = scaled_state(s, a.scale);
+  if (a.m_out) a.m_out[row] = o.m;
+  if (a.d_out) a.d_out[row] = o.d;
+  if (a.lse_out) a.lse_out[row] = lse_of(o);
 }
 
 // Cross entropy of row `row` against its label ("从原始Softmax到在线Softmax", section
@@ -57,7 +62,7 @@ __device__ __forceinline__ void write_loss(const RowArgs& a, int64_t row, const 
     l = __int_as_float(0x7fc00000);
     atomicOr(a.status, kStatusBadLabel);
   } else {
-    l = ce_loss(s, D::load1(xr, label));
+    l = ce_loss(s, D::load1(xr, label), a.scale);
   }
   a.loss[row] = l;
 }
@@ -79,11 +84,10 @@ __global__ void __launch_bounds__(kRegThreads) k_oneread_reg(RowArgs a) {
   const int g = warp / WPR, wig = warp % WPR;
   const int gt = threadIdx.x - g * GT;
   const int64_t nunits = a.N / E;
-  const int64_t row_bytes = a.N * D::kBytes;
 
   int it = 0;
   for (int64_t row = (int64_t)blockIdx.x * G + g; row < a.M; row += (int64_t)gridDim.x * G, ++it) {
-    const unsigned char* xr = a.x + row * row_bytes;
+    const unsigned char* xr = a.x + row * a.x_pitch;
     float v[VPT][E];
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
@@ -111,26 +115,26 @@ __global__ void __launch_bounds__(kRegThreads) k_oneread_reg(RowArgs a) {
     for (int k = 0; k < VPT; ++k)
 #pragma unroll
       for (int e = 0; e < E; ++e) {
-        if constexpr (LOG) {  // x stays in registers for y = (x - m) - ln d
-          dt += exp_diff(v[k][e], mts);
+        if constexpr (LOG) {  // x stays in registers for y = scale (x - m) - ln d
+          dt += exp_diff(v[k][e], mts, a.c);
         } else {
-          v[k][e] = exp_diff(v[k][e], mts);
+          v[k][e] = exp_diff(v[k][e], mts, a.c);
           dt += v[k][e];
         }
       }
-    const State s = group_merge(State{mt, dt}, &slots[it & 1][g * WPR], WPR, wig, lane,
-                                [&] { named_barrier_sync(1 + g, GT); });
+    const State s = group_merge(
+        State{mt, dt}, &slots[it & 1][g * WPR], WPR, wig, lane, [&] { named_barrier_sync(1 + g, GT); }, a.c);
     float scale = 0.f;
     LogNorm ln{};
     if constexpr (LOG) ln = log_norm(s);
-    else scale = __fmul_rn(exp_diff(mt, safe_max(s.m)), safe_inv(s.d));
-    unsigned char* yr = a.y + row * row_bytes;
+    else scale = __fmul_rn(exp_diff(mt, safe_max(s.m), a.c), safe_inv(s.d));
+    unsigned char* yr = a.y + row * a.y_pitch;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int64_t u = gt + (int64_t)k * GT;
       if (u < nunits) {
 #pragma unroll
-        for (int e = 0; e < E; ++e) v[k][e] = LOG ? log_prob(v[k][e], ln) : __fmul_rn(v[k][e], scale);
+        for (int e = 0; e < E; ++e) v[k][e] = LOG ? log_prob(v[k][e], ln, a.scale) : __fmul_rn(v[k][e], scale);
         if constexpr (VEC) {
           st_stream16(yr + u * 16, D::pack(v[k]));
         } else {
@@ -185,8 +189,11 @@ int blocks_per_sm(const void* fn, int threads, size_t smem) {
 }
 
 RowArgs row_args(const RowProblem& p, const DeviceInfo& dev) {
+  const int64_t row_bytes = p.N * elem_bytes(p.dtype);
   return RowArgs{static_cast<const unsigned char*>(p.x), static_cast<unsigned char*>(p.y),
-                 p.m_out, p.d_out, p.lse_out, p.M, p.N, 1, 0, p.labels, p.loss, dev.status};
+                 p.m_out, p.d_out, p.lse_out, p.M, p.N, 1, 0, p.labels, p.loss, dev.status,
+                 p.x_pitch ? p.x_pitch : row_bytes, p.y_pitch ? p.y_pitch : row_bytes, p.scale,
+                 p.scale * kLog2e};
 }
 
 // ------------------------------------------------------------------------------------------
@@ -226,11 +233,10 @@ __global__ void __launch_bounds__(kTwoPassMaxThreads) k_twopass(RowArgs a) {
   const int nt = blockDim.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t nunits = a.N / E;
-  const int64_t row_bytes = a.N * D::kBytes;
 
   int it = 0;
   for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x, ++it) {
-    const unsigned char* xr = a.x + row * row_bytes;
+    const unsigned char* xr = a.x + row * a.x_pitch;
     // live elements and units: all of them, or the causal prefix (the rest is never read)
     int64_t L = a.N;
     if constexpr (CAUSAL) {
@@ -265,8 +271,8 @@ __global__ void __launch_bounds__(kTwoPassMaxThreads) k_twopass(RowArgs a) {
 #pragma unroll
       for (int k = 0; k < U; ++k)
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc += exp_diff(v[k][e], ms);
-      const float r = exp_diff(m, ms);  // rescale of the running sum; 0 when m was -inf
+        for (int e = 0; e < E; ++e) acc += exp_diff(v[k][e], ms, a.c);
+      const float r = exp_diff(m, ms, a.c);  // rescale of the running sum; 0 when m was -inf
       const float ds = __fmul_rn(d, r);
       c = __fmul_rn(c, r);
       const float yk = __fsub_rn(acc, c);
@@ -275,14 +281,13 @@ __global__ void __launch_bounds__(kTwoPassMaxThreads) k_twopass(RowArgs a) {
       d = t;
       m = m_new;
     }
-    const State s = group_merge(State{m, d}, slots[it & 1], nt >> 5, warp, lane,
-                                [] { __syncthreads(); });
+    const State s = group_merge(State{m, d}, slots[it & 1], nt >> 5, warp, lane, [] { __syncthreads(); }, a.c);
     if constexpr (WRITE_Y) {
       // pass 2: re-read and normalise
       const float ms = safe_max(s.m);
       const float inv = safe_inv(s.d);
       const LogNorm ln = log_norm(s);
-      unsigned char* yr = a.y + row * row_bytes;
+      unsigned char* yr = a.y + row * a.y_pitch;
       for (int64_t base = threadIdx.x; base < nunits; base += (int64_t)nt * U) {
         float v[U][E];
 #pragma unroll
@@ -300,7 +305,8 @@ __global__ void __launch_bounds__(kTwoPassMaxThreads) k_twopass(RowArgs a) {
               }
             }
 #pragma unroll
-            for (int e = 0; e < E; ++e) v[k][e] = LOG ? log_prob(v[k][e], ln) : __fmul_rn(exp_diff(v[k][e], ms), inv);
+            for (int e = 0; e < E; ++e)
+              v[k][e] = LOG ? log_prob(v[k][e], ln, a.scale) : __fmul_rn(exp_diff(v[k][e], ms, a.c), inv);
             if constexpr (VEC) {
               st_stream16(yr + u * 16, D::pack(v[k]));
             } else {

@@ -30,6 +30,8 @@ struct RowProblem {
   bool log_out = false;  // y = log-softmax instead of softmax (register, CTA bulk-copy, two-pass)
   const int64_t* labels = nullptr;  // cross entropy (two-pass, no y): loss[r] = LSE_r - x_r[labels[r]]
   float* loss = nullptr;
+  int64_t x_pitch = 0, y_pitch = 0;  // bytes between rows (0: N * element size); register, CTA
+  float scale = 1.f;                 // bulk-copy and two-pass kernels: softmax of scale * x
   cudaStream_t stream = nullptr;
 };
 

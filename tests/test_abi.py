@@ -81,6 +81,18 @@ def test_other_calls_argument_checks(lib):
     assert lib.cross_entropy_rows(X, X, None, None, 4, 4, 0, None) == rwo.ERR_INVALID_ARG  # no loss
     assert lib.cross_entropy_rows(X, X, X, None, 4, 0, 0, None) == rwo.ERR_INVALID_ARG  # N = 0
     assert lib.cross_entropy_rows(NULL, NULL, NULL, None, 0, 4, 0, None) == rwo.OK  # M = 0
+    st = lib.softmax_rows_strided
+    assert st(X, 3, X, 4, None, None, None, 4, 4, 0, 1.0, 0, 0, None) == rwo.ERR_INVALID_ARG  # ldx < N
+    assert st(X, 4, X, 3, None, None, None, 4, 4, 0, 1.0, 0, 0, None) == rwo.ERR_INVALID_ARG  # ldy < N
+    assert st(X, 4, X, 4, None, None, None, 4, 4, 0, 0.0, 0, 0, None) == rwo.ERR_INVALID_ARG  # scale 0
+    assert st(X, 4, X, 4, None, None, None, 4, 4, 0, -2.0, 0, 0, None) == rwo.ERR_INVALID_ARG
+    assert st(X, 4, X, 4, None, None, None, 4, 4, 0, float("inf"), 0, 0, None) == rwo.ERR_INVALID_ARG
+    assert st(X, 4, X, 4, None, None, None, 4, 4, 0, float("nan"), 0, 0, None) == rwo.ERR_INVALID_ARG
+    assert st(X, 4, X, 4, None, None, None, 4, 4, 0, 1.0, 2, 0, None) == rwo.ERR_INVALID_ARG  # unknown flag
+    assert st(X, 4, X, 4, None, None, None, 4, 4, 3, 1.0, 0, 0, None) == rwo.ERR_INVALID_ARG  # dtype
+    assert st(X, 4, NULL, 4, None, None, None, 4, 4, 0, 1.0, 0, 0, None) == rwo.ERR_INVALID_ARG  # no y
+    assert st(X, 2**62, X, 4, None, None, None, 4, 4, 0, 1.0, 0, 0, None) == rwo.ERR_INVALID_ARG  # overflow
+    assert st(NULL, 0, NULL, 0, None, None, None, 0, 4, 0, 1.0, 0, 0, None) == rwo.OK  # M = 0
 
 
 def test_status_strings(lib):
