@@ -93,9 +93,12 @@ def measured_hbm_peak() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(files=None) -> str:
+    """Hash of the named files of row_wise_online_gb300/csrc (all of them when files is None)."""
+    csrc = os.path.join(ROOT, "row_wise_online_gb300", "csrc")
+    paths = sorted(glob.glob(os.path.join(csrc, "*"))) if files is None else [os.path.join(csrc, f) for f in sorted(files)]
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "row_wise_online_gb300", "csrc", "*"))):
+    for p in paths:
         with open(p, "rb") as fh:
             h.update(os.path.basename(p).encode())
             h.update(fh.read())
@@ -103,17 +106,23 @@ def kernel_source_hash() -> str:
 
 
 def profiled_traffic(kernel: str, workload: str) -> float | None:
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current sources."""
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current sources
+    (the summary names the source files its kernel is built from, and their hash)."""
     path = os.path.join(ROOT, "profiles", f"{kernel}__{workload}.md")
     try:
         text = open(path, encoding="utf-8").read()
     except OSError:
         return None
     src = re.search(r"source_hash:\s*([0-9a-f]+)", text)
+    files = re.search(r"source_files:\s*(.+)", text)
     tb = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not src or not tb or src.group(1) != kernel_source_hash():
+    if not src or not tb:
         return None
-    return float(tb.group(1))
+    try:
+        current = kernel_source_hash(files.group(1).split() if files else None)
+    except OSError:
+        return None
+    return float(tb.group(1)) if src.group(1) == current else None
 
 
 class ClockSampler:
