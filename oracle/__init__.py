@@ -13,6 +13,10 @@ The arithmetic lives in ``oracle.c`` (plain C, double precision):
 * ``log_softmax_rows`` -- log_probs = x - max - log(sum exp(x - max)), and
   ``cross_entropy_rows`` -- the per-row loss -log_probs[r, label_r]
   ("从原始Softmax到在线Softmax", section "softmax实际代码实现").
+* ``attention_rows`` -- attention forward O = softmax(scale Q K^T) V (and LSE) for selected query
+  rows, the plain definition of the worked example "标准 Attention 中的 Softmax"
+  ("从原始Softmax到在线Softmax"); ``attention_online`` -- the same page's blocked (m, l, o~)
+  recurrence for one query.
 * ``online_state`` -- the element-by-element (m, d) recurrence,
   "5.2 CUDA Online Softmax 实现优化" §2.1.
 * ``merge_state`` -- the merge of two partial states,
@@ -73,6 +77,11 @@ def _load():
             lib.oracle_log_softmax_rows.restype = ctypes.c_int
             lib.oracle_cross_entropy_rows.argtypes = [vp, ctypes.c_int, i64, vp, i64, vp, ctypes.c_int]
             lib.oracle_cross_entropy_rows.restype = ctypes.c_int
+            lib.oracle_attention_rows.argtypes = [vp, vp, vp, ctypes.c_int, i64, i64, i64, ctypes.c_double,
+                                                  ctypes.c_int, vp, i64, vp, vp, ctypes.c_int]
+            lib.oracle_attention_rows.restype = ctypes.c_int
+            lib.oracle_attention_online.argtypes = [vp, vp, i64, i64, i64, vp]
+            lib.oracle_attention_online.restype = None
             _lib = lib
     return _lib
 
@@ -168,6 +177,45 @@ def cross_entropy_rows(x: np.ndarray, labels, dtype: int | None = None, *, nthre
     if rc != 0:
         raise RuntimeError("oracle_cross_entropy_rows rejected its arguments")
     return loss
+
+
+def attention_rows(q, k, v, rows, *, dtype: int | None = None, scale: float | None = None, causal: bool = False,
+                   nthreads: int | None = None):
+    """fp64 attention forward for selected query rows: O = softmax(scale Q K^T) V, and LSE.
+
+    q: [BH, Sq, d], k and v: [BH, Sk, d] (float32, or uint16 bf16 / fp16 bits with dtype given);
+    rows: sequence of (head, query row).  scale defaults to 1/sqrt(d); causal: row i sees keys
+    j <= i + Sk - Sq.  Returns (o [nrows, d], lse [nrows]) as float64."""
+    q, k, v = (np.ascontiguousarray(a) for a in (q, k, v))
+    if q.ndim != 3 or k.shape != v.shape or k.ndim != 3 or q.shape[0] != k.shape[0] or q.shape[2] != k.shape[2]:
+        raise ValueError("q [BH, Sq, d], k and v [BH, Sk, d]")
+    if dtype is None:
+        dtype = F32 if q.dtype == np.float32 else BF16
+    BH, Sq, d = q.shape
+    Sk = k.shape[1]
+    sel = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 2))
+    if sel.size and (sel[:, 0].min() < 0 or sel[:, 0].max() >= BH or sel[:, 1].min() < 0 or sel[:, 1].max() >= Sq):
+        raise IndexError("row out of range")
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    o = np.empty((len(sel), d), np.float64)
+    lse = np.empty(len(sel), np.float64)
+    if len(sel) == 0:
+        return o, lse
+    rc = _load().oracle_attention_rows(_ptr(q), _ptr(k), _ptr(v), dtype, Sq, Sk, d, float(scale), int(bool(causal)),
+                                       _ptr(sel), len(sel), _ptr(o), _ptr(lse), nthreads or default_threads())
+    if rc != 0:
+        raise RuntimeError("oracle_attention_rows rejected its arguments")
+    return o, lse
+
+
+def attention_online(scores, v, block: int):
+    """The blocked (m, l, o~) recurrence for one query: scores [n], v [n, d] (float64)."""
+    s = np.ascontiguousarray(np.asarray(scores, dtype=np.float64).reshape(-1))
+    vv = np.ascontiguousarray(np.asarray(v, dtype=np.float64).reshape(len(s), -1))
+    o = np.empty(vv.shape[1], np.float64)
+    _load().oracle_attention_online(_ptr(s), _ptr(vv), len(s), vv.shape[1], int(block), _ptr(o))
+    return o
 
 
 def online_state(xs) -> tuple[float, float]:

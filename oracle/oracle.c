@@ -328,3 +328,130 @@ void oracle_merge_state(double m_a, double d_a, double m_b, double d_b,
   *m_out = m;
   *d_out = d_a * scaled_exp(m_a, m) + d_b * scaled_exp(m_b, m);
 }
+
+/*
+ * Attention forward, the plain definition ("从原始Softmax到在线Softmax", worked example
+ * "标准 Attention 中的 Softmax": S = Q K^T / sqrt(d), row-wise softmax, O = P V), in double:
+ * for the selected query rows, with q, k, v row-major [BH][S][d] of dtype (ORACLE_F32,
+ * ORACLE_BF16 or ORACLE_F16) and row i of head h attending keys j < Sk (causal: j <= i + Sk - Sq,
+ * the last query row sees every key):
+ *     s_j = scale * sum_c q[h][i][c] k[h][j][c],  m = max_j s_j,  l = sum_j e^(s_j - m)
+ *     o = sum_j e^(s_j - m) v[h][j] / l,  lse = m + log l.
+ * sel[2 * t] = head, sel[2 * t + 1] = query row of the t-th selected row; o is nsel x d, lse has
+ * nsel entries.  A row that sees no key gets o = 0, lse = -inf.  Returns 0, or -1 on a bad argument.
+ */
+typedef struct {
+  const void *q, *k, *v;
+  int dtype;
+  int64_t Sq, Sk, d;
+  double scale;
+  int causal;
+  const int64_t* sel;
+  double *o, *lse;
+  int64_t begin, end;
+} oracle_attn_job;
+
+static void* oracle_attn_worker(void* arg) {
+  oracle_attn_job* jb = (oracle_attn_job*)arg;
+  double* s = (double*)malloc(sizeof(double) * (size_t)(jb->Sk > 0 ? jb->Sk : 1));
+  if (!s) return NULL;
+  for (int64_t t = jb->begin; t < jb->end; ++t) {
+    const int64_t h = jb->sel[2 * t], i = jb->sel[2 * t + 1];
+    int64_t nk = jb->Sk;
+    if (jb->causal) {
+      nk = i + jb->Sk - jb->Sq + 1;
+      if (nk < 0) nk = 0;
+      if (nk > jb->Sk) nk = jb->Sk;
+    }
+    const int64_t qb = (h * jb->Sq + i) * jb->d;
+    double m = -INFINITY;
+    for (int64_t j = 0; j < nk; ++j) {
+      const int64_t kb = (h * jb->Sk + j) * jb->d;
+      double dot = 0.0;
+      for (int64_t c = 0; c < jb->d; ++c) dot += load_elem(jb->q, jb->dtype, qb + c) * load_elem(jb->k, jb->dtype, kb + c);
+      s[j] = jb->scale * dot;
+      if (s[j] > m) m = s[j];
+    }
+    double* o = jb->o + t * jb->d;
+    for (int64_t c = 0; c < jb->d; ++c) o[c] = 0.0;
+    double l = 0.0;
+    for (int64_t j = 0; j < nk; ++j) {
+      const double p = exp(s[j] - m);
+      l += p;
+      const int64_t vb = (h * jb->Sk + j) * jb->d;
+      for (int64_t c = 0; c < jb->d; ++c) o[c] += p * load_elem(jb->v, jb->dtype, vb + c);
+    }
+    if (nk > 0)
+      for (int64_t c = 0; c < jb->d; ++c) o[c] /= l;
+    jb->lse[t] = nk > 0 ? m + log(l) : -INFINITY;
+  }
+  free(s);
+  return NULL;
+}
+
+int oracle_attention_rows(const void* q, const void* k, const void* v, int dtype, int64_t Sq, int64_t Sk,
+                          int64_t d, double scale, int causal, const int64_t* sel, int64_t nsel, double* o,
+                          double* lse, int nthreads) {
+  if (!q || !k || !v || !sel || !o || !lse || Sq < 1 || Sk < 1 || d < 1 || nsel < 0) return -1;
+  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F16) return -1;
+  if (nsel == 0) return 0;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > nsel) nthreads = (int)nsel;
+  pthread_t* tids = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+  oracle_attn_job* jobs = (oracle_attn_job*)calloc((size_t)nthreads, sizeof(oracle_attn_job));
+  if (!tids || !jobs) {
+    free(tids);
+    free(jobs);
+    return -1;
+  }
+  for (int t = 0; t < nthreads; ++t) {
+    oracle_attn_job jb = {q, k, v, dtype, Sq, Sk, d, scale, causal, sel, o, lse,
+                          nsel * t / nthreads, nsel * (t + 1) / nthreads};
+    jobs[t] = jb;
+    if (t == 0) continue;
+    if (pthread_create(&tids[t], NULL, oracle_attn_worker, &jobs[t]) != 0) {
+      oracle_attn_worker(&jobs[t]);
+      tids[t] = (pthread_t)0;
+    }
+  }
+  oracle_attn_worker(&jobs[0]);
+  for (int t = 1; t < nthreads; ++t)
+    if (tids[t] != (pthread_t)0) pthread_join(tids[t], NULL);
+  free(tids);
+  free(jobs);
+  return 0;
+}
+
+/*
+ * The block recurrence of the same page ("从原始Softmax到在线Softmax", the online-softmax form
+ * of the blocked computation): for one query, scores s[0..n) and value rows v[n][d], blocks of
+ * `block` keys, starting from m = -inf, l = 0, o~ = 0:
+ *     m' = max(m, max of the block)
+ *     o~ = e^(m - m') o~ + sum_{k in block} e^(s_k - m') v_k
+ *     l  = e^(m - m') l  + sum_{k in block} e^(s_k - m')
+ * then o = o~ / l (written to o[0..d)).  e^(-inf - m') is taken as 0.
+ */
+void oracle_attention_online(const double* s, const double* v, int64_t n, int64_t d, int64_t block, double* o) {
+  double m = -INFINITY, l = 0.0;
+  for (int64_t c = 0; c < d; ++c) o[c] = 0.0;
+  if (block < 1) block = 1;
+  for (int64_t b0 = 0; b0 < n; b0 += block) {
+    const int64_t b1 = b0 + block < n ? b0 + block : n;
+    double mb = -INFINITY;
+    for (int64_t k = b0; k < b1; ++k)
+      if (s[k] > mb) mb = s[k];
+    const double m_new = mb > m ? mb : m;
+    if (m_new == -INFINITY) continue;
+    const double corr = scaled_exp(m, m_new);
+    l *= corr;
+    for (int64_t c = 0; c < d; ++c) o[c] *= corr;
+    for (int64_t k = b0; k < b1; ++k) {
+      const double p = scaled_exp(s[k], m_new);
+      l += p;
+      for (int64_t c = 0; c < d; ++c) o[c] += p * v[k * d + c];
+    }
+    m = m_new;
+  }
+  if (l > 0.0)
+    for (int64_t c = 0; c < d; ++c) o[c] /= l;
+}

@@ -74,6 +74,17 @@ def test_golden_worked_examples():
             assert abs(d - float(kv["d"])) <= tol
             _, m3, d3, _ = oracle.softmax_rows(np.asarray([x], dtype=np.float32), want_y=False)
             assert abs(d3[0] - float(kv["d"])) <= tol
+        elif kind == "attention":
+            mat = lambda t: np.array([[float(x) for x in r.split(",")] for r in t.split(";")], np.float32)
+            q, k, v, o_page = mat(kv["q"]), mat(kv["k"]), mat(kv["v"]), mat(kv["o"])
+            o, _ = oracle.attention_rows(q[None], k[None], v[None], [(0, i) for i in range(len(q))],
+                                         scale=1.0 / math.sqrt(q.shape[1]))
+            assert np.allclose(o, o_page, rtol=0, atol=tol), (o, o_page)
+        elif kind == "attention_online":
+            sc = _vec(kv["s"])
+            v = np.array([[float(x) for x in r.split(",")] for r in kv["v"].split(";")])
+            o = oracle.attention_online(sc, v, int(kv["block"]))
+            assert np.allclose(o, _vec(kv["o"]), rtol=0, atol=tol) and np.allclose(o, _vec(kv["o_online"]), rtol=0, atol=tol)
         elif kind == "merge":
             a = _vec(kv["a"])
             b = _vec(kv["b"])
@@ -452,3 +463,66 @@ def test_scaled_softmax_pins():
             assert abs(d[r] - float(dz)) <= 1e-14 * float(dz)
     with pytest.raises(ValueError):
         oracle.softmax_rows(x, scale=0.0)
+
+
+# ---------------------------------------------------------------------------------------------
+# attention forward ("从原始Softmax到在线Softmax": the attention example and the blocked recurrence)
+# ---------------------------------------------------------------------------------------------
+
+
+def _mp_attention(q, k, v, scale, nk):
+    with mpmath.workdps(40):
+        s = [mpmath.mpf(scale) * mpmath.fsum(mpmath.mpf(float(a)) * mpmath.mpf(float(b)) for a, b in zip(q, k[j]))
+             for j in range(nk)]
+        m = max(s)
+        p = [mpmath.exp(t - m) for t in s]
+        l = mpmath.fsum(p)
+        o = [float(mpmath.fsum(p[j] * mpmath.mpf(float(v[j][c])) for j in range(nk)) / l) for c in range(v.shape[1])]
+        return np.array(o), float(m + mpmath.log(l))
+
+
+def test_attention_brute_force_and_causal_rule():
+    rng = np.random.default_rng(40)
+    BH, Sq, Sk, d = 2, 5, 7, 6
+    q = rng.standard_normal((BH, Sq, d)).astype(np.float32)
+    k = rng.standard_normal((BH, Sk, d)).astype(np.float32)
+    v = rng.standard_normal((BH, Sk, d)).astype(np.float32)
+    rows = [(h, i) for h in range(BH) for i in range(Sq)]
+    for causal in (False, True):
+        o, lse = oracle.attention_rows(q, k, v, rows, scale=0.3, causal=causal)
+        for t, (h, i) in enumerate(rows):
+            nk = min(Sk, i + Sk - Sq + 1) if causal else Sk
+            om, lm = _mp_attention(q[h, i], k[h], v[h], float(np.float64(0.3)), nk)
+            np.testing.assert_allclose(o[t], om, rtol=1e-13, atol=1e-14)
+            assert abs(lse[t] - lm) <= 1e-13 * max(1.0, abs(lm))
+
+
+def test_attention_closed_forms():
+    rng = np.random.default_rng(41)
+    d = 8
+    v = rng.standard_normal((1, 9, d)).astype(np.float32)
+    q = rng.standard_normal((1, 9, d)).astype(np.float32)
+    # causal row 0 sees only key 0: o = v_0, lse = s_00
+    k = rng.standard_normal((1, 9, d)).astype(np.float32)
+    o, lse = oracle.attention_rows(q, k, v, [(0, 0)], causal=True, scale=0.5)
+    np.testing.assert_array_equal(o[0], v[0, 0].astype(np.float64))
+    assert abs(lse[0] - 0.5 * float(np.dot(q[0, 0].astype(np.float64), k[0, 0].astype(np.float64)))) <= 1e-15
+    # identical keys: uniform weights, o = mean of v, lse = s + log n
+    kk = np.repeat(k[:, :1], 9, axis=1)
+    o, lse = oracle.attention_rows(q, kk, v, [(0, 4)], scale=0.5)
+    np.testing.assert_allclose(o[0], v[0].astype(np.float64).mean(axis=0), rtol=1e-14, atol=1e-15)
+    # one dominant key: o = its value row
+    k2 = np.zeros((1, 9, d), np.float32)
+    k2[0, 3] = 40.0 * q[0, 2] / np.linalg.norm(q[0, 2])
+    o, _ = oracle.attention_rows(q, k2, v, [(0, 2)], scale=1.0)
+    np.testing.assert_allclose(o[0], v[0, 3].astype(np.float64), rtol=0, atol=1e-12)
+
+
+def test_attention_online_equals_direct():
+    rng = np.random.default_rng(42)
+    for n, block in ((1, 1), (7, 3), (64, 16), (100, 128), (33, 1)):
+        s = rng.standard_normal(n) * 5
+        v = rng.standard_normal((n, 5))
+        p = np.exp(s - s.max())
+        direct = (p[:, None] * v).sum(axis=0) / p.sum()
+        np.testing.assert_allclose(oracle.attention_online(s, v, block), direct, rtol=1e-13, atol=1e-14)
