@@ -442,12 +442,108 @@ def bench_reference(args) -> dict | None:
             "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+ATTN_WORKLOADS = {
+    # name: (BH, S, d, causal) -- 4 x 32 heads of 4096 queries over 4096 keys, head dimension 128
+    "attn_bf16_4x32x4096x128_causal": (128, 4096, 128, True),
+    "attn_bf16_4x32x4096x128": (128, 4096, 128, False),
+}
+
+
+def attention_flops(BH: int, S: int, d: int, causal: bool) -> int:
+    """2 S x S x d products (Q K^T and P V), 2 flops per multiply-add; causal: keys j <= i only."""
+    pairs = S * (S + 1) // 2 if causal else S * S
+    return 4 * BH * pairs * d
+
+
+def measured_tensor_peak() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            return float(json.load(fh)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
+def bench_attention(args) -> dict | None:
+    """attention_forward on the attention workload: TFLOP/s of the two products."""
+    import torch
+
+    import row_wise_online_gb300 as rwo
+    from row_wise_online_gb300 import _build
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local if torch.cuda.device_count() > 1 else 0)
+    if rank == 0 or not _build.up_to_date():
+        _build.build()
+    barrier(world)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    BH, S, d, causal = ATTN_WORKLOADS[args.workload]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7 + rank)
+    q, k, v = (torch.randn((BH, S, d), device=dev, generator=gen).to(torch.bfloat16) for _ in range(3))
+    o = torch.empty_like(q)
+    lse = torch.empty((BH, S), device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i):
+        rwo.attention_forward(q, k, v, o, lse, causal=causal, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    stream.synchronize()
+    graphs, full, rest = _graph_time(step, args.steps, stream, max(1, min(args.steps, 64)))
+    with torch.cuda.stream(stream):
+        graphs[0][0].replay()
+    stream.synchronize()
+    sampler = ClockSampler(dev.index)
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(full):
+            graphs[0][0].replay()
+        if rest:
+            graphs[-1][0].replay()
+        ev1.record(stream)
+    stream.synchronize()
+    barrier(world)
+    clk = sampler.stop()
+    status = rwo.get_status(stream)
+    if status != rwo.OK:
+        raise rwo.SoftmaxError(status, "kernel status after timing")
+    ms = reduce_max(ev0.elapsed_time(ev1), world)
+    if rank != 0:
+        return None
+    flops = attention_flops(BH, S, d, causal)
+    tflops = world * flops * args.steps / (ms * 1e-3) / 1e12
+    peak, kind = measured_tensor_peak()
+    per_launch = ms / args.steps
+    return {
+        "metric": "attention forward TFLOP/s (Q K^T and P V, 2 flops per multiply-add)",
+        "value": round(tflops, 1), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(per_launch, 6), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "BH": BH, "S": S, "d": d, "causal": causal,
+                   "parallelism": f"heads sharded over {world} GPU(s)",
+                   "l2": "q, k, v 384 MiB (larger than L2)",
+                   "timing": "CUDA graph replays between CUDA events on the launching stream"},
+        "roofline": {"bound": "tensor", "achieved": round(tflops / world, 1), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(tflops / world / peak, 4), "traffic": None,
+                     "peak_source": f"{kind} (MEASURED_PEAKS.json bf16_tflops, burst)", "kernel": "k_attention_fwd"},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+
+
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50000)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS) + sorted(ATTN_WORKLOADS))
     ap.add_argument("--variant", default="auto",
                     choices=["auto", "reg", "smem", "twopass", "splitrow", "causal", "log", "ce"],
                     help="causal: softmax_rows_causal on a causal workload (masked keys not read); "
@@ -460,7 +556,14 @@ def main(argv=None) -> int:
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    res = bench_reference(args) if args.impl == "reference" else bench_ours(args)
+    if args.workload in ATTN_WORKLOADS:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the attention forward has no CPU reference arm "
+                              "(the fp64 oracle checks sampled rows in the tests)"}), flush=True)
+            return 0
+        res = bench_attention(args)
+    else:
+        res = bench_reference(args) if args.impl == "reference" else bench_ours(args)
     if res is not None:
         print(json.dumps(res), flush=True)
     rank, world, _ = dist_env()

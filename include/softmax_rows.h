@@ -181,6 +181,25 @@ int cross_entropy_rows(const void* x, const int64_t* labels, float* loss, float*
                        int dtype, void* stream);
 
 /*
+ * attention_forward -- O = softmax(scale Q K^T) V row by row, without forming S = Q K^T in memory:
+ * the blocked online recurrence of "从原始Softmax到在线Softmax" (m' = max(m, block max),
+ * l = e^(m - m') l + sum e^(s - m'), o~ = e^(m - m') o~ + sum e^(s - m') v, o = o~ / l), the
+ * FlashAttention forward tile of "5.2 CUDA Online Softmax 实现优化" §8.2, on the tensor cores.
+ *   q       -- device, [BH][Sq][d] row-major, dtype elements.
+ *   k, v    -- device, [BH][Sk][d].
+ *   o       -- device, [BH][Sq][d] (written).
+ *   lse_out -- device, fp32 [BH][Sq]: m + ln l of each row (natural log, of scale Q K^T), or NULL.
+ *   scale   -- finite, > 0 (1/sqrt(d) in attention).
+ *   causal  -- 1: query row i sees keys j <= i + Sk - Sq (the last query sees every key); 0: all.
+ * A row that sees no key gets o = 0, LSE = -inf.  Supported: dtype SOFTMAX_BF16 with d = 128
+ * (fp32 accumulation, P rounded to bf16 for the P V product); other dtypes or head sizes return
+ * SOFTMAX_ERR_UNSUPPORTED.  BH <= 65535.  Pointers 16-byte aligned (else SOFTMAX_ERR_MISALIGNED).
+ * BH == 0 is a no-op.  A bounded wait that runs out is reported by softmax_get_status.
+ */
+int attention_forward(const void* q, const void* k, const void* v, void* o, float* lse_out, int64_t BH, int64_t Sq,
+                      int64_t Sk, int64_t d, float scale, int causal, int dtype, void* stream);
+
+/*
  * softmax_row_state -- only the per-row state (m, d) and LSE: the first pass
  * of the online method ("5.2 CUDA Online Softmax 实现优化", §2.2, pass 1;
  * "Softmax 数值稳定性与 IO-Aware Attention" §四, the mergeable state).  Reads x

@@ -39,7 +39,7 @@ EXPORTED = (
     "softmax_rows", "softmax_rows_ex", "softmax_row_state", "merge_states", "softmax_rows_host",
     "softmax_get_status", "softmax_status_string", "softmax_last_cuda_error", "softmax_last_variant",
     "softmax_debug_set_fault", "softmax_debug_set_wait_limit_ns", "softmax_rows_splitrow_noalloc",
-    "softmax_rows_causal", "log_softmax_rows", "cross_entropy_rows", "softmax_rows_strided",
+    "softmax_rows_causal", "log_softmax_rows", "cross_entropy_rows", "softmax_rows_strided", "attention_forward",
 )
 
 
@@ -84,11 +84,12 @@ def capi() -> ctypes.CDLL:
         lib.log_softmax_rows.argtypes = [vp, vp, fp, fp, fp, i64, i64, ci, ci, vp]
         lib.cross_entropy_rows.argtypes = [vp, vp, fp, fp, i64, i64, ci, vp]
         lib.softmax_rows_strided.argtypes = [vp, i64, vp, i64, fp, fp, fp, i64, i64, ci, ctypes.c_float, ci, ci, vp]
+        lib.attention_forward.argtypes = [vp, vp, vp, vp, fp, i64, i64, i64, i64, ctypes.c_float, ci, ci, vp]
         lib.softmax_debug_set_wait_limit_ns.restype = i64
         for name in ("softmax_rows", "softmax_rows_ex", "softmax_row_state", "merge_states",
                      "softmax_rows_host", "softmax_get_status", "softmax_last_variant",
                      "softmax_debug_set_fault", "softmax_rows_splitrow_noalloc", "softmax_rows_causal",
-                     "log_softmax_rows", "cross_entropy_rows", "softmax_rows_strided"):
+                     "log_softmax_rows", "cross_entropy_rows", "softmax_rows_strided", "attention_forward"):
             getattr(lib, name).restype = ci
         _lib = lib
     return _lib
@@ -232,6 +233,30 @@ def softmax_rows_strided(x, y=None, m_out=None, d_out=None, lse_out=None, scale:
                                      _stream(stream))
     _check(st, "softmax_rows_strided")
     return y
+
+
+def attention_forward(q, k, v, o=None, lse_out=None, scale: float | None = None, causal: bool = False, stream=None):
+    """O = softmax(scale Q K^T) V for q [BH, Sq, d], k and v [BH, Sk, d] (contiguous CUDA tensors; bf16,
+    d = 128).  scale defaults to 1/sqrt(d).  Returns o (and fills lse_out [BH, Sq] fp32 if given)."""
+    import torch
+
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        if not t.is_cuda or t.dim() != 3 or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous 3-D CUDA tensor")
+    BH, Sq, d = (int(s) for s in q.shape)
+    if k.shape != v.shape or k.shape[0] != BH or k.shape[2] != d or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("k and v must be [BH, Sk, d] with q's dtype")
+    Sk = int(k.shape[1])
+    if o is None:
+        o = torch.empty_like(q)
+    if lse_out is not None and (lse_out.dtype != torch.float32 or lse_out.numel() != BH * Sq or not lse_out.is_cuda):
+        raise ValueError("lse_out must be a CUDA float32 tensor of BH * Sq entries")
+    if scale is None:
+        scale = 1.0 / float(d) ** 0.5
+    st = capi().attention_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse_out), BH, Sq, Sk, d, float(scale),
+                                  1 if causal else 0, _dtype_code(q), _stream(stream))
+    _check(st, "attention_forward")
+    return o
 
 
 def log_softmax_rows(x, y=None, m_out=None, d_out=None, lse_out=None, variant: int = VARIANT_AUTO, stream=None):

@@ -379,6 +379,29 @@ int cross_entropy_rows(const void* x, const int64_t* labels, float* loss, float*
   return run_state_only(p, *dev);
 }
 
+int attention_forward(const void* q, const void* k, const void* v, void* o, float* lse_out, int64_t BH, int64_t Sq,
+                      int64_t Sk, int64_t d, float scale, int causal, int dtype, void* stream) {
+  if (dtype != SOFTMAX_F32 && dtype != SOFTMAX_BF16 && dtype != SOFTMAX_F16) return SOFTMAX_ERR_INVALID_ARG;
+  if (BH < 0 || Sq < 1 || Sk < 1 || d < 1) return SOFTMAX_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !(scale <= 3.4028234663852886e38f)) return SOFTMAX_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return SOFTMAX_ERR_INVALID_ARG;
+  if (!attention_fits(d, dtype)) return SOFTMAX_ERR_UNSUPPORTED;
+  if (BH > 65535 || Sq > (int64_t(1) << 31) * 128 - 1) return SOFTMAX_ERR_UNSUPPORTED;  // grid limits
+  const int64_t row = d * elem_bytes(dtype);
+  if (Sq > INT64_MAX / row / (BH > 0 ? BH : 1) || Sk > INT64_MAX / row / (BH > 0 ? BH : 1))
+    return SOFTMAX_ERR_INVALID_ARG;
+  if (BH == 0) return SOFTMAX_OK;
+  if (!q || !k || !v || !o) return SOFTMAX_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return SOFTMAX_ERR_MISALIGNED;
+  const DeviceInfo* dev = nullptr;
+  int st = current_device_info(&dev);
+  if (st != SOFTMAX_OK) return st;
+  cudaError_t err = launch_attention(q, k, v, o, lse_out, BH, Sq, Sk, scale, causal != 0,
+                                     static_cast<cudaStream_t>(stream), *dev);
+  if (err != cudaSuccess) return cuda_fail(err);
+  return SOFTMAX_OK;
+}
+
 int softmax_row_state(const void* x, float* m_out, float* d_out, float* lse_out, int64_t M, int64_t N,
                       int dtype, void* stream) {
   bool noop = false;

@@ -1,0 +1,100 @@
+"""attention_forward (the FlashAttention forward tile on tcgen05) against the fp64 oracle.
+
+Tolerance, derived from the arithmetic: scores and the row state are fp32 (bf16 products are exact
+in fp32); P is rounded to bf16 before the P V product (relative 2^-9 per weight) while l sums the
+unrounded weights, so |O - O_ref| <= 2^-9 max_j |v_j| plus the output's own bf16 rounding; the test
+allows 2^-8 max|v| + one bf16 ulp of O_ref.  LSE within 1e-4 max(1, |LSE|).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import row_wise_online_gb300 as rwo
+import synth
+from gpu_util import to_device, to_host
+from tolerances import bf16_ulp
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from row_wise_online_gb300 import _build
+
+    _build.build()
+    torch.cuda.set_device(0)
+
+
+def _qkv(BH, Sq, Sk, d, seed, q_sd=1.0):
+    gen = lambda M, N, s, sd: synth.generate(synth.custom("attn", synth.BF16, M, N, seed=s, p1=sd))
+    q = gen(BH * Sq, d, seed, q_sd).reshape(BH, Sq, d)
+    k = gen(BH * Sk, d, seed + 1, 1.0).reshape(BH, Sk, d)
+    v = gen(BH * Sk, d, seed + 2, 1.0).reshape(BH, Sk, d)
+    return q, k, v
+
+
+def _check(o_gpu, lse_gpu, q, k, v, rows, causal, scale, what):
+    o_ref, lse_ref = oracle.attention_rows(q, k, v, rows, dtype=synth.BF16, scale=scale, causal=causal)
+    vmax = np.abs(synth.bf16_to_f32(v).astype(np.float64)).max(axis=(1, 2))
+    idx = np.asarray(rows)
+    og = synth.bf16_to_f32(o_gpu[idx[:, 0], idx[:, 1]]).astype(np.float64)
+    bound = (2.0 ** -8) * vmax[idx[:, 0]][:, None] + bf16_ulp(o_ref)
+    err = np.abs(og - o_ref)
+    bad = ~(err <= bound)
+    assert not bad.any(), f"{what}: {bad.sum()} outputs off; worst {err.max()} at {np.unravel_index(np.argmax(err), err.shape)}"
+    lg = lse_gpu[idx[:, 0], idx[:, 1]].astype(np.float64)
+    fin = np.isfinite(lse_ref)
+    assert np.all(np.isneginf(lg[~fin]))
+    assert np.all(np.abs(lg[fin] - lse_ref[fin]) <= 1e-4 * np.maximum(1.0, np.abs(lse_ref[fin]))), f"{what}: LSE"
+
+
+@pytest.mark.parametrize("BH,Sq,Sk", [(1, 128, 128), (2, 300, 300), (3, 1, 1), (2, 128, 1000), (2, 513, 513),
+                                     (2, 1000, 77), (1, 77, 1000), (2, 256, 384)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_attention_against_oracle(BH, Sq, Sk, causal):
+    d = 128
+    q, k, v = _qkv(BH, Sq, Sk, d, seed=Sq * 7 + Sk)
+    lse = torch.full((BH, Sq), float("nan"), device="cuda")
+    o = rwo.attention_forward(to_device(q), to_device(k), to_device(v), lse_out=lse, causal=causal)
+    assert rwo.get_status() == rwo.OK
+    rows = [(h, i) for h in range(BH) for i in range(Sq)]
+    _check(to_host(o), lse.cpu().numpy(), q, k, v, rows, causal, 1.0 / np.sqrt(d), f"attn {BH}x{Sq}x{Sk} causal={causal}")
+
+
+def test_attention_large_scores_and_scale():
+    """Scores spread over hundreds (sharp rows) with a non-default scale."""
+    BH, S, d = 2, 384, 128
+    q, k, v = _qkv(BH, S, S, d, seed=91, q_sd=8.0)
+    lse = torch.empty((BH, S), device="cuda")
+    o = rwo.attention_forward(to_device(q), to_device(k), to_device(v), lse_out=lse, scale=0.3, causal=True)
+    assert rwo.get_status() == rwo.OK
+    _check(to_host(o), lse.cpu().numpy(), q, k, v, [(h, i) for h in range(BH) for i in range(S)], True, 0.3, "sharp")
+
+
+def test_attention_causal_workload_full_size():
+    """4 x 32 heads, 4096 queries and keys, d = 128, causal: sampled rows against the oracle."""
+    BH, S, d = 128, 4096, 128
+    q, k, v = _qkv(BH, S, S, d, seed=5)
+    lse = torch.empty((BH, S), device="cuda")
+    o = rwo.attention_forward(to_device(q), to_device(k), to_device(v), lse_out=lse, causal=True)
+    assert rwo.get_status() == rwo.OK
+    rng = np.random.default_rng(3)
+    rows = [(int(h), int(i)) for h, i in zip(rng.integers(0, BH, 48), rng.integers(0, S, 48))]
+    rows += [(0, 0), (0, 127), (0, 128), (77, 4095), (127, 4095), (127, 2048)]
+    _check(to_host(o), lse.cpu().numpy(), q, k, v, rows, True, 1.0 / np.sqrt(d), "causal 128x4096")
+
+
+def test_attention_unsupported_and_errors():
+    q = torch.zeros((1, 16, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(rwo.SoftmaxError) as ei:
+        rwo.attention_forward(q, q, q)  # d = 64
+    assert ei.value.status == rwo.ERR_UNSUPPORTED
+    q = torch.zeros((1, 16, 128), dtype=torch.float32, device="cuda")
+    with pytest.raises(rwo.SoftmaxError) as ei:
+        rwo.attention_forward(q, q, q)  # fp32
+    assert ei.value.status == rwo.ERR_UNSUPPORTED
+    q = torch.zeros((1, 16, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(rwo.SoftmaxError) as ei:
+        rwo.attention_forward(q, q, q, scale=-1.0)
+    assert ei.value.status == rwo.ERR_INVALID_ARG
