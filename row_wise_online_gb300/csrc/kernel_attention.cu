@@ -7,21 +7,28 @@
 // IO-Aware Attention" §八 describe the same recurrence as FlashAttention, where S = Q K^T never
 // leaves the chip.  One CTA owns 128 query rows of one head:
 //
-//  * a loader warp streams Q once and K, V tiles of 128 keys through two shared-memory stages
-//    with 16-byte cp.async copies placed directly in the tensor cores' no-swizzle canonical
-//    layouts (Q and K: K-major core matrices; V: MN-major, so it needs no transpose);
+//  * one producer lane streams Q once and K, V tiles of 128 keys through two shared-memory
+//    stages with TMA (cp.async.bulk.tensor, boxes of 8 elements x 128 rows, zero fill past the
+//    sequence end), which lands them directly in the tensor cores' no-swizzle canonical layouts
+//    (Q and K: K-major; V: MN-major, so it needs no transpose); K_j and V_j are issued as soon
+//    as their stage is free, each on its own barrier;
 //  * one thread issues tcgen05.mma (bf16 x bf16 -> fp32, M = N = 128, K = 16 per instruction):
 //    S_j = Q K_j^T into one of two TMEM buffers, so S_{j+1} is computed while S_j is softmaxed,
 //    and O += P_j V_j into a third TMEM region; completion is signalled with tcgen05.commit;
 //  * four softmax warps: thread t owns query row t (TMEM lane t).  Per tile it loads its row of
-//    S from TMEM, takes the running maximum m (in log2 units of scale * s), rescales l and, once
-//    the previous P V product has landed, the row of O in TMEM by 2^(m_old - m_new), writes
+//    S from TMEM in one read, takes the running maximum m (in log2 units of scale * s; moved only
+//    when a tile exceeds it by more than 2^8, so O and l are rarely rescaled) and, once the
+//    previous P V product has landed, rescales the row of O in TMEM by 2^(m_old - m_new), writes
 //    P = 2^(s - m) as bf16 into shared memory (the A operand of the P V product) and hands it
 //    to the MMA thread.  Masked keys (causal rule, the ragged end of the keys) give P = 0; tiles
 //    wholly above the causal diagonal are not visited.
 //  * epilogue: O / l as bf16 and LSE = m + ln l per row.
 // Every wait is bounded (%globaltimer); a wait that runs out sets the status word and the
 // kernel still terminates.
+#include <cuda.h>
+
+#include <mutex>
+
 #include "device_common.cuh"
 #include "launch.h"
 
@@ -62,16 +69,27 @@ constexpr int kSmem = kOffBar + kNumBars * 8 + 16;
 constexpr int kBarQFull = 0, kBarKFull = 1 /*2*/, kBarVFull = 3 /*2*/, kBarKFree = 5 /*2*/, kBarVFree = 7 /*2*/,
               kBarSFull = 9 /*2*/, kBarPFull = 11, kBarODone = 12;
 
-// Byte offset of 16-byte chunk (row r, chunk c) of a K-major tile: core matrices of 8 rows x 16 B,
-// consecutive along K (128 B apart), 8-row groups 2048 B apart.
-__device__ __forceinline__ uint32_t kmajor_off(int r, int c) { return uint32_t(((r >> 3) * 16 + c) * 128 + (r & 7) * 16); }
-// The same for V read as the MN-major B operand: row r = key (K), chunk c = 8 values of d (N).
-__device__ __forceinline__ uint32_t mnmajor_off(int r, int c) { return uint32_t((c * 16 + (r >> 3)) * 128 + (r & 7) * 16); }
+// Tiles in shared memory: 16-byte chunk c (8 consecutive elements of a row) of row r at byte
+// c * 2048 + r * 16 -- what a TMA box of 8 elements x 128 rows writes, one box per chunk.  In the
+// tensor cores' no-swizzle canonical layout this is, for Q, K and P (K-major: chunks run along
+// K), core matrices 2048 B apart along K and 128 B apart along M / N; for V (MN-major: rows are
+// keys, i.e. K; chunks run along N = d), 128 B apart along K and 2048 B along N.
+__device__ __forceinline__ uint32_t tile_off(int r, int c) { return uint32_t(c * 2048 + r * 16); }
 
 // Shared memory matrix descriptor (tcgen05): start >> 4, leading byte offset (core-matrix stride
 // along K) >> 4, stride byte offset (along M or N) >> 4, descriptor version 1, no swizzle.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
-  return uint64_t((saddr >> 4) & 0x3FFFu) | (uint64_t(128u >> 4) << 16) | (uint64_t(2048u >> 4) << 32) | (1ull << 46);
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return uint64_t((saddr >> 4) & 0x3FFFu) | (uint64_t(lbo >> 4) << 16) | (uint64_t(sbo >> 4) << 32) | (1ull << 46);
+}
+constexpr uint32_t kKmajLbo = 2048, kKmajSbo = 128, kKmajStep = 4096;  // K step of one MMA: 2 chunks
+constexpr uint32_t kMnLbo = 128, kMnSbo = 2048, kMnStep = 256;         // 16 keys
+
+// TMA: box (8 elements, 128 rows) at (x = element, y = row, z = head) of a [BH][S][128] tensor.
+__device__ __forceinline__ void tma_load_box(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A K-major, B K-major
@@ -95,48 +113,25 @@ __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence:
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_cta() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// 32 columns of this warp's 32 TMEM lanes: thread `lane` gets lane (32 w + lane), columns col..col+31.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
+// 64 columns of this warp's 32 TMEM lanes into v (no wait: call tmem_wait_ld before using v).
+__device__ __forceinline__ void tmem_ld64_nowait(uint32_t taddr, uint32_t (&r)[64]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
-      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
-      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
-      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
-      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
-      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
-      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
-      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]), "r"(r[32]), "r"(r[33]), "r"(r[34]), "r"(r[35]), "r"(r[36]), "r"(r[37]), "r"(r[38]), "r"(r[39]), "r"(r[40]), "r"(r[41]), "r"(r[42]), "r"(r[43]), "r"(r[44]), "r"(r[45]), "r"(r[46]), "r"(r[47]), "r"(r[48]), "r"(r[49]), "r"(r[50]), "r"(r[51]), "r"(r[52]), "r"(r[53]), "r"(r[54]), "r"(r[55]), "r"(r[56]), "r"(r[57]), "r"(r[58]), "r"(r[59]), "r"(r[60]), "r"(r[61]), "r"(r[62]), "r"(r[63])
       : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-__global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(AttnArgs a) {
+__global__ void __launch_bounds__(kThreads, 1)
+    k_attention_fwd(AttnArgs a, const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                    const __grid_constant__ CUtensorMap tv) {
   extern __shared__ __align__(1024) unsigned char smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + kNumBars * 8);
@@ -156,10 +151,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(AttnArgs a) {
   const int nt = int((kend + kBN - 1) / kBN);
 
   if (tid == 0) {
-    mbar_init(bar(kBarQFull), 32);
+    mbar_init(bar(kBarQFull), 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(kBarKFull + s), 32);
-      mbar_init(bar(kBarVFull + s), 32);
+      mbar_init(bar(kBarKFull + s), 1);
+      mbar_init(bar(kBarVFull + s), 1);
       mbar_init(bar(kBarKFree + s), 1);
       mbar_init(bar(kBarVFree + s), 1);
       mbar_init(bar(kBarSFull + s), 1);
@@ -180,65 +175,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(AttnArgs a) {
   bool timed_out = false;
 
   if (warp == kLoaderWarp) {
-    // ---------------- loader: Q once, then K and V tiles through two stages ----------------
-    const unsigned char* qh = a.q + bh * a.Sq * (kD * 2);
-    const unsigned char* kh = a.k + bh * a.Sk * (kD * 2);
-    const unsigned char* vh = a.v + bh * a.Sk * (kD * 2);
-    const uint32_t sq = smem_addr(smem + kOffQ);
-    for (int idx = lane; idx < kBM * 16; idx += 32) {
-      const int r = idx >> 4, c = idx & 15;
-      if (q0 + r < a.Sq) cp_async16(sq + kmajor_off(r, c), qh + (q0 + r) * (kD * 2) + c * 16);
-      else *reinterpret_cast<uint4*>(smem + kOffQ + kmajor_off(r, c)) = make_uint4(0, 0, 0, 0);
-    }
-    cp_async_commit();
-    auto issue_tile = [&](int j) {
-      const int s = j & 1;
-      const uint32_t sk = smem_addr(smem + kOffK + s * kTile), sv = smem_addr(smem + kOffV + s * kTile);
-      for (int idx = lane; idx < kBN * 16; idx += 32) {
-        const int r = idx >> 4, c = idx & 15;
-        const int64_t key = int64_t(j) * kBN + r;
-        if (key < a.Sk) {
-          cp_async16(sk + kmajor_off(r, c), kh + key * (kD * 2) + c * 16);
-          cp_async16(sv + mnmajor_off(r, c), vh + key * (kD * 2) + c * 16);
-        } else {
-          *reinterpret_cast<uint4*>(smem + kOffK + s * kTile + kmajor_off(r, c)) = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(smem + kOffV + s * kTile + mnmajor_off(r, c)) = make_uint4(0, 0, 0, 0);
-        }
-      }
-      cp_async_commit();
-    };
-    // The copies of a group are visible to the tensor cores once this thread has waited for the
-    // group and fenced the async proxy; then it arrives on the tile's barriers.
-    auto land = [&](int j) {
-      fence_proxy_async_cta();
-      mbar_arrive(bar(kBarKFull + (j & 1)));
-      mbar_arrive(bar(kBarVFull + (j & 1)));
-    };
-    if (nt > 0) issue_tile(0);
-    cp_async_wait<1>();  // Q (the groups are Q, then tile 0)
-    fence_proxy_async_cta();
-    mbar_arrive(bar(kBarQFull));
-    int landed = -1;  // last tile handed over
-    for (int j = 1; j < nt; ++j) {
-      if (j == 1) {
-        issue_tile(1);
-        cp_async_wait<1>();  // tile 0 has landed (tile 1 may still be in flight)
-        land(0);
-        landed = 0;
-      } else {
-        // Hand tile j - 1 over before waiting for stage j & 1: the products that free the stage
-        // (S_{j-2}, P_{j-2} V_{j-2}) come after S_{j-1} in the MMA thread's order.
-        cp_async_wait<0>();
-        land(j - 1);
-        landed = j - 1;
+    // ---------------- producer (one lane): TMA loads of Q once, then K_j and V_j ----------------
+    if (lane == 0) {
+      const int z = int(bh);
+      auto load_tile = [&](const CUtensorMap* map, uint32_t dst, int64_t row0, uint32_t b) {
+        mbar_arrive_expect_tx(b, uint32_t(kTile));
+        for (int c = 0; c < kD / 8; ++c) tma_load_box(dst + uint32_t(c) * 2048u, map, c * 8, int(row0), z, b);
+      };
+      load_tile(&tq, smem_addr(smem + kOffQ), q0, bar(kBarQFull));
+      for (int j = 0; j < nt; ++j) {
+        const int s = j & 1;
         const uint32_t par = uint32_t(((j >> 1) - 1) & 1);
-        if (!mbar_wait(bar(kBarKFree + (j & 1)), par, a.wait_ns)) timed_out = true;
-        if (!mbar_wait(bar(kBarVFree + (j & 1)), par, a.wait_ns)) timed_out = true;
-        issue_tile(j);
+        if (j >= 2 && !mbar_wait(bar(kBarKFree + s), par, a.wait_ns)) timed_out = true;  // S_{j-2} done
+        load_tile(&tk, smem_addr(smem + kOffK + s * kTile), int64_t(j) * kBN, bar(kBarKFull + s));
+        if (j >= 2 && !mbar_wait(bar(kBarVFree + s), par, a.wait_ns)) timed_out = true;  // P V_{j-2} done
+        load_tile(&tv, smem_addr(smem + kOffV + s * kTile), int64_t(j) * kBN, bar(kBarVFull + s));
       }
+      // every copy has landed before the CTA may exit (the MMA thread normally saw them all)
+      for (int j = nt > 2 ? nt - 2 : 0; j < nt; ++j) {
+        if (!mbar_wait(bar(kBarKFull + (j & 1)), uint32_t((j >> 1) & 1), a.wait_ns)) timed_out = true;
+        if (!mbar_wait(bar(kBarVFull + (j & 1)), uint32_t((j >> 1) & 1), a.wait_ns)) timed_out = true;
+      }
+      if (nt == 0 && !mbar_wait(bar(kBarQFull), 0u, a.wait_ns)) timed_out = true;
     }
-    cp_async_wait<0>();
-    for (int j = landed + 1; j < nt; ++j) land(j);
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issue (one thread) ----------------
     if (lane == 0) {
@@ -251,7 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(AttnArgs a) {
         const uint32_t sk = smem_addr(smem + kOffK + s * kTile);
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
-          mma_bf16(tmem + uint32_t(s * kBN), smem_desc(sq + kk * 256), smem_desc(sk + kk * 256), idS, kk > 0);
+          mma_bf16(tmem + uint32_t(s * kBN), smem_desc(sq + kk * kKmajStep, kKmajLbo, kKmajSbo),
+                   smem_desc(sk + kk * kKmajStep, kKmajLbo, kKmajSbo), idS, kk > 0);
         mma_commit(bar(kBarSFull + s));
         mma_commit(bar(kBarKFree + s));
       };
@@ -266,7 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(AttnArgs a) {
         const uint32_t sv = smem_addr(smem + kOffV + (j & 1) * kTile);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_bf16(tmem + 256u, smem_desc(sp + kk * 256), smem_desc(sv + kk * 256), idPV, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16(tmem + 256u, smem_desc(sp + kk * kKmajStep, kKmajLbo, kKmajSbo),
+                   smem_desc(sv + kk * kMnStep, kMnLbo, kMnSbo), idPV, (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar(kBarODone));
         mma_commit(bar(kBarVFree + (j & 1)));
         if (j + 2 < nt) issue_s(j + 2);  // S buffer j & 1 was read before P_j was handed over
@@ -277,8 +238,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(AttnArgs a) {
     const int t = tid;                 // 0..127, TMEM lane t
     const int64_t qi = q0 + t;         // global query row
     const int64_t klim = a.causal ? qi + a.Sk - a.Sq + 1 : a.Sk;  // keys < klim are visible
+    // keys below kfull are visible to every row of the tile: tiles under it need no mask
+    const int64_t kfull = a.causal ? (q0 + a.Sk - a.Sq + 1 < a.Sk ? q0 + a.Sk - a.Sq + 1 : a.Sk) : a.Sk;
     const uint32_t lane_base = uint32_t(warp * 32) << 16;
-    float m = -INFINITY;  // running maximum of c * s (log2 units)
+    // Running maximum m of c * s (log2 units), moved only when a tile's maximum exceeds it by more
+    // than 8: until then P = 2^(c s - m) stays below 2^8 (exact enough in bf16 and fp32) and O, l
+    // need no rescale; O / l and LSE = m ln 2 + ln l are the same for any m.
+    constexpr float kSlack = 8.f;
+    float m = -INFINITY;
     float l = 0.f;
     unsigned char* prow = smem + kOffP;
     for (int j = 0; j < nt; ++j) {
@@ -287,19 +254,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(AttnArgs a) {
       tc_fence_after();
       const uint32_t ts = tmem + lane_base + uint32_t(s * kBN);
       const int64_t k0 = int64_t(j) * kBN;
-      // the row's maximum over this tile (masked keys excluded)
+      uint32_t sv[2][64];  // the row of S, one TMEM read
+      tmem_ld64_nowait(ts, sv[0]);
+      tmem_ld64_nowait(ts + 64, sv[1]);
+      tmem_wait_ld();
+      const bool masked = k0 + kBN > kfull;  // uniform over the CTA
       float mt = -INFINITY;
-#pragma unroll 1
-      for (int c0 = 0; c0 < kBN; c0 += 32) {
-        float sv[32];
-        tmem_ld32(ts + c0, sv);
+      if (!masked) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (k0 + c0 + i < klim) mt = fmaxf(mt, sv[i]);
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int i = 0; i < 64; ++i) mt = fmaxf(mt, __uint_as_float(sv[h][i]));
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (k0 + h * 64 + i < klim) mt = fmaxf(mt, __uint_as_float(sv[h][i]));
       }
-      const float m_new = fmaxf(m, __fmul_rn(mt, a.c));
+      const float mtc = __fmul_rn(mt, a.c);
+      const bool move = mtc > m + kSlack;  // m = -inf: any visible key moves it
+      const float m_new = move ? mtc : m;
+      const float alpha = move ? ex2(m - m_new) : 1.f;  // 0 while the row had seen nothing
       const float ms = m_new == -INFINITY ? 0.f : m_new;
-      const float alpha = ex2(m - ms);  // 0 while the row has seen nothing
       // the previous P V product has landed: P's buffer is free and O can be rescaled
       if (j > 0) {
         if (!mbar_wait(bar(kBarODone), uint32_t((j - 1) & 1), a.wait_ns)) timed_out = true;
@@ -307,35 +284,42 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(AttnArgs a) {
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
           const uint32_t to = tmem + lane_base + 256u;
 #pragma unroll 1
-          for (int c0 = 0; c0 < kD; c0 += 32) {
-            float ov[32];
-            tmem_ld32(to + c0, ov);
+          for (int h = 0; h < 2; ++h) {  // rare (the maximum moved): half a row at a time
+            uint32_t ov[64];
+            tmem_ld64_nowait(to + h * 64, ov);
+            tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = __fmul_rn(ov[i], alpha);
-            tmem_st32(to + c0, ov);
+            for (int i = 0; i < 64; ++i) ov[i] = __float_as_uint(__fmul_rn(__uint_as_float(ov[i]), alpha));
+            tmem_st64(to + h * 64, ov);
+            tmem_wait_st();
           }
         }
       }
       // P = 2^(c s - m) as bf16 in the A operand layout; the row sum in fp32
-      float sum = 0.f;
-#pragma unroll 1
-      for (int c0 = 0; c0 < kBN; c0 += 32) {
-        float sv[32];
-        tmem_ld32(ts + c0, sv);
-        uint32_t pk[16];
+      const float nms = -ms;
+      float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float p0 = k0 + c0 + i < klim ? ex2(__fsub_rn(__fmul_rn(sv[i], a.c), ms)) : 0.f;
-          const float p1 = k0 + c0 + i + 1 < klim ? ex2(__fsub_rn(__fmul_rn(sv[i + 1], a.c), ms)) : 0.f;
-          sum += p0 + p1;
-          pk[i >> 1] = pack_bf16x2(p0, p1);
+      for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {  // 8 chunks of 8 keys per half
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const int i = c8 * 8 + e;
+            float p0 = ex2(__fmaf_rn(__uint_as_float(sv[h][i]), a.c, nms));
+            float p1 = ex2(__fmaf_rn(__uint_as_float(sv[h][i + 1]), a.c, nms));
+            if (masked) {
+              if (k0 + h * 64 + i >= klim) p0 = 0.f;
+              if (k0 + h * 64 + i + 1 >= klim) p1 = 0.f;
+            }
+            sum0 += p0;
+            sum1 += p1;
+            pk[e >> 1] = pack_bf16x2(p0, p1);
+          }
+          *reinterpret_cast<uint4*>(prow + tile_off(t, h * 8 + c8)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          *reinterpret_cast<uint4*>(prow + kmajor_off(t, (c0 >> 3) + q)) =
-              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
       }
-      l = __fadd_rn(__fmul_rn(l, alpha), sum);
+      l = __fadd_rn(__fmul_rn(l, alpha), __fadd_rn(sum0, sum1));
       m = m_new;
       fence_proxy_async_cta();  // P's generic stores -> the tensor cores' async proxy
       tc_fence_before();        // O's TMEM stores before the next product
@@ -351,23 +335,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(AttnArgs a) {
     const uint32_t to = tmem + lane_base + 256u;
     unsigned char* orow = a.o + (bh * a.Sq + qi) * (kD * 2);
 #pragma unroll 1
-    for (int c0 = 0; c0 < kD; c0 += 32) {
-      float ov[32];
+    for (int h = 0; h < 2; ++h) {
+      uint32_t ov[64];
       if (nt > 0) {
-        tmem_ld32(to + c0, ov);
+        tmem_ld64_nowait(to + h * 64, ov);
+        tmem_wait_ld();
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) ov[i] = 0.f;
+        for (int i = 0; i < 64; ++i) ov[i] = 0u;
       }
       if (qi < a.Sq) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 8; ++q) {
+          const float* f = reinterpret_cast<const float*>(ov + 8 * q);
           uint4 w;
-          w.x = pack_bf16x2(__fmul_rn(ov[8 * q + 0], inv), __fmul_rn(ov[8 * q + 1], inv));
-          w.y = pack_bf16x2(__fmul_rn(ov[8 * q + 2], inv), __fmul_rn(ov[8 * q + 3], inv));
-          w.z = pack_bf16x2(__fmul_rn(ov[8 * q + 4], inv), __fmul_rn(ov[8 * q + 5], inv));
-          w.w = pack_bf16x2(__fmul_rn(ov[8 * q + 6], inv), __fmul_rn(ov[8 * q + 7], inv));
-          *reinterpret_cast<uint4*>(orow + (c0 + 8 * q) * 2) = w;
+          w.x = pack_bf16x2(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv));
+          w.y = pack_bf16x2(__fmul_rn(f[2], inv), __fmul_rn(f[3], inv));
+          w.z = pack_bf16x2(__fmul_rn(f[4], inv), __fmul_rn(f[5], inv));
+          w.w = pack_bf16x2(__fmul_rn(f[6], inv), __fmul_rn(f[7], inv));
+          *reinterpret_cast<uint4*>(orow + (h * 64 + 8 * q) * 2) = w;
         }
       }
     }
@@ -384,15 +370,55 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(AttnArgs a) {
 
 bool attention_fits(int64_t d, int dtype) { return d == kD && dtype == 1; }
 
+namespace {
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up once through the runtime (no link to the driver library).
+EncodeTiled encode_tiled() {
+  static std::once_flag once;
+  static EncodeTiled fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// [BH][S][128] bf16, boxes of 8 elements x 128 rows x 1 head; rows past S read as zeros.
+bool make_map(CUtensorMap* m, const void* base, int64_t S, int64_t BH) {
+  EncodeTiled fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {cuuint64_t(kD), cuuint64_t(S), cuuint64_t(BH)};
+  const cuuint64_t strides[2] = {cuuint64_t(kD) * 2, cuuint64_t(S) * kD * 2};
+  const cuuint32_t box[3] = {8, cuuint32_t(kBM), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 cudaError_t launch_attention(const void* q, const void* k, const void* v, void* o, float* lse, int64_t BH, int64_t Sq,
                              int64_t Sk, float scale, bool causal, cudaStream_t stream, const DeviceInfo& dev) {
   cudaError_t err = cudaFuncSetAttribute((const void*)k_attention_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (err != cudaSuccess) return err;
+  alignas(64) CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, q, Sq, BH) || !make_map(&tk, k, Sk, BH) || !make_map(&tv, v, Sk, BH))
+    return cudaErrorInvalidValue;
   AttnArgs a{static_cast<const unsigned char*>(q), static_cast<const unsigned char*>(k),
              static_cast<const unsigned char*>(v), static_cast<unsigned char*>(o), lse, Sq, Sk, scale * kLog2e,
              causal ? 1 : 0, dev.status, local_wait_limit_ns()};
   const dim3 grid(unsigned((Sq + kBM - 1) / kBM), unsigned(BH));
-  k_attention_fwd<<<grid, kThreads, kSmem, stream>>>(a);
+  k_attention_fwd<<<grid, kThreads, kSmem, stream>>>(a, tq, tk, tv);
   return cudaGetLastError();
 }
 
