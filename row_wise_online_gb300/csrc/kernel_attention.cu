@@ -8,10 +8,12 @@
 // leaves the chip.  One CTA owns 128 query rows of one head:
 //
 //  * one producer lane streams Q once and K, V tiles of 128 keys through two shared-memory
-//    stages with TMA (cp.async.bulk.tensor, boxes of 8 elements x 128 rows, zero fill past the
-//    sequence end), which lands them directly in the tensor cores' no-swizzle canonical layouts
-//    (Q and K: K-major; V: MN-major, so it needs no transpose); K_j and V_j are issued as soon
-//    as their stage is free, each on its own barrier;
+//    stages with TMA (cp.async.bulk.tensor, two boxes of 64 elements x 128 rows per tile with the
+//    128-byte swizzle, zero fill past the sequence end), which lands them directly in the tensor
+//    cores' 128-byte-swizzled canonical layouts (Q and K: K-major; V: MN-major, so it needs no
+//    transpose); K_j and V_j are issued as soon as their stage is free, each on its own barrier.
+//    Rows of 128 bytes per request keep the copy engine and L2 efficient (boxes 16 bytes wide
+//    cost one request per 16 bytes and starved the tensor cores);
 //  * one thread issues tcgen05.mma (bf16 x bf16 -> fp32, M = N = 128, K = 16 per instruction):
 //    S_j = Q K_j^T into one of two TMEM buffers, so S_{j+1} is computed while S_j is softmaxed,
 //    and O += P_j V_j into a third TMEM region; completion is signalled with tcgen05.commit;
@@ -57,34 +59,45 @@ struct AttnArgs {
   uint64_t wait_ns;
 };
 
-// Shared memory: Q | K[2] | V[2] | P | barriers | TMEM address.
+// Shared memory (from a 1024-byte aligned base, as the 128-byte swizzle needs):
+// Q | K[2] | V[2] | P | barriers | TMEM address.
 constexpr int kOffQ = 0;
 constexpr int kOffK = kTile;
 constexpr int kOffV = 3 * kTile;
 constexpr int kOffP = 5 * kTile;
 constexpr int kOffBar = 6 * kTile;
 constexpr int kNumBars = 14;
-constexpr int kSmem = kOffBar + kNumBars * 8 + 16;
+constexpr int kSmem = kOffBar + kNumBars * 8 + 16 + 1024;  // + alignment slack
 // barrier indices
 constexpr int kBarQFull = 0, kBarKFull = 1 /*2*/, kBarVFull = 3 /*2*/, kBarKFree = 5 /*2*/, kBarVFree = 7 /*2*/,
               kBarSFull = 9 /*2*/, kBarPFull = 11, kBarODone = 12;
 
-// Tiles in shared memory: 16-byte chunk c (8 consecutive elements of a row) of row r at byte
-// c * 2048 + r * 16 -- what a TMA box of 8 elements x 128 rows writes, one box per chunk.  In the
-// tensor cores' no-swizzle canonical layout this is, for Q, K and P (K-major: chunks run along
-// K), core matrices 2048 B apart along K and 128 B apart along M / N; for V (MN-major: rows are
-// keys, i.e. K; chunks run along N = d), 128 B apart along K and 2048 B along N.
+// Q, K and V tiles in shared memory: two blocks of 16 KB (elements 0-63 and 64-127 of each row);
+// in a block, row r's 128 bytes at (r / 8) * 1024 + (r % 8) * 128 with its 16-byte chunk c
+// stored at chunk position c ^ (r % 8) -- what a TMA box of 64 elements x 128 rows writes with
+// the 128-byte swizzle, and the tensor cores' 128-byte-swizzled canonical layout: for Q and K
+// (K-major) 8-row groups 1024 B apart (SBO), one MMA's 16 elements of K 32 B further along the
+// row; for V (MN-major: rows are keys = K, elements run along N = d) 8-key groups 1024 B apart
+// (SBO), the two 64-element halves of N 16 KB apart (LBO), 16 keys per MMA = 2048 B.
+//
+// P (written by the softmax threads, no swizzle): 16-byte chunk c (8 keys) of row r at byte
+// c * 2048 + r * 16, i.e. K-major core matrices 2048 B apart along K and 128 B apart along M.
 __device__ __forceinline__ uint32_t tile_off(int r, int c) { return uint32_t(c * 2048 + r * 16); }
 
-// Shared memory matrix descriptor (tcgen05): start >> 4, leading byte offset (core-matrix stride
-// along K) >> 4, stride byte offset (along M or N) >> 4, descriptor version 1, no swizzle.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return uint64_t((saddr >> 4) & 0x3FFFu) | (uint64_t(lbo >> 4) << 16) | (uint64_t(sbo >> 4) << 32) | (1ull << 46);
+// Shared memory matrix descriptor (tcgen05): start >> 4, leading byte offset >> 4, stride byte
+// offset >> 4, descriptor version 1, layout (bits 61-63: 0 no swizzle, 2 the 128-byte swizzle).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint64_t layout = 0) {
+  return uint64_t((saddr >> 4) & 0x3FFFu) | (uint64_t(lbo >> 4) << 16) | (uint64_t(sbo >> 4) << 32) | (1ull << 46) |
+         (layout << 61);
 }
-constexpr uint32_t kKmajLbo = 2048, kKmajSbo = 128, kKmajStep = 4096;  // K step of one MMA: 2 chunks
-constexpr uint32_t kMnLbo = 128, kMnSbo = 2048, kMnStep = 256;         // 16 keys
+constexpr uint64_t kSw128 = 2;
+constexpr uint32_t kBlock = 16384;                                      // one 64-element half of a tile
+constexpr uint32_t kPLbo = 2048, kPSbo = 128, kPStep = 4096;            // P, no swizzle: 2 chunks per K step
+constexpr uint32_t kSwSbo = 1024;                                       // 8 rows of 128 B
+__device__ __forceinline__ uint32_t kmaj_step(int kk) { return uint32_t(kk >> 2) * kBlock + uint32_t(kk & 3) * 32u; }
+constexpr uint32_t kVStep = 2048;                                       // 16 keys of V
 
-// TMA: box (8 elements, 128 rows) at (x = element, y = row, z = head) of a [BH][S][128] tensor.
+// TMA: box (64 elements, 128 rows) at (x = element, y = row, z = head) of a [BH][S][128] tensor.
 __device__ __forceinline__ void tma_load_box(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
@@ -132,7 +145,8 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 __global__ void __launch_bounds__(kThreads, 1)
     k_attention_fwd(AttnArgs a, const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv) {
-  extern __shared__ __align__(1024) unsigned char smem[];
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + kNumBars * 8);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -180,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int z = int(bh);
       auto load_tile = [&](const CUtensorMap* map, uint32_t dst, int64_t row0, uint32_t b) {
         mbar_arrive_expect_tx(b, uint32_t(kTile));
-        for (int c = 0; c < kD / 8; ++c) tma_load_box(dst + uint32_t(c) * 2048u, map, c * 8, int(row0), z, b);
+        for (int c = 0; c < kD / 64; ++c) tma_load_box(dst + uint32_t(c) * kBlock, map, c * 64, int(row0), z, b);
       };
       load_tile(&tq, smem_addr(smem + kOffQ), q0, bar(kBarQFull));
       for (int j = 0; j < nt; ++j) {
@@ -210,8 +224,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sk = smem_addr(smem + kOffK + s * kTile);
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
-          mma_bf16(tmem + uint32_t(s * kBN), smem_desc(sq + kk * kKmajStep, kKmajLbo, kKmajSbo),
-                   smem_desc(sk + kk * kKmajStep, kKmajLbo, kKmajSbo), idS, kk > 0);
+          mma_bf16(tmem + uint32_t(s * kBN), smem_desc(sq + kmaj_step(kk), 16u, kSwSbo, kSw128),
+                   smem_desc(sk + kmaj_step(kk), 16u, kSwSbo, kSw128), idS, kk > 0);
         mma_commit(bar(kBarSFull + s));
         mma_commit(bar(kBarKFree + s));
       };
@@ -226,8 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sv = smem_addr(smem + kOffV + (j & 1) * kTile);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_bf16(tmem + 256u, smem_desc(sp + kk * kKmajStep, kKmajLbo, kKmajSbo),
-                   smem_desc(sv + kk * kMnStep, kMnLbo, kMnSbo), idPV, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16(tmem + 256u, smem_desc(sp + kk * kPStep, kPLbo, kPSbo),
+                   smem_desc(sv + kk * kVStep, kBlock, kSwSbo, kSw128), idPV, (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar(kBarODone));
         mma_commit(bar(kBarVFree + (j & 1)));
         if (j + 2 < nt) issue_s(j + 2);  // S buffer j & 1 was read before P_j was handed over
@@ -259,19 +273,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld64_nowait(ts + 64, sv[1]);
       tmem_wait_ld();
       const bool masked = k0 + kBN > kfull;  // uniform over the CTA
-      float mt = -INFINITY;
-      if (!masked) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int i = 0; i < 64; ++i) mt = fmaxf(mt, __uint_as_float(sv[h][i]));
-      } else {
+      if (masked) {  // keys past the row's limit count as -inf
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int i = 0; i < 64; ++i)
-            if (k0 + h * 64 + i < klim) mt = fmaxf(mt, __uint_as_float(sv[h][i]));
+            if (k0 + h * 64 + i >= klim) sv[h][i] = 0xff800000u;
       }
+      float mx[8];  // eight partial maxima: short dependency chains
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(__uint_as_float(sv[0][i]), __uint_as_float(sv[1][i]));
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int i = 8; i < 64; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(sv[h][i]));
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const float mtc = __fmul_rn(mt, a.c);
       const bool move = mtc > m + kSlack;  // m = -inf: any visible key moves it
       const float m_new = move ? mtc : m;
@@ -295,9 +311,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // P = 2^(c s - m) as bf16 in the A operand layout; the row sum in fp32
-      const float nms = -ms;
-      float sum0 = 0.f, sum1 = 0.f;
+      // P = 2^(c s - m) as bf16 in the A operand layout (masked keys: 2^-inf = 0); the row sum in
+      // fp32, four pairs of partial sums; the exponent by one packed fused multiply-add per pair
+      const float2 c2 = make_float2(a.c, a.c), nm2 = make_float2(-ms, -ms);
+      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
 #pragma unroll
@@ -306,20 +323,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 8; e += 2) {
             const int i = c8 * 8 + e;
-            float p0 = ex2(__fmaf_rn(__uint_as_float(sv[h][i]), a.c, nms));
-            float p1 = ex2(__fmaf_rn(__uint_as_float(sv[h][i + 1]), a.c, nms));
-            if (masked) {
-              if (k0 + h * 64 + i >= klim) p0 = 0.f;
-              if (k0 + h * 64 + i + 1 >= klim) p1 = 0.f;
-            }
-            sum0 += p0;
-            sum1 += p1;
-            pk[e >> 1] = pack_bf16x2(p0, p1);
+            const float2 t2 = __ffma2_rn(make_float2(__uint_as_float(sv[h][i]), __uint_as_float(sv[h][i + 1])), c2, nm2);
+            const float2 p = make_float2(ex2(t2.x), ex2(t2.y));
+            acc[e >> 1] = __fadd2_rn(acc[e >> 1], p);
+            pk[e >> 1] = pack_bf16x2(p.x, p.y);
           }
           *reinterpret_cast<uint4*>(prow + tile_off(t, h * 8 + c8)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
       }
-      l = __fadd_rn(__fmul_rn(l, alpha), __fadd_rn(sum0, sum1));
+      const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
+      const float2 aa = __fadd2_rn(a01, a23);
+      l = __fadd_rn(__fmul_rn(l, alpha), __fadd_rn(aa.x, aa.y));
       m = m_new;
       fence_proxy_async_cta();  // P's generic stores -> the tensor cores' async proxy
       tc_fence_before();        // O's TMEM stores before the next product
@@ -398,10 +412,10 @@ bool make_map(CUtensorMap* m, const void* base, int64_t S, int64_t BH) {
   if (!fn) return false;
   const cuuint64_t dims[3] = {cuuint64_t(kD), cuuint64_t(S), cuuint64_t(BH)};
   const cuuint64_t strides[2] = {cuuint64_t(kD) * 2, cuuint64_t(S) * kD * 2};
-  const cuuint32_t box[3] = {8, cuuint32_t(kBM), 1};
+  const cuuint32_t box[3] = {64, cuuint32_t(kBM), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
