@@ -5,7 +5,8 @@
 // j, m' = max(m, max of the block), l = e^(m - m') l + sum e^(s - m'), o~ = e^(m - m') o~ + sum
 // e^(s - m') v, o = o~ / l; "5.2 CUDA Online Softmax 实现优化" §8.2 and "Softmax 数值稳定性与
 // IO-Aware Attention" §八 describe the same recurrence as FlashAttention, where S = Q K^T never
-// leaves the chip.  One CTA owns 128 query rows of one head:
+// leaves the chip.  One CTA owns two tiles of 128 query rows (X = 0, 1) of one head, which take
+// turns on the tensor cores: while one tile's softmax runs, the other tile's products run.
 //
 //  * one producer lane streams Q once and K, V tiles of 128 keys through two shared-memory
 //    stages with TMA (cp.async.bulk.tensor, two boxes of 64 elements x 128 rows per tile with the
@@ -14,16 +15,18 @@
 //    transpose); K_j and V_j are issued as soon as their stage is free, each on its own barrier.
 //    Rows of 128 bytes per request keep the copy engine and L2 efficient (boxes 16 bytes wide
 //    cost one request per 16 bytes and starved the tensor cores);
-//  * one thread issues tcgen05.mma (bf16 x bf16 -> fp32, M = N = 128, K = 16 per instruction):
-//    S_j = Q K_j^T into one of two TMEM buffers, so S_{j+1} is computed while S_j is softmaxed,
-//    and O += P_j V_j into a third TMEM region; completion is signalled with tcgen05.commit;
-//  * four softmax warps: thread t owns query row t (TMEM lane t).  Per tile it loads its row of
-//    S from TMEM in one read, takes the running maximum m (in log2 units of scale * s; moved only
-//    when a tile exceeds it by more than 2^8, so O and l are rarely rescaled) and, once the
-//    previous P V product has landed, rescales the row of O in TMEM by 2^(m_old - m_new), writes
-//    P = 2^(s - m) as bf16 into shared memory (the A operand of the P V product) and hands it
-//    to the MMA thread.  Masked keys (causal rule, the ragged end of the keys) give P = 0; tiles
-//    wholly above the causal diagonal are not visited.
+//  * one thread issues tcgen05.mma (bf16 x bf16 -> fp32, M = N = 128, K = 16 per instruction) in
+//    the order P V_0(j), S_0(j+1), P V_1(j), S_1(j+1): S_X = Q_X K^T into TMEM region S_X, and
+//    O_X += P_X V with P_X read from TMEM (A operand in tensor memory); completion is signalled
+//    with tcgen05.commit, which covers every earlier product of the thread -- so S_X(j+1) landing
+//    also means O_X holds P V_X(j);
+//  * two softmax warpgroups, one per query tile: thread t owns query row t (TMEM lane t).  Per key
+//    tile it loads its row of S from TMEM, takes the running maximum m (in log2 units of
+//    scale * s; moved only when a tile exceeds it by more than 2^8, so O and l are rarely
+//    rescaled), rescales its row of O in TMEM by 2^(m_old - m_new) when m moved, and writes
+//    P = 2^(s - m) as packed bf16 over the first 64 columns of its S region, which the P V
+//    product reads.  Masked keys (causal rule, the ragged end of the keys) give P = 0; key tiles
+//    wholly above a query tile's causal diagonal are not visited;
 //  * epilogue: O / l as bf16 and LSE = m + ln l per row.
 // Every wait is bounded (%globaltimer); a wait that runs out sets the status word and the
 // kernel still terminates.
@@ -37,14 +40,15 @@
 namespace rwo {
 namespace {
 
-constexpr int kBM = 128;             // query rows per CTA
+constexpr int kBM = 128;             // query rows per tile (two tiles per CTA)
 constexpr int kBN = 128;             // keys per tile
 constexpr int kD = 128;              // head dimension
-constexpr int kTile = kBN * kD * 2;  // bytes of a K or V tile (and of Q and P)
-constexpr int kThreads = 6 * 32;     // 4 softmax warps, 1 loader warp, 1 MMA warp
-constexpr int kLoaderWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr uint32_t kTmemCols = 512;  // S0 [0, 128), S1 [128, 256), O [256, 384)
+constexpr int kTile = kBN * kD * 2;  // bytes of a Q, K or V tile
+constexpr int kThreads = 10 * 32;    // 2 x 4 softmax warps, 1 loader warp, 1 MMA warp
+constexpr int kLoaderWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;  // S_0 [0, 128), S_1 [128, 256), O_0 [256, 384), O_1 [384, 512)
+constexpr uint32_t kTmemO = 256;
 
 struct AttnArgs {
   const unsigned char* q;  // [BH][Sq][d] bf16
@@ -60,17 +64,16 @@ struct AttnArgs {
 };
 
 // Shared memory (from a 1024-byte aligned base, as the 128-byte swizzle needs):
-// Q | K[2] | V[2] | P | barriers | TMEM address.
+// Q[2] | K[2] | V[2] | barriers | TMEM address.
 constexpr int kOffQ = 0;
-constexpr int kOffK = kTile;
-constexpr int kOffV = 3 * kTile;
-constexpr int kOffP = 5 * kTile;
+constexpr int kOffK = 2 * kTile;
+constexpr int kOffV = 4 * kTile;
 constexpr int kOffBar = 6 * kTile;
-constexpr int kNumBars = 14;
+constexpr int kNumBars = 16;
 constexpr int kSmem = kOffBar + kNumBars * 8 + 16 + 1024;  // + alignment slack
 // barrier indices
 constexpr int kBarQFull = 0, kBarKFull = 1 /*2*/, kBarVFull = 3 /*2*/, kBarKFree = 5 /*2*/, kBarVFree = 7 /*2*/,
-              kBarSFull = 9 /*2*/, kBarPFull = 11, kBarODone = 12;
+              kBarSFull = 9 /*X*/, kBarPFull = 11 /*X*/, kBarODone = 13 /*X*/;
 
 // Q, K and V tiles in shared memory: two blocks of 16 KB (elements 0-63 and 64-127 of each row);
 // in a block, row r's 128 bytes at (r / 8) * 1024 + (r % 8) * 128 with its 16-byte chunk c
@@ -80,9 +83,8 @@ constexpr int kBarQFull = 0, kBarKFull = 1 /*2*/, kBarVFull = 3 /*2*/, kBarKFree
 // row; for V (MN-major: rows are keys = K, elements run along N = d) 8-key groups 1024 B apart
 // (SBO), the two 64-element halves of N 16 KB apart (LBO), 16 keys per MMA = 2048 B.
 //
-// P (written by the softmax threads, no swizzle): 16-byte chunk c (8 keys) of row r at byte
-// c * 2048 + r * 16, i.e. K-major core matrices 2048 B apart along K and 128 B apart along M.
-__device__ __forceinline__ uint32_t tile_off(int r, int c) { return uint32_t(c * 2048 + r * 16); }
+// P in TMEM (the A operand of P V): row r in lane r, keys 2c and 2c + 1 in column c (low and high
+// half), 8 columns per MMA's 16 keys.
 
 // Shared memory matrix descriptor (tcgen05): start >> 4, leading byte offset >> 4, stride byte
 // offset >> 4, descriptor version 1, layout (bits 61-63: 0 no swizzle, 2 the 128-byte swizzle).
@@ -92,7 +94,6 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 }
 constexpr uint64_t kSw128 = 2;
 constexpr uint32_t kBlock = 16384;                                      // one 64-element half of a tile
-constexpr uint32_t kPLbo = 2048, kPSbo = 128, kPStep = 4096;            // P, no swizzle: 2 chunks per K step
 constexpr uint32_t kSwSbo = 1024;                                       // 8 rows of 128 B
 __device__ __forceinline__ uint32_t kmaj_step(int kk) { return uint32_t(kk >> 2) * kBlock + uint32_t(kk & 3) * 32u; }
 constexpr uint32_t kVStep = 2048;                                       // 16 keys of V
@@ -118,13 +119,20 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b
       "l"(a), "l"(b), "r"(idesc), "r"(acc));
 }
 
+// A from tensor memory (K-major, two bf16 per column), B from shared memory.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(b), "r"(idesc), "r"(acc));
+}
+
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void fence_proxy_async_cta() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // 64 columns of this warp's 32 TMEM lanes into v (no wait: call tmem_wait_ld before using v).
 __device__ __forceinline__ void tmem_ld64_nowait(uint32_t taddr, uint32_t (&r)[64]) {
@@ -133,15 +141,29 @@ __device__ __forceinline__ void tmem_ld64_nowait(uint32_t taddr, uint32_t (&r)[6
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
       : "r"(taddr));
 }
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64]) {
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]), "r"(r[32]), "r"(r[33]), "r"(r[34]), "r"(r[35]), "r"(r[36]), "r"(r[37]), "r"(r[38]), "r"(r[39]), "r"(r[40]), "r"(r[41]), "r"(r[42]), "r"(r[43]), "r"(r[44]), "r"(r[45]), "r"(r[46]), "r"(r[47]), "r"(r[48]), "r"(r[49]), "r"(r[50]), "r"(r[51]), "r"(r[52]), "r"(r[53]), "r"(r[54]), "r"(r[55]), "r"(r[56]), "r"(r[57]), "r"(r[58]), "r"(r[59]), "r"(r[60]), "r"(r[61]), "r"(r[62]), "r"(r[63])
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Keys at or past the row's limit count as -inf.
+__device__ __forceinline__ void mask_keys(uint32_t (&sv)[64], int64_t key0, int64_t klim) {
+#pragma unroll
+  for (int i = 0; i < 64; ++i)
+    if (key0 + i >= klim) sv[i] = 0xff800000u;
+}
+
+// 320 threads, at most 168 registers a thread: three warps share a sub-partition's 16K registers.
 __global__ void __launch_bounds__(kThreads, 1)
     k_attention_fwd(AttnArgs a, const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv) {
@@ -152,17 +174,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   auto bar = [&](int i) { return smem_addr(&bars[i]); };
 
-  const int64_t nqt = (a.Sq + kBM - 1) / kBM;
-  const int64_t qt = nqt - 1 - int64_t(blockIdx.x);  // the heaviest causal tiles first
+  const int64_t ncta = (a.Sq + 2 * kBM - 1) / (2 * kBM);
+  const int64_t q0 = (ncta - 1 - int64_t(blockIdx.x)) * (2 * kBM);  // the heaviest causal tiles first
   const int64_t bh = blockIdx.y;
-  const int64_t q0 = qt * kBM;
-  // keys this tile visits: all, or (causal) up to the last row's diagonal
-  int64_t kend = a.Sk;
-  if (a.causal) {
-    const int64_t last = (q0 + kBM - 1 < a.Sq - 1 ? q0 + kBM - 1 : a.Sq - 1) + a.Sk - a.Sq + 1;
-    kend = last < 0 ? 0 : (last < a.Sk ? last : a.Sk);
+  // key tiles visited by query tile X: all, or (causal, bottom-right aligned) those that hold a
+  // key <= the tile's last row + Sk - Sq; none for a tile past the end of the queries
+  int nt[2];
+  for (int x = 0; x < 2; ++x) {
+    const int64_t qx = q0 + x * kBM;
+    int64_t kend = qx < a.Sq ? a.Sk : 0;
+    if (a.causal && qx < a.Sq) {
+      const int64_t last = (qx + kBM - 1 < a.Sq - 1 ? qx + kBM - 1 : a.Sq - 1) + a.Sk - a.Sq + 1;
+      kend = last < 0 ? 0 : (last < a.Sk ? last : a.Sk);
+    }
+    nt[x] = int((kend + kBN - 1) / kBN);
   }
-  const int nt = int((kend + kBN - 1) / kBN);
+  const int ntmax = nt[0] > nt[1] ? nt[0] : nt[1];
 
   if (tid == 0) {
     mbar_init(bar(kBarQFull), 1);
@@ -172,9 +199,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarKFree + s), 1);
       mbar_init(bar(kBarVFree + s), 1);
       mbar_init(bar(kBarSFull + s), 1);
+      mbar_init(bar(kBarPFull + s), 4);
+      mbar_init(bar(kBarODone + s), 1);
     }
-    mbar_init(bar(kBarPFull), 4);
-    mbar_init(bar(kBarODone), 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -189,169 +216,179 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool timed_out = false;
 
   if (warp == kLoaderWarp) {
-    // ---------------- producer (one lane): TMA loads of Q once, then K_j and V_j ----------------
+    // ---- producer: Q_0 and Q_1 once, then K_j, V_j into stage j & 1 ----
     if (lane == 0) {
       const int z = int(bh);
       auto load_tile = [&](const CUtensorMap* map, uint32_t dst, int64_t row0, uint32_t b) {
-        mbar_arrive_expect_tx(b, uint32_t(kTile));
         for (int c = 0; c < kD / 64; ++c) tma_load_box(dst + uint32_t(c) * kBlock, map, c * 64, int(row0), z, b);
       };
+      mbar_arrive_expect_tx(bar(kBarQFull), uint32_t(2 * kTile));
       load_tile(&tq, smem_addr(smem + kOffQ), q0, bar(kBarQFull));
-      for (int j = 0; j < nt; ++j) {
+      load_tile(&tq, smem_addr(smem + kOffQ + kTile), q0 + kBM, bar(kBarQFull));
+      for (int j = 0; j < ntmax; ++j) {
         const int s = j & 1;
         const uint32_t par = uint32_t(((j >> 1) - 1) & 1);
-        if (j >= 2 && !mbar_wait(bar(kBarKFree + s), par, a.wait_ns)) timed_out = true;  // S_{j-2} done
+        if (j >= 2 && !mbar_wait(bar(kBarKFree + s), par, a.wait_ns)) timed_out = true;  // S(j-2) done
+        mbar_arrive_expect_tx(bar(kBarKFull + s), uint32_t(kTile));
         load_tile(&tk, smem_addr(smem + kOffK + s * kTile), int64_t(j) * kBN, bar(kBarKFull + s));
-        if (j >= 2 && !mbar_wait(bar(kBarVFree + s), par, a.wait_ns)) timed_out = true;  // P V_{j-2} done
+        if (j >= 2 && !mbar_wait(bar(kBarVFree + s), par, a.wait_ns)) timed_out = true;  // P V(j-2) done
+        mbar_arrive_expect_tx(bar(kBarVFull + s), uint32_t(kTile));
         load_tile(&tv, smem_addr(smem + kOffV + s * kTile), int64_t(j) * kBN, bar(kBarVFull + s));
       }
-      // every copy has landed before the CTA may exit (the MMA thread normally saw them all)
-      for (int j = nt > 2 ? nt - 2 : 0; j < nt; ++j) {
+      // no copy may still be in flight when the CTA exits
+      for (int j = ntmax > 2 ? ntmax - 2 : 0; j < ntmax; ++j) {
         if (!mbar_wait(bar(kBarKFull + (j & 1)), uint32_t((j >> 1) & 1), a.wait_ns)) timed_out = true;
         if (!mbar_wait(bar(kBarVFull + (j & 1)), uint32_t((j >> 1) & 1), a.wait_ns)) timed_out = true;
       }
-      if (nt == 0 && !mbar_wait(bar(kBarQFull), 0u, a.wait_ns)) timed_out = true;
+      if (!mbar_wait(bar(kBarQFull), 0u, a.wait_ns)) timed_out = true;
     }
   } else if (warp == kMmaWarp) {
-    // ---------------- MMA issue (one thread) ----------------
-    if (lane == 0) {
+    // ---- MMA issuer: S_X(0); then per key tile j: P V_0(j), S_0(j+1), P V_1(j), S_1(j+1) ----
+    if (lane == 0 && ntmax > 0) {
       const uint32_t idS = idesc_bf16(0), idPV = idesc_bf16(1);
-      const uint32_t sq = smem_addr(smem + kOffQ), sp = smem_addr(smem + kOffP);
-      auto issue_s = [&](int j) {
-        const int s = j & 1;
-        if (!mbar_wait(bar(kBarKFull + s), uint32_t((j >> 1) & 1), a.wait_ns)) timed_out = true;
-        tc_fence_after();
-        const uint32_t sk = smem_addr(smem + kOffK + s * kTile);
+      auto issue_s = [&](int x, int j) {  // S_x(j) = Q_x K_j^T into S_x; K_j has landed
+        const uint32_t sq = smem_addr(smem + kOffQ + x * kTile), sk = smem_addr(smem + kOffK + (j & 1) * kTile);
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
-          mma_bf16(tmem + uint32_t(s * kBN), smem_desc(sq + kmaj_step(kk), 16u, kSwSbo, kSw128),
+          mma_bf16(tmem + uint32_t(x * kBN), smem_desc(sq + kmaj_step(kk), 16u, kSwSbo, kSw128),
                    smem_desc(sk + kmaj_step(kk), 16u, kSwSbo, kSw128), idS, kk > 0);
-        mma_commit(bar(kBarSFull + s));
-        mma_commit(bar(kBarKFree + s));
+        mma_commit(bar(kBarSFull + x));
       };
       if (!mbar_wait(bar(kBarQFull), 0, a.wait_ns)) timed_out = true;
-      if (nt > 0) issue_s(0);
-      if (nt > 1) issue_s(1);
-      for (int j = 0; j < nt; ++j) {
-        // P_j written (and S_j read, and O rescaled) by the softmax warps
-        if (!mbar_wait(bar(kBarPFull), uint32_t(j & 1), a.wait_ns)) timed_out = true;
-        if (!mbar_wait(bar(kBarVFull + (j & 1)), uint32_t((j >> 1) & 1), a.wait_ns)) timed_out = true;
-        tc_fence_after();
-        const uint32_t sv = smem_addr(smem + kOffV + (j & 1) * kTile);
+      if (!mbar_wait(bar(kBarKFull), 0, a.wait_ns)) timed_out = true;
+      tc_fence_after();
+      for (int x = 0; x < 2; ++x)
+        if (nt[x] > 0) issue_s(x, 0);
+      mma_commit(bar(kBarKFree));
+      for (int j = 0; j < ntmax; ++j) {
+        const int s = j & 1;
+        if (!mbar_wait(bar(kBarVFull + s), uint32_t((j >> 1) & 1), a.wait_ns)) timed_out = true;
+        const bool next_k = j + 1 < ntmax;
+        bool k_ready = false;
+        const uint32_t sv = smem_addr(smem + kOffV + s * kTile);
+        for (int x = 0; x < 2; ++x) {
+          if (j >= nt[x]) continue;
+          if (!mbar_wait(bar(kBarPFull + x), uint32_t(j & 1), a.wait_ns)) timed_out = true;
+          tc_fence_after();
+          const uint32_t tp = tmem + uint32_t(x * kBN), to = tmem + kTmemO + uint32_t(x * kD);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_bf16(tmem + 256u, smem_desc(sp + kk * kPStep, kPLbo, kPSbo),
-                   smem_desc(sv + kk * kVStep, kBlock, kSwSbo, kSw128), idPV, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(kBarODone));
-        mma_commit(bar(kBarVFree + (j & 1)));
-        if (j + 2 < nt) issue_s(j + 2);  // S buffer j & 1 was read before P_j was handed over
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_bf16_ts(to, tp + uint32_t(kk) * 8u, smem_desc(sv + kk * kVStep, kBlock, kSwSbo, kSw128), idPV,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+          if (j + 1 < nt[x]) {
+            if (!k_ready) {
+              if (!mbar_wait(bar(kBarKFull + (s ^ 1)), uint32_t(((j + 1) >> 1) & 1), a.wait_ns)) timed_out = true;
+              tc_fence_after();
+              k_ready = true;
+            }
+            issue_s(x, j + 1);  // overwrites P_x(j) after P V_x(j) has read it (in-order pipe)
+          } else {
+            mma_commit(bar(kBarODone + x));
+          }
+        }
+        mma_commit(bar(kBarVFree + s));
+        if (next_k) mma_commit(bar(kBarKFree + (s ^ 1)));
       }
+      // the last commit has arrived before the barriers' memory is released
+      const int jl = ntmax - 1;
+      if (!mbar_wait(bar(kBarVFree + (jl & 1)), uint32_t((jl >> 1) & 1), a.wait_ns)) timed_out = true;
     }
   } else {
-    // ---------------- softmax warps: thread t owns query row t ----------------
-    const int t = tid;                 // 0..127, TMEM lane t
-    const int64_t qi = q0 + t;         // global query row
+    // ---- softmax warpgroup x: warps 4x .. 4x + 3, thread t = TMEM lane t = query row q0 + 128x + t ----
+    const int x = warp >> 2;
+    const int t = tid & 127;
+    const int ntx = nt[x];
+    const int64_t qx = q0 + int64_t(x) * kBM;
+    const int64_t qi = qx + t;  // global query row
     const int64_t klim = a.causal ? qi + a.Sk - a.Sq + 1 : a.Sk;  // keys < klim are visible
-    // keys below kfull are visible to every row of the tile: tiles under it need no mask
-    const int64_t kfull = a.causal ? (q0 + a.Sk - a.Sq + 1 < a.Sk ? q0 + a.Sk - a.Sq + 1 : a.Sk) : a.Sk;
-    const uint32_t lane_base = uint32_t(warp * 32) << 16;
-    // Running maximum m of c * s (log2 units), moved only when a tile's maximum exceeds it by more
-    // than 8: until then P = 2^(c s - m) stays below 2^8 (exact enough in bf16 and fp32) and O, l
-    // need no rescale; O / l and LSE = m ln 2 + ln l are the same for any m.
+    // first key at which any row of the tile can be masked (tiles starting past it take the check)
+    const int64_t kfull = a.causal ? (qx + a.Sk - a.Sq + 1 < a.Sk ? qx + a.Sk - a.Sq + 1 : a.Sk) : a.Sk;
+    const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
+    const uint32_t ts = tmem + lane_base + uint32_t(x * kBN);
+    const uint32_t to = tmem + lane_base + kTmemO + uint32_t(x * kD);
+    // running state in log2 units: m = max of c * s (lagging by up to 2^8), l = sum 2^(c s - m)
     constexpr float kSlack = 8.f;
     float m = -INFINITY;
     float l = 0.f;
-    unsigned char* prow = smem + kOffP;
-    for (int j = 0; j < nt; ++j) {
-      const int s = j & 1;
-      if (!mbar_wait(bar(kBarSFull + s), uint32_t((j >> 1) & 1), a.wait_ns)) timed_out = true;
+    for (int j = 0; j < ntx; ++j) {
+      if (!mbar_wait(bar(kBarSFull + x), uint32_t(j & 1), a.wait_ns)) timed_out = true;
       tc_fence_after();
-      const uint32_t ts = tmem + lane_base + uint32_t(s * kBN);
       const int64_t k0 = int64_t(j) * kBN;
-      uint32_t sv[2][64];  // the row of S, one TMEM read
-      tmem_ld64_nowait(ts, sv[0]);
-      tmem_ld64_nowait(ts + 64, sv[1]);
-      tmem_wait_ld();
-      const bool masked = k0 + kBN > kfull;  // uniform over the CTA
-      if (masked) {  // keys past the row's limit count as -inf
+      // the row maximum, half a row (64 keys) at a time: keys 64-127 first, so that keys 0-63 are
+      // still in registers for the exponentials (their P goes over columns 0-31, which they held)
+      const bool masked = k0 + kBN > kfull;  // uniform over the warpgroup
+      uint32_t sv[64];
+      float mx[8];
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+      for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
 #pragma unroll
-          for (int i = 0; i < 64; ++i)
-            if (k0 + h * 64 + i >= klim) sv[h][i] = 0xff800000u;
+      for (int hh = 0; hh < 2; ++hh) {
+        const int h = 1 - hh;
+        tmem_ld64_nowait(ts + uint32_t(h * 64), sv);
+        tmem_wait_ld();
+        if (masked) mask_keys(sv, k0 + h * 64, klim);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(sv[i]));
       }
-      float mx[8];  // eight partial maxima: short dependency chains
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(__uint_as_float(sv[0][i]), __uint_as_float(sv[1][i]));
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int i = 8; i < 64; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(sv[h][i]));
       const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const float mtc = __fmul_rn(mt, a.c);
       const bool move = mtc > m + kSlack;  // m = -inf: any visible key moves it
       const float m_new = move ? mtc : m;
       const float alpha = move ? ex2(m - m_new) : 1.f;  // 0 while the row had seen nothing
       const float ms = m_new == -INFINITY ? 0.f : m_new;
-      // the previous P V product has landed: P's buffer is free and O can be rescaled
-      if (j > 0) {
-        if (!mbar_wait(bar(kBarODone), uint32_t((j - 1) & 1), a.wait_ns)) timed_out = true;
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          const uint32_t to = tmem + lane_base + 256u;
+      // S_x(j) landing means O_x holds P V_x(j - 1), and P V_x(j) waits for this P: rescale O now
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-          for (int h = 0; h < 2; ++h) {  // rare (the maximum moved): half a row at a time
-            uint32_t ov[64];
-            tmem_ld64_nowait(to + h * 64, ov);
-            tmem_wait_ld();
+        for (int h = 0; h < 4; ++h) {  // rare (the maximum moved): a quarter row at a time
+          uint32_t ov[32];
+          tmem_ld32_nowait(to + h * 32, ov);
+          tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 64; ++i) ov[i] = __float_as_uint(__fmul_rn(__uint_as_float(ov[i]), alpha));
-            tmem_st64(to + h * 64, ov);
-            tmem_wait_st();
-          }
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__fmul_rn(__uint_as_float(ov[i]), alpha));
+          tmem_st32(to + h * 32, ov);
         }
       }
-      // P = 2^(c s - m) as bf16 in the A operand layout (masked keys: 2^-inf = 0); the row sum in
-      // fp32, four pairs of partial sums; the exponent by one packed fused multiply-add per pair
+      // P = 2^(c s - m) as packed bf16 over columns 0-63 of S_x (masked keys: 2^-inf = 0); the row
+      // sum in fp32, four pairs of partial sums; the exponent by one packed fused multiply-add per pair
       const float2 c2 = make_float2(a.c, a.c), nm2 = make_float2(-ms, -ms);
       float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-#pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {  // 8 chunks of 8 keys per half
-          uint32_t pk[4];
-#pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            const int i = c8 * 8 + e;
-            const float2 t2 = __ffma2_rn(make_float2(__uint_as_float(sv[h][i]), __uint_as_float(sv[h][i + 1])), c2, nm2);
-            const float2 p = make_float2(ex2(t2.x), ex2(t2.y));
-            acc[e >> 1] = __fadd2_rn(acc[e >> 1], p);
-            pk[e >> 1] = pack_bf16x2(p.x, p.y);
-          }
-          *reinterpret_cast<uint4*>(prow + tile_off(t, h * 8 + c8)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        if (h == 1) {  // keys 64-127 again (columns 64-127 are untouched by P)
+          tmem_ld64_nowait(ts + 64u, sv);
+          tmem_wait_ld();
+          if (masked) mask_keys(sv, k0 + 64, klim);
         }
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) {
+          const float2 t2 = __ffma2_rn(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), c2, nm2);
+          const float2 p = make_float2(ex2(t2.x), ex2(t2.y));
+          acc[(i >> 1) & 3] = __fadd2_rn(acc[(i >> 1) & 3], p);
+          pk[i >> 1] = pack_bf16x2(p.x, p.y);
+        }
+        tmem_st32(ts + uint32_t(h * 32), pk);  // keys 64h .. 64h + 63 -> columns 32h .. 32h + 31
       }
       const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
       const float2 aa = __fadd2_rn(a01, a23);
       l = __fadd_rn(__fmul_rn(l, alpha), __fadd_rn(aa.x, aa.y));
       m = m_new;
-      fence_proxy_async_cta();  // P's generic stores -> the tensor cores' async proxy
-      tc_fence_before();        // O's TMEM stores before the next product
+      tmem_wait_st();    // P (and O's rescale) in TMEM before the product that reads them
+      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarPFull));
+      if (lane == 0) mbar_arrive(bar(kBarPFull + x));
     }
-    // epilogue: O / l, LSE = m ln 2 + ln l
-    if (nt > 0) {
-      if (!mbar_wait(bar(kBarODone), uint32_t((nt - 1) & 1), a.wait_ns)) timed_out = true;
+    // ---- epilogue: O / l and LSE ----
+    if (ntx > 0) {
+      if (!mbar_wait(bar(kBarODone + x), 0u, a.wait_ns)) timed_out = true;
       tc_fence_after();
     }
     const float inv = l > 0.f ? __frcp_rn(l) : 0.f;
-    const uint32_t to = tmem + lane_base + 256u;
     unsigned char* orow = a.o + (bh * a.Sq + qi) * (kD * 2);
 #pragma unroll 1
     for (int h = 0; h < 2; ++h) {
       uint32_t ov[64];
-      if (nt > 0) {
+      if (ntx > 0) {
         tmem_ld64_nowait(to + h * 64, ov);
         tmem_wait_ld();
       } else {
@@ -431,7 +468,7 @@ cudaError_t launch_attention(const void* q, const void* k, const void* v, void* 
   AttnArgs a{static_cast<const unsigned char*>(q), static_cast<const unsigned char*>(k),
              static_cast<const unsigned char*>(v), static_cast<unsigned char*>(o), lse, Sq, Sk, scale * kLog2e,
              causal ? 1 : 0, dev.status, local_wait_limit_ns()};
-  const dim3 grid(unsigned((Sq + kBM - 1) / kBM), unsigned(BH));
+  const dim3 grid(unsigned((Sq + 2 * kBM - 1) / (2 * kBM)), unsigned(BH));
   k_attention_fwd<<<grid, kThreads, kSmem, stream>>>(a, tq, tk, tv);
   return cudaGetLastError();
 }
