@@ -156,6 +156,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Keys at or past the row's limit count as -inf.
 __device__ __forceinline__ void mask_keys(uint32_t (&sv)[64], int64_t key0, int64_t klim) {
 #pragma unroll
@@ -328,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         if (masked) mask_keys(sv, k0 + h * 64, klim);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(sv[i]));
+        for (int i = 0; i < 64; i += 2) mx[(i >> 1) & 7] = fmax3(mx[(i >> 1) & 7], __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
       }
       const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const float mtc = __fmul_rn(mt, a.c);
