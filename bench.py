@@ -531,7 +531,8 @@ def bench_attention(args) -> dict | None:
                    "l2": "q, k, v 384 MiB (larger than L2)",
                    "timing": "CUDA graph replays between CUDA events on the launching stream"},
         "roofline": {"bound": "tensor", "achieved": round(tflops / world, 1), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(tflops / world / peak, 4), "traffic": None,
+                     "frac": round(tflops / world / peak, 4),
+                     "traffic": profiled_traffic("k_attention_fwd", args.workload),
                      "peak_source": f"{kind} (MEASURED_PEAKS.json bf16_tflops, burst)", "kernel": "k_attention_fwd"},
         "gpu_launches": args.steps,
         "clocks": clk,

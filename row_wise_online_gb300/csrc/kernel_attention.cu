@@ -64,13 +64,17 @@ struct AttnArgs {
 };
 
 // Shared memory (from a 1024-byte aligned base, as the 128-byte swizzle needs):
-// Q[2] | K[2] | V[2] | barriers | TMEM address.
+// Q[2] | K[2] | V[2] | barriers, TMEM address | O staging, 4 KB per softmax warp (32 rows x 64
+// elements, the layout of a 128-byte-swizzled TMA box).
 constexpr int kOffQ = 0;
 constexpr int kOffK = 2 * kTile;
 constexpr int kOffV = 4 * kTile;
 constexpr int kOffBar = 6 * kTile;
 constexpr int kNumBars = 16;
-constexpr int kSmem = kOffBar + kNumBars * 8 + 16 + 1024;  // + alignment slack
+constexpr int kOffOStage = kOffBar + 1024;
+constexpr int kOStage = 32 * 128;
+constexpr int kSmem = kOffOStage + 8 * kOStage + 1024;  // + alignment slack
+static_assert(kNumBars * 8 + 4 <= 1024, "barriers overflow their slot");
 // barrier indices
 constexpr int kBarQFull = 0, kBarKFull = 1 /*2*/, kBarVFull = 3 /*2*/, kBarKFree = 5 /*2*/, kBarVFree = 7 /*2*/,
               kBarSFull = 9 /*X*/, kBarPFull = 11 /*X*/, kBarODone = 13 /*X*/;
@@ -105,6 +109,18 @@ __device__ __forceinline__ void tma_load_box(uint32_t dst, const CUtensorMap* ma
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
 }
+
+// TMA store of a box (64 elements, 32 rows) from shared memory, and waiting until the copy engine
+// has read the staging buffer.
+__device__ __forceinline__ void tma_store_box(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y), "r"(z)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void tma_store_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_cta() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A K-major, B K-major
 // (b_mn = 0) or MN-major (b_mn = 1), N = 128, M = 128.
@@ -172,7 +188,7 @@ __device__ __forceinline__ void mask_keys(uint32_t (&sv)[64], int64_t key0, int6
 // 320 threads, at most 168 registers a thread: three warps share a sub-partition's 16K registers.
 __global__ void __launch_bounds__(kThreads, 1)
     k_attention_fwd(AttnArgs a, const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                    const __grid_constant__ CUtensorMap tv) {
+                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tout) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
@@ -181,8 +197,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return smem_addr(&bars[i]); };
 
   const int64_t ncta = (a.Sq + 2 * kBM - 1) / (2 * kBM);
-  const int64_t q0 = (ncta - 1 - int64_t(blockIdx.x)) * (2 * kBM);  // the heaviest causal tiles first
-  const int64_t bh = blockIdx.y;
+  // causal: grid (heads, query-tile pairs), heads fastest, so every head's heaviest tiles (the last
+  // rows) start first and the lightest fill the tail; otherwise (query-tile pairs, heads), a head's
+  // CTAs side by side while its K and V sit in L2
+  const int64_t rank = a.causal ? blockIdx.y : blockIdx.x;
+  const int64_t q0 = (ncta - 1 - rank) * (2 * kBM);
+  const int64_t bh = a.causal ? blockIdx.x : blockIdx.y;
   // key tiles visited by query tile X: all, or (causal, bottom-right aligned) those that hold a
   // key <= the tile's last row + Sk - Sq; none for a tile past the end of the queries
   int nt[2];
@@ -390,29 +410,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
     }
     const float inv = l > 0.f ? __frcp_rn(l) : 0.f;
-    unsigned char* orow = a.o + (bh * a.Sq + qi) * (kD * 2);
+    // O / l as bf16 through this warp's staging buffer (row = lane, 16-byte chunk c at position
+    // c ^ (lane % 8)), one TMA store per 64 columns; rows past Sq are clipped by the copy
+    unsigned char* stage = smem + kOffOStage + warp * kOStage;
 #pragma unroll 1
-    for (int h = 0; h < 2; ++h) {
-      uint32_t ov[64];
-      if (ntx > 0) {
-        tmem_ld64_nowait(to + h * 64, ov);
-        tmem_wait_ld();
-      } else {
+    for (int hc = 0; hc < 2; ++hc) {
+#pragma unroll 1
+      for (int q2 = 0; q2 < 2; ++q2) {
+        uint32_t ov[32];
+        if (ntx > 0) {
+          tmem_ld32_nowait(to + uint32_t(hc * 64 + q2 * 32), ov);
+          tmem_wait_ld();
+        } else {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) ov[i] = 0u;
-      }
-      if (qi < a.Sq) {
+          for (int i = 0; i < 32; ++i) ov[i] = 0u;
+        }
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float* f = reinterpret_cast<const float*>(ov + 8 * q);
+        for (int cc = 0; cc < 4; ++cc) {
+          const float* f = reinterpret_cast<const float*>(ov + 8 * cc);
           uint4 w;
           w.x = pack_bf16x2(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv));
           w.y = pack_bf16x2(__fmul_rn(f[2], inv), __fmul_rn(f[3], inv));
           w.z = pack_bf16x2(__fmul_rn(f[4], inv), __fmul_rn(f[5], inv));
           w.w = pack_bf16x2(__fmul_rn(f[6], inv), __fmul_rn(f[7], inv));
-          *reinterpret_cast<uint4*>(orow + (h * 64 + 8 * q) * 2) = w;
+          const int c = q2 * 4 + cc;
+          *reinterpret_cast<uint4*>(stage + lane * 128 + ((c ^ (lane & 7)) << 4)) = w;
         }
       }
+      fence_proxy_async_cta();  // the staging writes -> the copy engine
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_box(&tout, smem_addr(stage), hc * 64, int(qx + (warp & 3) * 32), int(bh));
+        tma_store_wait_read();  // the buffer is reused (and released at exit) only once read
+      }
+      __syncwarp();
     }
     if (qi < a.Sq && a.lse)
       a.lse[bh * a.Sq + qi] = l > 0.f ? __fadd_rn(__fmul_rn(m, 0.6931471805599453f), logf(l)) : -INFINITY;
@@ -449,13 +480,14 @@ EncodeTiled encode_tiled() {
   return fn;
 }
 
-// [BH][S][128] bf16, boxes of 8 elements x 128 rows x 1 head; rows past S read as zeros.
-bool make_map(CUtensorMap* m, const void* base, int64_t S, int64_t BH) {
+// [BH][S][128] bf16, boxes of 64 elements x `rows` rows x 1 head, 128-byte swizzle; rows past S
+// read as zeros (loads) or are not written (stores).
+bool make_map(CUtensorMap* m, const void* base, int64_t S, int64_t BH, uint32_t rows) {
   EncodeTiled fn = encode_tiled();
   if (!fn) return false;
   const cuuint64_t dims[3] = {cuuint64_t(kD), cuuint64_t(S), cuuint64_t(BH)};
   const cuuint64_t strides[2] = {cuuint64_t(kD) * 2, cuuint64_t(S) * kD * 2};
-  const cuuint32_t box[3] = {64, cuuint32_t(kBM), 1};
+  const cuuint32_t box[3] = {64, rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -468,14 +500,16 @@ cudaError_t launch_attention(const void* q, const void* k, const void* v, void* 
                              int64_t Sk, float scale, bool causal, cudaStream_t stream, const DeviceInfo& dev) {
   cudaError_t err = cudaFuncSetAttribute((const void*)k_attention_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (err != cudaSuccess) return err;
-  alignas(64) CUtensorMap tq, tk, tv;
-  if (!make_map(&tq, q, Sq, BH) || !make_map(&tk, k, Sk, BH) || !make_map(&tv, v, Sk, BH))
+  alignas(64) CUtensorMap tq, tk, tv, to;
+  if (!make_map(&tq, q, Sq, BH, kBM) || !make_map(&tk, k, Sk, BH, kBN) || !make_map(&tv, v, Sk, BH, kBN) ||
+      !make_map(&to, o, Sq, BH, 32))
     return cudaErrorInvalidValue;
   AttnArgs a{static_cast<const unsigned char*>(q), static_cast<const unsigned char*>(k),
              static_cast<const unsigned char*>(v), static_cast<unsigned char*>(o), lse, Sq, Sk, scale * kLog2e,
              causal ? 1 : 0, dev.status, local_wait_limit_ns()};
-  const dim3 grid(unsigned((Sq + 2 * kBM - 1) / (2 * kBM)), unsigned(BH));
-  k_attention_fwd<<<grid, kThreads, kSmem, stream>>>(a, tq, tk, tv);
+  const unsigned ncta = unsigned((Sq + 2 * kBM - 1) / (2 * kBM));
+  const dim3 grid = causal ? dim3(unsigned(BH), ncta) : dim3(ncta, unsigned(BH));
+  k_attention_fwd<<<grid, kThreads, kSmem, stream>>>(a, tq, tk, tv, to);
   return cudaGetLastError();
 }
 

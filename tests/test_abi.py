@@ -93,6 +93,18 @@ def test_other_calls_argument_checks(lib):
     assert st(X, 4, NULL, 4, None, None, None, 4, 4, 0, 1.0, 0, 0, None) == rwo.ERR_INVALID_ARG  # no y
     assert st(X, 2**62, X, 4, None, None, None, 4, 4, 0, 1.0, 0, 0, None) == rwo.ERR_INVALID_ARG  # overflow
     assert st(NULL, 0, NULL, 0, None, None, None, 0, 4, 0, 1.0, 0, 0, None) == rwo.OK  # M = 0
+    at = lib.attention_forward  # (q, k, v, o, lse, BH, Sq, Sk, d, scale, causal, dtype, stream)
+    assert at(X, X, X, X, None, 1, 16, 16, 64, 1.0, 0, 1, None) == rwo.ERR_UNSUPPORTED  # d = 64
+    assert at(X, X, X, X, None, 1, 16, 16, 128, 1.0, 0, 0, None) == rwo.ERR_UNSUPPORTED  # fp32
+    assert at(X, X, X, X, None, 1, 16, 16, 128, 0.0, 0, 1, None) == rwo.ERR_INVALID_ARG  # scale
+    assert at(X, X, X, X, None, 1, 16, 16, 128, 1.0, 2, 1, None) == rwo.ERR_INVALID_ARG  # causal flag
+    assert at(X, X, X, X, None, 1, 0, 16, 128, 1.0, 0, 1, None) == rwo.ERR_INVALID_ARG  # Sq = 0
+    assert at(X, X, X, X, None, 65536, 16, 16, 128, 1.0, 0, 1, None) == rwo.ERR_UNSUPPORTED  # BH
+    assert at(X, X, X, X, None, 1, 2**31, 16, 128, 1.0, 0, 1, None) == rwo.ERR_UNSUPPORTED  # 32-bit rows
+    assert at(X, X, X, X, None, 1, 16, 2**31, 128, 1.0, 0, 1, None) == rwo.ERR_UNSUPPORTED
+    assert at(X, X, X, X, None, 1, 65536 * 256, 16, 128, 1.0, 1, 1, None) == rwo.ERR_UNSUPPORTED  # causal grid
+    assert at(NULL, NULL, NULL, NULL, None, 1, 16, 16, 128, 1.0, 0, 1, None) == rwo.ERR_INVALID_ARG  # pointers
+    assert at(NULL, NULL, NULL, NULL, None, 0, 16, 16, 128, 1.0, 0, 1, None) == rwo.OK  # BH = 0
 
 
 def test_status_strings(lib):
