@@ -191,8 +191,9 @@ int cross_entropy_rows(const void* x, const int64_t* labels, float* loss, float*
  *   lse_out -- device, fp32 [BH][Sq]: m + ln l of each row (natural log, of scale Q K^T), or NULL.
  *   scale   -- finite, > 0 (1/sqrt(d) in attention).
  *   causal  -- 1: query row i sees keys j <= i + Sk - Sq (the last query sees every key); 0: all.
- * A row that sees no key gets o = 0, LSE = -inf.  Supported: dtype SOFTMAX_BF16 with d = 128
- * (fp32 accumulation, P rounded to bf16 for the P V product); other dtypes or head sizes return
+ * A row that sees no key gets o = 0, LSE = -inf.  Supported: dtype SOFTMAX_BF16 or SOFTMAX_F16
+ * with d = 128 (fp32 accumulation; P rounded to the element type for the P V product; fp16
+ * weights stay below 2^8, O below max |v|); other dtypes or head sizes return
  * SOFTMAX_ERR_UNSUPPORTED, as do BH > 65535, Sq or Sk > 2^31 - 256, and (causal) Sq > 65535 * 256.
  * Pointers 16-byte aligned (else SOFTMAX_ERR_MISALIGNED).
  * BH == 0 is a no-op.  A bounded wait that runs out is reported by softmax_get_status.

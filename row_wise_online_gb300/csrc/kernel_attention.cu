@@ -35,6 +35,7 @@
 #include <mutex>
 
 #include "device_common.cuh"
+#include "attention.h"
 #include "launch.h"
 
 namespace rwo {
@@ -122,10 +123,17 @@ __device__ __forceinline__ void tma_store_box(const CUtensorMap* map, uint32_t s
 __device__ __forceinline__ void tma_store_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_cta() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A K-major, B K-major
-// (b_mn = 0) or MN-major (b_mn = 1), N = 128, M = 128.
-__device__ __forceinline__ uint32_t idesc_bf16(uint32_t b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn << 16) | ((uint32_t(kBN) >> 3) << 17) | ((uint32_t(kBM) >> 4) << 24);
+// Instruction descriptor, kind::f16: fp32 accumulator, A and B both bf16 (fmt 1) or both fp16
+// (fmt 0), A K-major, B K-major (b_mn = 0) or MN-major (b_mn = 1), N = 128, M = 128.
+__device__ __forceinline__ uint32_t idesc_f16kind(uint32_t fmt, uint32_t b_mn) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | (b_mn << 16) | ((uint32_t(kBN) >> 3) << 17) | ((uint32_t(kBM) >> 4) << 24);
+}
+
+// Two fp32 values rounded to the element type (bf16 or fp16), low half first.
+template <bool H>
+__device__ __forceinline__ uint32_t pack_elem2(float lo, float hi) {
+  if constexpr (H) return pack_f16x2(lo, hi);
+  else return pack_bf16x2(lo, hi);
 }
 
 __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -186,6 +194,8 @@ __device__ __forceinline__ void mask_keys(uint32_t (&sv)[64], int64_t key0, int6
 }
 
 // 320 threads, at most 168 registers a thread: three warps share a sub-partition's 16K registers.
+// H: fp16 elements (else bf16).
+template <bool H>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attention_fwd(AttnArgs a, const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tout) {
@@ -271,7 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ---- MMA issuer: S_X(0); then per key tile j: P V_0(j), S_0(j+1), P V_1(j), S_1(j+1) ----
     if (lane == 0 && ntmax > 0) {
-      const uint32_t idS = idesc_bf16(0), idPV = idesc_bf16(1);
+      const uint32_t fmt = H ? 0u : 1u;
+      const uint32_t idS = idesc_f16kind(fmt, 0), idPV = idesc_f16kind(fmt, 1);
       auto issue_s = [&](int x, int j) {  // S_x(j) = Q_x K_j^T into S_x; K_j has landed
         const uint32_t sq = smem_addr(smem + kOffQ + x * kTile), sk = smem_addr(smem + kOffK + (j & 1) * kTile);
 #pragma unroll
@@ -391,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 t2 = __ffma2_rn(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), c2, nm2);
           const float2 p = make_float2(ex2(t2.x), ex2(t2.y));
           acc[(i >> 1) & 3] = __fadd2_rn(acc[(i >> 1) & 3], p);
-          pk[i >> 1] = pack_bf16x2(p.x, p.y);
+          pk[i >> 1] = pack_elem2<H>(p.x, p.y);
         }
         tmem_st32(ts + uint32_t(h * 32), pk);  // keys 64h .. 64h + 63 -> columns 32h .. 32h + 31
       }
@@ -429,10 +440,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cc = 0; cc < 4; ++cc) {
           const float* f = reinterpret_cast<const float*>(ov + 8 * cc);
           uint4 w;
-          w.x = pack_bf16x2(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv));
-          w.y = pack_bf16x2(__fmul_rn(f[2], inv), __fmul_rn(f[3], inv));
-          w.z = pack_bf16x2(__fmul_rn(f[4], inv), __fmul_rn(f[5], inv));
-          w.w = pack_bf16x2(__fmul_rn(f[6], inv), __fmul_rn(f[7], inv));
+          w.x = pack_elem2<H>(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv));
+          w.y = pack_elem2<H>(__fmul_rn(f[2], inv), __fmul_rn(f[3], inv));
+          w.z = pack_elem2<H>(__fmul_rn(f[4], inv), __fmul_rn(f[5], inv));
+          w.w = pack_elem2<H>(__fmul_rn(f[6], inv), __fmul_rn(f[7], inv));
           const int c = q2 * 4 + cc;
           *reinterpret_cast<uint4*>(stage + lane * 128 + ((c ^ (lane & 7)) << 4)) = w;
         }
@@ -456,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-bool attention_fits(int64_t d, int dtype) { return d == kD && dtype == 1; }
+bool attention_fits(int64_t d, int dtype) { return d == kD && (dtype == 1 || dtype == 2); }
 
 namespace {
 
@@ -482,14 +493,14 @@ EncodeTiled encode_tiled() {
 
 // [BH][S][128] bf16, boxes of 64 elements x `rows` rows x 1 head, 128-byte swizzle; rows past S
 // read as zeros (loads) or are not written (stores).
-bool make_map(CUtensorMap* m, const void* base, int64_t S, int64_t BH, uint32_t rows) {
+bool make_map(CUtensorMap* m, const void* base, int64_t S, int64_t BH, uint32_t rows, bool f16) {
   EncodeTiled fn = encode_tiled();
   if (!fn) return false;
   const cuuint64_t dims[3] = {cuuint64_t(kD), cuuint64_t(S), cuuint64_t(BH)};
   const cuuint64_t strides[2] = {cuuint64_t(kD) * 2, cuuint64_t(S) * kD * 2};
   const cuuint32_t box[3] = {64, rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+  return fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -497,19 +508,22 @@ bool make_map(CUtensorMap* m, const void* base, int64_t S, int64_t BH, uint32_t 
 }  // namespace
 
 cudaError_t launch_attention(const void* q, const void* k, const void* v, void* o, float* lse, int64_t BH, int64_t Sq,
-                             int64_t Sk, float scale, bool causal, cudaStream_t stream, const DeviceInfo& dev) {
-  cudaError_t err = cudaFuncSetAttribute((const void*)k_attention_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+                             int64_t Sk, float scale, bool causal, int dtype, cudaStream_t stream,
+                             const DeviceInfo& dev) {
+  const bool f16 = dtype == 2;
+  auto* kern = f16 ? k_attention_fwd<true> : k_attention_fwd<false>;
+  cudaError_t err = cudaFuncSetAttribute((const void*)kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (err != cudaSuccess) return err;
   alignas(64) CUtensorMap tq, tk, tv, to;
-  if (!make_map(&tq, q, Sq, BH, kBM) || !make_map(&tk, k, Sk, BH, kBN) || !make_map(&tv, v, Sk, BH, kBN) ||
-      !make_map(&to, o, Sq, BH, 32))
+  if (!make_map(&tq, q, Sq, BH, kBM, f16) || !make_map(&tk, k, Sk, BH, kBN, f16) ||
+      !make_map(&tv, v, Sk, BH, kBN, f16) || !make_map(&to, o, Sq, BH, 32, f16))
     return cudaErrorInvalidValue;
   AttnArgs a{static_cast<const unsigned char*>(q), static_cast<const unsigned char*>(k),
              static_cast<const unsigned char*>(v), static_cast<unsigned char*>(o), lse, Sq, Sk, scale * kLog2e,
              causal ? 1 : 0, dev.status, local_wait_limit_ns()};
   const unsigned ncta = unsigned((Sq + 2 * kBM - 1) / (2 * kBM));
   const dim3 grid = causal ? dim3(unsigned(BH), ncta) : dim3(ncta, unsigned(BH));
-  k_attention_fwd<<<grid, kThreads, kSmem, stream>>>(a, tq, tk, tv, to);
+  kern<<<grid, kThreads, kSmem, stream>>>(a, tq, tk, tv, to);
   return cudaGetLastError();
 }
 

@@ -76,11 +76,6 @@ cudaError_t launch_splitrow(const RowProblem& p, const DeviceInfo& dev);
 cudaError_t launch_splitrow_scratch(const RowProblem& p, const DeviceInfo& dev, unsigned long long* pub,
                                     size_t pub_slots, bool* too_big);
 
-// Attention forward (tcgen05): q [BH][Sq][d], k and v [BH][Sk][d], o [BH][Sq][d], bf16, d = 128.
-bool attention_fits(int64_t d, int dtype);
-cudaError_t launch_attention(const void* q, const void* k, const void* v, void* o, float* lse, int64_t BH, int64_t Sq,
-                             int64_t Sk, float scale, bool causal, cudaStream_t stream, const DeviceInfo& dev);
-
 // The current device's properties (softmax_status code), for entry points outside api.cu.
 int current_device(const DeviceInfo** out);
 // Records err as the thread's last CUDA error and returns SOFTMAX_ERR_CUDA.

@@ -1,9 +1,10 @@
 """attention_forward (the FlashAttention forward tile on tcgen05) against the fp64 oracle.
 
-Tolerance, derived from the arithmetic: scores and the row state are fp32 (bf16 products are exact
-in fp32); P is rounded to bf16 before the P V product (relative 2^-9 per weight) while l sums the
-unrounded weights, so |O - O_ref| <= 2^-9 max_j |v_j| plus the output's own bf16 rounding; the test
-allows 2^-8 max|v| + one bf16 ulp of O_ref.  LSE within 1e-4 max(1, |LSE|).
+Tolerance, derived from the arithmetic: scores and the row state are fp32 (bf16 and fp16 products
+are exact in fp32); P is rounded to the element type before the P V product (relative 2^-9 per
+weight for bf16, 2^-11 for fp16) while l sums the unrounded weights, so |O - O_ref| <= 2^-9 (2^-11)
+max_j |v_j| plus the output's own rounding; the test allows 2^-8 (bf16) or 2^-10 (fp16) max|v| + one
+ulp of O_ref in the element type.  LSE within 1e-4 max(1, |LSE|).
 """
 import numpy as np
 import pytest
@@ -13,7 +14,7 @@ import oracle
 import row_wise_online_gb300 as rwo
 import synth
 from gpu_util import to_device, to_host
-from tolerances import bf16_ulp
+from tolerances import bf16_ulp, f16_ulp
 
 pytestmark = pytest.mark.gpu
 
@@ -26,20 +27,24 @@ def _built():
     torch.cuda.set_device(0)
 
 
-def _qkv(BH, Sq, Sk, d, seed, q_sd=1.0):
-    gen = lambda M, N, s, sd: synth.generate(synth.custom("attn", synth.BF16, M, N, seed=s, p1=sd))
+def _qkv(BH, Sq, Sk, d, seed, q_sd=1.0, dtype=synth.BF16):
+    gen = lambda M, N, s, sd: synth.generate(synth.custom("attn", dtype, M, N, seed=s, p1=sd))
     q = gen(BH * Sq, d, seed, q_sd).reshape(BH, Sq, d)
     k = gen(BH * Sk, d, seed + 1, 1.0).reshape(BH, Sk, d)
     v = gen(BH * Sk, d, seed + 2, 1.0).reshape(BH, Sk, d)
     return q, k, v
 
 
-def _check(o_gpu, lse_gpu, q, k, v, rows, causal, scale, what):
-    o_ref, lse_ref = oracle.attention_rows(q, k, v, rows, dtype=synth.BF16, scale=scale, causal=causal)
-    vmax = np.abs(synth.bf16_to_f32(v).astype(np.float64)).max(axis=(1, 2))
+def _check(o_gpu, lse_gpu, q, k, v, rows, causal, scale, what, dtype=synth.BF16):
+    o_ref, lse_ref = oracle.attention_rows(q, k, v, rows, dtype=dtype, scale=scale, causal=causal)
+    widen = synth.f16_to_f32 if dtype == synth.F16 else synth.bf16_to_f32
+    vmax = np.abs(widen(v).astype(np.float64)).max(axis=(1, 2))
     idx = np.asarray(rows)
-    og = synth.bf16_to_f32(o_gpu[idx[:, 0], idx[:, 1]]).astype(np.float64)
-    bound = (2.0 ** -8) * vmax[idx[:, 0]][:, None] + bf16_ulp(o_ref)
+    og = widen(o_gpu[idx[:, 0], idx[:, 1]]).astype(np.float64)
+    if dtype == synth.F16:
+        bound = (2.0 ** -10) * vmax[idx[:, 0]][:, None] + f16_ulp(o_ref)
+    else:
+        bound = (2.0 ** -8) * vmax[idx[:, 0]][:, None] + bf16_ulp(o_ref)
     err = np.abs(og - o_ref)
     bad = ~(err <= bound)
     assert not bad.any(), f"{what}: {bad.sum()} outputs off; worst {err.max()} at {np.unravel_index(np.argmax(err), err.shape)}"
@@ -60,6 +65,20 @@ def test_attention_against_oracle(BH, Sq, Sk, causal):
     assert rwo.get_status() == rwo.OK
     rows = [(h, i) for h in range(BH) for i in range(Sq)]
     _check(to_host(o), lse.cpu().numpy(), q, k, v, rows, causal, 1.0 / np.sqrt(d), f"attn {BH}x{Sq}x{Sk} causal={causal}")
+
+
+@pytest.mark.parametrize("BH,Sq,Sk", [(2, 300, 300), (1, 77, 1000), (2, 256, 384), (2, 1000, 77)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_attention_f16_against_oracle(BH, Sq, Sk, causal):
+    d = 128
+    q, k, v = _qkv(BH, Sq, Sk, d, seed=Sq * 5 + Sk, dtype=synth.F16)
+    lse = torch.full((BH, Sq), float("nan"), device="cuda")
+    qd, kd, vd = (to_device(t, synth.F16) for t in (q, k, v))
+    o = rwo.attention_forward(qd, kd, vd, lse_out=lse, causal=causal)
+    assert o.dtype == torch.float16
+    rows = [(h, i) for h in range(BH) for i in range(Sq)]
+    _check(to_host(o), lse.cpu().numpy(), q, k, v, rows, causal, 1.0 / np.sqrt(d),
+           f"attn fp16 {BH}x{Sq}x{Sk} causal={causal}", dtype=synth.F16)
 
 
 def test_attention_large_scores_and_scale():
