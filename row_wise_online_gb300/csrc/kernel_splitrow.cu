@@ -14,9 +14,13 @@
 //         evict_first, served from L2 (measured: DRAM reads stay at one read of x for 16 MiB rows).
 //
 // The producer picks each next piece: a P2 piece of the oldest row whose exchange is done, else a
-// P1 piece of a row at most kL2Lag rows ahead of the oldest row still waiting for its P2, else it
-// waits.  Each slot carries a tag (row, piece, pass); the consumers follow the ring in order, so
-// they never wait for an exchange and HBM reads keep flowing while rows wait for theirs.  Nothing
+// P1 piece of a row at most kL2Lag rows ahead of the oldest row still waiting for its P2, else the
+// next P2 piece of that row before its exchange is done (its data does not depend on the
+// exchange; only its arithmetic does).  Each slot carries a tag (row, piece, pass); the consumers
+// follow the ring in order and wait for a row's state only at a P2 piece whose row's exchange is
+// still running -- every P1 piece the exchange needs precedes it in the ring -- so HBM reads keep
+// flowing while rows wait for their exchange and the first P2 pieces are already on chip when it
+// completes.  Nothing
 // of a row is held on chip, so the row length is not bounded by registers or shared memory (a row
 // larger than L2 is still correct; its P2 then also reads HBM).
 //
@@ -264,23 +268,11 @@ __global__ void __launch_bounds__(kSplitThreads, 1) k_splitrow(SplitArgs a) {
       int ps = 0;              // ring slot of piece n, and the parity of its lap (kept
       uint32_t pph = 0;        // incrementally: a 64-bit division per piece costs ~0.1 us)
       for (int64_t n = 0; n < total; ++n) {
-        // choose the next piece (bounded: a missing exchange signal ends the wait)
-        bool second = false;
-        const uint64_t t0 = global_timer_ns();
-        while (true) {
-          if (!ready2) ready2 = mbar_test(smem_addr(&row_ready[r2 % RB]), uint32_t((r2 / RB) & 1));
-          if (ready2) {
-            second = true;
-            break;
-          }
-          if (r1 < a.M && r1 <= r2 + kL2Lag) break;
-          service();
-          if (global_timer_ns() - t0 > a.local_wait_ns) {
-            timed_out = true;
-            second = r1 >= a.M || r1 > r2 + kL2Lag;  // keep the stream going either way
-            break;
-          }
-        }
+        // choose the next piece: a P2 piece of a row whose exchange is done, else a P1 piece within
+        // the lag, else the next P2 piece anyway -- its data does not depend on the exchange, so it
+        // is loaded while the exchange finishes, and the consumers wait for the row's state
+        if (!ready2) ready2 = mbar_test(smem_addr(&row_ready[r2 % RB]), uint32_t((r2 / RB) & 1));
+        const bool second = ready2 || !(r1 < a.M && r1 <= r2 + kL2Lag);
         const int s = ps;
         if (n >= NS) {
           const uint32_t bar = smem_addr(&freed[s]);
@@ -401,6 +393,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1) k_splitrow(SplitArgs a) {
         }
       } else {
         // P2: normalise the re-read piece with the row's state and store y
+        // the row's state (the piece may have been loaded before the row's exchange completed)
+        if (!mbar_wait(smem_addr(&row_ready[r % RB]), uint32_t((r / RB) & 1), a.local_wait_ns)) timed_out = true;
         const State row = rowst[r % RB];
         const float ms = safe_max(row.m);
         const float inv = safe_inv(row.d);
