@@ -78,7 +78,7 @@ constexpr int kSmem = kOffOStage + 8 * kOStage + 1024;  // + alignment slack
 static_assert(kNumBars * 8 + 4 <= 1024, "barriers overflow their slot");
 // barrier indices
 constexpr int kBarQFull = 0, kBarKFull = 1 /*2*/, kBarVFull = 3 /*2*/, kBarKFree = 5 /*2*/, kBarVFree = 7 /*2*/,
-              kBarSFull = 9 /*X*/, kBarPFull = 11 /*X*/, kBarODone = 13 /*X*/;
+              kBarSFull = 9 /*X*/, kBarPFull = 11 /*X*/, kBarODone = 13 /*X*/, kBarQFull1 = 15;
 
 // Q, K and V tiles in shared memory: two blocks of 16 KB (elements 0-63 and 64-127 of each row);
 // in a block, row r's 128 bytes at (r / 8) * 1024 + (r % 8) * 128 with its 16-byte chunk c
@@ -227,8 +227,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int ntmax = nt[0] > nt[1] ? nt[0] : nt[1];
 
-  if (tid == 0) {
+  // The loader lane initialises the barriers and issues the first loads (Q_0 and K_0 first: all
+  // that S_0(0) needs) before the block-wide TMEM allocation and barrier.
+  const int z = int(bh);
+  auto load_tile = [&](const CUtensorMap* map, uint32_t dst, int64_t row0, uint32_t b) {
+    for (int c = 0; c < kD / 64; ++c) tma_load_box(dst + uint32_t(c) * kBlock, map, c * 64, int(row0), z, b);
+  };
+  if (warp == kLoaderWarp && lane == 0) {
     mbar_init(bar(kBarQFull), 1);
+    mbar_init(bar(kBarQFull1), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(kBarKFull + s), 1);
       mbar_init(bar(kBarVFull + s), 1);
@@ -239,6 +246,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarODone + s), 1);
     }
     fence_mbar_init();
+    mbar_arrive_expect_tx(bar(kBarQFull), uint32_t(kTile));
+    load_tile(&tq, smem_addr(smem + kOffQ), q0, bar(kBarQFull));
+    if (ntmax > 0) {
+      mbar_arrive_expect_tx(bar(kBarKFull), uint32_t(kTile));
+      load_tile(&tk, smem_addr(smem + kOffK), 0, bar(kBarKFull));
+    }
+    mbar_arrive_expect_tx(bar(kBarQFull1), uint32_t(kTile));
+    load_tile(&tq, smem_addr(smem + kOffQ + kTile), q0 + kBM, bar(kBarQFull1));
+    if (ntmax > 0) {
+      mbar_arrive_expect_tx(bar(kBarVFull), uint32_t(kTile));
+      load_tile(&tv, smem_addr(smem + kOffV), 0, bar(kBarVFull));
+    }
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
@@ -252,16 +271,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool timed_out = false;
 
   if (warp == kLoaderWarp) {
-    // ---- producer: Q_0 and Q_1 once, then K_j, V_j into stage j & 1 ----
+    // ---- producer: (Q_0, K_0, Q_1, V_0 issued above) K_j, V_j into stage j & 1 ----
     if (lane == 0) {
-      const int z = int(bh);
-      auto load_tile = [&](const CUtensorMap* map, uint32_t dst, int64_t row0, uint32_t b) {
-        for (int c = 0; c < kD / 64; ++c) tma_load_box(dst + uint32_t(c) * kBlock, map, c * 64, int(row0), z, b);
-      };
-      mbar_arrive_expect_tx(bar(kBarQFull), uint32_t(2 * kTile));
-      load_tile(&tq, smem_addr(smem + kOffQ), q0, bar(kBarQFull));
-      load_tile(&tq, smem_addr(smem + kOffQ + kTile), q0 + kBM, bar(kBarQFull));
-      for (int j = 0; j < ntmax; ++j) {
+      for (int j = 1; j < ntmax; ++j) {
         const int s = j & 1;
         const uint32_t par = uint32_t(((j >> 1) - 1) & 1);
         if (j >= 2 && !mbar_wait(bar(kBarKFree + s), par, a.wait_ns)) timed_out = true;  // S(j-2) done
@@ -277,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(bar(kBarVFull + (j & 1)), uint32_t((j >> 1) & 1), a.wait_ns)) timed_out = true;
       }
       if (!mbar_wait(bar(kBarQFull), 0u, a.wait_ns)) timed_out = true;
+      if (!mbar_wait(bar(kBarQFull1), 0u, a.wait_ns)) timed_out = true;
     }
   } else if (warp == kMmaWarp) {
     // ---- MMA issuer: S_X(0); then per key tile j: P V_0(j), S_0(j+1), P V_1(j), S_1(j+1) ----
@@ -294,8 +307,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(bar(kBarQFull), 0, a.wait_ns)) timed_out = true;
       if (!mbar_wait(bar(kBarKFull), 0, a.wait_ns)) timed_out = true;
       tc_fence_after();
-      for (int x = 0; x < 2; ++x)
-        if (nt[x] > 0) issue_s(x, 0);
+      if (nt[0] > 0) issue_s(0, 0);
+      if (nt[1] > 0) {
+        if (!mbar_wait(bar(kBarQFull1), 0, a.wait_ns)) timed_out = true;
+        tc_fence_after();
+        issue_s(1, 0);
+      }
       mma_commit(bar(kBarKFree));
       for (int j = 0; j < ntmax; ++j) {
         const int s = j & 1;
