@@ -387,11 +387,10 @@ int attention_forward(const void* q, const void* k, const void* v, void* o, floa
   if (!(scale > 0.f) || !(scale <= 3.4028234663852886e38f)) return SOFTMAX_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return SOFTMAX_ERR_INVALID_ARG;
   if (!attention_fits(d, dtype)) return SOFTMAX_ERR_UNSUPPORTED;
-  // grid and copy-coordinate limits: BH and (causal) the query-tile pairs index a grid dimension of
-  // at most 65535; rows are 32-bit copy coordinates
+  // grid and copy-coordinate limits: BH indexes a grid dimension of at most 65535; rows are 32-bit
+  // copy coordinates
   constexpr int64_t kMaxRows = (int64_t(1) << 31) - 256;
   if (BH > 65535 || Sq > kMaxRows || Sk > kMaxRows) return SOFTMAX_ERR_UNSUPPORTED;
-  if (causal && (Sq + 255) / 256 > 65535) return SOFTMAX_ERR_UNSUPPORTED;
   const int64_t row = d * elem_bytes(dtype);
   if (Sq > INT64_MAX / row / (BH > 0 ? BH : 1) || Sk > INT64_MAX / row / (BH > 0 ? BH : 1))
     return SOFTMAX_ERR_INVALID_ARG;

@@ -57,7 +57,7 @@ struct AttnArgs {
   const unsigned char* v;  // [BH][Sk][d]
   unsigned char* o;        // [BH][Sq][d]
   float* lse;              // [BH][Sq] or null
-  int64_t Sq, Sk;
+  int64_t BH, Sq, Sk;
   float c;                 // scale * log2 e
   int causal;
   unsigned* status;
@@ -207,12 +207,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return smem_addr(&bars[i]); };
 
   const int64_t ncta = (a.Sq + 2 * kBM - 1) / (2 * kBM);
-  // causal: grid (heads, query-tile pairs), heads fastest, so every head's heaviest tiles (the last
-  // rows) start first and the lightest fill the tail; otherwise (query-tile pairs, heads), a head's
-  // CTAs side by side while its K and V sit in L2
-  const int64_t rank = a.causal ? blockIdx.y : blockIdx.x;
+  // CTA order (launch index L): without a mask, a head's tile pairs side by side while its K and
+  // V sit in L2.  Causal: heads in groups of hg (about 128 CTAs a group), and within a group the
+  // heaviest pairs (the last rows) of every head first, so the light pairs of one group run beside
+  // the heavy pairs of the next and the tail is light, while a group's K and V stay in L2
+  // (measured on 128 heads x 16 pairs: groups of 8 heads 0.429 ms; every head's heaviest first
+  // across all heads 0.445 ms, with 4x the DRAM traffic; one head after another 0.453 ms).
+  int64_t rank, bh;
+  {
+    const int64_t L = int64_t(blockIdx.y) * gridDim.x + blockIdx.x;
+    if (a.causal) {
+      const int64_t hg = ncta >= 128 ? 1 : 128 / ncta;
+      const int64_t group = L / (hg * ncta), base = group * hg * ncta;
+      const int64_t gs = a.BH - group * hg < hg ? a.BH - group * hg : hg;
+      rank = (L - base) / gs;
+      bh = group * hg + (L - base) % gs;
+    } else {
+      bh = L / ncta;
+      rank = L - bh * ncta;
+    }
+  }
   const int64_t q0 = (ncta - 1 - rank) * (2 * kBM);
-  const int64_t bh = a.causal ? blockIdx.x : blockIdx.y;
   // key tiles visited by query tile X: all, or (causal, bottom-right aligned) those that hold a
   // key <= the tile's last row + Sk - Sq; none for a tile past the end of the queries
   int nt[2];
@@ -536,10 +551,10 @@ cudaError_t launch_attention(const void* q, const void* k, const void* v, void* 
       !make_map(&tv, v, Sk, BH, kBN, f16) || !make_map(&to, o, Sq, BH, 32, f16))
     return cudaErrorInvalidValue;
   AttnArgs a{static_cast<const unsigned char*>(q), static_cast<const unsigned char*>(k),
-             static_cast<const unsigned char*>(v), static_cast<unsigned char*>(o), lse, Sq, Sk, scale * kLog2e,
+             static_cast<const unsigned char*>(v), static_cast<unsigned char*>(o), lse, BH, Sq, Sk, scale * kLog2e,
              causal ? 1 : 0, dev.status, local_wait_limit_ns()};
   const unsigned ncta = unsigned((Sq + 2 * kBM - 1) / (2 * kBM));
-  const dim3 grid = causal ? dim3(unsigned(BH), ncta) : dim3(ncta, unsigned(BH));
+  const dim3 grid(ncta, unsigned(BH));
   kern<<<grid, kThreads, kSmem, stream>>>(a, tq, tk, tv, to);
   return cudaGetLastError();
 }

@@ -102,7 +102,7 @@ def test_other_calls_argument_checks(lib):
     assert at(X, X, X, X, None, 65536, 16, 16, 128, 1.0, 0, 1, None) == rwo.ERR_UNSUPPORTED  # BH
     assert at(X, X, X, X, None, 1, 2**31, 16, 128, 1.0, 0, 1, None) == rwo.ERR_UNSUPPORTED  # 32-bit rows
     assert at(X, X, X, X, None, 1, 16, 2**31, 128, 1.0, 0, 1, None) == rwo.ERR_UNSUPPORTED
-    assert at(X, X, X, X, None, 1, 65536 * 256, 16, 128, 1.0, 1, 1, None) == rwo.ERR_UNSUPPORTED  # causal grid
+    assert at(X, X, X, X, None, 1, 2**31 - 255, 16, 128, 1.0, 1, 1, None) == rwo.ERR_UNSUPPORTED  # causal rows
     assert at(NULL, NULL, NULL, NULL, None, 1, 16, 16, 128, 1.0, 0, 1, None) == rwo.ERR_INVALID_ARG  # pointers
     assert at(NULL, NULL, NULL, NULL, None, 0, 16, 16, 128, 1.0, 0, 1, None) == rwo.OK  # BH = 0
 
