@@ -91,6 +91,24 @@ def test_attention_large_scores_and_scale():
     _check(to_host(o), lse.cpu().numpy(), q, k, v, [(h, i) for h in range(BH) for i in range(S)], True, 0.3, "sharp")
 
 
+@pytest.mark.parametrize("BH,S", [(70, 384), (3, 33000)])
+def test_attention_causal_cta_order(BH, S):
+    """Causal CTAs run in head groups of ~128 CTAs: a partial last group (70 heads of 2 pairs:
+    groups of 64) and one head per group (129 pairs of 256 rows); sampled rows against the oracle,
+    every row's LSE finite and every head's first and last rows included."""
+    d = 128
+    q, k, v = _qkv(BH, S, S, d, seed=BH * 3 + S)
+    lse = torch.full((BH, S), float("nan"), device="cuda")
+    o = rwo.attention_forward(to_device(q), to_device(k), to_device(v), lse_out=lse, causal=True)
+    assert rwo.get_status() == rwo.OK
+    lse_h = lse.cpu().numpy()
+    assert np.all(np.isfinite(lse_h)), "every row sees at least its own key"
+    rng = np.random.default_rng(BH + S)
+    rows = sorted({(h, i) for h in range(BH) for i in (0, S - 1)} |
+                  {(int(h), int(i)) for h, i in zip(rng.integers(0, BH, 96), rng.integers(0, S, 96))})
+    _check(to_host(o), lse_h, q, k, v, rows, True, 1.0 / np.sqrt(d), f"causal order {BH}x{S}")
+
+
 def test_attention_causal_workload_full_size():
     """4 x 32 heads, 4096 queries and keys, d = 128, causal: sampled rows against the oracle."""
     BH, S, d = 128, 4096, 128
