@@ -469,6 +469,7 @@ int softmax_rows_host(const void* x_host, void* y_host, int64_t M, int64_t N, in
       p.N = N;
       p.dtype = dtype;
       p.stream = user;
+      p.host_mem = true;
       const bool aligned = aligned16(dx) && aligned16(dy) && row_bytes % 16 == 0;
       if (oneread_reg_fits(p, aligned)) {
         cudaError_t err = launch_oneread_reg(p, aligned, *dev);

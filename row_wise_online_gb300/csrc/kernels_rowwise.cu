@@ -362,7 +362,10 @@ cudaError_t launch_oneread_reg(const RowProblem& p, bool vec, const DeviceInfo& 
   // hardware hands a finished SM the next CTA, which balances SMs that run at different speeds
   // (measured: 4096 x 4096 fp32 21.5 -> 20.9 us, 262144 x 256 fp32 93 -> 80 us against one
   // resident wave walking the rows).
-  const int64_t cap = int64_t(dev.sm_count) * blocks_per_sm((const void*)fn, kRegThreads, 0) * kGridWaves;
+  // Rows in host memory: one resident wave (measured on the host-link path: 254 GB/s against 247
+  // with 8 waves, whose extra CTAs only add requests in flight on an already saturated link).
+  const int64_t waves = p.host_mem ? 1 : kGridWaves;
+  const int64_t cap = int64_t(dev.sm_count) * blocks_per_sm((const void*)fn, kRegThreads, 0) * waves;
   const int grid = int(want < cap ? want : cap);
   fn<<<grid, kRegThreads, 0, p.stream>>>(row_args(p, dev));
   return cudaGetLastError();

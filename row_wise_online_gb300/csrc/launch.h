@@ -33,6 +33,7 @@ struct RowProblem {
   int64_t x_pitch = 0, y_pitch = 0;  // bytes between rows (0: N * element size); register, CTA
   float scale = 1.f;                 // bulk-copy and two-pass kernels: softmax of scale * x
   cudaStream_t stream = nullptr;
+  bool host_mem = false;  // x and y are page-locked host memory read and written over the host link
 };
 
 // Status bits a kernel may set in the per-device status word.
