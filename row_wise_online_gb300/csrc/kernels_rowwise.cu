@@ -6,8 +6,8 @@
 // max, forms e = 2^((x - m_t) log2 e) once per element and sums it: the thread's (m, d)
 // state.  States are merged across the warp by a butterfly and across the group's warps
 // through shared memory; then y = e * 2^((m_t - m) log2 e) / d is stored from the same
-// registers.  One exponential per element.  Persistent CTAs walk rows with a grid stride
-// (§7 of the same page).
+// registers.  One exponential per element.  Up to kGridWaves waves of CTAs take one row group
+// each; beyond that, CTAs walk rows with a grid stride (§7 of the same page).
 //
 // Two-pass ("5.2 ..." §2.2 and §5: the online recurrence with 128-bit loads).  A CTA owns a
 // row.  Pass 1 streams the row, four vectors per thread per step, folding each step into
