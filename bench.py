@@ -444,8 +444,11 @@ def bench_reference(args) -> dict | None:
 
 ATTN_WORKLOADS = {
     # name: (BH, S, d, causal) -- 4 x 32 heads of 4096 queries over 4096 keys, head dimension 128
+    # (and 4 x 64 heads of head dimension 64: the same bytes of q, k and v)
     "attn_bf16_4x32x4096x128_causal": (128, 4096, 128, True),
     "attn_bf16_4x32x4096x128": (128, 4096, 128, False),
+    "attn_bf16_4x64x4096x64_causal": (256, 4096, 64, True),
+    "attn_bf16_4x64x4096x64": (256, 4096, 64, False),
 }
 
 

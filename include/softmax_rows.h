@@ -192,7 +192,7 @@ int cross_entropy_rows(const void* x, const int64_t* labels, float* loss, float*
  *   scale   -- finite, > 0 (1/sqrt(d) in attention).
  *   causal  -- 1: query row i sees keys j <= i + Sk - Sq (the last query sees every key); 0: all.
  * A row that sees no key gets o = 0, LSE = -inf.  Supported: dtype SOFTMAX_BF16 or SOFTMAX_F16
- * with d = 128 (fp32 accumulation; P rounded to the element type for the P V product; fp16
+ * with d = 64 or 128 (fp32 accumulation; P rounded to the element type for the P V product; fp16
  * weights stay below 2^8, O below max |v|); other dtypes or head sizes return
  * SOFTMAX_ERR_UNSUPPORTED, as do BH > 65535 and Sq or Sk > 2^31 - 256.
  * Pointers 16-byte aligned (else SOFTMAX_ERR_MISALIGNED).

@@ -237,7 +237,7 @@ def softmax_rows_strided(x, y=None, m_out=None, d_out=None, lse_out=None, scale:
 
 def attention_forward(q, k, v, o=None, lse_out=None, scale: float | None = None, causal: bool = False, stream=None):
     """O = softmax(scale Q K^T) V for q [BH, Sq, d], k and v [BH, Sk, d] (contiguous CUDA tensors; bf16 or
-    fp16, d = 128).  scale defaults to 1/sqrt(d).  Returns o (and fills lse_out [BH, Sq] fp32 if given)."""
+    fp16, d = 64 or 128).  scale defaults to 1/sqrt(d).  Returns o (and fills lse_out [BH, Sq] fp32 if given)."""
     import torch
 
     for t, n in ((q, "q"), (k, "k"), (v, "v")):

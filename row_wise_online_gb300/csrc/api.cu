@@ -400,7 +400,7 @@ int attention_forward(const void* q, const void* k, const void* v, void* o, floa
   const DeviceInfo* dev = nullptr;
   int st = current_device_info(&dev);
   if (st != SOFTMAX_OK) return st;
-  cudaError_t err = launch_attention(q, k, v, o, lse_out, BH, Sq, Sk, scale, causal != 0, dtype,
+  cudaError_t err = launch_attention(q, k, v, o, lse_out, BH, Sq, Sk, d, scale, causal != 0, dtype,
                                      static_cast<cudaStream_t>(stream), *dev);
   if (err != cudaSuccess) return cuda_fail(err);
   return SOFTMAX_OK;

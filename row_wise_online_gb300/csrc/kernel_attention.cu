@@ -43,12 +43,10 @@ namespace {
 
 constexpr int kBM = 128;             // query rows per tile (two tiles per CTA)
 constexpr int kBN = 128;             // keys per tile
-constexpr int kD = 128;              // head dimension
-constexpr int kTile = kBN * kD * 2;  // bytes of a Q, K or V tile
 constexpr int kThreads = 10 * 32;    // 2 x 4 softmax warps, 1 loader warp, 1 MMA warp
 constexpr int kLoaderWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr uint32_t kTmemCols = 512;  // S_0 [0, 128), S_1 [128, 256), O_0 [256, 384), O_1 [384, 512)
+constexpr uint32_t kTmemCols = 512;  // S_0 [0, 128), S_1 [128, 256), O_0 [256, 256 + d), O_1 after it
 constexpr uint32_t kTmemO = 256;
 
 struct AttnArgs {
@@ -64,17 +62,22 @@ struct AttnArgs {
   uint64_t wait_ns;
 };
 
-// Shared memory (from a 1024-byte aligned base, as the 128-byte swizzle needs):
-// Q[2] | K[2] | V[2] | barriers, TMEM address | O staging, 4 KB per softmax warp (32 rows x 64
-// elements, the layout of a 128-byte-swizzled TMA box).
-constexpr int kOffQ = 0;
-constexpr int kOffK = 2 * kTile;
-constexpr int kOffV = 4 * kTile;
-constexpr int kOffBar = 6 * kTile;
+// Shared memory for head dimension DH (64 or 128), from a 1024-byte aligned base, as the 128-byte
+// swizzle needs: Q[2] | K[2] | V[2] | barriers, TMEM address | O staging, 4 KB per softmax warp
+// (32 rows x 64 elements, the layout of a 128-byte-swizzled TMA box).
 constexpr int kNumBars = 16;
-constexpr int kOffOStage = kOffBar + 1024;
 constexpr int kOStage = 32 * 128;
-constexpr int kSmem = kOffOStage + 8 * kOStage + 1024;  // + alignment slack
+template <int DH>
+struct Geo {
+  static_assert(DH == 64 || DH == 128, "head dimension 64 or 128");
+  static constexpr int kTile = kBN * DH * 2;  // bytes of a Q, K or V tile
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = 2 * kTile;
+  static constexpr int kOffV = 4 * kTile;
+  static constexpr int kOffBar = 6 * kTile;
+  static constexpr int kOffOStage = kOffBar + 1024;
+  static constexpr int kSmem = kOffOStage + 8 * kOStage + 1024;  // + alignment slack
+};
 static_assert(kNumBars * 8 + 4 <= 1024, "barriers overflow their slot");
 // barrier indices
 constexpr int kBarQFull = 0, kBarKFull = 1 /*2*/, kBarVFull = 3 /*2*/, kBarKFree = 5 /*2*/, kBarVFree = 7 /*2*/,
@@ -124,9 +127,9 @@ __device__ __forceinline__ void tma_store_wait_read() { asm volatile("cp.async.b
 __device__ __forceinline__ void fence_proxy_async_cta() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, A and B both bf16 (fmt 1) or both fp16
-// (fmt 0), A K-major, B K-major (b_mn = 0) or MN-major (b_mn = 1), N = 128, M = 128.
-__device__ __forceinline__ uint32_t idesc_f16kind(uint32_t fmt, uint32_t b_mn) {
-  return (1u << 4) | (fmt << 7) | (fmt << 10) | (b_mn << 16) | ((uint32_t(kBN) >> 3) << 17) | ((uint32_t(kBM) >> 4) << 24);
+// (fmt 0), A K-major, B K-major (b_mn = 0) or MN-major (b_mn = 1), N columns, M = 128.
+__device__ __forceinline__ uint32_t idesc_f16kind(uint32_t fmt, uint32_t b_mn, uint32_t n) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | (b_mn << 16) | ((n >> 3) << 17) | ((uint32_t(kBM) >> 4) << 24);
 }
 
 // Two fp32 values rounded to the element type (bf16 or fp16), low half first.
@@ -194,13 +197,16 @@ __device__ __forceinline__ void mask_keys(uint32_t (&sv)[64], int64_t key0, int6
 }
 
 // 320 threads, at most 168 registers a thread: three warps share a sub-partition's 16K registers.
-// H: fp16 elements (else bf16).
-template <bool H>
+// H: fp16 elements (else bf16); DH: head dimension (64 or 128).
+template <bool H, int DH>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attention_fwd(AttnArgs a, const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tout) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  using GM = Geo<DH>;
+  constexpr int kTile = GM::kTile, kOffQ = GM::kOffQ, kOffK = GM::kOffK, kOffV = GM::kOffV, kOffBar = GM::kOffBar,
+                kOffOStage = GM::kOffOStage, kD = DH;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + kNumBars * 8);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -310,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- MMA issuer: S_X(0); then per key tile j: P V_0(j), S_0(j+1), P V_1(j), S_1(j+1) ----
     if (lane == 0 && ntmax > 0) {
       const uint32_t fmt = H ? 0u : 1u;
-      const uint32_t idS = idesc_f16kind(fmt, 0), idPV = idesc_f16kind(fmt, 1);
+      const uint32_t idS = idesc_f16kind(fmt, 0, uint32_t(kBN)), idPV = idesc_f16kind(fmt, 1, uint32_t(kD));
       auto issue_s = [&](int x, int j) {  // S_x(j) = Q_x K_j^T into S_x; K_j has landed
         const uint32_t sq = smem_addr(smem + kOffQ + x * kTile), sk = smem_addr(smem + kOffK + (j & 1) * kTile);
 #pragma unroll
@@ -408,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S_x(j) landing means O_x holds P V_x(j - 1), and P V_x(j) waits for this P: rescale O now
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-        for (int h = 0; h < 4; ++h) {  // rare (the maximum moved): a quarter row at a time
+        for (int h = 0; h < kD / 32; ++h) {  // rare (the maximum moved): 32 columns at a time
           uint32_t ov[32];
           tmem_ld32_nowait(to + h * 32, ov);
           tmem_wait_ld();
@@ -457,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // c ^ (lane % 8)), one TMA store per 64 columns; rows past Sq are clipped by the copy
     unsigned char* stage = smem + kOffOStage + warp * kOStage;
 #pragma unroll 1
-    for (int hc = 0; hc < 2; ++hc) {
+    for (int hc = 0; hc < kD / 64; ++hc) {
 #pragma unroll 1
       for (int q2 = 0; q2 < 2; ++q2) {
         uint32_t ov[32];
@@ -499,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-bool attention_fits(int64_t d, int dtype) { return d == kD && (dtype == 1 || dtype == 2); }
+bool attention_fits(int64_t d, int dtype) { return (d == 64 || d == 128) && (dtype == 1 || dtype == 2); }
 
 namespace {
 
@@ -523,13 +529,13 @@ EncodeTiled encode_tiled() {
   return fn;
 }
 
-// [BH][S][128] bf16, boxes of 64 elements x `rows` rows x 1 head, 128-byte swizzle; rows past S
-// read as zeros (loads) or are not written (stores).
-bool make_map(CUtensorMap* m, const void* base, int64_t S, int64_t BH, uint32_t rows, bool f16) {
+// [BH][S][d] bf16 or fp16, boxes of 64 elements x `rows` rows x 1 head, 128-byte swizzle; rows
+// past S read as zeros (loads) or are not written (stores).
+bool make_map(CUtensorMap* m, const void* base, int64_t S, int64_t BH, int64_t d, uint32_t rows, bool f16) {
   EncodeTiled fn = encode_tiled();
   if (!fn) return false;
-  const cuuint64_t dims[3] = {cuuint64_t(kD), cuuint64_t(S), cuuint64_t(BH)};
-  const cuuint64_t strides[2] = {cuuint64_t(kD) * 2, cuuint64_t(S) * kD * 2};
+  const cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(S), cuuint64_t(BH)};
+  const cuuint64_t strides[2] = {cuuint64_t(d) * 2, cuuint64_t(S) * d * 2};
   const cuuint32_t box[3] = {64, rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
@@ -540,22 +546,25 @@ bool make_map(CUtensorMap* m, const void* base, int64_t S, int64_t BH, uint32_t 
 }  // namespace
 
 cudaError_t launch_attention(const void* q, const void* k, const void* v, void* o, float* lse, int64_t BH, int64_t Sq,
-                             int64_t Sk, float scale, bool causal, int dtype, cudaStream_t stream,
+                             int64_t Sk, int64_t d, float scale, bool causal, int dtype, cudaStream_t stream,
                              const DeviceInfo& dev) {
   const bool f16 = dtype == 2;
-  auto* kern = f16 ? k_attention_fwd<true> : k_attention_fwd<false>;
-  cudaError_t err = cudaFuncSetAttribute((const void*)kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  using Kern = void (*)(AttnArgs, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap);
+  Kern kern = d == 64 ? (f16 ? (Kern)k_attention_fwd<true, 64> : (Kern)k_attention_fwd<false, 64>)
+                      : (f16 ? (Kern)k_attention_fwd<true, 128> : (Kern)k_attention_fwd<false, 128>);
+  const int smem = d == 64 ? Geo<64>::kSmem : Geo<128>::kSmem;
+  cudaError_t err = cudaFuncSetAttribute((const void*)kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   alignas(64) CUtensorMap tq, tk, tv, to;
-  if (!make_map(&tq, q, Sq, BH, kBM, f16) || !make_map(&tk, k, Sk, BH, kBN, f16) ||
-      !make_map(&tv, v, Sk, BH, kBN, f16) || !make_map(&to, o, Sq, BH, 32, f16))
+  if (!make_map(&tq, q, Sq, BH, d, kBM, f16) || !make_map(&tk, k, Sk, BH, d, kBN, f16) ||
+      !make_map(&tv, v, Sk, BH, d, kBN, f16) || !make_map(&to, o, Sq, BH, d, 32, f16))
     return cudaErrorInvalidValue;
   AttnArgs a{static_cast<const unsigned char*>(q), static_cast<const unsigned char*>(k),
              static_cast<const unsigned char*>(v), static_cast<unsigned char*>(o), lse, BH, Sq, Sk, scale * kLog2e,
              causal ? 1 : 0, dev.status, local_wait_limit_ns()};
   const unsigned ncta = unsigned((Sq + 2 * kBM - 1) / (2 * kBM));
   const dim3 grid(ncta, unsigned(BH));
-  kern<<<grid, kThreads, kSmem, stream>>>(a, tq, tk, tv, to);
+  kern<<<grid, kThreads, smem, stream>>>(a, tq, tk, tv, to);
   return cudaGetLastError();
 }
 

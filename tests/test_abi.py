@@ -94,7 +94,7 @@ def test_other_calls_argument_checks(lib):
     assert st(X, 2**62, X, 4, None, None, None, 4, 4, 0, 1.0, 0, 0, None) == rwo.ERR_INVALID_ARG  # overflow
     assert st(NULL, 0, NULL, 0, None, None, None, 0, 4, 0, 1.0, 0, 0, None) == rwo.OK  # M = 0
     at = lib.attention_forward  # (q, k, v, o, lse, BH, Sq, Sk, d, scale, causal, dtype, stream)
-    assert at(X, X, X, X, None, 1, 16, 16, 64, 1.0, 0, 1, None) == rwo.ERR_UNSUPPORTED  # d = 64
+    assert at(X, X, X, X, None, 1, 16, 16, 96, 1.0, 0, 1, None) == rwo.ERR_UNSUPPORTED  # d = 96
     assert at(X, X, X, X, None, 1, 16, 16, 128, 1.0, 0, 0, None) == rwo.ERR_UNSUPPORTED  # fp32
     assert at(X, X, X, X, None, 1, 16, 16, 128, 0.0, 0, 1, None) == rwo.ERR_INVALID_ARG  # scale
     assert at(X, X, X, X, None, 1, 16, 16, 128, 1.0, 2, 1, None) == rwo.ERR_INVALID_ARG  # causal flag

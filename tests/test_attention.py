@@ -81,6 +81,21 @@ def test_attention_f16_against_oracle(BH, Sq, Sk, causal):
            f"attn fp16 {BH}x{Sq}x{Sk} causal={causal}", dtype=synth.F16)
 
 
+@pytest.mark.parametrize("dtype", [synth.BF16, synth.F16])
+@pytest.mark.parametrize("BH,Sq,Sk", [(2, 300, 300), (1, 77, 1000), (2, 256, 384), (2, 1000, 77), (3, 1, 1)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_attention_d64_against_oracle(dtype, BH, Sq, Sk, causal):
+    d = 64
+    q, k, v = _qkv(BH, Sq, Sk, d, seed=Sq * 3 + Sk + d, dtype=dtype)
+    lse = torch.full((BH, Sq), float("nan"), device="cuda")
+    qd, kd, vd = (to_device(t, dtype) for t in (q, k, v))
+    o = rwo.attention_forward(qd, kd, vd, lse_out=lse, causal=causal)
+    assert rwo.get_status() == rwo.OK
+    rows = [(h, i) for h in range(BH) for i in range(Sq)]
+    _check(to_host(o), lse.cpu().numpy(), q, k, v, rows, causal, 1.0 / np.sqrt(d),
+           f"attn d=64 {BH}x{Sq}x{Sk} causal={causal}", dtype=dtype)
+
+
 def test_attention_large_scores_and_scale():
     """Scores spread over hundreds (sharp rows) with a non-default scale."""
     BH, S, d = 2, 384, 128
@@ -123,9 +138,9 @@ def test_attention_causal_workload_full_size():
 
 
 def test_attention_unsupported_and_errors():
-    q = torch.zeros((1, 16, 64), dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros((1, 16, 96), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(rwo.SoftmaxError) as ei:
-        rwo.attention_forward(q, q, q)  # d = 64
+        rwo.attention_forward(q, q, q)  # d = 96
     assert ei.value.status == rwo.ERR_UNSUPPORTED
     q = torch.zeros((1, 16, 128), dtype=torch.float32, device="cuda")
     with pytest.raises(rwo.SoftmaxError) as ei:
