@@ -284,12 +284,15 @@ int softmax_last_variant(void);
  * softmax_debug_set_fault -- test hook.  fault = 1 makes the next
  * split-row launches skip one cluster's state publication, so every other
  * cluster's bounded wait runs out and the kernel records SOFTMAX_ERR_TIMEOUT
- * instead of hanging; fault = 0 restores normal behaviour.  Returns the
- * previous value.  Process-wide; not for production use.
+ * instead of hanging; fault = 2 makes the next attention_forward launches skip
+ * the copy of the first V tile, with the same outcome (the output is then
+ * undefined); fault = 0 restores normal behaviour.  Returns the previous
+ * value.  Process-wide; not for production use.
  */
 int softmax_debug_set_fault(int fault);
 
-/* The wait limit of the split-row exchange, in nanoseconds (default 200 ms).  Returns the old value. */
+/* The wait limit of the split-row exchange and of every wait in attention_forward, in nanoseconds
+ * (default 200 ms).  Returns the old value. */
 int64_t softmax_debug_set_wait_limit_ns(int64_t ns);
 
 #ifdef __cplusplus

@@ -212,7 +212,12 @@ uint64_t exchange_wait_limit_ns() {
 
 int debug_fault() {
   std::lock_guard<std::mutex> lock(g_debug_mutex);
-  return g_debug_fault;
+  return g_debug_fault == 1 ? 1 : 0;
+}
+
+int debug_fault_attention() {
+  std::lock_guard<std::mutex> lock(g_debug_mutex);
+  return g_debug_fault == 2 ? 1 : 0;
 }
 
 }  // namespace rwo

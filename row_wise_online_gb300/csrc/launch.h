@@ -45,7 +45,8 @@ inline int elem_bytes(int dtype) { return dtype == 0 ? 4 : 2; }
 // Host-side wait limits handed to kernels (nanoseconds).
 uint64_t local_wait_limit_ns();     // waits on this CTA's own copies and threads
 uint64_t exchange_wait_limit_ns();  // waits on other clusters (split row)
-int debug_fault();                  // test hook value (split row)
+int debug_fault();                  // test hook (split row): 1 = cluster 0 never publishes
+int debug_fault_attention();        // test hook (attention): 1 = the first V tile is never copied
 
 // Each `*_fits` says whether the variant can take the problem (alignment already checked by
 // the caller where the variant needs it).  Each `launch_*` enqueues the work and returns a

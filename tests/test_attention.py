@@ -137,6 +137,28 @@ def test_attention_causal_workload_full_size():
     _check(to_host(o), lse.cpu().numpy(), q, k, v, rows, True, 1.0 / np.sqrt(d), "causal 128x4096")
 
 
+def test_attention_wait_runs_out_and_reports_timeout():
+    """A V tile that is never copied: every wait on it runs out (bounded), the kernel terminates
+    with SOFTMAX_ERR_TIMEOUT, and the next launch is correct."""
+    BH, S, d = 1, 256, 128
+    q, k, v = _qkv(BH, S, S, d, seed=3)
+    qd, kd, vd = to_device(q), to_device(k), to_device(v)
+    assert rwo.get_status() == rwo.OK
+    old_limit = rwo.debug_set_wait_limit_ns(5_000_000)  # 5 ms
+    old_fault = rwo.debug_set_fault(2)
+    try:
+        rwo.attention_forward(qd, kd, vd)
+        assert rwo.get_status() == rwo.ERR_TIMEOUT
+    finally:
+        rwo.debug_set_fault(old_fault)
+        rwo.debug_set_wait_limit_ns(old_limit)
+    assert rwo.get_status() == rwo.OK
+    lse = torch.empty((BH, S), device="cuda")
+    o = rwo.attention_forward(qd, kd, vd, lse_out=lse)
+    assert rwo.get_status() == rwo.OK
+    _check(to_host(o), lse.cpu().numpy(), q, k, v, [(0, i) for i in range(S)], False, 1.0 / np.sqrt(d), "after timeout")
+
+
 def test_attention_unsupported_and_errors():
     q = torch.zeros((1, 16, 96), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(rwo.SoftmaxError) as ei:
