@@ -93,15 +93,41 @@ def measured_hbm_peak() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def code_only(text: str) -> str:
+    """C++ / CUDA source without its comments (string and character literals kept), blank lines
+    and runs of white space (one space between tokens): what a change of comments or layout
+    leaves unchanged."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(" ".join(line.split()) for line in "".join(out).splitlines() if line.strip())
+
+
 def kernel_source_hash(files=None) -> str:
-    """Hash of the named files of row_wise_online_gb300/csrc (all of them when files is None)."""
+    """Hash of the code (comments excluded) of the named files of row_wise_online_gb300/csrc (all
+    of them when files is None)."""
     csrc = os.path.join(ROOT, "row_wise_online_gb300", "csrc")
     paths = sorted(glob.glob(os.path.join(csrc, "*"))) if files is None else [os.path.join(csrc, f) for f in sorted(files)]
     h = hashlib.sha256()
     for p in paths:
-        with open(p, "rb") as fh:
+        with open(p, encoding="utf-8") as fh:
             h.update(os.path.basename(p).encode())
-            h.update(fh.read())
+            h.update(code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -8,14 +8,16 @@
 // leaves the chip.  One CTA owns two tiles of 128 query rows (X = 0, 1) of one head, which take
 // turns on the tensor cores: while one tile's softmax runs, the other tile's products run.
 //
+//  Elements are bf16 or fp16, the head dimension d is 64 or 128.
 //  * one producer lane streams Q once and K, V tiles of 128 keys through two shared-memory
-//    stages with TMA (cp.async.bulk.tensor, two boxes of 64 elements x 128 rows per tile with the
-//    128-byte swizzle, zero fill past the sequence end), which lands them directly in the tensor
+//    stages with TMA (cp.async.bulk.tensor, d / 64 boxes of 64 elements x 128 rows per tile with
+//    the 128-byte swizzle, zero fill past the sequence end), which lands them directly in the tensor
 //    cores' 128-byte-swizzled canonical layouts (Q and K: K-major; V: MN-major, so it needs no
 //    transpose); K_j and V_j are issued as soon as their stage is free, each on its own barrier.
 //    Rows of 128 bytes per request keep the copy engine and L2 efficient (boxes 16 bytes wide
 //    cost one request per 16 bytes and starved the tensor cores);
-//  * one thread issues tcgen05.mma (bf16 x bf16 -> fp32, M = N = 128, K = 16 per instruction) in
+//  * one thread issues tcgen05.mma (16-bit operands -> fp32, K = 16 per instruction; S: M = N =
+//    128; P V: M = 128, N = d) in
 //    the order P V_0(j), S_0(j+1), P V_1(j), S_1(j+1): S_X = Q_X K^T into TMEM region S_X, and
 //    O_X += P_X V with P_X read from TMEM (A operand in tensor memory); completion is signalled
 //    with tcgen05.commit, which covers every earlier product of the thread -- so S_X(j+1) landing
@@ -24,10 +26,11 @@
 //    tile it loads its row of S from TMEM, takes the running maximum m (in log2 units of
 //    scale * s; moved only when a tile exceeds it by more than 2^8, so O and l are rarely
 //    rescaled), rescales its row of O in TMEM by 2^(m_old - m_new) when m moved, and writes
-//    P = 2^(s - m) as packed bf16 over the first 64 columns of its S region, which the P V
+//    P = 2^(s - m) as packed 16-bit values over the first 64 columns of its S region, which the P V
 //    product reads.  Masked keys (causal rule, the ragged end of the keys) give P = 0; key tiles
 //    wholly above a query tile's causal diagonal are not visited;
-//  * epilogue: O / l as bf16 and LSE = m + ln l per row.
+//  * epilogue: O / l rounded to the element type, through a per-warp staging buffer and TMA
+//    stores, and LSE = m + ln l per row.
 // Every wait is bounded (%globaltimer); a wait that runs out sets the status word and the
 // kernel still terminates.
 #include <cuda.h>
