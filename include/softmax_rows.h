@@ -74,9 +74,9 @@ enum softmax_variant {
   /* One read: the row is loaded once into registers with 128-bit loads (rows up to 32 KiB). */
   SOFTMAX_VARIANT_ONEREAD_REG = 1,
   /* One read: bulk copies (cp.async.bulk + mbarrier) stage whole rows in shared memory.  Rows
-     up to 16 KiB: each warp owns a row at a time and a private ring of row slots that its lane 0
-     refills; rows up to 64 KiB: a producer warp feeds a CTA-wide consumer group that copies the
-     row to registers and frees the slot at once. */
+     up to 8 KiB: each warp owns a row at a time and a private ring of row slots that its lane 0
+     refills; longer rows (up to 64 KiB): a producer warp feeds a CTA-wide consumer group that
+     copies the row to registers and frees the slot at once. */
   SOFTMAX_VARIANT_ONEREAD_SMEM = 2,
   /* Two passes over global memory: online fold with 128-bit loads, then re-read and normalise
      (any N; the re-read is served from L2 while the row is still resident). */
