@@ -79,14 +79,18 @@ enum softmax_variant {
      copies the row to registers and frees the slot at once. */
   SOFTMAX_VARIANT_ONEREAD_SMEM = 2,
   /* Two passes over global memory: online fold with 128-bit loads, then re-read and normalise
-     (any N; the re-read is served from L2 while the row is still resident). */
+     (any N; the re-read is served from L2 while the row is still resident).  Aligned rows above
+     256 KiB are shared by a thread-block cluster (2-16 CTAs, states merged over distributed
+     shared memory), so that the rows in flight stay within L2. */
   SOFTMAX_VARIANT_TWOPASS = 3,
   /* Split row: one row is spread over every CTA of the grid; CTAs of a thread-block cluster merge
      (m, d) over distributed shared memory, clusters exchange 8-byte states through global memory
-     (for few, very long rows, 16-byte aligned).  Each CTA holds its segment of the row waiting
-     for its exchange in registers (up to 112 KiB fp32 / 84 KiB bf16 per SM, so rows up to about
-     that times the SM count) while it folds the next row from shared memory.  It needs every
-     cluster resident at once, so it must not share the GPU with other kernels. */
+     (16-byte aligned rows of any length above about 150 KiB).  Every CTA streams its segment
+     twice through a ring of shared-memory slots: the fold, then the normalisation, whose
+     re-read is served from L2 while the next rows fold.  AUTO takes it for rows above 64 KiB
+     when there are at most half as many rows as SMs, and for rows of 8 MiB and more at any
+     row count.  It needs every cluster resident at once, so it must not share the GPU with
+     other kernels (softmax_rows_host never uses it). */
   SOFTMAX_VARIANT_SPLITROW = 4
 };
 

@@ -122,6 +122,17 @@ int validate_rows(const void* x, int64_t M, int64_t N, int dtype, bool* noop) {
   return SOFTMAX_OK;
 }
 
+// Rows above this length take the two passes with a cluster per row: a CTA per row (one per SM)
+// would keep more than ~40 MB of rows in flight, and the second read would start to leave L2
+// (measured at 256 KiB rows: bf16 5.27 TB/s with a CTA per row against 4.46 with clusters of 2).
+constexpr int64_t kClusterRowMinBytes = int64_t(256) << 10;
+
+cudaError_t launch_twopass_any(const RowProblem& p, bool aligned, const DeviceInfo& dev) {
+  if (aligned && p.N * elem_bytes(p.dtype) > kClusterRowMinBytes && clusterrow_fits(p, dev))
+    return launch_clusterrow(p, dev);
+  return launch_twopass(p, aligned, dev);
+}
+
 int run_variant(RowProblem& p, int variant, const DeviceInfo& dev) {
   const bool aligned = aligned16(p.x) && (p.y == nullptr || aligned16(p.y)) &&
                        (p.N * elem_bytes(p.dtype)) % 16 == 0;
@@ -138,7 +149,11 @@ int run_variant(RowProblem& p, int variant, const DeviceInfo& dev) {
         variant = SOFTMAX_VARIANT_ONEREAD_REG;
       else if (oneread_tma_fits(p, dev))
         variant = SOFTMAX_VARIANT_ONEREAD_SMEM;
-      else if (p.M * 2 <= dev.sm_count && splitrow_fits(p, dev))
+      else if (!p.shares_gpu && (p.M * 2 <= dev.sm_count || row_bytes >= (int64_t(8) << 20)) &&
+               splitrow_fits(p, dev))
+        // few long rows, or rows of 8 MiB and more at any count: a CTA per row would keep more
+        // rows in flight than L2 holds, and the two-pass re-read would come from HBM (measured:
+        // 152 x 16 MiB fp32 865 us split against 1150 us two-pass, 300 x 8 MiB 1064 against 1132)
         variant = SOFTMAX_VARIANT_SPLITROW;
       else
         variant = SOFTMAX_VARIANT_TWOPASS;
@@ -168,7 +183,7 @@ int run_variant(RowProblem& p, int variant, const DeviceInfo& dev) {
         return SOFTMAX_ERR_UNSUPPORTED;
       break;
     case SOFTMAX_VARIANT_TWOPASS:
-      err = launch_twopass(p, aligned, dev);
+      err = launch_twopass_any(p, aligned, dev);
       break;
     case SOFTMAX_VARIANT_SPLITROW:
       if (!aligned) return SOFTMAX_ERR_MISALIGNED;
@@ -353,7 +368,7 @@ int softmax_rows_strided(const void* x, int64_t ldx, void* y, int64_t ldy, float
       err = launch_oneread_tma(p, *dev);
       break;
     case SOFTMAX_VARIANT_TWOPASS:
-      err = launch_twopass(p, aligned, *dev);
+      err = launch_twopass_any(p, aligned, *dev);
       break;
     default:  // SOFTMAX_VARIANT_SPLITROW
       return SOFTMAX_ERR_UNSUPPORTED;
@@ -532,6 +547,7 @@ int softmax_rows_host(const void* x_host, void* y_host, int64_t M, int64_t N, in
     p.N = N;
     p.dtype = dtype;
     p.stream = hp.lanes[li];
+    p.shares_gpu = true;  // the lanes' kernels overlap: none may need the whole GPU resident
     if ((st = run_variant(p, SOFTMAX_VARIANT_AUTO, *dev)) != SOFTMAX_OK) {
       result = st;
       break;

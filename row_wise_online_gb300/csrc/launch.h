@@ -26,7 +26,7 @@ struct RowProblem {
   float* lse_out = nullptr;
   int64_t M = 0;
   int64_t N = 0;
-  int dtype = 0;  // 0 = fp32, 1 = bf16
+  int dtype = 0;  // 0 = fp32, 1 = bf16, 2 = fp16
   bool log_out = false;  // y = log-softmax instead of softmax (register, CTA bulk-copy, two-pass)
   const int64_t* labels = nullptr;  // cross entropy (two-pass, no y): loss[r] = LSE_r - x_r[labels[r]]
   float* loss = nullptr;
@@ -34,6 +34,7 @@ struct RowProblem {
   float scale = 1.f;                 // bulk-copy and two-pass kernels: softmax of scale * x
   cudaStream_t stream = nullptr;
   bool host_mem = false;  // x and y are page-locked host memory read and written over the host link
+  bool shares_gpu = false;  // other kernels may run beside this launch (the split-row kernel is then off)
 };
 
 // Status bits a kernel may set in the per-device status word.
@@ -46,7 +47,7 @@ inline int elem_bytes(int dtype) { return dtype == 0 ? 4 : 2; }
 uint64_t local_wait_limit_ns();     // waits on this CTA's own copies and threads
 uint64_t exchange_wait_limit_ns();  // waits on other clusters (split row)
 int debug_fault();                  // test hook (split row): 1 = cluster 0 never publishes
-int debug_fault_attention();        // test hook (attention): 1 = the first V tile is never copied
+int debug_fault_attention();        // test hook (attention): 2 = the first V tile is never copied
 
 // Each `*_fits` says whether the variant can take the problem (alignment already checked by
 // the caller where the variant needs it).  Each `launch_*` enqueues the work and returns a
@@ -68,6 +69,12 @@ cudaError_t launch_oneread_tma(const RowProblem& p, const DeviceInfo& dev);
 // q_period >= 1 applies the causal rule above; 0 processes whole rows.
 cudaError_t launch_twopass(const RowProblem& p, bool vec, const DeviceInfo& dev, int64_t q_period = 0,
                            int64_t key_offset = 0);
+
+// Two passes with a thread-block cluster per row (16-byte aligned rows and pitches, y written,
+// no cross entropy); for long rows at many rows, where a CTA per row would keep more rows in
+// flight than L2 holds.
+bool clusterrow_fits(const RowProblem& p, const DeviceInfo& dev);
+cudaError_t launch_clusterrow(const RowProblem& p, const DeviceInfo& dev);
 
 bool splitrow_fits(const RowProblem& p, const DeviceInfo& dev);
 cudaError_t launch_splitrow(const RowProblem& p, const DeviceInfo& dev);

@@ -5,7 +5,7 @@ tests and benchmark, and the fp64 oracle, read the same bytes.  It holds no
 softmax arithmetic -- only a counter-based random source (splitmix64), value
 distributions and structural edits, all in ``synth.c``.
 
-The five workloads follow the shapes of the pages' problem ("5.2 CUDA Online
+The workloads follow the shapes of the pages' problem ("5.2 CUDA Online
 Softmax 实现优化" §2.4 measures M = N = 4096 in fp32) and of the logits /
 attention-score uses they describe:
 
@@ -20,6 +20,8 @@ fp32_longrow_32x4194304        32x4Mi     fp32, x ~ U[-20, 20), seed 3; each row
                                           last quarter at a hashed column
 bf16_causal_4x32x4096x4096     524288x4k  bf16, x = bf16(z / sqrt(128)), z ~ N(0, 1), seed 4; row r is query
                                           q = r % 4096 and keys j > q are -inf
+fp32_rows_600x262144           600x256Ki  fp32, x = 3 * N(0, 1), seed 5 (many 1 MiB rows: more than L2
+                                          holds at a row per SM; not one of the pages' shapes)
 =============================  =========  =========================================================
 
 Every value depends only on (seed, global row, column), so any row range can
@@ -128,6 +130,7 @@ WORKLOADS = {
         Workload("fp32_longrow_32x4194304", F32, 32, 4194304, 3, UNIFORM, -20.0, 20.0, late_max=20.0),
         Workload("bf16_causal_4x32x4096x4096", BF16, 4 * 32 * 4096, 4096, 4, NORMAL, 0.0, 1.0 / np.sqrt(128.0),
                  causal_q=4096),
+        Workload("fp32_rows_600x262144", F32, 600, 262144, 5, NORMAL, 0.0, 3.0),
     )
 }
 

@@ -175,6 +175,20 @@ def test_host_buffers_staged_pipeline():
     check_y(yt.numpy().view(np.uint16), y_ref, w.dtype, "host pipeline, long rows")
 
 
+def test_host_buffers_staged_very_long_rows():
+    """Rows of 1 MiB through the staging lanes, whose kernels overlap: AUTO must not take the
+    split-row kernel (it needs the whole GPU resident) and the result still matches."""
+    w = synth.custom("host-vlong", synth.F32, 20, 1 << 18, seed=13, p1=3.0)
+    x_host = synth.generate(w)
+    xt = torch.from_numpy(x_host)
+    yt = torch.empty_like(xt)
+    rwo.softmax_rows_host(xt, yt)
+    assert rwo.get_status() == rwo.OK
+    assert rwo.last_variant() == rwo.VARIANT_TWOPASS
+    y_ref, *_ = oracle.softmax_rows(x_host)
+    check_y(yt.numpy(), y_ref, w.dtype, "host pipeline, 1 MiB rows")
+
+
 def test_host_buffers_pipeline():
     w = synth.custom("host", synth.F32, 5000, 4096, seed=10, p1=3.0)
     x_host = synth.generate(w)

@@ -78,6 +78,30 @@ def test_auto_takes_splitrow_for_few_long_rows():
     assert rwo.last_variant() == rwo.VARIANT_SPLITROW
 
 
+def test_auto_takes_splitrow_for_many_rows_of_8mib():
+    """Rows of 8 MiB and more go to the split kernel at any row count (here 100 rows, more than
+    half the SMs); 4 MiB rows at the same count stay with the two-pass kernel.  Sampled rows
+    against the oracle, every row's sum."""
+    M, N = 100, 1 << 21
+    w = synth.custom("split-many", synth.F32, M, N, seed=41, p1=3.0)
+    x_host = synth.generate(w)
+    x = to_device(x_host)
+    y, m, d, lse = run_softmax(x, rwo.VARIANT_AUTO)
+    assert rwo.last_variant() == rwo.VARIANT_SPLITROW
+    yh = to_host(y)
+    check_rowsums(yh, synth.F32, None, "split 100 x 8 MiB")
+    pick = [0, 37, 76, 77, 99]
+    y_ref, m_ref, d_ref, lse_ref = oracle.softmax_rows(x_host[pick])
+    check_y(yh[pick], y_ref, synth.F32, "split 100 x 8 MiB (sampled rows)")
+    check_state(m.cpu().numpy()[pick], d.cpu().numpy()[pick], lse.cpu().numpy()[pick], m_ref, d_ref, lse_ref,
+                "split 100 x 8 MiB (sampled rows)")
+    del x, y
+    x = to_device(x_host[:, : N // 2].copy())
+    rwo.softmax_rows(x)
+    torch.cuda.synchronize()
+    assert rwo.last_variant() == rwo.VARIANT_TWOPASS
+
+
 def test_exchange_wait_runs_out_and_reports_timeout():
     w = synth.custom("fault", synth.F32, 3, 1 << 21, seed=1, p1=2.0)
     x_host = synth.generate(w)
