@@ -25,6 +25,8 @@
 // The clusters walk the rows with a stride of the cluster count.  A cluster barrier is a
 // hardware barrier over CTAs that are co-scheduled by construction (a cluster launches whole),
 // so it needs no time limit.
+#include <mutex>
+
 #include "device_common.cuh"
 #include "launch.h"
 
@@ -211,21 +213,45 @@ int max_active_clusters(ClusterRowKernel fn, int cs) {
   return n;
 }
 
+constexpr int kCrSizes[4] = {2, 4, 8, 16};
+
+// Resident clusters of each size, per device and kernel: queried once (the occupancy queries
+// cost far more than a launch).
+struct ResidentClusters {
+  int n[4] = {0, 0, 0, 0};
+};
+std::mutex g_cr_mutex;
+ResidentClusters g_cr[64][3][2];
+bool g_cr_ready[64][3][2];
+
+ResidentClusters resident_clusters(int dtype, bool log, const DeviceInfo& dev) {
+  std::lock_guard<std::mutex> lock(g_cr_mutex);
+  const bool cache = dev.device >= 0 && dev.device < 64;
+  if (cache && g_cr_ready[dev.device][dtype][log]) return g_cr[dev.device][dtype][log];
+  ResidentClusters r;
+  ClusterRowKernel fn = clusterrow_kernel(dtype, log);
+  if (cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+    cudaGetLastError();  // clusters of 16 then report no residency
+  for (int i = 0; i < 4; ++i) r.n[i] = max_active_clusters(fn, kCrSizes[i]);
+  if (cache) {
+    g_cr[dev.device][dtype][log] = r;
+    g_cr_ready[dev.device][dtype][log] = true;
+  }
+  return r;
+}
+
 // The smallest cluster (2 .. 16 CTAs) whose resident clusters keep at most kCrInflightBytes of
 // rows in flight; the largest one when none does.
 ClusterRowPlan plan_clusterrow(const RowProblem& p, const DeviceInfo& dev) {
   ClusterRowPlan plan;
   if (!dev.cluster_launch) return plan;
-  ClusterRowKernel fn = clusterrow_kernel(p.dtype, p.log_out);
-  if (cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-    cudaGetLastError();
+  const ResidentClusters r = resident_clusters(p.dtype, p.log_out, dev);
   const int64_t row_bytes = p.N * elem_bytes(p.dtype);
-  for (int cs : {2, 4, 8, 16}) {
-    const int n = max_active_clusters(fn, cs);
-    if (n < 1) continue;
-    plan.cluster = cs;
-    plan.clusters = n;
-    if (int64_t(n) * row_bytes <= kCrInflightBytes) break;
+  for (int i = 0; i < 4; ++i) {
+    if (r.n[i] < 1) continue;
+    plan.cluster = kCrSizes[i];
+    plan.clusters = r.n[i];
+    if (int64_t(r.n[i]) * row_bytes <= kCrInflightBytes) break;
   }
   return plan;
 }
