@@ -412,12 +412,11 @@ def bench_ours(args) -> dict | None:
 # the oracle (CPU) arms
 # ----------------------------------------------------------------------------------------------
 
-def cpu_baseline(w: synth.Workload, target_s: float = 1.5) -> dict:
-    """The fp64 oracle as it stands, on the host cores, on a bounded sample of the workload:
-    as many whole passes over (up to) the full matrix as fit in about `target_s` seconds."""
+def _oracle_rate(w: synth.Workload, threads: int, target_s: float):
+    """Whole passes of the fp64 oracle over (up to) the full matrix for about `target_s` seconds
+    on `threads` host threads: (GB/s on the read-once + write-once basis, passes, rows, seconds)."""
     import oracle
 
-    threads = oracle.default_threads()
     probe = synth.generate(w, row0=0, nrows=min(w.M, 4 * threads))
     t0 = time.perf_counter()
     oracle.softmax_rows(probe, nthreads=threads)
@@ -430,11 +429,26 @@ def cpu_baseline(w: synth.Workload, target_s: float = 1.5) -> dict:
         oracle.softmax_rows(x, nthreads=threads)
         reps += 1
         t = time.perf_counter() - t0
-    gbs = 2 * nrows * w.N * w.elem_bytes * reps / t / 1e9
-    return {"value": round(gbs, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{reps} pass(es) over rows 0..{nrows - 1} of {w.name} ({nrows} x {w.N}), fp64 three-pass, "
-                      f"{t:.2f} s wall on {threads} threads (~{t * threads:.0f} CPU-s)",
-            "rows_per_s": round(nrows * reps / t, 1)}
+    return 2 * nrows * w.N * w.elem_bytes * reps / t / 1e9, reps, nrows, t
+
+
+def cpu_baseline(w: synth.Workload, target_s: float = 1.5) -> dict:
+    """The fp64 oracle as it stands, on the host cores, on a bounded sample of the workload:
+    as many whole passes over (up to) the full matrix as fit in about `target_s` seconds.  For
+    the two fp32 workloads of 64 x 1024 and 4096 x 4096 also on one thread."""
+    import oracle
+
+    threads = oracle.default_threads()
+    gbs, reps, nrows, t = _oracle_rate(w, threads, target_s)
+    out = {"value": round(gbs, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
+           "sample": f"{reps} pass(es) over rows 0..{nrows - 1} of {w.name} ({nrows} x {w.N}), fp64 three-pass, "
+                     f"{t:.2f} s wall on {threads} threads (~{t * threads:.0f} CPU-s)",
+           "rows_per_s": round(nrows * reps / t, 1)}
+    if w.name in ("fp32_64x1024", "fp32_4096x4096"):
+        gbs1, reps1, nrows1, t1 = _oracle_rate(w, 1, target_s / 2)
+        out["single_thread"] = {"value": round(gbs1, 3), "unit": "GB/s", "cores": 1,
+                                "sample": f"{reps1} pass(es) over rows 0..{nrows1 - 1}, {t1:.2f} s wall"}
+    return out
 
 
 def bench_reference(args) -> dict | None:
