@@ -283,30 +283,34 @@ def bench_ours(args) -> dict | None:
         with torch.cuda.stream(stream):
             graphs[0][0].replay()  # untimed: page in the graph
         stream.synchronize()
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        # one event before the first replay and one after each: the whole span is the measurement,
+        # the spans of single replays give the median and best time per step
+        batches = [graphs[0]] * full + ([graphs[-1]] if rest else [])
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(batches) + 1)]
         sampler = ClockSampler(dev.index) if clocks else None
         if sampler:
             time.sleep(0.3)
         barrier(world)
         torch.cuda.synchronize(dev)
         with torch.cuda.stream(stream):
-            ev0.record(stream)
-            for _ in range(full):
-                graphs[0][0].replay()
-            if rest:
-                graphs[-1][0].replay()
-            ev1.record(stream)
+            evs[0].record(stream)
+            for i, (g, _) in enumerate(batches):
+                g.replay()
+                evs[i + 1].record(stream)
         stream.synchronize()
         torch.cuda.synchronize(dev)
         barrier(world)
         clk = sampler.stop() if sampler else None
-        ms = ev0.elapsed_time(ev1)
+        ms = evs[0].elapsed_time(evs[-1])
+        per_step = sorted(evs[i].elapsed_time(evs[i + 1]) / n for i, (_, n) in enumerate(batches))
+        spread = {"median": round(per_step[len(per_step) // 2] * 1e3, 3), "best": round(per_step[0] * 1e3, 3),
+                  "replays": len(per_step), "steps_per_replay": batches[0][1]}
         status = rwo.get_status(stream)
         if status != rwo.OK:
             raise rwo.SoftmaxError(status, "kernel status after timing")
-        return ms, used, clk
+        return ms, used, clk, spread
 
-    ms_local, used, clk = measure(variant, args.steps, args.warmup, clocks=True)
+    ms_local, used, clk, spread = measure(variant, args.steps, args.warmup, clocks=True)
     ms = reduce_max(ms_local, world)
     per_step_ms = ms / args.steps
     bytes_step = w.min_bytes
@@ -324,7 +328,7 @@ def bench_ours(args) -> dict | None:
                 continue
             try:
                 k = max(8, args.steps // 8)
-                vms, _, _ = measure(var, k, 3)
+                vms, _, _, _ = measure(var, k, 3)
                 variants[name] = {"gbs": round(bytes_step * k / (vms * 1e-3) / 1e9, 1),
                                   "us_per_step": round(vms * 1e3 / k, 2)}
             except rwo.SoftmaxError as e:
@@ -375,6 +379,7 @@ def bench_ours(args) -> dict | None:
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(per_step_ms, 6),
+        "step_us": spread,  # this rank's median and best µs per step over single graph replays
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": round(gbs / world / PAGE_GBS[w.name], 3) if w.name in PAGE_GBS else None,
