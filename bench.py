@@ -359,8 +359,8 @@ def bench_ours(args) -> dict | None:
               rwo.VARIANT_TWOPASS: "k_twopass", rwo.VARIANT_SPLITROW: "k_splitrow"}[used]
     if used == rwo.VARIANT_ONEREAD_SMEM and w.N * w.elem_bytes <= 16384 and not log_mode:
         kernel = "k_causal_warp" if causal else "k_oneread_warp"  # rows up to 16 KiB: one warp per row
-    if used == rwo.VARIANT_TWOPASS and w.N * w.elem_bytes > (256 << 10) and not ce_mode and not causal:
-        kernel = "k_clusterrow"  # aligned rows above 256 KiB: two passes with a cluster per row
+    if used == rwo.VARIANT_TWOPASS and w.N * w.elem_bytes > (64 << 10) and not ce_mode and not causal:
+        kernel = "k_clusterrow"  # aligned rows above 64 KiB: the cluster-row kernel's two passes
     # profile summaries are per kernel, output mode and workload
     profile_key = kernel + ("-log" if log_mode else "-ce" if ce_mode else "")
     alg_bytes = bytes_step

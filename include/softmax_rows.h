@@ -80,8 +80,9 @@ enum softmax_variant {
   SOFTMAX_VARIANT_ONEREAD_SMEM = 2,
   /* Two passes over global memory: online fold with 128-bit loads, then re-read and normalise
      (any N; the re-read is served from L2 while the row is still resident).  Aligned rows above
-     256 KiB are shared by a thread-block cluster (2-16 CTAs, states merged over distributed
-     shared memory), so that the rows in flight stay within L2. */
+     64 KiB run on the cluster-row kernel: rows of ~260 KiB and more are shared by a thread-block
+     cluster (2-16 CTAs, states merged over distributed shared memory), so that the rows in
+     flight stay within L2. */
   SOFTMAX_VARIANT_TWOPASS = 3,
   /* Split row: one row is spread over every CTA of the grid; CTAs of a thread-block cluster merge
      (m, d) over distributed shared memory, clusters exchange 8-byte states through global memory

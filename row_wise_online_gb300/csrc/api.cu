@@ -122,10 +122,10 @@ int validate_rows(const void* x, int64_t M, int64_t N, int dtype, bool* noop) {
   return SOFTMAX_OK;
 }
 
-// Rows above this length take the two passes with a cluster per row: a CTA per row (one per SM)
-// would keep more than ~40 MB of rows in flight, and the second read would start to leave L2
-// (measured at 256 KiB rows: bf16 5.27 TB/s with a CTA per row against 4.46 with clusters of 2).
-constexpr int64_t kClusterRowMinBytes = int64_t(256) << 10;
+// Aligned rows above this length take the cluster-row kernel for the two passes (clusters of one
+// CTA up to ~260 KiB rows, larger ones beyond, so that the rows in flight stay within L2); the
+// two-pass kernel keeps shorter and unaligned rows, whose thread count it sizes to the row.
+constexpr int64_t kClusterRowMinBytes = int64_t(64) << 10;
 
 cudaError_t launch_twopass_any(const RowProblem& p, bool aligned, const DeviceInfo& dev) {
   if (aligned && p.N * elem_bytes(p.dtype) > kClusterRowMinBytes && clusterrow_fits(p, dev))

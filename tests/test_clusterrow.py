@@ -1,4 +1,4 @@
-"""Two passes with a thread-block cluster per row (rows above 256 KiB, aligned): every CTA of the
+"""The cluster-row two-pass kernel (aligned rows above 64 KiB; clusters of several CTAs from ~260 KiB): every CTA of the
 cluster folds its segment of the row, the CTA states are merged over distributed shared memory,
 and every CTA normalises its segment.  Against the fp64 oracle; the variant is TWOPASS (forced or
 chosen by AUTO for many long rows)."""
@@ -25,6 +25,9 @@ def _built():
 
 
 @pytest.mark.parametrize("dtype,M,N", [
+    (synth.F32, 300, 40_000),      # 160 KB rows: clusters of one CTA (AUTO too: no one-read kernel holds them)
+    (synth.BF16, 500, 90_000),     # 180 KB rows
+    (synth.F16, 257, 40_008),      # 80 KB rows: AUTO takes a one-read kernel, TWOPASS the cluster-row kernel
     (synth.F32, 200, 80_000),      # 320 KB rows: clusters of 2
     (synth.F32, 90, 262_148),      # ~1 MiB rows, the units do not split evenly over the cluster
     (synth.BF16, 120, 1_000_008),  # ~2 MB rows
