@@ -147,6 +147,11 @@ int run_variant(RowProblem& p, int variant, const DeviceInfo& dev) {
         variant = SOFTMAX_VARIANT_ONEREAD_SMEM;
       else if (row_bytes <= 16384 && oneread_reg_fits(p, true))
         variant = SOFTMAX_VARIANT_ONEREAD_REG;
+      else if (p.dtype == SOFTMAX_F32 && row_bytes > 53248 && row_bytes <= 65536)
+        // fp32 rows of 52-64 KiB: two passes beat the CTA bulk-copy kernel (measured, ~640 MB per
+        // launch: 56 KiB 5.83 against 5.77 TB/s, 60 KiB 6.04 against 5.78, 64 KiB 6.18 against
+        // 5.82; 16-bit rows stay far faster with one read: fp16 64 KiB 6.68 against 5.34)
+        variant = SOFTMAX_VARIANT_TWOPASS;
       else if (oneread_tma_fits(p, dev))
         variant = SOFTMAX_VARIANT_ONEREAD_SMEM;
       else if (!p.shares_gpu && (p.M * 2 <= dev.sm_count || row_bytes >= (int64_t(8) << 20)) &&

@@ -175,6 +175,20 @@ def test_host_buffers_staged_pipeline():
     check_y(yt.numpy().view(np.uint16), y_ref, w.dtype, "host pipeline, long rows")
 
 
+@pytest.mark.parametrize("dtype,N,want", [
+    (synth.F32, 12288, V.VARIANT_ONEREAD_SMEM),   # 48 KiB rows: one read
+    (synth.F32, 16384, V.VARIANT_TWOPASS),        # 64 KiB fp32 rows: two passes measured faster
+    (synth.BF16, 32768, V.VARIANT_ONEREAD_SMEM),  # 64 KiB 16-bit rows: one read
+])
+def test_auto_choice_around_64kib(dtype, N, want):
+    w = synth.custom("auto64", dtype, 300, N, seed=N % 101, p1=3.0)
+    x_host = synth.generate(w)
+    y, *_ = run_softmax(to_device(x_host), V.VARIANT_AUTO, state=False)
+    assert rwo.last_variant() == want
+    y_ref, *_ = oracle.softmax_rows(x_host)
+    check_y(to_host(y), y_ref, dtype, f"auto {N}")
+
+
 def test_host_buffers_staged_very_long_rows():
     """Rows of 1 MiB through the staging lanes, whose kernels overlap: AUTO must not take the
     split-row kernel (it needs the whole GPU resident) and the result still matches."""
