@@ -3,9 +3,15 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
 A step is one softmax over the whole workload matrix (every kernel the path launches for it).
-The default workload is fp32 4096 x 4096 (x = 3 N(0,1), seed 1), the shape measured on
-"5.2 CUDA Online Softmax 实现优化" §2.4.  Inputs are synthetic (synth/) and already resident in
-HBM when timing starts.
+The default headline workload is the largest of the problem statement that fits one GPU: bf16
+attention-score-shaped rows, 4 x 32 heads x 4096 queries = 524,288 rows over 4096 keys, scores
+z / sqrt(128) with z ~ N(0, 1) (seed 4), keys after the query set to -inf in the matrix, every
+entry read.  By default (one GPU) the line also carries, under "configs", the other workloads
+of 4096 x 4096 and larger, each timed over the same K steps: fp32 4096 x 4096 (the shape
+measured on "5.2 CUDA Online Softmax 实现优化" §2.4; AUTO, the one-read shared-memory and the
+two-pass kernels), bf16 16384 x 32768 logits with per-row LSE, fp32 32 x 4,194,304 long rows,
+and the causal workload through softmax_rows_causal (masked keys not read).  Inputs are
+synthetic (synth/) and already resident in HBM when timing starts.
 
 Metric: effective HBM GB/s with minimum bytes = read x once + write y once (2 M N s), plus
 rows/s and the fraction of the HBM roofline.  L2: steps rotate over enough input/output buffer
@@ -40,7 +46,7 @@ import numpy as np  # noqa: E402
 import synth  # noqa: E402
 
 METRIC = "softmax effective HBM GB/s (read+write once) and % of GB300 HBM peak, rows/s"
-DEFAULT_WORKLOAD = "fp32_4096x4096"
+DEFAULT_WORKLOAD = "bf16_causal_4x32x4096x4096"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES_NOMINAL = 126 * 2 ** 20
@@ -220,6 +226,191 @@ def _graph_time(run_step, nsteps: int, stream, graph_batch: int):
     return graphs, full, rest
 
 
+# The configurations timed by default, in the order they run.  The first is the headline: the
+# largest workload of the problem statement (bf16 attention-score-shaped rows, 524,288 x 4096,
+# causal -inf written into the matrix, every entry read).  The others are the remaining
+# workloads of 4096 x 4096 and larger, with the variants the statement asks to measure.
+#   (label, workload, mode, forced variant or None, state outputs)
+SUITE = (
+    ("bf16_causal_4x32x4096x4096", "bf16_causal_4x32x4096x4096", "softmax", None, ""),
+    ("fp32_4096x4096", "fp32_4096x4096", "softmax", None, ""),
+    ("fp32_4096x4096/oneread_smem", "fp32_4096x4096", "softmax", "smem", ""),
+    ("fp32_4096x4096/twopass", "fp32_4096x4096", "softmax", "twopass", ""),
+    ("bf16_logits_16384x32768+lse", "bf16_logits_16384x32768", "softmax", None, "lse"),
+    ("fp32_longrow_32x4194304", "fp32_longrow_32x4194304", "softmax", None, ""),
+    ("bf16_causal_4x32x4096x4096/causal_skip", "bf16_causal_4x32x4096x4096", "causal", None, ""),
+)
+
+VARIANT_ARG = {"auto": 0, "reg": 1, "smem": 2, "twopass": 3, "splitrow": 4, "splitrow_stream": 5}
+
+
+class _Run:
+    """One workload's buffers on this rank's device, and the step that softmaxes it."""
+
+    def __init__(self, w: synth.Workload, row0: int, dev, stream, mode: str, state: str, host_x=None):
+        import torch
+
+        import row_wise_online_gb300 as rwo
+
+        self.w, self.mode, self.stream, self.rwo = w, mode, stream, rwo
+        if host_x is None:
+            host_x = _pinned_workload(w, row0)
+        self.host_x = host_x
+        set_bytes = 2 * w.M * w.N * w.elem_bytes
+        # rotate over enough buffer sets that a step's operands were evicted from L2 since last use
+        self.nbuf = 1 if set_bytes >= 4 * L2_BYTES_NOMINAL else max(2, -(-4 * L2_BYTES_NOMINAL // set_bytes))
+        self.set_bytes = set_bytes
+        self.xs = [host_x.to(dev) for _ in range(self.nbuf)]
+        self.ys = [torch.empty_like(self.xs[0]) for _ in range(self.nbuf)]
+        self.lse = torch.empty(w.M, dtype=torch.float32, device=dev) if "lse" in state else None
+        if mode == "ce":  # synthetic labels, uniform over the classes
+            self.labels = torch.from_numpy(np.random.default_rng(5).integers(0, w.N, w.M)).to(dev)
+            self.loss = torch.empty(w.M, dtype=torch.float32, device=dev)
+        self.variant = rwo.VARIANT_AUTO
+
+    def step(self, i: int) -> None:
+        rwo, w, k = self.rwo, self.w, i % self.nbuf
+        if self.mode == "causal":  # masked keys are not read: the causal rule replaces the -inf entries
+            rwo.softmax_rows_causal(self.xs[k], w.causal_q, 0, self.ys[k], lse_out=self.lse, stream=self.stream)
+        elif self.mode == "log":
+            rwo.log_softmax_rows(self.xs[k], self.ys[k], lse_out=self.lse, stream=self.stream)
+        elif self.mode == "ce":
+            rwo.cross_entropy_rows(self.xs[k], self.labels, self.loss, stream=self.stream)
+        else:
+            rwo.softmax_rows_ex(self.xs[k], self.ys[k], lse_out=self.lse, variant=self.variant, stream=self.stream)
+
+    def bytes_per_step(self) -> int:
+        """The metric's bytes: read x once + write y once (x + labels + losses for cross entropy)."""
+        w = self.w
+        if self.mode == "ce":
+            return w.M * w.N * w.elem_bytes + 12 * w.M
+        return w.min_bytes
+
+    def algorithmic_bytes(self, row0: int) -> int:
+        """Bytes the launch must move: the metric's bytes, or for the causal skip the live prefix of
+        every row (whole 16-byte vectors) plus all of y; state outputs add 4 bytes per row each."""
+        w = self.w
+        b = self.bytes_per_step()
+        if self.mode == "causal":
+            vec = 16 // w.elem_bytes
+            r = np.arange(row0, row0 + w.M, dtype=np.int64)
+            live = np.clip(r % w.causal_q + 1, 0, w.N)
+            b = int(((live + vec - 1) // vec).sum()) * 16 + w.M * w.N * w.elem_bytes
+        if self.lse is not None:
+            b += 4 * w.M
+        return b
+
+    def release(self) -> None:
+        self.xs = self.ys = None
+
+
+def _time_steps(run: _Run, nsteps: int, warm: int, world: int, dev) -> tuple[float, dict]:
+    """Time exactly nsteps steps of `run` between CUDA events on its stream; returns (ms, spread).
+
+    Warm-up steps run eagerly; the steps are then captured in CUDA graphs of up to 256 steps (a
+    multiple of the buffer rotation).  After the barrier and synchronisation that open the timed
+    region, one untimed replay is issued right before the first event, so the GPU is busy and at
+    its working clock when the first timed step starts (no idle gap, no launch latency inside).
+    """
+    import torch
+
+    stream = run.stream
+    with torch.cuda.stream(stream):
+        for i in range(warm):
+            run.step(i)
+    graph_batch = max(run.nbuf, min(nsteps, 256) // run.nbuf * run.nbuf)
+    graphs, full, rest = _graph_time(run.step, nsteps, stream, graph_batch)
+    with torch.cuda.stream(stream):
+        graphs[0][0].replay()  # page the graph in
+    stream.synchronize()
+    batches = [graphs[0]] * full + ([graphs[-1]] if rest else [])
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(batches) + 1)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        graphs[0][0].replay()  # untimed, immediately before the timed region
+        evs[0].record(stream)
+        for i, (g, _) in enumerate(batches):
+            g.replay()
+            evs[i + 1].record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    ms = evs[0].elapsed_time(evs[-1])
+    per_step = sorted(evs[i].elapsed_time(evs[i + 1]) / n for i, (_, n) in enumerate(batches))
+    spread = {"median": round(per_step[len(per_step) // 2] * 1e3, 3), "best": round(per_step[0] * 1e3, 3),
+              "replays": len(per_step), "steps_per_replay": batches[0][1]}
+    status = run.rwo.get_status(stream)
+    if status != run.rwo.OK:
+        raise run.rwo.SoftmaxError(status, "kernel status after timing")
+    return ms, spread
+
+
+def _kernel_name(rwo, used: int, w: synth.Workload, mode: str) -> str:
+    """The kernel a step of this workload launches (as the library's variant choice makes it)."""
+    row_bytes = w.N * w.elem_bytes
+    if mode == "causal":
+        return "k_causal_warp" if row_bytes <= 16384 else "k_twopass"
+    if used == rwo.VARIANT_ONEREAD_REG:
+        return "k_oneread_reg"
+    if used == rwo.VARIANT_ONEREAD_SMEM:
+        return "k_oneread_warp" if row_bytes <= 8192 and mode == "softmax" else "k_oneread_tma"
+    if used == rwo.VARIANT_SPLITROW:
+        return "k_splitrow_onchip"
+    if used == rwo.VARIANT_SPLITROW_STREAM:
+        return "k_splitrow"
+    if used == rwo.VARIANT_TWOPASS and row_bytes > (64 << 10) and mode != "ce":
+        return "k_clusterrow"
+    return "k_twopass"
+
+
+def measure_config(label: str, w: synth.Workload, mode: str, forced: str | None, state: str, args, world: int,
+                   rank: int, dev, stream, peak: float, host_x=None) -> tuple[dict, "_Run"]:
+    """Time one configuration over exactly --steps steps; returns its record and the run."""
+    import row_wise_online_gb300 as rwo
+
+    row0 = shard_row0(rank, w.M)
+    run = _Run(w, row0, dev, stream, mode, state, host_x=host_x)
+    run.variant = VARIANT_ARG[forced] if forced else rwo.VARIANT_AUTO
+    try:
+        run.step(0)
+    except rwo.SoftmaxError as e:
+        run.release()
+        return {"label": label, "workload": w.name, "unsupported": str(e)}, run
+    used = rwo.last_variant()
+    ms_local, spread = _time_steps(run, args.steps, args.warmup, world, dev)
+    ms = reduce_max(ms_local, world)
+    per_step_ms = ms / args.steps
+    bytes_step = run.bytes_per_step()
+    gbs = world * bytes_step * args.steps / (ms * 1e-3) / 1e9
+    kernel = _kernel_name(rwo, used, w, mode)
+    profile_key = kernel + ("-log" if mode == "log" else "-ce" if mode == "ce" else "")
+    alg = run.algorithmic_bytes(row0)
+    achieved = alg / (per_step_ms * 1e-3) / 1e9
+    variant_name = rwo.VARIANT_NAMES[used] + {"causal": "+causal_skip", "log": "+log_softmax",
+                                              "ce": "+cross_entropy"}.get(mode, "")
+    rec = {
+        "label": label, "workload": w.name, "M": w.M, "N": w.N,
+        "dtype": "f32" if w.dtype == synth.F32 else "bf16",
+        "variant": variant_name + ("" if not forced else " (forced)"),
+        "kernel": kernel,
+        "state_outputs": state or None,
+        "gbs": round(gbs, 1),
+        "us_per_step": round(per_step_ms * 1e3, 3),
+        "step_us": spread,
+        "rows_per_s": round(world * w.M * args.steps / (ms * 1e-3), 1),
+        "pct_of_8tbs": round(100 * gbs / world / NOMINAL_HBM_GBS, 2),
+        "frac": round(achieved / peak, 4),
+        "achieved_gbs": round(achieved, 1),
+        "algorithmic_bytes_per_launch": alg,
+        "traffic": profiled_traffic(profile_key, w.name),
+        "l2": (f"{run.nbuf} rotating x/y buffer sets ({run.nbuf * run.set_bytes >> 20} MiB > L2)" if run.nbuf > 1
+               else "inputs larger than L2"),
+        "steps": args.steps,
+    }
+    return rec, run
+
+
 def bench_ours(args) -> dict | None:
     import torch
 
@@ -238,105 +429,31 @@ def bench_ours(args) -> dict | None:
         _build.build()
     barrier(world)
     dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.Stream(device=dev)
+    peak, peak_kind = measured_hbm_peak()
 
     w = synth.WORKLOADS[args.workload]
     if args.rows:
         w = w.with_rows(args.rows)
-    row0 = shard_row0(rank, w.M)
-    host_x = _pinned_workload(w, row0)
-    set_bytes = 2 * w.M * w.N * w.elem_bytes
-    nbuf = 1 if set_bytes >= 4 * L2_BYTES_NOMINAL else max(2, -(-4 * L2_BYTES_NOMINAL // set_bytes))
-    xs = [host_x.to(dev) for _ in range(nbuf)]
-    ys = [torch.empty_like(xs[0]) for _ in range(nbuf)]
-    stream = torch.cuda.Stream(device=dev)
-    causal = args.variant == "causal"
-    if causal and not w.causal_q:
+    mode = {"causal": "causal", "log": "log", "ce": "ce"}.get(args.variant, "softmax")
+    if mode == "causal" and not w.causal_q:
         raise SystemExit("--variant causal needs a workload with a causal mask")
-    log_mode = args.variant == "log"
-    ce_mode = args.variant == "ce"
-    special = causal or log_mode or ce_mode  # another entry point than softmax_rows_ex
-    if ce_mode:  # synthetic labels, uniform over the classes
-        labels = torch.from_numpy(np.random.default_rng(5).integers(0, w.N, w.M)).to(dev)
-        loss = torch.empty(w.M, dtype=torch.float32, device=dev)
-    variant = {"auto": rwo.VARIANT_AUTO, "reg": rwo.VARIANT_ONEREAD_REG, "smem": rwo.VARIANT_ONEREAD_SMEM,
-               "twopass": rwo.VARIANT_TWOPASS, "splitrow": rwo.VARIANT_SPLITROW,
-               "causal": rwo.VARIANT_AUTO, "log": rwo.VARIANT_AUTO, "ce": rwo.VARIANT_AUTO}[args.variant]
+    forced = args.variant if args.variant in VARIANT_ARG and args.variant != "auto" else None
+    state = "lse" if args.workload == "bf16_logits_16384x32768" and mode == "softmax" else ""
 
-    def measure(var: int, nsteps: int, warm: int, clocks: bool = False):
-        def step(i):
-            if causal:  # masked keys are not read: the causal rule replaces the -inf entries
-                rwo.softmax_rows_causal(xs[i % nbuf], w.causal_q, 0, ys[i % nbuf], stream=stream)
-            elif log_mode:
-                rwo.log_softmax_rows(xs[i % nbuf], ys[i % nbuf], stream=stream)
-            elif ce_mode:
-                rwo.cross_entropy_rows(xs[i % nbuf], labels, loss, stream=stream)
-            else:
-                rwo.softmax_rows_ex(xs[i % nbuf], ys[i % nbuf], variant=var, stream=stream)
-
-        with torch.cuda.stream(stream):
-            for i in range(warm):
-                step(i)
-        stream.synchronize()
-        used = rwo.last_variant()
-        graph_batch = max(nbuf, min(nsteps, 256) // nbuf * nbuf)
-        graphs, full, rest = _graph_time(step, nsteps, stream, graph_batch)
-        with torch.cuda.stream(stream):
-            graphs[0][0].replay()  # untimed: page in the graph
-        stream.synchronize()
-        # one event before the first replay and one after each: the whole span is the measurement,
-        # the spans of single replays give the median and best time per step
-        batches = [graphs[0]] * full + ([graphs[-1]] if rest else [])
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(batches) + 1)]
-        sampler = ClockSampler(dev.index) if clocks else None
-        if sampler:
-            time.sleep(0.3)
-        barrier(world)
-        torch.cuda.synchronize(dev)
-        with torch.cuda.stream(stream):
-            evs[0].record(stream)
-            for i, (g, _) in enumerate(batches):
-                g.replay()
-                evs[i + 1].record(stream)
-        stream.synchronize()
-        torch.cuda.synchronize(dev)
-        barrier(world)
-        clk = sampler.stop() if sampler else None
-        ms = evs[0].elapsed_time(evs[-1])
-        per_step = sorted(evs[i].elapsed_time(evs[i + 1]) / n for i, (_, n) in enumerate(batches))
-        spread = {"median": round(per_step[len(per_step) // 2] * 1e3, 3), "best": round(per_step[0] * 1e3, 3),
-                  "replays": len(per_step), "steps_per_replay": batches[0][1]}
-        status = rwo.get_status(stream)
-        if status != rwo.OK:
-            raise rwo.SoftmaxError(status, "kernel status after timing")
-        return ms, used, clk, spread
-
-    ms_local, used, clk, spread = measure(variant, args.steps, args.warmup, clocks=True)
-    ms = reduce_max(ms_local, world)
-    per_step_ms = ms / args.steps
-    bytes_step = w.min_bytes
-    if ce_mode:  # x read once, labels read, losses written: no y
-        bytes_step = w.M * w.N * w.elem_bytes + 12 * w.M
-    gbs = world * bytes_step * args.steps / (ms * 1e-3) / 1e9
-    rows_s = world * w.M * args.steps / (ms * 1e-3)
-
-    # Other variants on the same workload (fewer steps), for the record.
-    variants = {}
-    if world == 1 and not args.quick and not special:
-        for name, var in (("oneread_reg", rwo.VARIANT_ONEREAD_REG), ("oneread_smem", rwo.VARIANT_ONEREAD_SMEM),
-                          ("twopass", rwo.VARIANT_TWOPASS), ("splitrow", rwo.VARIANT_SPLITROW)):
-            if var == used:
-                continue
-            try:
-                k = max(8, args.steps // 8)
-                vms, _, _, _ = measure(var, k, 3)
-                variants[name] = {"gbs": round(bytes_step * k / (vms * 1e-3) / 1e9, 1),
-                                  "us_per_step": round(vms * 1e3 / k, 2)}
-            except rwo.SoftmaxError as e:
-                variants[name] = {"unsupported": str(e)}
+    # nvidia-smi samples over every timed region of this run (started before the first warm-up)
+    sampler = ClockSampler(dev.index)
+    rec, run = measure_config(args.workload, w, mode, forced, state, args, world, rank, dev, stream, peak)
+    if "unsupported" in rec:
+        sampler.stop()
+        raise SystemExit(f"{args.workload}: {rec['unsupported']}")
 
     # End to end through the public host-buffer call: H2D of x, kernels, D2H of y, every step.
     e2e = None
-    if not args.no_e2e and not special:
+    if not args.no_e2e and mode == "softmax":
+        host_x = run.host_x
+        run.release()
+        torch.cuda.empty_cache()
         y_host = torch.empty_like(host_x).pin_memory()
         for _ in range(2):
             rwo.softmax_rows_host(host_x, y_host)
@@ -348,70 +465,67 @@ def bench_ours(args) -> dict | None:
             rwo.softmax_rows_host(host_x, y_host)
         torch.cuda.synchronize(dev)
         t = reduce_max(time.perf_counter() - t0, world)
-        e2e = {"value": round(world * bytes_step * k / t / 1e9, 2), "unit": "GB/s",
+        e2e = {"value": round(world * w.min_bytes * k / t / 1e9, 2), "unit": "GB/s",
                "h2d_bytes_per_step": w.M * w.N * w.elem_bytes, "d2h_bytes_per_step": w.M * w.N * w.elem_bytes,
-               "steps": k, "ms_per_step": round(t * 1e3 / k, 4)}
+               "steps": k, "ms_per_step": round(t * 1e3 / k, 4), "call": "softmax_rows_host (pinned host buffers)"}
+        del y_host
+    run.release()
+    del run
+    torch.cuda.empty_cache()
+
+    # The other configurations, each over exactly --steps steps (one GPU; --quick skips them).
+    configs = []
+    if world == 1 and not args.quick and args.workload == DEFAULT_WORKLOAD and not args.rows and args.variant == "auto":
+        for label, wname, cmode, cforced, cstate in SUITE[1:]:
+            cw = synth.WORKLOADS[wname]
+            crec, crun = measure_config(label, cw, cmode, cforced, cstate, args, world, rank, dev, stream, peak)
+            crun.release()
+            del crun
+            torch.cuda.empty_cache()
+            configs.append(crec)
+    clk = sampler.stop()
 
     if rank != 0:
         return None
-    peak, peak_kind = measured_hbm_peak()
-    kernel = {rwo.VARIANT_ONEREAD_REG: "k_oneread_reg", rwo.VARIANT_ONEREAD_SMEM: "k_oneread_tma",
-              rwo.VARIANT_TWOPASS: "k_twopass", rwo.VARIANT_SPLITROW: "k_splitrow"}[used]
-    if used == rwo.VARIANT_ONEREAD_SMEM and w.N * w.elem_bytes <= 16384 and not log_mode:
-        kernel = "k_causal_warp" if causal else "k_oneread_warp"  # rows up to 16 KiB: one warp per row
-    if used == rwo.VARIANT_TWOPASS and w.N * w.elem_bytes > (64 << 10) and not ce_mode and not causal:
-        kernel = "k_clusterrow"  # aligned rows above 64 KiB: the cluster-row kernel's two passes
-    # profile summaries are per kernel, output mode and workload
-    profile_key = kernel + ("-log" if log_mode else "-ce" if ce_mode else "")
-    alg_bytes = bytes_step
-    if causal:  # bytes the kernel needs: the live prefix of every row (whole 16-byte vectors) + all of y
-        vec = 16 // w.elem_bytes
-        r = np.arange(row0, row0 + w.M, dtype=np.int64)
-        live = np.clip(r % w.causal_q + 1, 0, w.N)
-        alg_bytes = int(((live + vec - 1) // vec).sum()) * 16 + w.M * w.N * w.elem_bytes
-    achieved = alg_bytes / (per_step_ms * 1e-3) / 1e9
-    traffic = profiled_traffic(profile_key, w.name)
     result = {
         "metric": METRIC,
-        "value": round(gbs, 1),
+        "value": round(rec["gbs"], 1),
         "unit": "GB/s",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(per_step_ms, 6),
-        "step_us": spread,  # this rank's median and best µs per step over single graph replays
+        "ms_per_step": round(rec["us_per_step"] / 1e3, 6),
+        "step_us": rec["step_us"],  # this rank's median and best µs per step over single graph replays
         "higher_is_better": True,
         "scaling": "weak",
-        "vs_baseline": round(gbs / world / PAGE_GBS[w.name], 3) if w.name in PAGE_GBS else None,
+        "vs_baseline": round(rec["gbs"] / world / PAGE_GBS[w.name], 3) if w.name in PAGE_GBS else None,
         "vs_baseline_ref": ("pages' V3 register one-pass kernel, ~1672 GB/s on A100 80GB SXM4 "
                             "(another machine: context, not the target)") if w.name in PAGE_GBS else None,
-        "dtype": "f32" if w.dtype == synth.F32 else "bf16",
+        "dtype": rec["dtype"],
         "data": "synthetic",
         "config": {"workload": w.name if not args.rows else f"{w.name}[rows={w.M}]", "M": w.M, "N": w.N,
-                   "rows_total": w.M * world,
-                   "variant": rwo.VARIANT_NAMES[used] + ("+causal_skip" if causal else "+log_softmax" if log_mode
-                                                         else "+cross_entropy" if ce_mode else ""),
-                   "parallelism": f"rows sharded over {world} GPU(s)",
-                   "l2": (f"{nbuf} rotating x/y buffer sets ({nbuf * set_bytes >> 20} MiB > L2)" if nbuf > 1
-                          else "inputs larger than L2"),
-                   "timing": "CUDA graph replays between CUDA events on the launching stream"},
-        "rows_per_s": round(rows_s, 1),
-        "pct_of_8tbs": round(100 * gbs / world / NOMINAL_HBM_GBS, 2),
-        "pct_of_measured_peak": round(100 * gbs / world / peak, 2),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                   "rows_total": w.M * world, "variant": rec["variant"], "state_outputs": rec["state_outputs"],
+                   "parallelism": f"rows sharded over {world} GPU(s)", "l2": rec["l2"],
+                   "timing": ("CUDA graph replays between CUDA events on the launching stream, an untimed "
+                              "replay issued right before the first event")},
+        "rows_per_s": rec["rows_per_s"],
+        "pct_of_8tbs": rec["pct_of_8tbs"],
+        "pct_of_measured_peak": round(100 * rec["gbs"] / world / peak, 2),
+        "roofline": {"bound": "hbm", "achieved": rec["achieved_gbs"], "peak": peak, "unit": "GB/s",
+                     "frac": rec["frac"], "traffic": rec["traffic"],
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-                     else "fallback 6.8 TB/s", "kernel": kernel,
-                     "algorithmic_bytes_per_launch": alg_bytes},
+                     else "fallback 6.8 TB/s", "kernel": rec["kernel"],
+                     "algorithmic_bytes_per_launch": rec["algorithmic_bytes_per_launch"]},
         "gpu_launches": args.steps,
         "e2e": e2e,
         "clocks": clk,
-        "variants": variants,
+        "configs": configs,
     }
+    if configs:
+        result["gpu_launches_all_configs"] = args.steps * (1 + sum(1 for c in configs if "gbs" in c))
     if world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w)
     return result
-
 
 # ----------------------------------------------------------------------------------------------
 # the oracle (CPU) arms
@@ -538,6 +652,7 @@ def bench_attention(args) -> dict | None:
     def step(i):
         rwo.attention_forward(q, k, v, o, lse, causal=causal, stream=stream)
 
+    sampler = ClockSampler(dev.index)  # nvidia-smi samples from before the warm-up to the end
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
             step(i)
@@ -546,12 +661,11 @@ def bench_attention(args) -> dict | None:
     with torch.cuda.stream(stream):
         graphs[0][0].replay()
     stream.synchronize()
-    sampler = ClockSampler(dev.index)
-    time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize(dev)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
+        graphs[0][0].replay()  # untimed, immediately before the timed region
         ev0.record(stream)
         for _ in range(full):
             graphs[0][0].replay()
@@ -559,6 +673,7 @@ def bench_attention(args) -> dict | None:
             graphs[-1][0].replay()
         ev1.record(stream)
     stream.synchronize()
+    torch.cuda.synchronize(dev)
     barrier(world)
     clk = sampler.stop()
     status = rwo.get_status(stream)
@@ -596,7 +711,7 @@ def main(argv=None) -> int:
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS) + sorted(ATTN_WORKLOADS))
     ap.add_argument("--variant", default="auto",
-                    choices=["auto", "reg", "smem", "twopass", "splitrow", "causal", "log", "ce"],
+                    choices=["auto", "reg", "smem", "twopass", "splitrow", "splitrow_stream", "causal", "log", "ce"],
                     help="causal: softmax_rows_causal on a causal workload (masked keys not read); "
                          "log: log_softmax_rows; ce: cross_entropy_rows with uniform synthetic labels")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
