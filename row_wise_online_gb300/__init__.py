@@ -17,17 +17,18 @@ import os
 
 __all__ = [
     "F32", "BF16", "VARIANT_AUTO", "VARIANT_ONEREAD_REG", "VARIANT_ONEREAD_SMEM", "VARIANT_TWOPASS",
-    "VARIANT_SPLITROW", "VARIANT_NAMES", "SoftmaxError", "softmax_rows", "softmax_rows_ex",
+    "VARIANT_SPLITROW", "VARIANT_SPLITROW_STREAM", "VARIANT_NAMES", "SoftmaxError", "softmax_rows", "softmax_rows_ex",
     "softmax_row_state", "merge_states", "softmax_rows_host", "get_status", "status_string",
     "last_variant", "debug_set_fault", "debug_set_wait_limit_ns", "capi", "library_path",
     "softmax_rows_splitrow_noalloc", "softmax_rows_causal",
 ]
 
 F32, BF16, F16 = 0, 1, 2
-VARIANT_AUTO, VARIANT_ONEREAD_REG, VARIANT_ONEREAD_SMEM, VARIANT_TWOPASS, VARIANT_SPLITROW = range(5)
+(VARIANT_AUTO, VARIANT_ONEREAD_REG, VARIANT_ONEREAD_SMEM, VARIANT_TWOPASS, VARIANT_SPLITROW,
+ VARIANT_SPLITROW_STREAM) = range(6)
 VARIANT_NAMES = {VARIANT_AUTO: "auto", VARIANT_ONEREAD_REG: "oneread_reg",
                  VARIANT_ONEREAD_SMEM: "oneread_smem", VARIANT_TWOPASS: "twopass",
-                 VARIANT_SPLITROW: "splitrow"}
+                 VARIANT_SPLITROW: "splitrow", VARIANT_SPLITROW_STREAM: "splitrow_stream"}
 
 OK, ERR_INVALID_ARG, ERR_MISALIGNED, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(6)
 
@@ -251,9 +252,8 @@ def attention_forward(q, k, v, o=None, lse_out=None, scale: float | None = None,
         o = torch.empty_like(q)
     if lse_out is not None and (lse_out.dtype != torch.float32 or lse_out.numel() != BH * Sq or not lse_out.is_cuda):
         raise ValueError("lse_out must be a CUDA float32 tensor of BH * Sq entries")
-    if scale is None:
-        scale = 1.0 / float(d) ** 0.5
-    st = capi().attention_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse_out), BH, Sq, Sk, d, float(scale),
+    st = capi().attention_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse_out), BH, Sq, Sk, d,
+                                  0.0 if scale is None else float(scale),  # 0: the library's 1/sqrt(d)
                                   1 if causal else 0, _dtype_code(q), _stream(stream))
     _check(st, "attention_forward")
     return o

@@ -75,7 +75,7 @@ def test_other_calls_argument_checks(lib):
     assert lib.softmax_rows_causal(X, NULL, None, None, None, 4, 4, 4, 0, 0, None) == rwo.ERR_INVALID_ARG
     assert lib.softmax_rows_causal(NULL, NULL, None, None, None, 0, 4, 4, 0, 0, None) == rwo.OK  # M = 0
     assert lib.log_softmax_rows(X, NULL, None, None, None, 4, 4, 0, 0, None) == rwo.ERR_INVALID_ARG  # no y
-    assert lib.log_softmax_rows(X, X, None, None, None, 4, 4, 0, 5, None) == rwo.ERR_INVALID_ARG  # variant
+    assert lib.log_softmax_rows(X, X, None, None, None, 4, 4, 0, 6, None) == rwo.ERR_INVALID_ARG  # variant
     assert lib.log_softmax_rows(NULL, NULL, None, None, None, 0, 4, 1, 0, None) == rwo.OK  # M = 0
     assert lib.cross_entropy_rows(X, NULL, X, None, 4, 4, 0, None) == rwo.ERR_INVALID_ARG  # no labels
     assert lib.cross_entropy_rows(X, X, None, None, 4, 4, 0, None) == rwo.ERR_INVALID_ARG  # no loss
@@ -96,7 +96,9 @@ def test_other_calls_argument_checks(lib):
     at = lib.attention_forward  # (q, k, v, o, lse, BH, Sq, Sk, d, scale, causal, dtype, stream)
     assert at(X, X, X, X, None, 1, 16, 16, 96, 1.0, 0, 1, None) == rwo.ERR_UNSUPPORTED  # d = 96
     assert at(X, X, X, X, None, 1, 16, 16, 128, 1.0, 0, 0, None) == rwo.ERR_UNSUPPORTED  # fp32
-    assert at(X, X, X, X, None, 1, 16, 16, 128, 0.0, 0, 1, None) == rwo.ERR_INVALID_ARG  # scale
+    assert at(X, X, X, X, None, 1, 16, 16, 128, -1.0, 0, 1, None) == rwo.ERR_INVALID_ARG  # scale
+    assert at(X, X, X, X, None, 1, 16, 16, 128, float("inf"), 0, 1, None) == rwo.ERR_INVALID_ARG
+    assert at(NULL, NULL, NULL, NULL, None, 1, 16, 16, 128, 0.0, 0, 1, None) == rwo.ERR_INVALID_ARG  # 0: default
     assert at(X, X, X, X, None, 1, 16, 16, 128, 1.0, 2, 1, None) == rwo.ERR_INVALID_ARG  # causal flag
     assert at(X, X, X, X, None, 1, 0, 16, 128, 1.0, 0, 1, None) == rwo.ERR_INVALID_ARG  # Sq = 0
     assert at(X, X, X, X, None, 65536, 16, 16, 128, 1.0, 0, 1, None) == rwo.ERR_UNSUPPORTED  # BH

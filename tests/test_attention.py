@@ -106,6 +106,20 @@ def test_attention_large_scores_and_scale():
     _check(to_host(o), lse.cpu().numpy(), q, k, v, [(h, i) for h in range(BH) for i in range(S)], True, 0.3, "sharp")
 
 
+def test_attention_default_scale_is_one_over_sqrt_d():
+    """scale 0 (the binding's default) is the library's 1/sqrt(d): bitwise the explicit value."""
+    for d in (64, 128):
+        q, k, v = _qkv(1, 200, 300, d, seed=95)
+        qd, kd, vd = to_device(q), to_device(k), to_device(v)
+        la, lb = torch.empty((1, 200), device="cuda"), torch.empty((1, 200), device="cuda")
+        oa = rwo.attention_forward(qd, kd, vd, lse_out=la)
+        ob = rwo.attention_forward(qd, kd, vd, lse_out=lb, scale=float(np.float32(1.0 / np.sqrt(d))))
+        assert rwo.get_status() == rwo.OK
+        assert torch.equal(oa, ob) and torch.equal(la, lb)
+        _check(to_host(oa), la.cpu().numpy(), q, k, v, [(0, i) for i in range(0, 200, 7)], False, 1.0 / np.sqrt(d),
+               f"default scale d={d}")
+
+
 @pytest.mark.parametrize("BH,S", [(70, 384), (3, 33000)])
 def test_attention_causal_cta_order(BH, S):
     """Causal CTAs run in head groups of ~128 CTAs: a partial last group (70 heads of 2 pairs:
