@@ -86,13 +86,21 @@ enum softmax_variant {
   SOFTMAX_VARIANT_TWOPASS = 3,
   /* Split row: one row is spread over every CTA of the grid; CTAs of a thread-block cluster merge
      (m, d) over distributed shared memory, clusters exchange 8-byte states through global memory
-     (16-byte aligned rows of any length above about 150 KiB).  Every CTA streams its segment
-     twice through a ring of shared-memory slots: the fold, then the normalisation, whose
-     re-read is served from L2 while the next rows fold.  AUTO takes it for rows above 64 KiB
-     when there are at most half as many rows as SMs, and for rows of 8 MiB and more at any
-     row count.  It needs every cluster resident at once, so it must not share the GPU with
-     other kernels (softmax_rows_host never uses it). */
-  SOFTMAX_VARIANT_SPLITROW = 4
+     (16-byte aligned rows above about 150 KiB).  Each CTA holds its segment of a row in shared
+     memory from the load until the normalisation, so x is read once: rows up to about 17 MB on
+     a 152-SM GB300 (at least two segments per SM fit in shared memory; shorter rows keep up to
+     eight in flight).  Longer rows run SOFTMAX_VARIANT_SPLITROW_STREAM instead (and
+     softmax_last_variant() reports that).  AUTO takes the split row for rows above 64 KiB when
+     there are at most half as many rows as SMs, and for rows of 8 MiB and more at any row count.
+     It needs every cluster resident at once, so it must not share the GPU with other kernels
+     (softmax_rows_host never uses it): kernels running beside it on other streams can keep
+     clusters off the GPU until the exchange wait runs out (SOFTMAX_ERR_TIMEOUT, y undefined). */
+  SOFTMAX_VARIANT_SPLITROW = 4,
+  /* Split row, streaming: as SOFTMAX_VARIANT_SPLITROW, but nothing of a row is held on chip, so
+     rows of any length are taken: every CTA streams its segment twice through a ring of
+     shared-memory slots, the fold, then the normalisation, whose re-read is served from L2 while
+     the next rows fold. */
+  SOFTMAX_VARIANT_SPLITROW_STREAM = 5
 };
 
 /*
@@ -104,7 +112,13 @@ int softmax_rows(const void* x, void* y, int64_t M, int64_t N, int dtype, void* 
 
 /*
  * softmax_rows_ex -- softmax_rows with optional per-row state outputs
- * (m_out, d_out, lse_out: fp32[M] or NULL) and a forced variant.
+ * (m_out, d_out, lse_out: fp32[M] or NULL) and a forced variant.  The state
+ * is the (m, d) pair each row's online fold ends with ("5.2 CUDA Online
+ * Softmax 实现优化", §2.1; "Softmax 数值稳定性与 IO-Aware Attention" §四, the
+ * mergeable state) and LSE = m + ln d ("从原始Softmax到在线Softmax",
+ * log-sum-exp); the variants are the page's kernel designs re-made for this
+ * GPU: the register one-read kernel of §6, the two passes of §2.2 with the
+ * vector loads of §5, and the split rows of §7.1.
  * A forced variant that needs 16-byte alignment returns SOFTMAX_ERR_MISALIGNED
  * when x, y or the row pitch N * sizeof(dtype) is not a multiple of 16;
  * AUTO never does (it falls back to scalar-access kernels).
@@ -194,7 +208,7 @@ int cross_entropy_rows(const void* x, const int64_t* labels, float* loss, float*
  *   k, v    -- device, [BH][Sk][d].
  *   o       -- device, [BH][Sq][d] (written).
  *   lse_out -- device, fp32 [BH][Sq]: m + ln l of each row (natural log, of scale Q K^T), or NULL.
- *   scale   -- finite, > 0 (1/sqrt(d) in attention).
+ *   scale   -- finite, > 0; 0 means 1/sqrt(d), attention's usual scale (rounded to fp32).
  *   causal  -- 1: query row i sees keys j <= i + Sk - Sq (the last query sees every key); 0: all.
  * A row that sees no key gets o = 0, LSE = -inf.  Supported: dtype SOFTMAX_BF16 or SOFTMAX_F16
  * with d = 64 or 128 (fp32 accumulation; P rounded to the element type for the P V product; fp16
@@ -245,8 +259,9 @@ int softmax_rows_host(const void* x_host, void* y_host, int64_t M, int64_t N, in
                       void* stream);
 
 /*
- * softmax_rows_splitrow_noalloc -- the split-row softmax (SOFTMAX_VARIANT_SPLITROW) for callers
- * that cannot allocate device memory.  The pages describe no such call; it exists for callers
+ * softmax_rows_splitrow_noalloc -- the split-row softmax (SOFTMAX_VARIANT_SPLITROW, with the same
+ * choice between the on-chip and the streaming kernel) for callers that cannot allocate device
+ * memory.  The pages describe no such call; it exists for callers
  * such as code held to a device-memory budget fixed in advance, code whose framework allocator
  * owns the device memory, or host threads that must not make a call that may block or
  * synchronise the device.  It allocates nothing (no cudaMalloc, cudaMallocAsync, cudaFree or
@@ -260,6 +275,9 @@ int softmax_rows_host(const void* x_host, void* y_host, int64_t M, int64_t N, in
  *    or rows the split kernel cannot take, return SOFTMAX_ERR_UNSUPPORTED without launching.
  *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress, with
  *    that device current) and keeps it; make that first call before any stream capture.
+ *  - Like SOFTMAX_VARIANT_SPLITROW it needs every SM of the GPU: kernels running beside it on
+ *    other streams can keep its clusters off the GPU until the exchange wait runs out, and the
+ *    call then reports SOFTMAX_ERR_TIMEOUT (through softmax_get_status) with y undefined.
  *  - Every call shares the one array and resets the part it uses (a cudaMemsetAsync on `stream`
  *    before the kernel); calls whose executions overlap on the GPU -- on different streams, or
  *    from different threads -- race on it and must be serialised by the caller.
@@ -289,10 +307,11 @@ int softmax_last_variant(void);
  * softmax_debug_set_fault -- test hook.  fault = 1 makes the next
  * split-row launches skip one cluster's state publication, so every other
  * cluster's bounded wait runs out and the kernel records SOFTMAX_ERR_TIMEOUT
- * instead of hanging; fault = 2 makes the next attention_forward launches skip
- * the copy of the first V tile, with the same outcome (the output is then
- * undefined); fault = 0 restores normal behaviour.  Returns the previous
- * value.  Process-wide; not for production use.
+ * instead of hanging; fault = 2 makes the next attention_forward launches with
+ * at most 256 keys (Sk <= 256, two key tiles) skip the copy of the first V
+ * tile, with the same outcome (the output is then undefined); longer key
+ * sequences ignore it.  fault = 0 restores normal behaviour.  Returns the
+ * previous value.  Process-wide; not for production use.
  */
 int softmax_debug_set_fault(int fault);
 

@@ -3,6 +3,7 @@
 // Host side only: argument validation, per-device properties, variant choice, the per-device
 // status word, and the host-buffer pipeline.  Every step of the computation runs in the
 // kernels of kernels_rowwise.cu, kernel_oneread_tma.cu and kernel_splitrow.cu.
+#include <cmath>
 #include <mutex>
 #include <string>
 
@@ -158,8 +159,10 @@ int run_variant(RowProblem& p, int variant, const DeviceInfo& dev) {
                splitrow_fits(p, dev))
         // few long rows, or rows of 8 MiB and more at any count: a CTA per row would keep more
         // rows in flight than L2 holds, and the two-pass re-read would come from HBM (measured:
-        // 152 x 16 MiB fp32 865 us split against 1150 us two-pass, 300 x 8 MiB 1064 against 1132)
-        variant = SOFTMAX_VARIANT_SPLITROW;
+        // 152 x 16 MiB fp32 865 us split against 1150 us two-pass, 300 x 8 MiB 1064 against 1132);
+        // the streaming form (measured on 32 x 16 MiB fp32: 185 us against 222 us with the
+        // segments held on chip)
+        variant = SOFTMAX_VARIANT_SPLITROW_STREAM;
       else
         variant = SOFTMAX_VARIANT_TWOPASS;
     } else {
@@ -191,6 +194,17 @@ int run_variant(RowProblem& p, int variant, const DeviceInfo& dev) {
       err = launch_twopass_any(p, aligned, dev);
       break;
     case SOFTMAX_VARIANT_SPLITROW:
+      // the segment held on chip (one read) where it fits, else the streaming form
+      if (!aligned) return SOFTMAX_ERR_MISALIGNED;
+      if (splitrow_onchip_fits(p, dev)) {
+        err = launch_splitrow_onchip_pooled(p, dev);
+      } else {
+        if (!splitrow_fits(p, dev)) return SOFTMAX_ERR_UNSUPPORTED;
+        err = launch_splitrow(p, dev);
+        variant = SOFTMAX_VARIANT_SPLITROW_STREAM;
+      }
+      break;
+    case SOFTMAX_VARIANT_SPLITROW_STREAM:
       if (!aligned) return SOFTMAX_ERR_MISALIGNED;
       if (!splitrow_fits(p, dev)) return SOFTMAX_ERR_UNSUPPORTED;
       err = launch_splitrow(p, dev);
@@ -256,7 +270,7 @@ int softmax_rows_ex(const void* x, void* y, float* m_out, float* d_out, float* l
   bool noop = false;
   int st = validate_rows(x, M, N, dtype, &noop);
   if (st != SOFTMAX_OK) return st;
-  if (variant < SOFTMAX_VARIANT_AUTO || variant > SOFTMAX_VARIANT_SPLITROW) return SOFTMAX_ERR_INVALID_ARG;
+  if (variant < SOFTMAX_VARIANT_AUTO || variant > SOFTMAX_VARIANT_SPLITROW_STREAM) return SOFTMAX_ERR_INVALID_ARG;
   if (noop) return SOFTMAX_OK;
   if (!y) return SOFTMAX_ERR_INVALID_ARG;
   const DeviceInfo* dev = nullptr;
@@ -324,7 +338,7 @@ int softmax_rows_strided(const void* x, int64_t ldx, void* y, int64_t ldy, float
   bool noop = false;
   int st = validate_rows(x, M, N, dtype, &noop);
   if (st != SOFTMAX_OK) return st;
-  if (variant < SOFTMAX_VARIANT_AUTO || variant > SOFTMAX_VARIANT_SPLITROW) return SOFTMAX_ERR_INVALID_ARG;
+  if (variant < SOFTMAX_VARIANT_AUTO || variant > SOFTMAX_VARIANT_SPLITROW_STREAM) return SOFTMAX_ERR_INVALID_ARG;
   if (flags & ~SOFTMAX_FLAG_LOG) return SOFTMAX_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !(scale <= 3.4028234663852886e38f)) return SOFTMAX_ERR_INVALID_ARG;  // finite, > 0
   if (ldx == 0) ldx = N;
@@ -375,7 +389,7 @@ int softmax_rows_strided(const void* x, int64_t ldx, void* y, int64_t ldy, float
     case SOFTMAX_VARIANT_TWOPASS:
       err = launch_twopass_any(p, aligned, *dev);
       break;
-    default:  // SOFTMAX_VARIANT_SPLITROW
+    default:  // SOFTMAX_VARIANT_SPLITROW, SOFTMAX_VARIANT_SPLITROW_STREAM
       return SOFTMAX_ERR_UNSUPPORTED;
   }
   if (err != cudaSuccess) return cuda_fail(err);
@@ -414,6 +428,7 @@ int attention_forward(const void* q, const void* k, const void* v, void* o, floa
                       int64_t Sk, int64_t d, float scale, int causal, int dtype, void* stream) {
   if (dtype != SOFTMAX_F32 && dtype != SOFTMAX_BF16 && dtype != SOFTMAX_F16) return SOFTMAX_ERR_INVALID_ARG;
   if (BH < 0 || Sq < 1 || Sk < 1 || d < 1) return SOFTMAX_ERR_INVALID_ARG;
+  if (scale == 0.f) scale = float(1.0 / sqrt(double(d)));  // the attention default, 1 / sqrt(d)
   if (!(scale > 0.f) || !(scale <= 3.4028234663852886e38f)) return SOFTMAX_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return SOFTMAX_ERR_INVALID_ARG;
   if (!attention_fits(d, dtype)) return SOFTMAX_ERR_UNSUPPORTED;

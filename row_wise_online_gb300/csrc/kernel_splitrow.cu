@@ -76,7 +76,7 @@ struct SplitArgs {
   int64_t row_bytes;
   int slots;          // ring slots of kPieceBytes
   unsigned long long* pub;  // [M][clusters] published cluster states (m, d) as one 64-bit word;
-                            // all-ones (NaN) until published -- set before launch
+                            // all ones (kUnpublished) until published -- set before launch
   unsigned* status;
   uint64_t local_wait_ns;
   uint64_t exchange_wait_ns;
@@ -132,8 +132,13 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
   return v;
 }
 
+// The publication slots read all ones until a state is written.  A published word is never all
+// ones: a NaN d (a row holding NaN or +inf) is written as the canonical quiet NaN 0x7fffffff, so
+// a row's NaN propagates into that row's outputs instead of looking unpublished.
+constexpr unsigned long long kUnpublished = ~0ull;
 __device__ __forceinline__ unsigned long long pack_state(State s) {
-  return (static_cast<unsigned long long>(__float_as_uint(s.d)) << 32) | __float_as_uint(s.m);
+  const uint32_t d = s.d == s.d ? __float_as_uint(s.d) : 0x7fffffffu;
+  return (static_cast<unsigned long long>(d) << 32) | __float_as_uint(s.m);
 }
 
 __device__ __forceinline__ State unpack_state(unsigned long long v) {
@@ -342,7 +347,10 @@ __global__ void __launch_bounds__(kSplitThreads, 1) k_splitrow(SplitArgs a) {
   } else if (warp == kExchangeWarp) {
     bool abort = false;
     for (int64_t r = 0; r < a.M; ++r) {
-      const uint64_t t0 = global_timer_ns();
+      // every exit from this loop is taken by the whole warp: lane 0 alone reads the clock and
+      // decides when the wait has run out (lanes that read the clock themselves could disagree at
+      // the limit, and a lane that left would never reach the next full-warp collective)
+      const uint64_t t0 = __shfl_sync(0xffffffffu, global_timer_ns(), 0);
       State g;
       while (true) {
         __syncwarp();
@@ -350,16 +358,17 @@ __global__ void __launch_bounds__(kSplitThreads, 1) k_splitrow(SplitArgs a) {
         State gg = empty_state();
         if (!abort) {
           for (uint32_t i = lane; i < ncl; i += 32) {
-            const State cs = unpack_state(ld_acquire_u64(a.pub + r * ncl + i));
-            if (cs.d != cs.d) ready = false;  // NaN: not published yet
-            else gg = merge(gg, cs);
+            const unsigned long long v = ld_acquire_u64(a.pub + r * ncl + i);
+            if (v == kUnpublished) ready = false;
+            else gg = merge(gg, unpack_state(v));
           }
         }
         if (__all_sync(0xffffffffu, ready)) {
           g = warp_merge(gg);  // the same states in the same order in every CTA
           break;
         }
-        if (global_timer_ns() - t0 > a.exchange_wait_ns) {
+        const int expired = __shfl_sync(0xffffffffu, global_timer_ns() - t0 > a.exchange_wait_ns ? 1 : 0, 0);
+        if (expired) {
           abort = true;
           timed_out = true;
           g = warp_merge(gg);
@@ -526,6 +535,11 @@ bool splitrow_fits(const RowProblem& p, const DeviceInfo& dev) {
   const int64_t units = row_bytes / 16;
   if (units < G * 64) return false;  // rows this short belong to the one-read kernels
   return true;  // nothing of a row is held on chip: any length
+}
+
+size_t splitrow_slots(const RowProblem& p, const DeviceInfo& dev) {
+  const SplitPlan plan = plan_for(p.dtype, dev);
+  return plan.ok ? size_t(p.M) * plan.clusters : 0;
 }
 
 cudaError_t launch_splitrow(const RowProblem& p, const DeviceInfo& dev) {

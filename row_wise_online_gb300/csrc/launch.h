@@ -79,6 +79,17 @@ cudaError_t launch_clusterrow(const RowProblem& p, const DeviceInfo& dev);
 bool splitrow_fits(const RowProblem& p, const DeviceInfo& dev);
 cudaError_t launch_splitrow(const RowProblem& p, const DeviceInfo& dev);
 
+// Split row with each CTA's segment held in shared memory (one read of x): 16-byte aligned rows
+// whose per-CTA segment fits at least two row buffers.  `pub` holds M x splitrow_onchip_clusters()
+// 64-bit publication slots, all ones when the kernel starts (the _pooled form allocates and sets
+// them on the stream).
+bool splitrow_onchip_fits(const RowProblem& p, const DeviceInfo& dev);
+int splitrow_onchip_clusters(const RowProblem& p, const DeviceInfo& dev);
+cudaError_t launch_splitrow_onchip(const RowProblem& p, const DeviceInfo& dev, unsigned long long* pub);
+cudaError_t launch_splitrow_onchip_pooled(const RowProblem& p, const DeviceInfo& dev);
+// Publication slots the streaming split-row kernel needs (M x its clusters).
+size_t splitrow_slots(const RowProblem& p, const DeviceInfo& dev);
+
 // Split row with caller-provided scratch: `pub` holds `pub_slots` 64-bit publication slots
 // (device memory).  Nothing is allocated.  Returns cudaErrorInvalidValue when the problem
 // needs more slots than given (*too_big is then set).

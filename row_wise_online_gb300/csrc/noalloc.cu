@@ -5,9 +5,10 @@
 // call: one 64-bit publication slot per (row, cluster) for the cross-cluster exchange.  Some
 // callers cannot let a library allocate: code that must stay within a device-memory budget
 // fixed up front, code whose framework allocator owns all device memory, and host threads
-// that must not make a call that may block or synchronise the device.  This entry point runs
-// the same kernel with its scratch in a file-scope device array instead, so it allocates
-// nothing: no cudaMalloc / cudaMallocAsync / cudaFree, no library allocator.
+// that must not make a call that may block or synchronise the device.  This entry point makes
+// the same kernel choice (each CTA's segment held on chip where it fits, else the streaming
+// form) with its scratch in a file-scope device array instead, so it allocates nothing: no
+// cudaMalloc / cudaMallocAsync / cudaFree, no library allocator.
 #include <mutex>
 
 #include "../../include/softmax_rows.h"
@@ -69,13 +70,23 @@ extern "C" int softmax_rows_splitrow_noalloc(const void* x, void* y, float* m_ou
   p.N = N;
   p.dtype = dtype;
   p.stream = static_cast<cudaStream_t>(stream);
-  if (!splitrow_fits(p, *dev)) return SOFTMAX_ERR_UNSUPPORTED;
+  // the same kernel choice as SOFTMAX_VARIANT_SPLITROW: the segment held on chip where it fits
+  const bool onchip = splitrow_onchip_fits(p, *dev);
+  if (!onchip && !splitrow_fits(p, *dev)) return SOFTMAX_ERR_UNSUPPORTED;
+  const size_t slots = onchip ? size_t(M) * size_t(splitrow_onchip_clusters(p, *dev)) : splitrow_slots(p, *dev);
+  if (slots > kNoAllocSlots) return SOFTMAX_ERR_UNSUPPORTED;
   unsigned long long* pub = nullptr;
   cudaError_t err = noalloc_scratch(dev->device, &pub);
   if (err != cudaSuccess) return cuda_failure(err);
-  bool too_big = false;
-  err = launch_splitrow_scratch(p, *dev, pub, kNoAllocSlots, &too_big);
-  if (too_big) return SOFTMAX_ERR_UNSUPPORTED;
+  if (onchip) {
+    // the slots must read as "not published" (all ones) when the kernel starts
+    err = cudaMemsetAsync(pub, 0xFF, slots * sizeof(unsigned long long), p.stream);
+    if (err == cudaSuccess) err = launch_splitrow_onchip(p, *dev, pub);
+  } else {
+    bool too_big = false;
+    err = launch_splitrow_scratch(p, *dev, pub, kNoAllocSlots, &too_big);
+    if (too_big) return SOFTMAX_ERR_UNSUPPORTED;
+  }
   if (err != cudaSuccess) return cuda_failure(err);
   return SOFTMAX_OK;
 }

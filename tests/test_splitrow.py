@@ -25,16 +25,23 @@ def _built():
     torch.cuda.set_device(0)
 
 
+SPLIT_VARIANTS = [rwo.VARIANT_SPLITROW, rwo.VARIANT_SPLITROW_STREAM]
+
+
+@pytest.mark.parametrize("variant", SPLIT_VARIANTS)
 @pytest.mark.parametrize("dtype,M,N", [
     (synth.F32, 3, 1 << 21), (synth.F32, 5, 1_500_000), (synth.BF16, 2, 1 << 22), (synth.BF16, 7, 3_000_008),
-    (synth.F32, 1, 4_000_000),
+    (synth.F32, 1, 4_000_000), (synth.F32, 9, 4_194_304), (synth.BF16, 17, 777_784), (synth.F32, 2, 160_000),
 ])
-def test_splitrow_against_oracle(dtype, M, N):
+def test_splitrow_against_oracle(dtype, M, N, variant):
+    """Both split-row kernels, element by element: the segment held on chip (SPLITROW; rows of
+    ~1.5 - 16 MiB give 2 - 8 row buffers, ragged segments and a partial last piece) and the
+    streaming form."""
     w = synth.custom("split", dtype, M, N, seed=N % 1000, dist=synth.UNIFORM, p0=-20.0, p1=20.0, late_max=20.0)
     x_host = synth.generate(w)
     x = to_device(x_host)
-    y, m, d, lse = run_softmax(x, rwo.VARIANT_SPLITROW)
-    assert rwo.last_variant() == rwo.VARIANT_SPLITROW
+    y, m, d, lse = run_softmax(x, variant)
+    assert rwo.last_variant() == variant
     y_ref, m_ref, d_ref, lse_ref = oracle.softmax_rows(x_host)
     yh = to_host(y)
     check_y(yh, y_ref, dtype, f"split {M}x{N}")
@@ -42,16 +49,18 @@ def test_splitrow_against_oracle(dtype, M, N):
     check_state(m.cpu().numpy(), d.cpu().numpy(), lse.cpu().numpy(), m_ref, d_ref, lse_ref, "split")
 
 
-def test_splitrow_masked_segments_and_special_rows():
-    """Whole CTA segments and clusters that see only -inf must merge as the empty state."""
-    N = 1 << 21
+@pytest.mark.parametrize("N", [1 << 21, 1 << 22])
+@pytest.mark.parametrize("variant", SPLIT_VARIANTS)
+def test_splitrow_masked_segments_and_special_rows(variant, N):
+    """Whole CTA segments and clusters that see only -inf must merge as the empty state (8 MiB rows
+    keep four row buffers in shared memory; 16 MiB rows park folded segments in tensor memory)."""
     rows = np.random.default_rng(0).standard_normal((4, N)).astype(np.float32) * 3
     rows[0, : N - 1000] = -np.inf          # only the tail survives: most CTAs hold empty states
     rows[1, 1000:] = -np.inf               # only the head survives
     rows[2, :] = -np.inf                   # fully masked row
     rows[3, N // 2] = 1e30                 # one huge value
     x = to_device(rows)
-    y, m, d, lse = run_softmax(x, rwo.VARIANT_SPLITROW)
+    y, m, d, lse = run_softmax(x, variant)
     y_ref, m_ref, d_ref, lse_ref = oracle.softmax_rows(rows)
     yh = to_host(y)
     check_y(yh, y_ref, synth.F32, "split special")
@@ -60,11 +69,12 @@ def test_splitrow_masked_segments_and_special_rows():
     assert not np.isnan(yh).any()
 
 
-def test_splitrow_in_place():
+@pytest.mark.parametrize("variant", SPLIT_VARIANTS)
+def test_splitrow_in_place(variant):
     w = synth.custom("split-ip", synth.BF16, 3, 1 << 22, seed=5, p1=2.0)
     x_host = synth.generate(w)
     x = to_device(x_host)
-    rwo.softmax_rows_ex(x, x, variant=rwo.VARIANT_SPLITROW)
+    rwo.softmax_rows_ex(x, x, variant=variant)
     assert rwo.get_status() == rwo.OK
     y_ref, *_ = oracle.softmax_rows(x_host)
     check_y(to_host(x), y_ref, synth.BF16, "split in place")
@@ -75,7 +85,7 @@ def test_auto_takes_splitrow_for_few_long_rows():
     x = to_device(synth.generate(w))
     rwo.softmax_rows(x)
     torch.cuda.synchronize()
-    assert rwo.last_variant() == rwo.VARIANT_SPLITROW
+    assert rwo.last_variant() in (rwo.VARIANT_SPLITROW, rwo.VARIANT_SPLITROW_STREAM)
 
 
 def test_auto_takes_splitrow_for_many_rows_of_8mib():
@@ -87,7 +97,7 @@ def test_auto_takes_splitrow_for_many_rows_of_8mib():
     x_host = synth.generate(w)
     x = to_device(x_host)
     y, m, d, lse = run_softmax(x, rwo.VARIANT_AUTO)
-    assert rwo.last_variant() == rwo.VARIANT_SPLITROW
+    assert rwo.last_variant() in (rwo.VARIANT_SPLITROW, rwo.VARIANT_SPLITROW_STREAM)
     yh = to_host(y)
     check_rowsums(yh, synth.F32, None, "split 100 x 8 MiB")
     pick = [0, 37, 76, 77, 99]
@@ -102,8 +112,10 @@ def test_auto_takes_splitrow_for_many_rows_of_8mib():
     assert rwo.last_variant() == rwo.VARIANT_TWOPASS
 
 
-def test_exchange_wait_runs_out_and_reports_timeout():
-    w = synth.custom("fault", synth.F32, 3, 1 << 21, seed=1, p1=2.0)
+@pytest.mark.parametrize("M,N", [(3, 1 << 21), (5, 1 << 22)])
+@pytest.mark.parametrize("variant", SPLIT_VARIANTS)
+def test_exchange_wait_runs_out_and_reports_timeout(variant, M, N):
+    w = synth.custom("fault", synth.F32, M, N, seed=1, p1=2.0)
     x_host = synth.generate(w)
     x = to_device(x_host)
     y = torch.empty_like(x)
@@ -111,28 +123,29 @@ def test_exchange_wait_runs_out_and_reports_timeout():
     old_limit = rwo.debug_set_wait_limit_ns(20_000_000)  # 20 ms
     old_fault = rwo.debug_set_fault(1)
     try:
-        rwo.softmax_rows_ex(x, y, variant=rwo.VARIANT_SPLITROW)
+        rwo.softmax_rows_ex(x, y, variant=variant)
+        assert rwo.last_variant() == variant
         assert rwo.get_status() == rwo.ERR_TIMEOUT
     finally:
         rwo.debug_set_fault(old_fault)
         rwo.debug_set_wait_limit_ns(old_limit)
     # the context is intact and the next launch is correct
     assert rwo.get_status() == rwo.OK
-    rwo.softmax_rows_ex(x, y, variant=rwo.VARIANT_SPLITROW)
+    rwo.softmax_rows_ex(x, y, variant=variant)
     assert rwo.get_status() == rwo.OK
     y_ref, *_ = oracle.softmax_rows(x_host)
     check_y(to_host(y), y_ref, synth.F32, "after timeout")
 
 
 def test_rows_larger_than_l2():
-    """A single 32 Mi-element fp32 row (128 MiB, larger than L2): nothing of a row is held on chip,
-    so the split kernel takes it (its second pass then reads HBM again); AUTO picks it too."""
+    """A single 32 Mi-element fp32 row (128 MiB, larger than L2): too long to hold on chip, so the
+    streaming split kernel takes it (its second pass then reads HBM again); AUTO picks it too."""
     N = 1 << 25
     w = synth.custom("split-huge", synth.F32, 1, N, seed=77, dist=synth.UNIFORM, p0=-20.0, p1=20.0, late_max=20.0)
     x_host = synth.generate(w)
     x = to_device(x_host)
     y, m, d, lse = run_softmax(x, rwo.VARIANT_SPLITROW)
-    assert rwo.last_variant() == rwo.VARIANT_SPLITROW
+    assert rwo.last_variant() == rwo.VARIANT_SPLITROW_STREAM  # too long to hold on chip
     y_ref, m_ref, d_ref, lse_ref = oracle.softmax_rows(x_host)
     yh = to_host(y)
     check_y(yh, y_ref, synth.F32, "split 1 x 32Mi")
@@ -141,4 +154,27 @@ def test_rows_larger_than_l2():
     del y_ref
     rwo.softmax_rows(x)
     torch.cuda.synchronize()
-    assert rwo.last_variant() == rwo.VARIANT_SPLITROW
+    assert rwo.last_variant() == rwo.VARIANT_SPLITROW_STREAM
+
+
+@pytest.mark.parametrize("N", [1 << 21, 1 << 22])
+@pytest.mark.parametrize("variant", SPLIT_VARIANTS)
+def test_splitrow_nan_and_inf_rows_stay_in_their_row(variant, N):
+    """A row holding a NaN or +inf has a NaN state (e^(inf - inf)); it must be published and merged
+    like any other state, so only that row's outputs are NaN, the other rows are correct and the
+    exchange does not wait out its limit (no SOFTMAX_ERR_TIMEOUT)."""
+    rows = np.random.default_rng(3).standard_normal((4, N)).astype(np.float32) * 3
+    rows[1, N // 3] = np.nan
+    rows[2, 2 * N // 3] = np.inf
+    x = to_device(rows)
+    assert rwo.get_status() == rwo.OK
+    y, m, d, lse = run_softmax(x, variant)  # asserts status OK
+    yh = to_host(y)
+    good = [0, 3]
+    y_ref, m_ref, d_ref, lse_ref = oracle.softmax_rows(rows[good])
+    check_y(yh[good], y_ref, synth.F32, "split rows beside NaN / inf rows")
+    check_state(m.cpu().numpy()[good], d.cpu().numpy()[good], lse.cpu().numpy()[good], m_ref, d_ref, lse_ref,
+                "split rows beside NaN / inf rows")
+    dh = d.cpu().numpy()
+    assert np.isnan(dh[1]) and np.isnan(dh[2])
+    assert np.isnan(yh[1]).any() and np.isnan(yh[2]).any()
