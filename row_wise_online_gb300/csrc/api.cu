@@ -155,14 +155,15 @@ int run_variant(RowProblem& p, int variant, const DeviceInfo& dev) {
         variant = SOFTMAX_VARIANT_TWOPASS;
       else if (oneread_tma_fits(p, dev))
         variant = SOFTMAX_VARIANT_ONEREAD_SMEM;
-      else if (!p.shares_gpu && (p.M * 2 <= dev.sm_count || row_bytes >= (int64_t(8) << 20)) &&
+      else if (!p.shares_gpu && (row_bytes >= (int64_t(8) << 20) || (row_bytes >= (int64_t(4) << 20) && p.M <= 16)) &&
                splitrow_fits(p, dev))
-        // few long rows, or rows of 8 MiB and more at any count: a CTA per row would keep more
-        // rows in flight than L2 holds, and the two-pass re-read would come from HBM (measured:
-        // 152 x 16 MiB fp32 865 us split against 1150 us two-pass, 300 x 8 MiB 1064 against 1132);
-        // the streaming form (measured on 32 x 16 MiB fp32: 185 us against 222 us with the
-        // segments held on chip)
-        variant = SOFTMAX_VARIANT_SPLITROW_STREAM;
+        // rows of 8 MiB and more at any count, and rows of 4 MiB and more when there are at most
+        // 16: one row over the whole GPU, each CTA's segment held on chip where it fits (measured,
+        // fp32, split row against the cluster-row two passes: 32 x 16 MiB 163 against 272 us,
+        // 300 x 8 MiB 869 against 1076, 16 x 4 MiB 36.6 against 41.2; but 64 x 4 MiB 133 against
+        // 116, 8 x 2 MiB 20.8 against 17.1, 76 x 1 MiB 124 against 44.5: there each row's
+        // exchange costs more than the clusters' parallel rows)
+        variant = SOFTMAX_VARIANT_SPLITROW;
       else
         variant = SOFTMAX_VARIANT_TWOPASS;
     } else {

@@ -48,13 +48,15 @@ constexpr int kOcNcw = 16;                         // consumer warps
 constexpr int kOcNct = kOcNcw * 32;                // consumer threads
 constexpr int kOcExchangeWarp = kOcNcw;
 constexpr int kOcProducerWarp = kOcNcw + 1;
-constexpr int kOcThreads = (kOcNcw + 2) * 32;
+constexpr int kOcPublisherWarp = kOcNcw + 2;       // rank 0 of a cluster: merges and publishes
+constexpr int kOcThreads = (kOcNcw + 3) * 32;
 constexpr int kOcUpt = 4;                          // 16-byte units per consumer thread per piece
 constexpr int kOcPieceUnits = kOcNct * kOcUpt;     // 2048 units
 constexpr int kOcPieceBytes = kOcPieceUnits * 16;  // 32 KB
 constexpr int kOcMaxBufs = 8;
 constexpr int kOcMaxPieces = 8;
 constexpr int kOcMaxCluster = 8;
+constexpr int kOcPrefetchRows = 1;  // L2 prefetch distance in rows (measured on 32 x 16 MiB fp32: 170 us; 2 rows 176, 3 rows 200, none 190)
 
 struct OnchipArgs {
   const unsigned char* x;
@@ -243,7 +245,8 @@ __global__ void __launch_bounds__(kOcThreads, 1) k_splitrow_onchip(OnchipArgs a)
   const uint32_t cid = cluster_id_x();
   const uint32_t ncl = cluster_count_x();
 
-  // this CTA's segment: units [seg_start, seg_start + seg_units) of every row
+  // this CTA's segment: units [seg_start, seg_start + seg_units) of every row (measured: giving the
+  // even CTA of each SM pair 4% fewer units, as the streaming kernel does, changes nothing here)
   const int64_t G = gridDim.x, c = blockIdx.x;
   const int64_t base = a.units / G, rem = a.units % G;
   const int seg_units = int(base + (c < rem ? 1 : 0));
@@ -285,21 +288,25 @@ __global__ void __launch_bounds__(kOcThreads, 1) k_splitrow_onchip(OnchipArgs a)
     if (lane == 0) {
       const uint64_t drop = policy_evict_first();  // x is read once
       const uint64_t keep = policy_evict_last();   // prefetched lines wait in L2 for their load
-      // Row r + NB is prefetched into L2 when row r's loads are issued (rows NB .. 2 NB - 1 at the
-      // start): HBM reads then run about NB rows ahead of the buffers, so a buffer freed by the
-      // consumers refills from L2 instead of waiting for HBM.
-      for (int64_t r = NB; r < 2 * int64_t(NB) && r < a.M; ++r)
-        for (int p = 0; p < pc; ++p) {
-          const int rest = seg_units - p * kOcPieceUnits;
-          oc_prefetch_l2(a.x + r * a.row_bytes + seg_start * 16 + int64_t(p) * kOcPieceBytes,
-                         uint32_t(rest < kOcPieceUnits ? rest : kOcPieceUnits) * 16u, keep);
-        }
+      // Row r + PD is prefetched into L2 when row r's loads are issued (rows NB .. NB + PD - 1
+      // right after the first NB rows' loads, which go first so that the first fold starts
+      // early): HBM reads run PD rows ahead of the buffers, so a buffer freed by the consumers
+      // refills from L2 instead of waiting for HBM, and the reads of later rows fill the time
+      // the first rows wait for their exchange.
+      const int PD = kOcPrefetchRows;
       OcRing ring(NB);
       for (int64_t r = 0; r < a.M; ++r) {
         const int b = ring.idx;
         const int64_t lap = ring.lap;
         const unsigned char* src = a.x + r * a.row_bytes + seg_start * 16;
-        const bool pf = lap > 0 && r + NB < a.M;  // rows NB .. 2 NB - 1 were prefetched at the start
+        const bool pf = PD > 0 && lap > 0 && r + PD < a.M;  // rows NB .. NB + PD - 1: after the first loads
+        if (r == NB)
+          for (int64_t q = NB; q < NB + int64_t(PD) && q < a.M; ++q)
+            for (int p = 0; p < pc; ++p) {
+              const int rest = seg_units - p * kOcPieceUnits;
+              oc_prefetch_l2(a.x + q * a.row_bytes + seg_start * 16 + int64_t(p) * kOcPieceBytes,
+                             uint32_t(rest < kOcPieceUnits ? rest : kOcPieceUnits) * 16u, keep);
+            }
         for (int p = 0; p < pc; ++p) {
           if (lap > 0 && !mbar_wait(smem_addr(&freed[b * P + p]), uint32_t((lap - 1) & 1), lim)) {
             timed_out = true;  // (the wait is for row r - NB to have left this piece)
@@ -311,7 +318,7 @@ __global__ void __launch_bounds__(kOcThreads, 1) k_splitrow_onchip(OnchipArgs a)
           mbar_arrive_expect_tx(bar, bytes);
           bulk_g2s(bufs + uint32_t(b) * a.buf_bytes + uint32_t(p) * kOcPieceBytes, src + int64_t(p) * kOcPieceBytes,
                    bytes, bar, drop);
-          if (pf) oc_prefetch_l2(src + int64_t(NB) * a.row_bytes + int64_t(p) * kOcPieceBytes, bytes, keep);
+          if (pf) oc_prefetch_l2(src + int64_t(PD) * a.row_bytes + int64_t(p) * kOcPieceBytes, bytes, keep);
         }
         ring.next();
       }
@@ -323,25 +330,30 @@ __global__ void __launch_bounds__(kOcThreads, 1) k_splitrow_onchip(OnchipArgs a)
           if (!mbar_wait(smem_addr(&full[rb * P + p]), par, a.local_wait_ns)) timed_out = true;
       }
     }
+  } else if (warp == kOcPublisherWarp) {
+    // Rank 0's publisher lane: the cluster state of each row as soon as the cluster's CTA states
+    // have all arrived (a warp of its own, so that a publication never waits behind the exchange
+    // warp's polling round trips), in row order.
+    if (crank == 0 && lane == 0) {
+      OcRing ring(RB);
+      for (int64_t r = 0; r < a.M; ++r) {
+        const uint32_t bar = smem_addr(&cbar[ring.idx]);
+        if (!mbar_wait_cluster(bar, ring.parity(), lim)) {
+          timed_out = true;
+          lim = 0;
+        }
+        State cs = empty_state();
+        for (uint32_t i = 0; i < csize; ++i) cs = merge(cs, cstate[ring.idx * kOcMaxCluster + i]);
+        if (!(a.fault && cid == 0)) oc_st_release_u64(a.pub + r * ncl + cid, oc_pack(cs));
+        if (r + RB < a.M) mbar_arrive_expect_tx(bar, csize * 8u);
+        ring.next();
+      }
+    }
   } else if (warp == kOcExchangeWarp) {
     bool abort = false;
     OcRing ring(RB);
     for (int64_t r = 0; r < a.M; ++r) {
       const int b = ring.idx;
-      if (crank == 0) {
-        // the cluster's CTA states for row r -> one cluster state, published
-        if (lane == 0) {
-          if (!mbar_wait_cluster(smem_addr(&cbar[b]), ring.parity(), lim)) {
-            timed_out = true;
-            lim = 0;
-          }
-          State cs = empty_state();
-          for (uint32_t i = 0; i < csize; ++i) cs = merge(cs, cstate[b * kOcMaxCluster + i]);
-          if (!(a.fault && cid == 0)) oc_st_release_u64(a.pub + r * ncl + cid, oc_pack(cs));
-          if (r + RB < a.M) mbar_arrive_expect_tx(smem_addr(&cbar[b]), csize * 8u);
-        }
-        __syncwarp();
-      }
       // every exit from this loop is taken by the whole warp: lane 0 alone reads the clock and
       // decides when the wait has run out (lanes that read the clock themselves could disagree at
       // the limit, and a lane that left would never reach the next full-warp collective)
@@ -471,45 +483,30 @@ __global__ void __launch_bounds__(kOcThreads, 1) k_splitrow_onchip(OnchipArgs a)
     } else {
       // Rows in flight at the start of iteration r: r and r + 1 parked in tensor memory (slots
       // r mod 2, r + 1 mod 2), r + 2 folded in shared-memory buffer r mod 2, r + 3 landing in the
-      // other buffer.  Iteration r: normalise r from its slot; park r + 2 in that slot and free its
-      // buffer (row r + 4 is loaded there); fold r + 3.  A row's state has two iterations to
-      // arrive, and a buffer's load one.
+      // other buffer.  Iteration r, piece by piece: normalise piece p of row r from its slot, then
+      // park piece p of row r + 2 in its place and free that piece of the buffer (row r + 4's
+      // piece is loaded there at once); then fold r + 3.  A row's state has two iterations to
+      // arrive, and a buffer's load about one and a half.
       const uint32_t tmem = *tmem_slot;
       const uint32_t tlane = uint32_t(32 * (warp & 3)) << 16;
       const uint32_t tcol = uint32_t(warp >> 2) * kOcWarpCols;
       auto taddr = [&](int slot, int p) {
         return tmem + tlane + uint32_t(slot) * kOcSlotCols + tcol + uint32_t(p) * (kOcUpt * 4);
       };
-      // park(j): shared-memory buffer -> tensor-memory slot, each piece freed once read
-      auto park_row = [&](const OcRing& buf, int slot) {
-        for (int p = 0; p < pc; ++p) {
-          const uint32_t piece = bufs + uint32_t(buf.idx) * a.buf_bytes + uint32_t(p) * kOcPieceBytes;
-          const int rest = seg_units - p * kOcPieceUnits;
-          uint4 q[kOcUpt];
+      // piece p of the row in shared-memory buffer `buf` -> tensor-memory slot, the piece freed once read
+      auto park_piece = [&](const OcRing& buf, int slot, int p) {
+        const uint32_t piece = bufs + uint32_t(buf.idx) * a.buf_bytes + uint32_t(p) * kOcPieceBytes;
+        const int rest = seg_units - p * kOcPieceUnits;
+        uint4 q[kOcUpt];
 #pragma unroll
-          for (int i = 0; i < kOcUpt; ++i) {
-            const int u = tid + i * kOcNct;
-            q[i] = u < rest ? lds16(piece + uint32_t(u) * 16u) : make_uint4(0u, 0u, 0u, 0u);
-          }
-          __syncwarp();  // (tensor-memory accesses are warp-wide)
-          oc_tmem_st16(taddr(slot, p), q);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_addr(&freed[buf.idx * P + p]));
+        for (int i = 0; i < kOcUpt; ++i) {
+          const int u = tid + i * kOcNct;
+          q[i] = u < rest ? lds16(piece + uint32_t(u) * 16u) : make_uint4(0u, 0u, 0u, 0u);
         }
-        oc_tmem_wait_st();
-      };
-      auto normalise_parked = [&](int64_t r, int slot, const OcRing& st_ring) {
-        const State row = row_state(r, st_ring);
-        const float ms = safe_max(row.m);
-        const float inv = safe_inv(row.d);
-        const float2 nms = make_float2(-ms, -ms), inv2 = make_float2(inv, inv);
-        for (int p = 0; p < pc; ++p) {
-          uint4 q[kOcUpt];
-          __syncwarp();
-          oc_tmem_ld16(taddr(slot, p), q);
-          oc_tmem_wait_ld();
-          store_piece(r, p, q, nms, inv2);
-        }
+        __syncwarp();  // (tensor-memory accesses are warp-wide)
+        oc_tmem_st16(taddr(slot, p), q);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&freed[buf.idx * P + p]));
       };
       OcRing fbuf(2), fst(RB);  // next row to fold: its buffer and state slot
       OcRing pbuf(2);           // next row to park: its buffer
@@ -523,9 +520,10 @@ __global__ void __launch_bounds__(kOcThreads, 1) k_splitrow_onchip(OnchipArgs a)
           fst.next();
         }
       };
-      auto park_next = [&]() {
+      auto park_next = [&]() {  // a whole row (the first two rows)
         if (jp < a.M) {
-          park_row(pbuf, int(jp & 1));
+          for (int p = 0; p < pc; ++p) park_piece(pbuf, int(jp & 1), p);
+          oc_tmem_wait_st();
           ++jp;
           pbuf.next();
         }
@@ -536,9 +534,26 @@ __global__ void __launch_bounds__(kOcThreads, 1) k_splitrow_onchip(OnchipArgs a)
       park_next();
       fold_next();  // row 2
       for (int64_t r = 0; r < a.M; ++r) {
-        normalise_parked(r, int(r & 1), nst);
+        const int slot = int(r & 1);
+        const bool park = jp < a.M;  // row jp = r + 2 follows row r into its slot
+        const State row = row_state(r, nst);
         nst.next();
-        park_next();  // row r + 2 into slot r mod 2
+        const float ms = safe_max(row.m);
+        const float inv = safe_inv(row.d);
+        const float2 nms = make_float2(-ms, -ms), inv2 = make_float2(inv, inv);
+        for (int p = 0; p < pc; ++p) {
+          uint4 q[kOcUpt];
+          __syncwarp();
+          oc_tmem_ld16(taddr(slot, p), q);
+          oc_tmem_wait_ld();
+          store_piece(r, p, q, nms, inv2);
+          if (park) park_piece(pbuf, slot, p);
+        }
+        if (park) {
+          oc_tmem_wait_st();
+          ++jp;
+          pbuf.next();
+        }
         fold_next();  // row r + 3
       }
       // every consumer is done with tensor memory before it is released
