@@ -141,12 +141,14 @@ int run_variant(RowProblem& p, int variant, const DeviceInfo& dev) {
   if (variant == SOFTMAX_VARIANT_AUTO) {
     if (aligned) {
       // Measured on GB300: warp-per-row bulk-copy kernel for many rows of 2-8 KiB, register
-      // kernel for shorter rows, for few rows and for 8-16 KiB rows, CTA bulk-copy kernel for
-      // 16-64 KiB rows.
+      // kernel for shorter rows, for few rows, for 8-16 KiB rows and for fp32 rows up to 32 KiB
+      // (fp32 20-32 KiB rows: 6.87-6.90 TB/s against 5.69-5.92 on the bulk-copy kernel; 16-bit
+      // rows of 24-32 KiB the other way round, 4.8-4.9 against 5.9-6.0), CTA bulk-copy kernel
+      // for the other rows up to 64 KiB.
       if (row_bytes > 2048 && row_bytes <= 8192 && p.M >= 4 * int64_t(dev.sm_count) &&
           oneread_warp_fits(p, dev))
         variant = SOFTMAX_VARIANT_ONEREAD_SMEM;
-      else if (row_bytes <= 16384 && oneread_reg_fits(p, true))
+      else if ((row_bytes <= 16384 || (p.dtype == SOFTMAX_F32 && row_bytes <= 32768)) && oneread_reg_fits(p, true))
         variant = SOFTMAX_VARIANT_ONEREAD_REG;
       else if (p.dtype == SOFTMAX_F32 && row_bytes > 53248 && row_bytes <= 65536)
         // fp32 rows of 52-64 KiB: two passes beat the CTA bulk-copy kernel (measured, ~640 MB per

@@ -176,6 +176,8 @@ def test_host_buffers_staged_pipeline():
 
 
 @pytest.mark.parametrize("dtype,N,want", [
+    (synth.F32, 8192, V.VARIANT_ONEREAD_REG),     # 32 KiB fp32 rows: one read into registers
+    (synth.BF16, 16384, V.VARIANT_ONEREAD_SMEM),  # 32 KiB 16-bit rows: one read through shared memory
     (synth.F32, 12288, V.VARIANT_ONEREAD_SMEM),   # 48 KiB rows: one read
     (synth.F32, 16384, V.VARIANT_TWOPASS),        # 64 KiB fp32 rows: two passes measured faster
     (synth.BF16, 32768, V.VARIANT_ONEREAD_SMEM),  # 64 KiB 16-bit rows: one read
