@@ -354,6 +354,8 @@ def _kernel_name(rwo, used: int, w: synth.Workload, mode: str) -> str:
     if used == rwo.VARIANT_ONEREAD_REG:
         return "k_oneread_reg"
     if used == rwo.VARIANT_ONEREAD_SMEM:
+        if row_bytes > (64 << 10):
+            return "k_splitrow_onchip"  # a thread-block cluster per row, segments held on chip
         return "k_oneread_warp" if row_bytes <= 8192 and mode == "softmax" else "k_oneread_tma"
     if used == rwo.VARIANT_SPLITROW:
         return "k_splitrow_onchip"

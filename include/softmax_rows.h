@@ -76,7 +76,10 @@ enum softmax_variant {
   /* One read: bulk copies (cp.async.bulk + mbarrier) stage whole rows in shared memory.  Rows
      up to 8 KiB: each warp owns a row at a time and a private ring of row slots that its lane 0
      refills; longer rows (up to 64 KiB): a producer warp feeds a CTA-wide consumer group that
-     copies the row to registers and frees the slot at once. */
+     copies the row to registers and frees the slot at once; rows above 64 KiB (16-byte aligned,
+     up to 1 MiB): a thread-block cluster of 2-8 CTAs per row, each CTA's segment held in shared
+     and tensor memory until the row's state, merged over distributed shared memory, is known.
+     AUTO takes the last for many rows of 64 KiB - 1 MiB. */
   SOFTMAX_VARIANT_ONEREAD_SMEM = 2,
   /* Two passes over global memory: online fold with 128-bit loads, then re-read and normalise
      (any N; the re-read is served from L2 while the row is still resident).  Aligned rows above

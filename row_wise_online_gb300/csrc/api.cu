@@ -166,6 +166,16 @@ int run_variant(RowProblem& p, int variant, const DeviceInfo& dev) {
         // 116, 8 x 2 MiB 20.8 against 17.1, 76 x 1 MiB 124 against 44.5: there each row's
         // exchange costs more than the clusters' parallel rows)
         variant = SOFTMAX_VARIANT_SPLITROW;
+      else if (row_bytes >= (int64_t(128) << 10) &&
+               (row_bytes <= (int64_t(512) << 10) ? p.M >= int64_t(dev.sm_count)
+                                                  : row_bytes <= (int64_t(1) << 20) && p.M >= 256) &&
+               clusterrow_onchip_fits(p, dev))
+        // many rows of 128 KiB - 1 MiB: a thread-block cluster per row, its CTAs' segments held on
+        // chip (measured against the cluster-row two passes, fp32: 4000 x 128 KiB 169 against
+        // 182 us, 2000 x 256 KiB 168 / 193, 1000 x 512 KiB 161 / 196, 600 x 1 MiB 218 / 242; bf16
+        // 1000 x 512 KiB 167 / 206; but 8000 x 80 KB 282 / 252, 800 x 768 KB 238 / 221, and fewer
+        // rows of 1 MiB, 100: 46.8 / 46.3, 20: 19.6 / 17.4)
+        variant = SOFTMAX_VARIANT_ONEREAD_SMEM;
       else
         variant = SOFTMAX_VARIANT_TWOPASS;
     } else {
@@ -190,6 +200,8 @@ int run_variant(RowProblem& p, int variant, const DeviceInfo& dev) {
         err = launch_oneread_tma(p, dev);
       else if (oneread_warp_fits(p, dev))
         err = launch_oneread_warp(p, dev);
+      else if (clusterrow_onchip_fits(p, dev))  // rows above 64 KiB: a cluster per row, held on chip
+        err = launch_clusterrow_onchip(p, dev);
       else
         return SOFTMAX_ERR_UNSUPPORTED;
       break;

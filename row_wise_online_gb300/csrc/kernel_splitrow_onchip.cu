@@ -55,7 +55,7 @@ constexpr int kOcPieceUnits = kOcNct * kOcUpt;     // 2048 units
 constexpr int kOcPieceBytes = kOcPieceUnits * 16;  // 32 KB
 constexpr int kOcMaxBufs = 8;
 constexpr int kOcMaxPieces = 8;
-constexpr int kOcMaxCluster = 8;
+constexpr int kOcMaxCluster = 16;  // cluster states per row slot (clusters of up to 16 in local mode)
 constexpr int kOcPrefetchRows = 1;  // L2 prefetch distance in rows (measured on 32 x 16 MiB fp32: 170 us; 2 rows 176, 3 rows 200, none 190)
 
 struct OnchipArgs {
@@ -76,6 +76,7 @@ struct OnchipArgs {
   uint64_t local_wait_ns;
   uint64_t exchange_wait_ns;
   int fault;  // test hook: cluster 0 never publishes
+  int local;  // each cluster owns whole rows (cid, cid + clusters, ...): the state is merged over DSMEM only
 };
 
 constexpr unsigned long long kOcUnpublished = ~0ull;
@@ -223,8 +224,11 @@ size_t onchip_tail_bytes(int nb, int rb, int pieces) {
          size_t(rb) * kOcMaxCluster * sizeof(State) + 2 * kOcNcw * sizeof(State) + size_t(rb) * sizeof(State) + 16;
 }
 
-// HOLD: two shared-memory buffers (landing and fold), segments parked in tensor memory until their
-// row state arrives; else NB shared-memory buffers, fold NB - 1 rows ahead of the normalisation.
+// HOLD: one or two shared-memory buffers (landing and fold), segments parked in tensor memory until
+// their row state arrives; else NB shared-memory buffers, fold NB - 1 rows ahead of the normalisation.
+// Split mode (local = 0): every row is shared by all G CTAs, cluster states exchanged through global
+// memory.  Local mode: cluster k owns rows k, k + clusters, ... and its CS CTAs share each of them;
+// rank 0 merges the CTA states and hands the row state to every CTA of the cluster over DSMEM.
 template <class D, bool HOLD>
 __global__ void __launch_bounds__(kOcThreads, 1) k_splitrow_onchip(OnchipArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -244,10 +248,14 @@ __global__ void __launch_bounds__(kOcThreads, 1) k_splitrow_onchip(OnchipArgs a)
   const uint32_t csize = oc_cluster_nctarank();
   const uint32_t cid = cluster_id_x();
   const uint32_t ncl = cluster_count_x();
+  const bool local = a.local != 0;
+  // the rows this CTA takes part in: M of them, the j-th is row_of(j)
+  const int64_t M = local ? (a.M > int64_t(cid) ? (a.M - 1 - cid) / ncl + 1 : 0) : a.M;
+  auto row_of = [&](int64_t j) { return local ? int64_t(cid) + j * int64_t(ncl) : j; };
 
   // this CTA's segment: units [seg_start, seg_start + seg_units) of every row (measured: giving the
   // even CTA of each SM pair 4% fewer units, as the streaming kernel does, changes nothing here)
-  const int64_t G = gridDim.x, c = blockIdx.x;
+  const int64_t G = local ? int64_t(csize) : int64_t(gridDim.x), c = local ? int64_t(crank) : int64_t(blockIdx.x);
   const int64_t base = a.units / G, rem = a.units % G;
   const int seg_units = int(base + (c < rem ? 1 : 0));
   const int64_t seg_start = c * base + (c < rem ? c : rem);
@@ -264,7 +272,7 @@ __global__ void __launch_bounds__(kOcThreads, 1) k_splitrow_onchip(OnchipArgs a)
     }
     fence_mbar_init();
     if (crank == 0)
-      for (int i = 0; i < RB && i < a.M; ++i) mbar_arrive_expect_tx(smem_addr(&cbar[i]), csize * 8u);
+      for (int i = 0; i < RB && i < M; ++i) mbar_arrive_expect_tx(smem_addr(&cbar[i]), csize * 8u);
   }
   if constexpr (HOLD) {
     if (warp == 0) {  // all 512 columns: one CTA per SM (its shared memory admits no second one)
@@ -295,16 +303,16 @@ __global__ void __launch_bounds__(kOcThreads, 1) k_splitrow_onchip(OnchipArgs a)
       // the first rows wait for their exchange.
       const int PD = kOcPrefetchRows;
       OcRing ring(NB);
-      for (int64_t r = 0; r < a.M; ++r) {
+      for (int64_t r = 0; r < M; ++r) {
         const int b = ring.idx;
         const int64_t lap = ring.lap;
-        const unsigned char* src = a.x + r * a.row_bytes + seg_start * 16;
-        const bool pf = PD > 0 && lap > 0 && r + PD < a.M;  // rows NB .. NB + PD - 1: after the first loads
+        const unsigned char* src = a.x + row_of(r) * a.row_bytes + seg_start * 16;
+        const bool pf = PD > 0 && lap > 0 && r + PD < M;  // rows NB .. NB + PD - 1: after the first loads
         if (r == NB)
-          for (int64_t q = NB; q < NB + int64_t(PD) && q < a.M; ++q)
+          for (int64_t q = NB; q < NB + int64_t(PD) && q < M; ++q)
             for (int p = 0; p < pc; ++p) {
               const int rest = seg_units - p * kOcPieceUnits;
-              oc_prefetch_l2(a.x + q * a.row_bytes + seg_start * 16 + int64_t(p) * kOcPieceBytes,
+              oc_prefetch_l2(a.x + row_of(q) * a.row_bytes + seg_start * 16 + int64_t(p) * kOcPieceBytes,
                              uint32_t(rest < kOcPieceUnits ? rest : kOcPieceUnits) * 16u, keep);
             }
         for (int p = 0; p < pc; ++p) {
@@ -318,12 +326,14 @@ __global__ void __launch_bounds__(kOcThreads, 1) k_splitrow_onchip(OnchipArgs a)
           mbar_arrive_expect_tx(bar, bytes);
           bulk_g2s(bufs + uint32_t(b) * a.buf_bytes + uint32_t(p) * kOcPieceBytes, src + int64_t(p) * kOcPieceBytes,
                    bytes, bar, drop);
-          if (pf) oc_prefetch_l2(src + int64_t(PD) * a.row_bytes + int64_t(p) * kOcPieceBytes, bytes, keep);
+          if (pf)
+            oc_prefetch_l2(a.x + row_of(r + PD) * a.row_bytes + seg_start * 16 + int64_t(p) * kOcPieceBytes, bytes,
+                           keep);
         }
         ring.next();
       }
       // no copy may still be in flight when the CTA exits: the last copy of every piece has landed
-      for (int64_t r = a.M > NB ? a.M - NB : 0; r < a.M; ++r) {
+      for (int64_t r = M > NB ? M - NB : 0; r < M; ++r) {
         const int rb = int(r % NB);
         const uint32_t par = uint32_t((r / NB) & 1);
         for (int p = 0; p < pc; ++p)
@@ -336,7 +346,7 @@ __global__ void __launch_bounds__(kOcThreads, 1) k_splitrow_onchip(OnchipArgs a)
     // warp's polling round trips), in row order.
     if (crank == 0 && lane == 0) {
       OcRing ring(RB);
-      for (int64_t r = 0; r < a.M; ++r) {
+      for (int64_t r = 0; r < M; ++r) {
         const uint32_t bar = smem_addr(&cbar[ring.idx]);
         if (!mbar_wait_cluster(bar, ring.parity(), lim)) {
           timed_out = true;
@@ -344,15 +354,24 @@ __global__ void __launch_bounds__(kOcThreads, 1) k_splitrow_onchip(OnchipArgs a)
         }
         State cs = empty_state();
         for (uint32_t i = 0; i < csize; ++i) cs = merge(cs, cstate[ring.idx * kOcMaxCluster + i]);
-        if (!(a.fault && cid == 0)) oc_st_release_u64(a.pub + r * ncl + cid, oc_pack(cs));
-        if (r + RB < a.M) mbar_arrive_expect_tx(bar, csize * 8u);
+        if (!(a.fault && cid == 0)) {
+          if (local) {  // the row state into every CTA of the cluster, released by a remote arrive
+            for (uint32_t q = 0; q < csize; ++q) {
+              st_cluster_f32x2(map_to_rank(smem_addr(&rowst[ring.idx]), q), cs.m, cs.d);
+              mbar_arrive_remote(map_to_rank(smem_addr(&row_ready[ring.idx]), q));
+            }
+          } else {
+            oc_st_release_u64(a.pub + r * ncl + cid, oc_pack(cs));
+          }
+        }
+        if (r + RB < M) mbar_arrive_expect_tx(bar, csize * 8u);
         ring.next();
       }
     }
   } else if (warp == kOcExchangeWarp) {
     bool abort = false;
     OcRing ring(RB);
-    for (int64_t r = 0; r < a.M; ++r) {
+    for (int64_t r = 0; r < (local ? 0 : M); ++r) {
       const int b = ring.idx;
       // every exit from this loop is taken by the whole warp: lane 0 alone reads the clock and
       // decides when the wait has run out (lanes that read the clock themselves could disagree at
@@ -411,7 +430,7 @@ __global__ void __launch_bounds__(kOcThreads, 1) k_splitrow_onchip(OnchipArgs a)
     };
     // y = e^(x - m) / d for the four units of piece p held in q (unit p * kOcPieceUnits + i * kOcNct + tid)
     auto store_piece = [&](int64_t r, int p, const uint4 (&q)[kOcUpt], float2 nms, float2 inv2) {
-      unsigned char* yp = a.y + r * a.row_bytes + (seg_start + int64_t(p) * kOcPieceUnits) * 16;
+      unsigned char* yp = a.y + row_of(r) * a.row_bytes + (seg_start + int64_t(p) * kOcPieceUnits) * 16;
       const int rest = seg_units - p * kOcPieceUnits;
 #pragma unroll
       for (int i = 0; i < kOcUpt; ++i) {
@@ -425,17 +444,23 @@ __global__ void __launch_bounds__(kOcThreads, 1) k_splitrow_onchip(OnchipArgs a)
         }
       }
     };
-    // row r's state (slot `sb` of the state ring), and its outputs from CTA 0
+    // row r's state (slot `sb` of the state ring), and its outputs from CTA 0 (rank 0 in local
+    // mode, where the state arrives from rank 0 over DSMEM: a cluster-scope acquire, bounded by the
+    // exchange limit)
     auto row_state = [&](int64_t r, const OcRing& st_ring) {
-      if (!mbar_wait(smem_addr(&row_ready[st_ring.idx]), st_ring.parity(), lim)) {
+      const uint32_t bar = smem_addr(&row_ready[st_ring.idx]);
+      const bool ok = local ? mbar_wait_cluster(bar, st_ring.parity(), lim == 0 ? 0 : a.exchange_wait_ns)
+                            : mbar_wait(bar, st_ring.parity(), lim);
+      if (!ok) {
         timed_out = true;
         lim = 0;
       }
       const State row = rowst[st_ring.idx];
       if (c == 0 && tid == 0) {
-        if (a.m_out) a.m_out[r] = row.m;
-        if (a.d_out) a.d_out[r] = row.d;
-        if (a.lse_out) a.lse_out[r] = lse_of(row);
+        const int64_t gr = row_of(r);
+        if (a.m_out) a.m_out[gr] = row.m;
+        if (a.d_out) a.d_out[gr] = row.d;
+        if (a.lse_out) a.lse_out[gr] = lse_of(row);
       }
       return row;
     };
@@ -464,13 +489,13 @@ __global__ void __launch_bounds__(kOcThreads, 1) k_splitrow_onchip(OnchipArgs a)
       const int lag = NB - 1;
       OcRing fbuf(NB), fst(RB), nbuf(NB), nst(RB);
       int64_t j = 0;  // next row to fold
-      for (; j < lag && j < a.M; ++j) {
+      for (; j < lag && j < M; ++j) {
         fold_row(j, fbuf, fst.idx);
         fbuf.next();
         fst.next();
       }
-      for (int64_t r = 0; r < a.M; ++r) {
-        if (j < a.M) {
+      for (int64_t r = 0; r < M; ++r) {
+        if (j < M) {
           fold_row(j, fbuf, fst.idx);
           ++j;
           fbuf.next();
@@ -481,12 +506,12 @@ __global__ void __launch_bounds__(kOcThreads, 1) k_splitrow_onchip(OnchipArgs a)
         nst.next();
       }
     } else {
-      // Rows in flight at the start of iteration r: r and r + 1 parked in tensor memory (slots
-      // r mod 2, r + 1 mod 2), r + 2 folded in shared-memory buffer r mod 2, r + 3 landing in the
-      // other buffer.  Iteration r, piece by piece: normalise piece p of row r from its slot, then
-      // park piece p of row r + 2 in its place and free that piece of the buffer (row r + 4's
-      // piece is loaded there at once); then fold r + 3.  A row's state has two iterations to
-      // arrive, and a buffer's load about one and a half.
+      // Two shared-memory buffers: rows in flight at the start of iteration r are r and r + 1
+      // parked in tensor memory (slots r mod 2, r + 1 mod 2), r + 2 folded in shared-memory buffer
+      // r mod 2, r + 3 landing in the other buffer.  Iteration r, piece by piece: normalise piece p
+      // of row r from its slot, then park piece p of row r + 2 in its place and free that piece of
+      // the buffer (row r + 4's piece is loaded there at once); then fold r + 3.  A row's state has
+      // two iterations to arrive, and a buffer's load about one and a half.
       const uint32_t tmem = *tmem_slot;
       const uint32_t tlane = uint32_t(32 * (warp & 3)) << 16;
       const uint32_t tcol = uint32_t(warp >> 2) * kOcWarpCols;
@@ -508,34 +533,28 @@ __global__ void __launch_bounds__(kOcThreads, 1) k_splitrow_onchip(OnchipArgs a)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&freed[buf.idx * P + p]));
       };
-      OcRing fbuf(2), fst(RB);  // next row to fold: its buffer and state slot
-      OcRing pbuf(2);           // next row to park: its buffer
-      OcRing nst(RB);           // next row to normalise: its state slot
-      int64_t jf = 0, jp = 0;   // next rows to fold and to park
+      OcRing fbuf(NB), fst(RB);  // next row to fold: its buffer and state slot
+      OcRing pbuf(NB);           // next row to park: its buffer
+      OcRing nst(RB);            // next row to normalise: its state slot
+      int64_t jf = 0, jp = 0;    // next rows to fold and to park
       auto fold_next = [&]() {
-        if (jf < a.M) {
+        if (jf < M) {
           fold_row(jf, fbuf, fst.idx);
           ++jf;
           fbuf.next();
           fst.next();
         }
       };
-      auto park_next = [&]() {  // a whole row (the first two rows)
-        if (jp < a.M) {
+      auto park_next = [&]() {  // a whole row
+        if (jp < M) {
           for (int p = 0; p < pc; ++p) park_piece(pbuf, int(jp & 1), p);
           oc_tmem_wait_st();
           ++jp;
           pbuf.next();
         }
       };
-      fold_next();  // row 0
-      park_next();
-      fold_next();  // row 1
-      park_next();
-      fold_next();  // row 2
-      for (int64_t r = 0; r < a.M; ++r) {
+      auto normalise_parked = [&](int64_t r, bool park_behind) {
         const int slot = int(r & 1);
-        const bool park = jp < a.M;  // row jp = r + 2 follows row r into its slot
         const State row = row_state(r, nst);
         nst.next();
         const float ms = safe_max(row.m);
@@ -547,14 +566,35 @@ __global__ void __launch_bounds__(kOcThreads, 1) k_splitrow_onchip(OnchipArgs a)
           oc_tmem_ld16(taddr(slot, p), q);
           oc_tmem_wait_ld();
           store_piece(r, p, q, nms, inv2);
-          if (park) park_piece(pbuf, slot, p);
+          if (park_behind) park_piece(pbuf, slot, p);
         }
-        if (park) {
+        if (park_behind) {
           oc_tmem_wait_st();
           ++jp;
           pbuf.next();
         }
-        fold_next();  // row r + 3
+      };
+      if (NB >= 2) {
+        fold_next();  // row 0
+        park_next();
+        fold_next();  // row 1
+        park_next();
+        fold_next();  // row 2
+        for (int64_t r = 0; r < M; ++r) {
+          normalise_parked(r, jp < M);  // row jp = r + 2 follows row r into its slot, piece by piece
+          fold_next();                  // row r + 3
+        }
+      } else {
+        // One shared-memory buffer (segments of up to 128 KB).  Iteration r: park r + 1 in the slot
+        // row r - 1 left (its buffer is then loaded with row r + 2), normalise r, fold r + 2.
+        fold_next();  // row 0
+        park_next();
+        fold_next();  // row 1
+        for (int64_t r = 0; r < M; ++r) {
+          park_next();  // row r + 1
+          normalise_parked(r, false);
+          fold_next();  // row r + 2
+        }
       }
       // every consumer is done with tensor memory before it is released
       oc_tc_fence_before();
@@ -632,19 +672,47 @@ OnchipPlan onchip_plan(int dtype, const DeviceInfo& dev) {
   return best;
 }
 
-bool hold_fits(int64_t buf, int64_t pieces, size_t cap) {
-  return size_t(2) * size_t(buf) + onchip_tail_bytes(2, 4, int(pieces)) <= cap;
-}
-
 struct OnchipShape {
   bool ok = false;
-  bool hold = false;  // segments parked in tensor memory (two shared-memory buffers)
+  bool hold = false;  // segments parked in tensor memory (one or two shared-memory buffers)
+  bool local = false;
   int nb = 0, rb = 0, pieces = 0;
   uint32_t buf_bytes = 0;
   size_t smem = 0;
-  int G = 0, cluster = 0;
+  int G = 0, cluster = 0;  // CTAs launched, CTAs per cluster
 };
 
+// Buffers for segments of up to seg_max units: as many shared-memory buffers as fit (up to 8); with
+// two, folded segments are parked in tensor memory (two slots of kOcWarpCols columns per warp), and
+// with one too when `one_buffer` allows it.  False when the segments do not fit.
+bool segment_buffers(int64_t seg_max, int64_t rows, size_t cap, bool one_buffer, OnchipShape* s) {
+  const int64_t pieces = (seg_max + kOcPieceUnits - 1) / kOcPieceUnits;
+  if (pieces > kOcMaxPieces) return false;
+  const int64_t buf = (seg_max * 16 + 127) / 128 * 128;
+  const bool parkable = pieces * kOcUpt * 4 <= int64_t(kOcWarpCols);
+  int nb = kOcMaxBufs;
+  while (nb >= 1 && size_t(nb) * size_t(buf) + onchip_tail_bytes(nb, nb < 3 ? 4 : nb, int(pieces)) > cap) --nb;
+  if (nb >= 3) {
+    // fold NB - 1 rows ahead
+    if (rows < nb) nb = int(rows < 2 ? 2 : rows);
+    s->hold = false;
+    s->rb = nb;
+  } else if (parkable && (nb == 2 || (nb == 1 && one_buffer))) {
+    // park folded segments in tensor memory (rows r .. r + 3 in flight with two buffers, r .. r + 2
+    // with one)
+    s->hold = true;
+    s->rb = 4;
+  } else {
+    return false;
+  }
+  s->nb = nb;
+  s->pieces = int(pieces);
+  s->buf_bytes = uint32_t(buf);
+  s->smem = size_t(nb) * size_t(buf) + onchip_tail_bytes(nb, s->rb, int(pieces));
+  return true;
+}
+
+// Split mode: one row over every CTA of the grid.
 OnchipShape onchip_shape(const RowProblem& p, const DeviceInfo& dev) {
   OnchipShape s;
   const int64_t row_bytes = p.N * elem_bytes(p.dtype);
@@ -655,46 +723,97 @@ OnchipShape onchip_shape(const RowProblem& p, const DeviceInfo& dev) {
   const int64_t units = row_bytes / 16;
   if (units < G * 64) return s;  // rows this short belong to the one-read row kernels
   const int64_t seg_max = (units + G - 1) / G;
-  const int64_t pieces = (seg_max + kOcPieceUnits - 1) / kOcPieceUnits;
-  if (pieces > kOcMaxPieces) return s;
-  const int64_t buf = (seg_max * 16 + 127) / 128 * 128;
-  const size_t cap = size_t(dev.max_smem_per_block_optin);
-  int nb = kOcMaxBufs;
-  while (nb >= 2 && size_t(nb) * size_t(buf) + onchip_tail_bytes(nb, nb, int(pieces)) > cap) --nb;
-  if (nb < 2) return s;
-  int rb = nb;
-  bool hold = false;
-  if (nb == 2 && pieces * kOcUpt * 4 <= int64_t(kOcWarpCols) && hold_fits(buf, pieces, cap)) {
-    // two buffers only: park folded segments in tensor memory so that a row's state has two
-    // iterations to arrive (rows r .. r + 3 in flight)
-    hold = true;
-    rb = 4;
-  } else if (p.M < nb) {
-    nb = int(p.M < 2 ? 2 : p.M);
-    rb = nb;
-  }
+  if (!segment_buffers(seg_max, p.M, size_t(dev.max_smem_per_block_optin), false, &s)) return s;
   s.ok = true;
-  s.hold = hold;
-  s.nb = nb;
-  s.rb = rb;
-  s.pieces = int(pieces);
-  s.buf_bytes = uint32_t(buf);
-  s.smem = size_t(nb) * size_t(buf) + onchip_tail_bytes(nb, rb, int(pieces));
   s.G = int(G);
   s.cluster = plan.cluster;
   return s;
 }
 
-}  // namespace
+// Local mode: resident clusters of 2, 4, 8 and 16 CTAs (one CTA per SM), per device and element type.
+// Clusters of 16 are not used (measured, 300 x 2 MiB fp32 rows held on chip by clusters of 16:
+// 305 us against 239 us for the cluster-row two passes).
+constexpr int kOcLocalSizes[4] = {2, 4, 8, 16};
+constexpr int kOcLocalMaxCluster = 8;
+struct LocalPlan {
+  int n[4] = {0, 0, 0, 0};
+};
+std::mutex g_ocl_mutex;
+LocalPlan g_ocl[64][3];
+bool g_ocl_ready[64][3];
 
-bool splitrow_onchip_fits(const RowProblem& p, const DeviceInfo& dev) { return onchip_shape(p, dev).ok; }
+LocalPlan local_plan(int dtype, const DeviceInfo& dev) {
+  std::lock_guard<std::mutex> lock(g_ocl_mutex);
+  const bool cache = dev.device >= 0 && dev.device < 64;
+  if (cache && g_ocl_ready[dev.device][dtype]) return g_ocl[dev.device][dtype];
+  LocalPlan lp;
+  if (dev.cluster_launch) {
+    const size_t smem = size_t(dev.max_smem_per_block_optin);
+    for (bool hold : {false, true}) {  // both instances may launch clusters of 16
+      OnchipKernel fn = onchip_kernel(dtype, hold);
+      if (cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess ||
+          cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+        cudaGetLastError();
+    }
+    OnchipKernel fn = onchip_kernel(dtype, false);
+    for (int i = 0; i < 4; ++i) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = kOcLocalSizes[i];
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(kOcLocalSizes[i]);
+      cfg.blockDim = dim3(kOcThreads);
+      cfg.dynamicSmemBytes = smem;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, (const void*)fn, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+      }
+      lp.n[i] = n;
+    }
+  }
+  if (cache) {
+    g_ocl[dev.device][dtype] = lp;
+    g_ocl_ready[dev.device][dtype] = true;
+  }
+  return lp;
+}
 
-cudaError_t launch_splitrow_onchip(const RowProblem& p, const DeviceInfo& dev, unsigned long long* pub) {
-  const OnchipShape s = onchip_shape(p, dev);
-  if (!s.ok) return cudaErrorInvalidConfiguration;
+// Local mode: the smallest cluster whose segments fit on chip (one shared-memory buffer with
+// tensor-memory parking at the least), as many resident clusters as the occupancy query reports.
+OnchipShape onchip_local_shape(const RowProblem& p, const DeviceInfo& dev) {
+  OnchipShape s;
+  const int64_t row_bytes = p.N * elem_bytes(p.dtype);
+  if (row_bytes % 16 != 0 || p.y == nullptr || p.labels || p.loss || p.log_out) return s;
+  if ((p.x_pitch && p.x_pitch != row_bytes) || (p.y_pitch && p.y_pitch != row_bytes) || p.scale != 1.f) return s;
+  const int64_t units = row_bytes / 16;
+  const LocalPlan lp = local_plan(p.dtype, dev);
+  for (int i = 0; i < 4; ++i) {
+    const int cs = kOcLocalSizes[i];
+    if (cs > kOcLocalMaxCluster || lp.n[i] < 1 || units < int64_t(cs) * 64) continue;
+    const int64_t clusters = p.M < lp.n[i] ? p.M : lp.n[i];
+    const int64_t rows = (p.M + clusters - 1) / clusters;  // rows of the busiest cluster
+    if (!segment_buffers((units + cs - 1) / cs, rows, size_t(dev.max_smem_per_block_optin), true, &s)) continue;
+    s.ok = true;
+    s.local = true;
+    s.G = int(clusters * cs);
+    s.cluster = cs;
+    return s;
+  }
+  return s;
+}
+
+cudaError_t launch_onchip(const RowProblem& p, const DeviceInfo& dev, const OnchipShape& s, unsigned long long* pub) {
   OnchipKernel fn = onchip_kernel(p.dtype, s.hold);
   cudaError_t err = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(s.smem));
   if (err != cudaSuccess) return err;
+  if (s.cluster > 8 &&
+      (err = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
+    return err;
   OnchipArgs a;
   a.x = static_cast<const unsigned char*>(p.x);
   a.y = static_cast<unsigned char*>(p.y);
@@ -713,6 +832,7 @@ cudaError_t launch_splitrow_onchip(const RowProblem& p, const DeviceInfo& dev, u
   a.local_wait_ns = local_wait_limit_ns();
   a.exchange_wait_ns = exchange_wait_limit_ns();
   a.fault = debug_fault();
+  a.local = s.local ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -726,6 +846,24 @@ cudaError_t launch_splitrow_onchip(const RowProblem& p, const DeviceInfo& dev, u
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, fn, a);
+}
+
+}  // namespace
+
+bool splitrow_onchip_fits(const RowProblem& p, const DeviceInfo& dev) { return onchip_shape(p, dev).ok; }
+
+cudaError_t launch_splitrow_onchip(const RowProblem& p, const DeviceInfo& dev, unsigned long long* pub) {
+  const OnchipShape s = onchip_shape(p, dev);
+  if (!s.ok) return cudaErrorInvalidConfiguration;
+  return launch_onchip(p, dev, s, pub);
+}
+
+bool clusterrow_onchip_fits(const RowProblem& p, const DeviceInfo& dev) { return onchip_local_shape(p, dev).ok; }
+
+cudaError_t launch_clusterrow_onchip(const RowProblem& p, const DeviceInfo& dev) {
+  const OnchipShape s = onchip_local_shape(p, dev);
+  if (!s.ok) return cudaErrorInvalidConfiguration;
+  return launch_onchip(p, dev, s, nullptr);
 }
 
 int splitrow_onchip_clusters(const RowProblem& p, const DeviceInfo& dev) {

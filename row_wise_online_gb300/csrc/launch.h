@@ -87,6 +87,11 @@ bool splitrow_onchip_fits(const RowProblem& p, const DeviceInfo& dev);
 int splitrow_onchip_clusters(const RowProblem& p, const DeviceInfo& dev);
 cudaError_t launch_splitrow_onchip(const RowProblem& p, const DeviceInfo& dev, unsigned long long* pub);
 cudaError_t launch_splitrow_onchip_pooled(const RowProblem& p, const DeviceInfo& dev);
+// The same kernel with each thread-block cluster owning whole rows (rows k, k + clusters, ... for
+// cluster k; 16-byte aligned contiguous rows, y written, softmax without scale): the row's CTA states
+// merged over DSMEM only.  For many long rows (~256 KiB - 2 MiB).
+bool clusterrow_onchip_fits(const RowProblem& p, const DeviceInfo& dev);
+cudaError_t launch_clusterrow_onchip(const RowProblem& p, const DeviceInfo& dev);
 // Publication slots the streaming split-row kernel needs (M x its clusters).
 size_t splitrow_slots(const RowProblem& p, const DeviceInfo& dev);
 

@@ -51,12 +51,87 @@ def test_clusterrow_against_oracle(dtype, M, N, variant):
     check_state(m.cpu().numpy(), d.cpu().numpy(), lse.cpu().numpy(), m_ref, d_ref, lse_ref, what)
 
 
-def test_auto_takes_two_passes_for_many_long_rows():
+def test_auto_holds_many_long_rows_on_chip():
+    """Many 1 MiB rows: AUTO takes a thread-block cluster per row with its segments held on chip
+    (reported as ONEREAD_SMEM); forced TWOPASS keeps the cluster-row two passes."""
     w = synth.custom("crow-auto", synth.F32, 300, 1 << 18, seed=3, p1=3.0)
-    x = to_device(synth.generate(w))
-    rwo.softmax_rows(x)
-    torch.cuda.synchronize()
-    assert rwo.last_variant() == rwo.VARIANT_TWOPASS
+    x_host = synth.generate(w)
+    x = to_device(x_host)
+    y = rwo.softmax_rows(x)
+    assert rwo.get_status() == rwo.OK
+    assert rwo.last_variant() == rwo.VARIANT_ONEREAD_SMEM
+    pick = [0, 151, 152, 299]
+    y_ref, *_ = oracle.softmax_rows(x_host[pick])
+    check_y(to_host(y)[pick], y_ref, synth.F32, "cluster rows on chip (sampled rows)")
+    check_rowsums(to_host(y), synth.F32, None, "cluster rows on chip")
+    rwo.softmax_rows_ex(x, variant=rwo.VARIANT_TWOPASS)
+    assert rwo.get_status() == rwo.OK and rwo.last_variant() == rwo.VARIANT_TWOPASS
+
+
+@pytest.mark.parametrize("dtype,M,N", [
+    (synth.F32, 300, 1 << 18),     # 1 MiB rows: clusters of 8, one shared-memory buffer + tensor memory
+    (synth.F32, 37, 1 << 17),      # 512 KiB rows, fewer rows than clusters for some
+    (synth.BF16, 160, 1 << 18),    # 512 KiB rows
+    (synth.F32, 64, 150_000),      # 600 KB rows, ragged segments
+    (synth.F16, 41, 80_000),       # 160 KB rows
+    (synth.F32, 90, 262_140),      # just below 1 MiB: ragged segments over clusters of 8
+])
+def test_cluster_rows_held_on_chip_against_oracle(dtype, M, N):
+    w = synth.custom("crow-oc", dtype, M, N, seed=N % 991 + M, dist=synth.UNIFORM, p0=-20.0, p1=20.0, late_max=20.0)
+    x_host = synth.generate(w)
+    x = to_device(x_host, dtype)
+    y, m, d, lse = run_softmax(x, rwo.VARIANT_ONEREAD_SMEM)
+    assert rwo.last_variant() == rwo.VARIANT_ONEREAD_SMEM
+    what = f"cluster rows on chip {M}x{N}"
+    y_ref, m_ref, d_ref, lse_ref = oracle.softmax_rows(x_host, dtype=dtype)
+    yh = to_host(y)
+    check_y(yh, y_ref, dtype, what)
+    check_rowsums(yh, dtype, None, what)
+    check_state(m.cpu().numpy(), d.cpu().numpy(), lse.cpu().numpy(), m_ref, d_ref, lse_ref, what)
+
+
+def test_cluster_rows_on_chip_limit():
+    """Rows just above 1 MiB do not fit the segments of a cluster of 8 on chip: the forced one-read
+    variant reports SOFTMAX_ERR_UNSUPPORTED (AUTO takes the two passes)."""
+    x = torch.zeros((4, 262_148), device="cuda")
+    with pytest.raises(rwo.SoftmaxError) as ei:
+        rwo.softmax_rows_ex(x, variant=rwo.VARIANT_ONEREAD_SMEM)
+    assert ei.value.status == rwo.ERR_UNSUPPORTED
+    rwo.softmax_rows_ex(x)
+    assert rwo.get_status() == rwo.OK
+
+
+def test_cluster_rows_held_on_chip_special_rows_and_timeout():
+    """Masked segments, a fully masked row, one huge value, NaN and +inf rows beside correct rows;
+    then a cluster whose rank 0 never hands over its row states: its CTAs' waits run out
+    (SOFTMAX_ERR_TIMEOUT), the kernel ends, and the next launch is correct."""
+    M, N = 160, 1 << 18
+    rows = np.random.default_rng(6).standard_normal((M, N)).astype(np.float32) * 3
+    rows[0, : N - 1000] = -np.inf
+    rows[1, 1000:] = -np.inf
+    rows[2, :] = -np.inf
+    rows[3, N // 2] = 1e30
+    rows[5, 77] = np.nan
+    rows[6, 99] = np.inf
+    x = to_device(rows)
+    y, m, d, lse = run_softmax(x, rwo.VARIANT_ONEREAD_SMEM)  # status OK
+    good = [i for i in range(M) if i not in (5, 6)]
+    y_ref, m_ref, d_ref, lse_ref = oracle.softmax_rows(rows[good])
+    yh = to_host(y)
+    check_y(yh[good], y_ref, synth.F32, "cluster rows on chip special")
+    assert np.all(yh[2] == 0.0)
+    assert np.isnan(d.cpu().numpy()[5]) and np.isnan(d.cpu().numpy()[6])
+    old_limit = rwo.debug_set_wait_limit_ns(20_000_000)  # 20 ms
+    old_fault = rwo.debug_set_fault(1)
+    try:
+        rwo.softmax_rows_ex(x, y, variant=rwo.VARIANT_ONEREAD_SMEM)
+        assert rwo.get_status() == rwo.ERR_TIMEOUT
+    finally:
+        rwo.debug_set_fault(old_fault)
+        rwo.debug_set_wait_limit_ns(old_limit)
+    rwo.softmax_rows_ex(x, y, variant=rwo.VARIANT_ONEREAD_SMEM)
+    assert rwo.get_status() == rwo.OK
+    check_y(to_host(y)[good], y_ref, synth.F32, "cluster rows on chip after timeout")
 
 
 def test_clusterrow_masked_segments_and_special_rows():

@@ -200,7 +200,7 @@ def test_host_buffers_staged_very_long_rows():
     yt = torch.empty_like(xt)
     rwo.softmax_rows_host(xt, yt)
     assert rwo.get_status() == rwo.OK
-    assert rwo.last_variant() == rwo.VARIANT_TWOPASS
+    assert rwo.last_variant() not in (rwo.VARIANT_SPLITROW, rwo.VARIANT_SPLITROW_STREAM)
     y_ref, *_ = oracle.softmax_rows(x_host)
     check_y(yt.numpy(), y_ref, w.dtype, "host pipeline, 1 MiB rows")
 
