@@ -192,3 +192,33 @@ def test_splitrow_nan_and_inf_rows_stay_in_their_row(variant, N):
     dh = d.cpu().numpy()
     assert np.isnan(dh[1]) and np.isnan(dh[2])
     assert np.isnan(yh[1]).any() and np.isnan(yh[2]).any()
+
+
+def test_splitrow_replayed_from_a_cuda_graph():
+    """Captured in a CUDA graph, each on-chip split-row call becomes a pool allocation, a memset and
+    a free around the kernel: launches replayed back to back, with rows of another length in
+    between, all match the oracle on every replay."""
+    ws = [synth.custom("split-graph", synth.F32, 6, 1 << 22, seed=60 + i, dist=synth.UNIFORM, p0=-20.0, p1=20.0,
+                       late_max=20.0) for i in range(2)]
+    hosts = [synth.generate(w) for w in ws]
+    xs = [to_device(h) for h in hosts]
+    ys = [torch.empty_like(x) for x in xs]
+    short = to_device(synth.generate(synth.custom("split-graph-short", synth.F32, 3, 1 << 21, seed=62)))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):  # one eager call first (the kernel's attributes are set outside the capture)
+        rwo.softmax_rows_ex(xs[0], ys[0], variant=rwo.VARIANT_SPLITROW, stream=s)
+        assert rwo.last_variant() == rwo.VARIANT_SPLITROW
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in (0, 1, 0):
+            rwo.softmax_rows_ex(xs[i], ys[i], variant=rwo.VARIANT_SPLITROW, stream=s)
+            rwo.softmax_rows_ex(short, variant=rwo.VARIANT_SPLITROW, stream=s)
+    for _ in range(3):
+        for y in ys:
+            y.fill_(float("nan"))
+        g.replay()
+        assert rwo.get_status(s) == rwo.OK
+        for h, y in zip(hosts, ys):
+            y_ref, *_ = oracle.softmax_rows(h)
+            check_y(to_host(y), y_ref, synth.F32, "split row replayed from a graph")
