@@ -204,11 +204,12 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
-// Keys at or past the row's limit count as -inf.
-__device__ __forceinline__ void mask_keys(uint32_t (&sv)[64], int64_t key0, int64_t klim) {
+// Keys i >= vis of a run of 64 keys count as -inf (vis: the row's visible keys from the run's
+// start; one 32-bit compare with a constant per key).
+__device__ __forceinline__ void mask_keys(uint32_t (&sv)[64], int vis) {
 #pragma unroll
   for (int i = 0; i < 64; ++i)
-    if (key0 + i >= klim) sv[i] = 0xff800000u;
+    if (i >= vis) sv[i] = 0xff800000u;
 }
 
 // 320 threads, at most 168 registers a thread: three warps share a sub-partition's 16K registers.
@@ -412,6 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the row maximum, half a row (64 keys) at a time: keys 64-127 first, so that keys 0-63 are
       // still in registers for the exponentials (their P goes over columns 0-31, which they held)
       const bool masked = k0 + kBN > kfull;  // uniform over the warpgroup
+      const int vis = int(klim - k0 < 0 ? 0 : klim - k0 > kBN ? kBN : klim - k0);  // visible keys of the tile
       uint32_t sv[64];
       float mx[8];
 #pragma unroll
@@ -421,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = 1 - hh;
         tmem_ld64_nowait(ts + uint32_t(h * 64), sv);
         tmem_wait_ld();
-        if (masked) mask_keys(sv, k0 + h * 64, klim);
+        if (masked) mask_keys(sv, vis - h * 64);
 #pragma unroll
         for (int i = 0; i < 64; i += 2) mx[(i >> 1) & 7] = fmax3(mx[(i >> 1) & 7], __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
       }
@@ -452,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (h == 1) {  // keys 64-127 again (columns 64-127 are untouched by P)
           tmem_ld64_nowait(ts + 64u, sv);
           tmem_wait_ld();
-          if (masked) mask_keys(sv, k0 + 64, klim);
+          if (masked) mask_keys(sv, vis - 64);
         }
         uint32_t pk[32];
 #pragma unroll
