@@ -141,20 +141,17 @@ int run_variant(RowProblem& p, int variant, const DeviceInfo& dev) {
   if (variant == SOFTMAX_VARIANT_AUTO) {
     if (aligned) {
       // Measured on GB300: warp-per-row bulk-copy kernel for many rows of 2-8 KiB, register
-      // kernel for shorter rows, for few rows, for 8-16 KiB rows and for fp32 rows up to 32 KiB
-      // (fp32 20-32 KiB rows: 6.87-6.90 TB/s against 5.69-5.92 on the bulk-copy kernel; 16-bit
-      // rows of 24-32 KiB the other way round, 4.8-4.9 against 5.9-6.0), CTA bulk-copy kernel
-      // for the other rows up to 64 KiB.
+      // kernel for shorter rows, for few rows, for 8-16 KiB rows and for fp32 rows up to 64 KiB
+      // (fp32, 8192 rows: 20-32 KiB 6.87-6.90 TB/s against 5.69-5.92 on the bulk-copy kernel,
+      // 40 KiB 6.88 against 6.54, 48 KiB 6.88 against 5.96, 56 KiB 6.86 against 5.79 on two
+      // passes, 64 KiB 6.88 against 6.21; 16-bit rows the other way round: 24-32 KiB 4.8-4.9
+      // against 5.9-6.0, bf16 48 KiB 5.08 against 5.86, 64 KiB 3.94 against 6.70), CTA
+      // bulk-copy kernel for the other rows up to 64 KiB.
       if (row_bytes > 2048 && row_bytes <= 8192 && p.M >= 4 * int64_t(dev.sm_count) &&
           oneread_warp_fits(p, dev))
         variant = SOFTMAX_VARIANT_ONEREAD_SMEM;
-      else if ((row_bytes <= 16384 || (p.dtype == SOFTMAX_F32 && row_bytes <= 32768)) && oneread_reg_fits(p, true))
+      else if ((row_bytes <= 16384 || (p.dtype == SOFTMAX_F32 && row_bytes <= 65536)) && oneread_reg_fits(p, true))
         variant = SOFTMAX_VARIANT_ONEREAD_REG;
-      else if (p.dtype == SOFTMAX_F32 && row_bytes > 53248 && row_bytes <= 65536)
-        // fp32 rows of 52-64 KiB: two passes beat the CTA bulk-copy kernel (measured, ~640 MB per
-        // launch: 56 KiB 5.83 against 5.77 TB/s, 60 KiB 6.04 against 5.78, 64 KiB 6.18 against
-        // 5.82; 16-bit rows stay far faster with one read: fp16 64 KiB 6.68 against 5.34)
-        variant = SOFTMAX_VARIANT_TWOPASS;
       else if (oneread_tma_fits(p, dev))
         variant = SOFTMAX_VARIANT_ONEREAD_SMEM;
       else if (!p.shares_gpu && (row_bytes >= (int64_t(8) << 20) || (row_bytes >= (int64_t(4) << 20) && p.M <= 16)) &&
@@ -514,9 +511,9 @@ int softmax_rows_host(const void* x_host, void* y_host, int64_t M, int64_t N, in
   const int64_t row_bytes = N * elem_bytes(dtype);
 
   // Page-locked host buffers are directly addressable by the GPU (over NVLink-C2C on a
-  // Grace-Blackwell node).  When both are, and the register kernel takes the rows, that kernel
-  // reads x and writes y in host memory itself: no staging copies, one pass over the link each
-  // way.  It uses plain loads and stores only.
+  // Grace-Blackwell node).  When both are, and the rows are at most 32 KiB (the register kernel's
+  // range measured on this path), the register kernel reads x and writes y in host memory itself:
+  // no staging copies, one pass over the link each way.  It uses plain loads and stores only.
   {
     void* dx = nullptr;
     void* dy = nullptr;
@@ -531,7 +528,7 @@ int softmax_rows_host(const void* x_host, void* y_host, int64_t M, int64_t N, in
       p.stream = user;
       p.host_mem = true;
       const bool aligned = aligned16(dx) && aligned16(dy) && row_bytes % 16 == 0;
-      if (oneread_reg_fits(p, aligned)) {
+      if (row_bytes <= 32768 && oneread_reg_fits(p, aligned)) {
         cudaError_t err = launch_oneread_reg(p, aligned, *dev);
         if (err == cudaSuccess) err = cudaStreamSynchronize(user);
         if (err != cudaSuccess) return cuda_fail(err);

@@ -165,7 +165,8 @@ constexpr RegConfig reg_cfg() {
 
 // Ordered by capacity (units per row = 32 * wpr * vpt).
 const RegConfig kRegVec[] = {reg_cfg<2, 1, true>(), reg_cfg<4, 1, true>(), reg_cfg<8, 1, true>(),
-                             reg_cfg<8, 2, true>(), reg_cfg<8, 4, true>(), reg_cfg<8, 8, true>()};
+                             reg_cfg<8, 2, true>(), reg_cfg<8, 4, true>(), reg_cfg<8, 8, true>(),
+                             reg_cfg<12, 8, true>(), reg_cfg<16, 8, true>()};
 const RegConfig kRegScalar[] = {reg_cfg<4, 1, false>(), reg_cfg<16, 1, false>(),
                                 reg_cfg<8, 8, false>()};
 

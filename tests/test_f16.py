@@ -34,7 +34,8 @@ def _run(x, variant):
     return y, m, d, lse
 
 
-@pytest.mark.parametrize("M,N", [(64, 1024), (1000, 1000), (700, 4104), (300, 32768), (33, 40000), (5000, 2048)])
+@pytest.mark.parametrize("M,N", [(64, 1024), (1000, 1000), (700, 4104), (300, 32768), (33, 40000), (5000, 2048),
+                                 (77, 24584)])
 @pytest.mark.parametrize("variant", [V.VARIANT_AUTO, V.VARIANT_ONEREAD_REG, V.VARIANT_ONEREAD_SMEM, V.VARIANT_TWOPASS])
 def test_f16_softmax_against_oracle(M, N, variant):
     w = synth.custom("f16", F16, M, N, seed=500 + N, p1=3.0)

@@ -178,9 +178,11 @@ def test_host_buffers_staged_pipeline():
 @pytest.mark.parametrize("dtype,N,want", [
     (synth.F32, 8192, V.VARIANT_ONEREAD_REG),     # 32 KiB fp32 rows: one read into registers
     (synth.BF16, 16384, V.VARIANT_ONEREAD_SMEM),  # 32 KiB 16-bit rows: one read through shared memory
-    (synth.F32, 12288, V.VARIANT_ONEREAD_SMEM),   # 48 KiB rows: one read
-    (synth.F32, 16384, V.VARIANT_TWOPASS),        # 64 KiB fp32 rows: two passes measured faster
+    (synth.F32, 12288, V.VARIANT_ONEREAD_REG),    # 48 KiB fp32 rows: registers
+    (synth.F32, 16384, V.VARIANT_ONEREAD_REG),    # 64 KiB fp32 rows: registers (12 or 16 vectors a thread)
+    (synth.BF16, 24576, V.VARIANT_ONEREAD_SMEM),  # 48 KiB 16-bit rows: shared memory
     (synth.BF16, 32768, V.VARIANT_ONEREAD_SMEM),  # 64 KiB 16-bit rows: one read
+    (synth.F32, 16388, V.VARIANT_TWOPASS),        # just over 64 KiB of fp32: past every one-read kernel
 ])
 def test_auto_choice_around_64kib(dtype, N, want):
     w = synth.custom("auto64", dtype, 300, N, seed=N % 101, p1=3.0)
@@ -189,6 +191,18 @@ def test_auto_choice_around_64kib(dtype, N, want):
     assert rwo.last_variant() == want
     y_ref, *_ = oracle.softmax_rows(x_host)
     check_y(to_host(y), y_ref, dtype, f"auto {N}")
+
+
+@pytest.mark.parametrize("dtype,N", [(synth.F32, 8196), (synth.F32, 10244), (synth.F32, 12288),
+                                     (synth.F32, 16380), (synth.F32, 16384), (synth.BF16, 16392),
+                                     (synth.BF16, 32768)])
+def test_register_kernel_rows_of_32_to_64_kib(dtype, N):
+    """Rows past 32 KiB forced into registers (12 or 16 vectors a thread over 8 warps): ragged last
+    vectors, full rows, fp32 and bf16 (fp16 in its own file), with per-row state."""
+    w = synth.custom("reg64", dtype, 77, N, seed=N % 97, p1=4.0)
+    x_host = synth.generate(w)
+    _full_check(x_host, dtype, V.VARIANT_ONEREAD_REG, f"reg {N}")
+    assert rwo.last_variant() == V.VARIANT_ONEREAD_REG
 
 
 def test_host_buffers_staged_very_long_rows():
