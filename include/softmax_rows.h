@@ -75,11 +75,11 @@ enum softmax_variant {
   SOFTMAX_VARIANT_ONEREAD_REG = 1,
   /* One read: bulk copies (cp.async.bulk + mbarrier) stage whole rows in shared memory.  Rows
      up to 8 KiB: each warp owns a row at a time and a private ring of row slots that its lane 0
-     refills; longer rows (up to 64 KiB): a producer warp feeds a CTA-wide consumer group that
-     copies the row to registers and frees the slot at once; rows above 64 KiB (16-byte aligned,
-     up to 1 MiB): a thread-block cluster of 2-8 CTAs per row, each CTA's segment held in shared
-     and tensor memory until the row's state, merged over distributed shared memory, is known.
-     AUTO takes the last for many rows of 64 KiB - 1 MiB. */
+     refills; longer rows (up to 64 KiB, fp32 rows up to 128 KiB): a producer warp feeds a
+     CTA-wide consumer group that copies the row to registers and frees the slot at once; longer
+     rows (16-byte aligned, up to 1 MiB): a thread-block cluster of 2-8 CTAs per row, each CTA's
+     segment held in shared and tensor memory until the row's state, merged over distributed
+     shared memory, is known.  AUTO takes the last for many rows of 128 KiB - 1 MiB. */
   SOFTMAX_VARIANT_ONEREAD_SMEM = 2,
   /* Two passes over global memory: online fold with 128-bit loads, then re-read and normalise
      (any N; the re-read is served from L2 while the row is still resident).  Aligned rows above
@@ -93,8 +93,8 @@ enum softmax_variant {
      memory from the load until the normalisation, so x is read once: rows up to about 17 MB on
      a 152-SM GB300 (at least two segments per SM fit in shared memory; shorter rows keep up to
      eight in flight).  Longer rows run SOFTMAX_VARIANT_SPLITROW_STREAM instead (and
-     softmax_last_variant() reports that).  AUTO takes the split row for rows above 64 KiB when
-     there are at most half as many rows as SMs, and for rows of 8 MiB and more at any row count.
+     softmax_last_variant() reports that).  AUTO takes the split row for rows of 8 MiB and more at
+     any row count, and for rows of 4 MiB and more when there are at most 16 of them.
      It needs every cluster resident at once, so it must not share the GPU with other kernels
      (softmax_rows_host never uses it): kernels running beside it on other streams can keep
      clusters off the GPU until the exchange wait runs out (SOFTMAX_ERR_TIMEOUT, y undefined). */

@@ -269,13 +269,29 @@ constexpr TmaConfig tma_cfg() {
                      k_oneread_tma<F16, VPT, NCW, kTmaState>}}};
 }
 
-// Ordered by capacity (16-byte units per row = 32 * ncw * vpt).
-const TmaConfig kTma[] = {tma_cfg<2, 4>(), tma_cfg<4, 4>(), tma_cfg<4, 8>(), tma_cfg<8, 8>(),
-                          tma_cfg<8, 16>()};
+// fp32 rows of 64 - 128 KiB: 10, 12 or 16 vectors a thread over 16 warps (one CTA per SM); the
+// 16-bit types would hold up to 128 values a thread there, more than 544 threads' share of the
+// register file, and are left out.
+template <int VPT>
+constexpr TmaConfig tma_cfg_f32_wide() {
+  return TmaConfig{16, VPT,
+                   {{k_oneread_tma<F32, VPT, 16, kTmaProb>, nullptr, nullptr},
+                    {k_oneread_tma<F32, VPT, 16, kTmaLog>, nullptr, nullptr},
+                    {k_oneread_tma<F32, VPT, 16, kTmaState>, nullptr, nullptr}}};
+}
 
-const TmaConfig* pick_tma(int64_t units) {
+// Ordered by capacity (16-byte units per row = 32 * ncw * vpt).
+const TmaConfig kTma[] = {tma_cfg<2, 4>(),          tma_cfg<4, 4>(),          tma_cfg<4, 8>(),
+                          tma_cfg<8, 8>(),          tma_cfg<8, 16>(),         tma_cfg_f32_wide<10>(),
+                          tma_cfg_f32_wide<12>(),   tma_cfg_f32_wide<16>()};
+constexpr int kTmaWide16 = 7;  // index of the 16-vector fp32 configuration
+
+// The smallest configuration that holds the row, except fp32 rows of 64 - 68 KiB, which take the
+// 16-vector one (with two slots: see plan_tma).
+const TmaConfig* pick_tma(int64_t units, int dtype) {
+  if (dtype == 0 && units > 4096 && units <= 4352) return &kTma[kTmaWide16];  // fp32
   for (const TmaConfig& c : kTma)
-    if (units <= int64_t(32) * c.ncw * c.vpt) return &c;
+    if (units <= int64_t(32) * c.ncw * c.vpt) return c.fn[0][dtype] ? &c : nullptr;
   return nullptr;
 }
 
@@ -294,17 +310,23 @@ size_t tma_smem_bytes(int stages, uint32_t slot_bytes, int ncw) {
 
 // Two row slots per CTA, then as many CTAs per SM as shared memory and threads allow (measured
 // against 4 slots for rows up to 16 KiB and 3 above: fp32 4096 x 4096 24.1 -> 22.9 us, fp32 48 KiB
-// rows 336 -> 325 us, 64 KiB 360 -> 358 us, bf16 64 KiB rows unchanged).
+// rows 336 -> 325 us, 64 KiB 360 -> 358 us, bf16 64 KiB rows unchanged).  fp32 rows above 68 KiB
+// take one slot: the consumers free it as soon as the row is in registers, so the next row's load
+// still overlaps this row's normalisation and stores (measured, 8000 rows, TB/s one slot / two:
+// 16 vectors a thread 64 KiB 5.62 / 6.58, 68 KiB 5.77 / 6.43, 80 KiB 6.10 / 5.83, 112 KiB 6.68 /
+// 5.93; the fitted 10 and 12 vectors with one slot 72 KiB 6.28, 80 KiB 6.47, 88 KiB 6.56, 96 KiB
+// 6.68; 128 KiB (one slot only) 6.38).
 TmaPlan plan_tma(const RowProblem& p, const DeviceInfo& dev) {
   TmaPlan plan;
   const int64_t row_bytes = p.N * elem_bytes(p.dtype);
   if (row_bytes % 16 != 0 || row_bytes > (int64_t(1) << 20)) return plan;
-  const TmaConfig* cfg = pick_tma(row_bytes / 16);
+  const TmaConfig* cfg = pick_tma(row_bytes / 16, p.dtype);
   if (!cfg) return plan;
   const uint32_t slot = uint32_t((row_bytes + kSlotAlign - 1) / kSlotAlign * kSlotAlign);
   const size_t per_cta_reserved = 1024;  // the runtime's per-block reservation
   const int threads = (cfg->ncw + 1) * 32;
-  for (int stages = 2; stages >= 2; --stages) {
+  const int first = (p.dtype == 0 && row_bytes > 69632) ? 1 : 2;  // fp32 rows above 68 KiB
+  for (int stages = first; stages >= 1; --stages) {
     const size_t smem = tma_smem_bytes(stages, slot, cfg->ncw);
     if (smem > size_t(dev.max_smem_per_block_optin)) continue;
     int by_smem = int(size_t(dev.max_smem_per_sm) / (smem + per_cta_reserved));

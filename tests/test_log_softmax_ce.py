@@ -38,6 +38,7 @@ def _run_log(x, variant):
 SHAPES = [
     (synth.F32, 64, 1024), (synth.F32, 1000, 1000), (synth.F32, 300, 4100), (synth.F32, 65, 20000),
     (synth.BF16, 1000, 1000), (synth.BF16, 517, 4104), (synth.BF16, 70, 32768), (synth.BF16, 33, 40000),
+    (synth.F32, 400, 20480), (synth.F32, 400, 32764),  # fp32 rows of 80 and ~128 KiB: one row slot a CTA
 ]
 
 
@@ -135,7 +136,7 @@ def test_log_softmax_logits_workload_full_size():
 
 @pytest.mark.parametrize("dtype,M,N,shift", [
     (synth.F32, 64, 1024, 0), (synth.F32, 500, 1001, 1), (synth.BF16, 300, 32768, 0), (synth.BF16, 77, 50000, 1),
-    (synth.F32, 5, 1, 0),
+    (synth.F32, 5, 1, 0), (synth.F32, 400, 24576, 0),
 ])
 def test_cross_entropy_against_oracle(dtype, M, N, shift):
     w = synth.custom("ce", dtype, M, N, seed=40 + N, p1=4.0)

@@ -182,7 +182,8 @@ def test_host_buffers_staged_pipeline():
     (synth.F32, 16384, V.VARIANT_ONEREAD_REG),    # 64 KiB fp32 rows: registers (12 or 16 vectors a thread)
     (synth.BF16, 24576, V.VARIANT_ONEREAD_SMEM),  # 48 KiB 16-bit rows: shared memory
     (synth.BF16, 32768, V.VARIANT_ONEREAD_SMEM),  # 64 KiB 16-bit rows: one read
-    (synth.F32, 16388, V.VARIANT_TWOPASS),        # just over 64 KiB of fp32: past every one-read kernel
+    (synth.F32, 16388, V.VARIANT_ONEREAD_SMEM),   # just over 64 KiB of fp32: bulk copy, 16 warps a row
+    (synth.BF16, 32776, V.VARIANT_TWOPASS),       # just over 64 KiB of bf16: past every one-read kernel
 ])
 def test_auto_choice_around_64kib(dtype, N, want):
     w = synth.custom("auto64", dtype, 300, N, seed=N % 101, p1=3.0)
@@ -203,6 +204,20 @@ def test_register_kernel_rows_of_32_to_64_kib(dtype, N):
     x_host = synth.generate(w)
     _full_check(x_host, dtype, V.VARIANT_ONEREAD_REG, f"reg {N}")
     assert rwo.last_variant() == V.VARIANT_ONEREAD_REG
+
+
+@pytest.mark.parametrize("N", [16388, 17404, 18432, 20480, 20484, 24576, 24580, 30720, 32764, 32768])
+def test_bulk_copy_fp32_rows_of_64_to_128_kib(N):
+    """fp32 rows of 64 - 128 KiB on the CTA bulk-copy kernel, forced and through AUTO: 16 consumer
+    warps with 10, 12 or 16 vectors a thread (ragged rows straddle those), one row slot from 68 KiB
+    (each CTA takes several rows, so the slot is refilled while the previous row is normalised)."""
+    w = synth.custom("tma128", synth.F32, 400, N, seed=N % 89, p1=3.0)
+    x_host = synth.generate(w)
+    _full_check(x_host, synth.F32, V.VARIANT_ONEREAD_SMEM, f"bulk copy {N}")
+    assert rwo.last_variant() == V.VARIANT_ONEREAD_SMEM
+    if N in (20484, 32768):
+        _full_check(x_host, synth.F32, V.VARIANT_AUTO, f"auto {N}")
+        assert rwo.last_variant() == V.VARIANT_ONEREAD_SMEM
 
 
 def test_host_buffers_staged_very_long_rows():
