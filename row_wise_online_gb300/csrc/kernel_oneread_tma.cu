@@ -42,6 +42,9 @@ struct TmaArgs {
   float scale;               // softmax of scale * x
   float c;                   // scale * log2 e
 };
+// Each copy moves at most slot_bytes: the whole row (slot_bytes >= row_bytes), or in the
+// state-only mode, for rows longer than a slot, chunks of slot_bytes (a multiple of 128) and a
+// shorter last one -- ceil(row_bytes / slot_bytes) copies per row.
 
 constexpr int kSlotAlign = 128;
 
@@ -80,21 +83,31 @@ __global__ void __launch_bounds__((NCW + 1) * 32) k_oneread_tma(TmaArgs a) {
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       bool timed_out = false;
-      int s = 0;         // slot of row j and the parity of its lap, kept incrementally (a 64-bit
+      int s = 0;         // slot of copy j and the parity of its lap, kept incrementally (a 64-bit
       uint32_t ph = 0;   // division per row would cost ~0.1 us of this lane's time)
-      for (int64_t j = 0; j < nrows; ++j) {
+      int64_t r = 0;     // this CTA's row and the chunk of it that copy j carries
+      int ch = 0;
+      const int nch = int((a.row_bytes + a.slot_bytes - 1) / a.slot_bytes);
+      const int64_t ncopies = nrows * nch;
+      for (int64_t j = 0; j < ncopies; ++j) {
         if (j >= S && !mbar_wait(smem_addr(&freed[s]), ph ^ 1u, a.wait_ns)) timed_out = true;
         const uint32_t bar = smem_addr(&full[s]);
-        mbar_arrive_expect_tx(bar, a.row_bytes);
-        const int64_t row = blockIdx.x + j * gridDim.x;
-        bulk_g2s(smem_addr(slots + size_t(s) * a.slot_bytes), a.x + row * a.x_pitch, a.row_bytes, bar, pol);
+        const uint32_t off = uint32_t(ch) * a.slot_bytes;
+        const uint32_t bytes = a.row_bytes - off < a.slot_bytes ? a.row_bytes - off : a.slot_bytes;
+        mbar_arrive_expect_tx(bar, bytes);
+        const int64_t row = blockIdx.x + r * gridDim.x;
+        bulk_g2s(smem_addr(slots + size_t(s) * a.slot_bytes), a.x + row * a.x_pitch + off, bytes, bar, pol);
+        if (++ch == nch) {
+          ch = 0;
+          ++r;
+        }
         if (++s == S) {
           s = 0;
           ph ^= 1u;
         }
       }
       // Every load must have landed before the CTA may exit (the consumers normally saw them all).
-      for (int64_t j = nrows > S ? nrows - S : 0; j < nrows; ++j)
+      for (int64_t j = ncopies > S ? ncopies - S : 0; j < ncopies; ++j)
         if (!mbar_wait(smem_addr(&full[j % S]), uint32_t((j / S) & 1), a.wait_ns)) timed_out = true;
       if (timed_out) atomicOr(a.status, kStatusTimeout);
     }
@@ -103,35 +116,28 @@ __global__ void __launch_bounds__((NCW + 1) * 32) k_oneread_tma(TmaArgs a) {
 
   // ---------------- consumers ----------------
   bool timed_out = false;
-  int cs = 0;  // slot of row j and the parity of its lap (state-only mode)
+  int cs = 0;  // slot of the next copy and the parity of its lap (state-only mode)
   uint32_t cph = 0;
   for (int64_t j = 0; j < nrows; ++j) {
     // Kept incrementally in the state-only mode, whose consumers set the pace (measured 7% faster
     // on 64 KiB rows); the modes that write y measured 3% faster with the division here.
-    int s;
-    uint32_t par;
+    int s = 0;
+    uint32_t par = 0;
     if constexpr (WRITE_Y) {
       s = int(j % S);
       par = uint32_t((j / S) & 1);
-    } else {
-      s = cs;
-      par = cph;
-      if (++cs == S) {
-        cs = 0;
-        cph ^= 1u;
-      }
     }
     // cross entropy: thread 0 fetches the label before the row arrives
     int64_t label = -1;
     if constexpr (OUT == kTmaState) {
       if (a.loss && tid == 0) label = a.labels[blockIdx.x + j * gridDim.x];
     }
-    if (!mbar_wait(smem_addr(&full[s]), par, a.wait_ns)) timed_out = true;
-    const uint32_t slot = smem_addr(slots + size_t(s) * a.slot_bytes);
-    float x_label = 0.f;  // the labelled entry, read from the staged row before the slot is freed
-    if constexpr (OUT == kTmaState) {
-      if (a.loss && tid == 0 && label >= 0 && label < a.N) x_label = D::lds1(slot, label);
+    uint32_t slot = 0;
+    if constexpr (WRITE_Y) {
+      if (!mbar_wait(smem_addr(&full[s]), par, a.wait_ns)) timed_out = true;
+      slot = smem_addr(slots + size_t(s) * a.slot_bytes);
     }
+    float x_label = 0.f;  // the labelled entry, read from the staged row before the slot is freed
 
     // copy this thread's part of the row into registers and hand the slot back at once
     float mt = -INFINITY, dt = 0.f;
@@ -167,41 +173,66 @@ __global__ void __launch_bounds__((NCW + 1) * 32) k_oneread_tma(TmaArgs a) {
           }
         }
     } else {
-      // state only: keep the packed vectors, take the max on them (packed bf16 max), then the
-      // exponentials in pairs (packed f32x2 add and multiply)
-      uint4 q[VPT];
-#pragma unroll
-      for (int k = 0; k < VPT; ++k) {
-        const int u = tid + k * NCT;
-        q[k] = u < nunits ? lds16(slot + uint32_t(u) * 16u)
-                          : make_uint4(D::kNegInfWord, D::kNegInfWord, D::kNegInfWord, D::kNegInfWord);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&freed[s]));
-      mt = D::vmax_all(q);
-      const float mts = safe_max(mt);
-      float2 acc = make_float2(0.f, 0.f);
-      if (exp_shift_ok(mts)) {
-        const ExpShift sh = exp_shift(mts, a.c);
+      // State only: the row arrives in nch chunks (one unless it is longer than a slot), each
+      // folded into the thread's running state with the (m, d) merge.  Per chunk: keep the packed
+      // vectors, take the max on them (packed bf16 max), then the exponentials in pairs (packed
+      // f32x2 add and multiply).  For one chunk the merge with the empty state returns the
+      // chunk's state bit for bit.  Slots are counted incrementally here (measured 7% faster on
+      // 64 KiB rows than the division the other modes use).
+      const int64_t chunk_units = int64_t(a.slot_bytes) / 16;
+      const int nch = int((a.row_bytes + a.slot_bytes - 1) / a.slot_bytes);
+      State run = empty_state();
+      for (int ch = 0; ch < nch; ++ch) {
+        s = cs;
+        par = cph;
+        if (++cs == S) {
+          cs = 0;
+          cph ^= 1u;
+        }
+        if (!mbar_wait(smem_addr(&full[s]), par, a.wait_ns)) timed_out = true;
+        slot = smem_addr(slots + size_t(s) * a.slot_bytes);
+        const int64_t u0 = int64_t(ch) * chunk_units;  // the chunk's first unit in the row
+        const int64_t cu = nunits - u0 < chunk_units ? nunits - u0 : chunk_units;
+        if (a.loss && tid == 0 && label >= u0 * E && label < (u0 + cu) * E)
+          x_label = D::lds1(slot, label - u0 * E);
+        uint4 q[VPT];
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
-          float2 f[E / 2];
-          D::unpack2(q[k], f);
-#pragma unroll
-          for (int e = 0; e < E / 2; ++e) acc = __fadd2_rn(acc, exp_shifted2(f[e], sh));
+          const int u = tid + k * NCT;
+          q[k] = u < cu ? lds16(slot + uint32_t(u) * 16u)
+                        : make_uint4(D::kNegInfWord, D::kNegInfWord, D::kNegInfWord, D::kNegInfWord);
         }
-        dt = __fmul_rn(__fadd_rn(acc.x, acc.y), sh.unscale);
-      } else {
-        const float2 nms = make_float2(-mts, -mts);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&freed[s]));
+        const float mc = D::vmax_all(q);
+        const float mcs = safe_max(mc);
+        float2 acc = make_float2(0.f, 0.f);
+        float dc;
+        if (exp_shift_ok(mcs)) {
+          const ExpShift sh = exp_shift(mcs, a.c);
 #pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-          float2 f[E / 2];
-          D::unpack2(q[k], f);
+          for (int k = 0; k < VPT; ++k) {
+            float2 f[E / 2];
+            D::unpack2(q[k], f);
 #pragma unroll
-          for (int e = 0; e < E / 2; ++e) acc = __fadd2_rn(acc, exp_diff2(f[e], nms, a.c));
+            for (int e = 0; e < E / 2; ++e) acc = __fadd2_rn(acc, exp_shifted2(f[e], sh));
+          }
+          dc = __fmul_rn(__fadd_rn(acc.x, acc.y), sh.unscale);
+        } else {
+          const float2 nms = make_float2(-mcs, -mcs);
+#pragma unroll
+          for (int k = 0; k < VPT; ++k) {
+            float2 f[E / 2];
+            D::unpack2(q[k], f);
+#pragma unroll
+            for (int e = 0; e < E / 2; ++e) acc = __fadd2_rn(acc, exp_diff2(f[e], nms, a.c));
+          }
+          dc = __fadd_rn(acc.x, acc.y);
         }
-        dt = __fadd_rn(acc.x, acc.y);
+        run = merge(run, State{mc, dc}, a.c);
       }
+      mt = run.m;
+      dt = run.d;
     }
     State st;
     if constexpr (WRITE_Y)
@@ -316,16 +347,33 @@ size_t tma_smem_bytes(int stages, uint32_t slot_bytes, int ncw) {
 // 16 vectors a thread 64 KiB 5.62 / 6.58, 68 KiB 5.77 / 6.43, 80 KiB 6.10 / 5.83, 112 KiB 6.68 /
 // 5.93; the fitted 10 and 12 vectors with one slot 72 KiB 6.28, 80 KiB 6.47, 88 KiB 6.56, 96 KiB
 // 6.68; 128 KiB (one slot only) 6.38).
+// The state-only mode (row state, cross entropy) needs each element once and nothing kept, so rows
+// longer than 32 KiB stream through the slots in 32 KiB chunks, any length: measured (bf16,
+// ~1 GB per launch, cross entropy) 6.7-7.1 TB/s for rows of 64 - 297 KiB against 2.8-5.0 on the
+// two-pass kernel's first pass, and 6.7 against 6.3 TB/s for 64 KiB rows copied whole; 64 KiB
+// chunks measured 4.8-7.1.
+constexpr int64_t kStateChunk = 32768;
+
 TmaPlan plan_tma(const RowProblem& p, const DeviceInfo& dev) {
   TmaPlan plan;
   const int64_t row_bytes = p.N * elem_bytes(p.dtype);
-  if (row_bytes % 16 != 0 || row_bytes > (int64_t(1) << 20)) return plan;
-  const TmaConfig* cfg = pick_tma(row_bytes / 16, p.dtype);
+  if (row_bytes % 16 != 0) return plan;
+  int64_t copy_bytes = row_bytes;
+  const TmaConfig* cfg = nullptr;
+  if (p.y == nullptr && row_bytes > kStateChunk) {
+    // state only: the row streams through the slots in chunks (rows below 4 GiB)
+    if (row_bytes >= (int64_t(1) << 32)) return plan;
+    copy_bytes = kStateChunk;
+    cfg = pick_tma(kStateChunk / 16, p.dtype);
+  } else {
+    if (row_bytes > (int64_t(1) << 20)) return plan;
+    cfg = pick_tma(row_bytes / 16, p.dtype);
+  }
   if (!cfg) return plan;
-  const uint32_t slot = uint32_t((row_bytes + kSlotAlign - 1) / kSlotAlign * kSlotAlign);
+  const uint32_t slot = uint32_t((copy_bytes + kSlotAlign - 1) / kSlotAlign * kSlotAlign);
   const size_t per_cta_reserved = 1024;  // the runtime's per-block reservation
   const int threads = (cfg->ncw + 1) * 32;
-  const int first = (p.dtype == 0 && row_bytes > 69632) ? 1 : 2;  // fp32 rows above 68 KiB
+  const int first = (p.dtype == 0 && copy_bytes > 69632) ? 1 : 2;  // fp32 rows above 68 KiB
   for (int stages = first; stages >= 1; --stages) {
     const size_t smem = tma_smem_bytes(stages, slot, cfg->ncw);
     if (smem > size_t(dev.max_smem_per_block_optin)) continue;

@@ -183,6 +183,46 @@ def test_cross_entropy_masked_rows_and_bad_label():
     check_log_values(loss.cpu().numpy(), oracle.cross_entropy_rows(rows, bad), synth.F32, "ce bad label")
 
 
+@pytest.mark.parametrize("dtype,N", [(synth.F32, 8196), (synth.F32, 40000), (synth.BF16, 50264),
+                                     (synth.BF16, 151936), (synth.F16, 100000)])
+def test_cross_entropy_rows_streamed_in_chunks(dtype, N):
+    """Rows longer than 32 KiB reach the state-only kernel in 32 KiB chunks.  Labels on both sides
+    of every chunk boundary, on the first and last entries, ignored (-1); rows whose maximum sits
+    in the last chunk (every chunk's state rescaled at the merge), whose first chunk is all -inf,
+    whose only finite entry is the last one, and one that is all -inf (loss NaN); against the
+    fp64 oracle, with the LSE."""
+    M = 300
+    w = synth.custom("ce-chunks", dtype, M, N, seed=N % 83, p1=4.0)
+    x_host = synth.generate(w)
+    per_chunk = 32768 // (4 if dtype == synth.F32 else 2)
+    f32 = synth.bf16_to_f32 if dtype == synth.BF16 else synth.f16_to_f32 if dtype == synth.F16 else None
+    rows = x_host.astype(np.float32) if f32 is None else f32(x_host)
+    rows[0, N - 3] = 40.0           # the maximum in the last chunk
+    rows[1, :per_chunk] = -np.inf   # the first chunk empty
+    rows[2, :N - 1] = -np.inf       # only the last entry finite
+    rows[3, :] = -np.inf            # all -inf: NaN
+    if dtype == synth.F32:
+        x_host = rows
+    else:
+        x_host = synth.f32_to_bf16(rows) if dtype == synth.BF16 else synth.f32_to_f16(rows)
+    rng = np.random.default_rng(N)
+    labels = rng.integers(0, N, M)
+    edges = [0, N - 1] + [c * per_chunk + o for c in range(1, (N - 1) // per_chunk + 1) for o in (-1, 0)]
+    labels[4:4 + len(edges)] = edges
+    labels[::11] = -1
+    labels[1] = per_chunk // 2       # an -inf labelled entry: +inf loss
+    x = to_device(x_host, dtype) if dtype == synth.F16 else to_device(x_host)
+    lse = torch.full((M,), float("nan"), device="cuda")
+    loss = rwo.cross_entropy_rows(x, torch.from_numpy(labels).cuda(), lse_out=lse)
+    assert rwo.get_status() == rwo.OK
+    assert rwo.last_variant() == V.VARIANT_ONEREAD_SMEM
+    what = f"ce chunks {N}"
+    odt = {synth.F32: oracle.F32, synth.BF16: oracle.BF16, synth.F16: oracle.F16}[dtype]
+    check_log_values(loss.cpu().numpy(), oracle.cross_entropy_rows(x_host, labels, dtype=odt), synth.F32, what)
+    _, m_ref, d_ref, lse_ref = oracle.softmax_rows(x_host, dtype=odt, want_y=False)
+    check_state(None, None, lse.cpu().numpy(), m_ref, d_ref, lse_ref, what)
+
+
 @pytest.mark.parametrize("dtype", [synth.F32, synth.BF16])
 def test_cross_entropy_large_magnitude_rows(dtype):
     """Row maxima on both sides of 2^20 (the shifted-exponent fast path and its fallback), huge

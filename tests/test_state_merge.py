@@ -25,7 +25,10 @@ def _built():
 
 
 @pytest.mark.parametrize("dtype,M,N", [(synth.F32, 64, 1024), (synth.F32, 300, 4100), (synth.BF16, 100, 32768),
-                                       (synth.BF16, 9, 7), (synth.F32, 4, 1 << 20)])
+                                       (synth.BF16, 9, 7), (synth.F32, 4, 1 << 20),
+                                       # rows streamed in 32 KiB chunks: a 16-byte last chunk, ragged
+                                       # chunks, many rows per CTA
+                                       (synth.F32, 150, 8196), (synth.BF16, 700, 50264), (synth.F32, 500, 30000)])
 def test_row_state_against_oracle(dtype, M, N):
     w = synth.custom("state", dtype, M, N, seed=N % 97, p1=4.0)
     x_host = synth.generate(w)
