@@ -52,10 +52,14 @@ constexpr int kSlotAlign = 128;
 // row state alone, optionally the cross-entropy loss).
 enum TmaOut { kTmaProb = 0, kTmaLog = 1, kTmaState = 2 };
 
-template <class D, int VPT, int NCW, int OUT>
+// PK (16-bit types, rows of 64 - 128 KiB): the consumers keep x as the packed 16-byte vectors (4
+// registers each instead of 8) and form y from them after the merge, a second exponential per
+// element in the softmax.
+template <class D, int VPT, int NCW, int OUT, bool PK = false>
 __global__ void __launch_bounds__((NCW + 1) * 32) k_oneread_tma(TmaArgs a) {
   constexpr bool LOG = OUT == kTmaLog;
   constexpr bool WRITE_Y = OUT != kTmaState;
+  static_assert(!PK || WRITE_Y, "the state-only mode packs anyway");
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int E = D::kVec;
   constexpr int NCT = NCW * 32;
@@ -141,8 +145,30 @@ __global__ void __launch_bounds__((NCW + 1) * 32) k_oneread_tma(TmaArgs a) {
 
     // copy this thread's part of the row into registers and hand the slot back at once
     float mt = -INFINITY, dt = 0.f;
-    float v[WRITE_Y ? VPT : 1][E];  // values kept for the normalisation (not in state-only mode)
-    if constexpr (WRITE_Y) {
+    float v[WRITE_Y && !PK ? VPT : 1][E];  // values kept for the normalisation (unpacked modes)
+    uint4 qk[PK ? VPT : 1];                // the same, packed
+    if constexpr (PK) {
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int u = tid + k * NCT;
+        qk[k] = u < nunits ? lds16(slot + uint32_t(u) * 16u)
+                           : make_uint4(D::kNegInfWord, D::kNegInfWord, D::kNegInfWord, D::kNegInfWord);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&freed[s]));
+      mt = D::vmax_all(qk);
+      const float mts = safe_max(mt);
+      const float2 nms = make_float2(-mts, -mts);
+      float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        float2 f[E / 2];
+        D::unpack2(qk[k], f);
+#pragma unroll
+        for (int e = 0; e < E / 2; ++e) acc = __fadd2_rn(acc, exp_diff2(f[e], nms, a.c));
+      }
+      dt = __fadd_rn(acc.x, acc.y);
+    } else if constexpr (WRITE_Y) {
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
         const int u = tid + k * NCT;
@@ -242,7 +268,26 @@ __global__ void __launch_bounds__((NCW + 1) * 32) k_oneread_tma(TmaArgs a) {
       st = group_merge_nary(
           State{mt, dt}, wstate + (j & 1) * NCW, NCW, warp, lane, [] { named_barrier_sync(1, NCT); }, a.c);
     const int64_t row = blockIdx.x + j * gridDim.x;
-    if constexpr (WRITE_Y) {
+    if constexpr (PK) {
+      // y from the packed x: softmax 2^((x - m) c) / d, log softmax (x - m) scale - ln d, in pairs
+      unsigned char* yr = a.y + row * a.y_pitch;
+      const LogNorm ln = log_norm(st);
+      const float ms = safe_max(st.m);
+      const float2 nms = make_float2(-ms, -ms), inv2 = make_float2(safe_inv(st.d), safe_inv(st.d));
+      const float2 sc2 = make_float2(a.scale, a.scale), nlnd2 = make_float2(-ln.lnd, -ln.lnd);
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int u = tid + k * NCT;
+        if (u < nunits) {
+          float2 f[E / 2];
+          D::unpack2(qk[k], f);
+#pragma unroll
+          for (int e = 0; e < E / 2; ++e)
+            f[e] = LOG ? __ffma2_rn(__fadd2_rn(f[e], nms), sc2, nlnd2) : __fmul2_rn(exp_diff2(f[e], nms, a.c), inv2);
+          st_stream16(yr + int64_t(u) * 16, D::pack2(f));
+        }
+      }
+    } else if constexpr (WRITE_Y) {
       float scale = 0.f;
       LogNorm ln{};
       if constexpr (LOG) ln = log_norm(st);
@@ -300,27 +345,42 @@ constexpr TmaConfig tma_cfg() {
                      k_oneread_tma<F16, VPT, NCW, kTmaState>}}};
 }
 
-// fp32 rows of 64 - 128 KiB: 10, 12 or 16 vectors a thread over 16 warps (one CTA per SM); the
-// 16-bit types would hold up to 128 values a thread there, more than 544 threads' share of the
-// register file, and are left out.
+// fp32 rows of 64 - 128 KiB: 10, 12 or 16 vectors a thread over 16 warps (one CTA per SM).
+// 16-bit rows of 64 - 105 KiB: the vectors kept packed, 10, 12 or 14 a thread over 15 warps (16
+// warps in all, so that a thread may take 128 registers: with 17 warps on four sub-partitions it
+// gets 96, and even the packed form spilled).  The state-only mode streams such rows in chunks
+// through the smaller configurations and has no entry here.
 template <int VPT>
-constexpr TmaConfig tma_cfg_f32_wide() {
+constexpr TmaConfig tma_cfg_wide() {
   return TmaConfig{16, VPT,
                    {{k_oneread_tma<F32, VPT, 16, kTmaProb>, nullptr, nullptr},
                     {k_oneread_tma<F32, VPT, 16, kTmaLog>, nullptr, nullptr},
-                    {k_oneread_tma<F32, VPT, 16, kTmaState>, nullptr, nullptr}}};
+                    {nullptr, nullptr, nullptr}}};
 }
+template <int VPT>
+constexpr TmaConfig tma_cfg_packed() {
+  return TmaConfig{15, VPT,
+                   {{nullptr, k_oneread_tma<BF16, VPT, 15, kTmaProb, true>, k_oneread_tma<F16, VPT, 15, kTmaProb, true>},
+                    {nullptr, k_oneread_tma<BF16, VPT, 15, kTmaLog, true>, k_oneread_tma<F16, VPT, 15, kTmaLog, true>},
+                    {nullptr, nullptr, nullptr}}};
+}
+const TmaConfig kTmaPacked[] = {tma_cfg_packed<10>(), tma_cfg_packed<12>(), tma_cfg_packed<14>()};
 
 // Ordered by capacity (16-byte units per row = 32 * ncw * vpt).
 const TmaConfig kTma[] = {tma_cfg<2, 4>(),          tma_cfg<4, 4>(),          tma_cfg<4, 8>(),
-                          tma_cfg<8, 8>(),          tma_cfg<8, 16>(),         tma_cfg_f32_wide<10>(),
-                          tma_cfg_f32_wide<12>(),   tma_cfg_f32_wide<16>()};
+                          tma_cfg<8, 8>(),          tma_cfg<8, 16>(),         tma_cfg_wide<10>(),
+                          tma_cfg_wide<12>(),   tma_cfg_wide<16>()};
 constexpr int kTmaWide16 = 7;  // index of the 16-vector fp32 configuration
 
 // The smallest configuration that holds the row, except fp32 rows of 64 - 68 KiB, which take the
 // 16-vector one (with two slots: see plan_tma).
 const TmaConfig* pick_tma(int64_t units, int dtype) {
   if (dtype == 0 && units > 4096 && units <= 4352) return &kTma[kTmaWide16];  // fp32
+  if (dtype != 0 && units > 4096) {
+    for (const TmaConfig& c : kTmaPacked)
+      if (units <= int64_t(32) * c.ncw * c.vpt) return &c;
+    return nullptr;
+  }
   for (const TmaConfig& c : kTma)
     if (units <= int64_t(32) * c.ncw * c.vpt) return c.fn[0][dtype] ? &c : nullptr;
   return nullptr;
@@ -346,7 +406,11 @@ size_t tma_smem_bytes(int stages, uint32_t slot_bytes, int ncw) {
 // still overlaps this row's normalisation and stores (measured, 8000 rows, TB/s one slot / two:
 // 16 vectors a thread 64 KiB 5.62 / 6.58, 68 KiB 5.77 / 6.43, 80 KiB 6.10 / 5.83, 112 KiB 6.68 /
 // 5.93; the fitted 10 and 12 vectors with one slot 72 KiB 6.28, 80 KiB 6.47, 88 KiB 6.56, 96 KiB
-// 6.68; 128 KiB (one slot only) 6.38).
+// 6.68; 128 KiB (one slot only) 6.38).  16-bit rows of 64 - 105 KiB, x kept packed (bf16, ~1 GB
+// per launch, softmax / log softmax TB/s, one slot against two): 64 KiB + 16 B 5.96 / 5.82
+// against 6.28 / 6.50, 80 KiB 6.20 / 5.98 against 6.18 / 6.25, 88 KiB 6.44 / 6.24 against
+// 6.20 / 6.15, 98 KiB 6.30 / 6.36 against 5.85 / 6.10, 105 KiB 6.43 / 6.48 against 6.09 / 6.20
+// (two passes: 4.66-5.02).
 // The state-only mode (row state, cross entropy) needs each element once and nothing kept, so rows
 // longer than 32 KiB stream through the slots in 32 KiB chunks, any length: measured (bf16,
 // ~1 GB per launch, cross entropy) 6.7-7.1 TB/s for rows of 64 - 297 KiB against 2.8-5.0 on the
@@ -373,7 +437,8 @@ TmaPlan plan_tma(const RowProblem& p, const DeviceInfo& dev) {
   const uint32_t slot = uint32_t((copy_bytes + kSlotAlign - 1) / kSlotAlign * kSlotAlign);
   const size_t per_cta_reserved = 1024;  // the runtime's per-block reservation
   const int threads = (cfg->ncw + 1) * 32;
-  const int first = (p.dtype == 0 && copy_bytes > 69632) ? 1 : 2;  // fp32 rows above 68 KiB
+  // one slot for fp32 rows above 68 KiB and 16-bit rows above 80 KiB
+  const int first = copy_bytes > (p.dtype == 0 ? 69632 : 81920) ? 1 : 2;
   for (int stages = first; stages >= 1; --stages) {
     const size_t smem = tma_smem_bytes(stages, slot, cfg->ncw);
     if (smem > size_t(dev.max_smem_per_block_optin)) continue;
@@ -404,6 +469,7 @@ cudaError_t launch_oneread_tma(const RowProblem& p, const DeviceInfo& dev) {
   const int out = p.y == nullptr ? kTmaState : p.log_out ? kTmaLog : kTmaProb;
   if (p.loss && out != kTmaState) return cudaErrorInvalidValue;
   TmaKernel fn = plan.cfg->fn[out][p.dtype];
+  if (!fn) return cudaErrorInvalidValue;
   cudaError_t err = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(plan.smem));
   if (err != cudaSuccess) return err;

@@ -13,7 +13,7 @@ import oracle
 import row_wise_online_gb300 as rwo
 import synth
 from gpu_util import run_softmax, to_device, to_host
-from tolerances import check_rowsums, check_state, check_y
+from tolerances import check_log_values, check_rowsums, check_state, check_y
 
 pytestmark = pytest.mark.gpu
 
@@ -183,7 +183,8 @@ def test_host_buffers_staged_pipeline():
     (synth.BF16, 24576, V.VARIANT_ONEREAD_SMEM),  # 48 KiB 16-bit rows: shared memory
     (synth.BF16, 32768, V.VARIANT_ONEREAD_SMEM),  # 64 KiB 16-bit rows: one read
     (synth.F32, 16388, V.VARIANT_ONEREAD_SMEM),   # just over 64 KiB of fp32: bulk copy, 16 warps a row
-    (synth.BF16, 32776, V.VARIANT_TWOPASS),       # just over 64 KiB of bf16: past every one-read kernel
+    (synth.BF16, 32776, V.VARIANT_ONEREAD_SMEM),  # just over 64 KiB of bf16: bulk copy, x kept packed
+    (synth.BF16, 53768, V.VARIANT_TWOPASS),       # just over 105 KiB of bf16: past every one-read kernel
 ])
 def test_auto_choice_around_64kib(dtype, N, want):
     w = synth.custom("auto64", dtype, 300, N, seed=N % 101, p1=3.0)
@@ -218,6 +219,31 @@ def test_bulk_copy_fp32_rows_of_64_to_128_kib(N):
     if N in (20484, 32768):
         _full_check(x_host, synth.F32, V.VARIANT_AUTO, f"auto {N}")
         assert rwo.last_variant() == V.VARIANT_ONEREAD_SMEM
+
+
+@pytest.mark.parametrize("dtype,N", [(synth.BF16, 32776), (synth.BF16, 40000), (synth.BF16, 45064),
+                                     (synth.BF16, 53760), (synth.F16, 36872)])
+def test_bulk_copy_16bit_rows_of_64_to_105_kib(dtype, N):
+    """16-bit rows of 64 - 105 KiB on the CTA bulk-copy kernel with x kept packed in registers (15
+    consumer warps, 10, 12 or 14 vectors a thread; one row slot above 80 KiB): softmax with the
+    state, forced and through AUTO, and log softmax, against the fp64 oracle."""
+    w = synth.custom("tma16", dtype, 400, N, seed=N % 79, p1=4.0)
+    x_host = synth.generate(w)
+    odt = oracle.F16 if dtype == synth.F16 else oracle.BF16
+    x = to_device(x_host, dtype)
+    for variant in (V.VARIANT_ONEREAD_SMEM, V.VARIANT_AUTO):
+        m, d, lse = (torch.full((w.M,), float("nan"), device="cuda") for _ in range(3))
+        y = rwo.softmax_rows_ex(x, m_out=m, d_out=d, lse_out=lse, variant=variant)
+        assert rwo.get_status() == rwo.OK and rwo.last_variant() == V.VARIANT_ONEREAD_SMEM
+        y_ref, m_ref, d_ref, lse_ref = oracle.softmax_rows(x_host, dtype=odt)
+        what = f"packed {N}/{V.VARIANT_NAMES[variant]}"
+        check_y(to_host(y), y_ref, dtype, what)
+        check_rowsums(to_host(y), dtype, ~np.isfinite(m_ref), what)
+        check_state(m.cpu().numpy(), d.cpu().numpy(), lse.cpu().numpy(), m_ref, d_ref, lse_ref, what)
+        del y_ref
+    ly = rwo.log_softmax_rows(x, variant=V.VARIANT_ONEREAD_SMEM)
+    assert rwo.get_status() == rwo.OK
+    check_log_values(to_host(ly), oracle.log_softmax_rows(x_host, dtype=odt), dtype, f"packed log {N}")
 
 
 def test_host_buffers_staged_very_long_rows():
