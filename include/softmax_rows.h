@@ -161,8 +161,9 @@ enum softmax_flags { SOFTMAX_FLAG_LOG = 1 /* y = log softmax instead of softmax 
  *   ldx, ldy -- row pitches in ELEMENTS, >= N (0 means N).
  *   scale    -- finite and > 0 (else SOFTMAX_ERR_INVALID_ARG); 1 gives softmax_rows_ex's result.
  *   flags    -- 0 or SOFTMAX_FLAG_LOG.
- *   variant  -- AUTO, ONEREAD_REG, ONEREAD_SMEM (the CTA bulk-copy kernel) or TWOPASS; SPLITROW
- *               gives SOFTMAX_ERR_UNSUPPORTED.  The vector and bulk-copy paths also need ldx * s and
+ *   variant  -- AUTO, ONEREAD_REG, ONEREAD_SMEM (the CTA bulk-copy kernel; for contiguous rows
+ *               at scale 1 beyond its reach, the cluster kernel that holds each row on chip) or
+ *               TWOPASS; SPLITROW gives SOFTMAX_ERR_UNSUPPORTED.  The vector and bulk-copy paths also need ldx * s and
  *               ldy * s to be multiples of 16 bytes (a forced ONEREAD_SMEM otherwise returns
  *               SOFTMAX_ERR_MISALIGNED; AUTO takes the scalar paths).
  * x and y may be the same matrix (x == y, ldx == ldy); other overlaps are undefined.  Other
@@ -178,7 +179,8 @@ int softmax_rows_strided(const void* x, int64_t ldx, void* y, int64_t ldy, float
  * log(sum_exp), the step before the cross-entropy loss).  Computed as (x_j - m) - ln d from the
  * online state, so x is read once as for softmax.  An all -inf row gives y = -inf everywhere
  * (log 0).  Arguments, layout, outputs and errors as softmax_rows_ex; `variant` may be AUTO,
- * ONEREAD_REG, ONEREAD_SMEM (the CTA bulk-copy kernel) or TWOPASS.  SPLITROW gives
+ * ONEREAD_REG, ONEREAD_SMEM (the bulk-copy kernels, and for many rows of 128 KiB - 1 MiB a
+ * thread-block cluster per row held on chip) or TWOPASS.  SPLITROW gives
  * SOFTMAX_ERR_UNSUPPORTED; AUTO never picks it (a single very long row runs TWOPASS).
  */
 int log_softmax_rows(const void* x, void* y, float* m_out, float* d_out, float* lse_out, int64_t M,

@@ -17,6 +17,8 @@ __device__ unsigned g_status;  // per-device status word (kernels atomicOr statu
 
 namespace {
 
+bool cluster_local_rows(const RowProblem& p, const DeviceInfo& dev);
+
 constexpr int kMaxDevices = 64;
 
 std::mutex g_dev_mutex;
@@ -163,15 +165,7 @@ int run_variant(RowProblem& p, int variant, const DeviceInfo& dev) {
         // 116, 8 x 2 MiB 20.8 against 17.1, 76 x 1 MiB 124 against 44.5: there each row's
         // exchange costs more than the clusters' parallel rows)
         variant = SOFTMAX_VARIANT_SPLITROW;
-      else if (row_bytes >= (int64_t(128) << 10) &&
-               (row_bytes <= (int64_t(512) << 10) ? p.M >= int64_t(dev.sm_count)
-                                                  : row_bytes <= (int64_t(1) << 20) && p.M >= 256) &&
-               clusterrow_onchip_fits(p, dev))
-        // many rows of 128 KiB - 1 MiB: a thread-block cluster per row, its CTAs' segments held on
-        // chip (measured against the cluster-row two passes, fp32: 4000 x 128 KiB 169 against
-        // 182 us, 2000 x 256 KiB 168 / 193, 1000 x 512 KiB 161 / 196, 600 x 1 MiB 218 / 242; bf16
-        // 1000 x 512 KiB 167 / 206; but 8000 x 80 KB 282 / 252, 800 x 768 KB 238 / 221, and fewer
-        // rows of 1 MiB, 100: 46.8 / 46.3, 20: 19.6 / 17.4)
+      else if (cluster_local_rows(p, dev))
         variant = SOFTMAX_VARIANT_ONEREAD_SMEM;
       else
         variant = SOFTMAX_VARIANT_TWOPASS;
@@ -227,6 +221,19 @@ int run_variant(RowProblem& p, int variant, const DeviceInfo& dev) {
   if (err != cudaSuccess) return cuda_fail(err);
   t_last_variant = variant;
   return SOFTMAX_OK;
+}
+
+// Many rows of 128 KiB - 1 MiB: a thread-block cluster per row, its CTAs' segments held on chip
+// (measured against the cluster-row two passes, fp32: 4000 x 128 KiB 169 against 182 us, 2000 x
+// 256 KiB 168 / 193, 1000 x 512 KiB 161 / 196, 600 x 1 MiB 218 / 242; bf16 1000 x 512 KiB 167 /
+// 206; but 8000 x 80 KB 282 / 252, 800 x 768 KB 238 / 221, and fewer rows of 1 MiB, 100: 46.8 /
+// 46.3, 20: 19.6 / 17.4).  Softmax and log softmax (contiguous rows, scale 1).
+bool cluster_local_rows(const RowProblem& p, const DeviceInfo& dev) {
+  const int64_t row_bytes = p.N * elem_bytes(p.dtype);
+  return row_bytes >= (int64_t(128) << 10) &&
+         (row_bytes <= (int64_t(512) << 10) ? p.M >= int64_t(dev.sm_count)
+                                            : row_bytes <= (int64_t(1) << 20) && p.M >= 256) &&
+         clusterrow_onchip_fits(p, dev);
 }
 
 // Row state only (optionally with the cross-entropy loss): the CTA bulk-copy kernel, whose copy
@@ -379,11 +386,13 @@ int softmax_rows_strided(const void* x, int64_t ldx, void* y, int64_t ldy, float
   const int64_t row_bytes = N * s;
   const bool aligned = aligned16(x) && aligned16(y) && row_bytes % 16 == 0 && p.x_pitch % 16 == 0 &&
                        p.y_pitch % 16 == 0;
-  if (variant == SOFTMAX_VARIANT_AUTO) {  // the kernels that take a pitch and a scale
+  if (variant == SOFTMAX_VARIANT_AUTO) {  // the kernels that take a pitch and a scale (and, for
+                                          // contiguous rows at scale 1, the cluster kernel)
     if (aligned)
-      variant = row_bytes <= 16384 && oneread_reg_fits(p, true) ? SOFTMAX_VARIANT_ONEREAD_REG
-                : oneread_tma_fits(p, *dev)                     ? SOFTMAX_VARIANT_ONEREAD_SMEM
-                                                                : SOFTMAX_VARIANT_TWOPASS;
+      variant = (row_bytes <= 16384 || (dtype == SOFTMAX_F32 && row_bytes <= 65536)) && oneread_reg_fits(p, true)
+                    ? SOFTMAX_VARIANT_ONEREAD_REG
+                : oneread_tma_fits(p, *dev) || cluster_local_rows(p, *dev) ? SOFTMAX_VARIANT_ONEREAD_SMEM
+                                                                           : SOFTMAX_VARIANT_TWOPASS;
     else
       variant = (N <= 512 && oneread_reg_fits(p, false)) ? SOFTMAX_VARIANT_ONEREAD_REG : SOFTMAX_VARIANT_TWOPASS;
   }
@@ -395,8 +404,12 @@ int softmax_rows_strided(const void* x, int64_t ldx, void* y, int64_t ldy, float
       break;
     case SOFTMAX_VARIANT_ONEREAD_SMEM:
       if (!aligned) return SOFTMAX_ERR_MISALIGNED;
-      if (!oneread_tma_fits(p, *dev)) return SOFTMAX_ERR_UNSUPPORTED;
-      err = launch_oneread_tma(p, *dev);
+      if (oneread_tma_fits(p, *dev))
+        err = launch_oneread_tma(p, *dev);
+      else if (clusterrow_onchip_fits(p, *dev))  // contiguous rows above the ring's reach, scale 1
+        err = launch_clusterrow_onchip(p, *dev);
+      else
+        return SOFTMAX_ERR_UNSUPPORTED;
       break;
     case SOFTMAX_VARIANT_TWOPASS:
       err = launch_twopass_any(p, aligned, *dev);

@@ -229,7 +229,7 @@ size_t onchip_tail_bytes(int nb, int rb, int pieces) {
 // Split mode (local = 0): every row is shared by all G CTAs, cluster states exchanged through global
 // memory.  Local mode: cluster k owns rows k, k + clusters, ... and its CS CTAs share each of them;
 // rank 0 merges the CTA states and hands the row state to every CTA of the cluster over DSMEM.
-template <class D, bool HOLD>
+template <class D, bool HOLD, bool LOG>
 __global__ void __launch_bounds__(kOcThreads, 1) k_splitrow_onchip(OnchipArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int E = D::kVec;
@@ -428,8 +428,9 @@ __global__ void __launch_bounds__(kOcThreads, 1) k_splitrow_onchip(OnchipArgs a)
         oc_st_async_f32x2(map_to_rank(smem_addr(&cstate[sb * kOcMaxCluster + crank]), 0), cs.m, cs.d,
                           map_to_rank(smem_addr(&cbar[sb]), 0));
     };
-    // y = e^(x - m) / d for the four units of piece p held in q (unit p * kOcPieceUnits + i * kOcNct + tid)
-    auto store_piece = [&](int64_t r, int p, const uint4 (&q)[kOcUpt], float2 nms, float2 inv2) {
+    // y = e^(x - m) / d (b2 = 1 / d), or in the log mode y = (x - m) - ln d (b2 = -ln d), for the
+    // four units of piece p held in q (unit p * kOcPieceUnits + i * kOcNct + tid)
+    auto store_piece = [&](int64_t r, int p, const uint4 (&q)[kOcUpt], float2 nms, float2 b2) {
       unsigned char* yp = a.y + row_of(r) * a.row_bytes + (seg_start + int64_t(p) * kOcPieceUnits) * 16;
       const int rest = seg_units - p * kOcPieceUnits;
 #pragma unroll
@@ -439,7 +440,8 @@ __global__ void __launch_bounds__(kOcThreads, 1) k_splitrow_onchip(OnchipArgs a)
           float2 f[E / 2];
           D::unpack2(q[i], f);
 #pragma unroll
-          for (int e = 0; e < E / 2; ++e) f[e] = __fmul2_rn(exp_diff2(f[e], nms), inv2);
+          for (int e = 0; e < E / 2; ++e)
+            f[e] = LOG ? __fadd2_rn(__fadd2_rn(f[e], nms), b2) : __fmul2_rn(exp_diff2(f[e], nms), b2);
           st_stream16(yp + int64_t(u) * 16, D::pack2(f));
         }
       }
@@ -470,7 +472,7 @@ __global__ void __launch_bounds__(kOcThreads, 1) k_splitrow_onchip(OnchipArgs a)
       auto normalise_row = [&](int64_t r, const OcRing& buf, const OcRing& st_ring) {
         const State row = row_state(r, st_ring);
         const float ms = safe_max(row.m);
-        const float inv = safe_inv(row.d);
+        const float inv = LOG ? -log_norm(row).lnd : safe_inv(row.d);
         const float2 nms = make_float2(-ms, -ms), inv2 = make_float2(inv, inv);
         for (int p = 0; p < pc; ++p) {
           const uint32_t piece = bufs + uint32_t(buf.idx) * a.buf_bytes + uint32_t(p) * kOcPieceBytes;
@@ -558,7 +560,7 @@ __global__ void __launch_bounds__(kOcThreads, 1) k_splitrow_onchip(OnchipArgs a)
         const State row = row_state(r, nst);
         nst.next();
         const float ms = safe_max(row.m);
-        const float inv = safe_inv(row.d);
+        const float inv = LOG ? -log_norm(row).lnd : safe_inv(row.d);
         const float2 nms = make_float2(-ms, -ms), inv2 = make_float2(inv, inv);
         for (int p = 0; p < pc; ++p) {
           uint4 q[kOcUpt];
@@ -610,11 +612,17 @@ __global__ void __launch_bounds__(kOcThreads, 1) k_splitrow_onchip(OnchipArgs a)
 
 using OnchipKernel = void (*)(OnchipArgs);
 
-OnchipKernel onchip_kernel(int dtype, bool hold) {
-  if (hold) return dtype == 0 ? k_splitrow_onchip<F32, true> : dtype == 1 ? k_splitrow_onchip<BF16, true>
-                                                                         : k_splitrow_onchip<F16, true>;
-  return dtype == 0 ? k_splitrow_onchip<F32, false> : dtype == 1 ? k_splitrow_onchip<BF16, false>
-                                                                 : k_splitrow_onchip<F16, false>;
+template <bool LOG>
+OnchipKernel onchip_kernel_of(int dtype, bool hold) {
+  if (hold) return dtype == 0 ? k_splitrow_onchip<F32, true, LOG> : dtype == 1 ? k_splitrow_onchip<BF16, true, LOG>
+                                                                              : k_splitrow_onchip<F16, true, LOG>;
+  return dtype == 0 ? k_splitrow_onchip<F32, false, LOG> : dtype == 1 ? k_splitrow_onchip<BF16, false, LOG>
+                                                                      : k_splitrow_onchip<F16, false, LOG>;
+}
+// The log-softmax instances (local mode only) use the registers and shared memory of the others,
+// so the residency plans below, taken with the softmax instance, hold for them too.
+OnchipKernel onchip_kernel(int dtype, bool hold, bool log = false) {
+  return log ? onchip_kernel_of<true>(dtype, hold) : onchip_kernel_of<false>(dtype, hold);
 }
 
 // Cluster size and count for the largest shared-memory footprint (one CTA per SM), per device and
@@ -716,7 +724,7 @@ bool segment_buffers(int64_t seg_max, int64_t rows, size_t cap, bool one_buffer,
 OnchipShape onchip_shape(const RowProblem& p, const DeviceInfo& dev) {
   OnchipShape s;
   const int64_t row_bytes = p.N * elem_bytes(p.dtype);
-  if (row_bytes % 16 != 0) return s;
+  if (row_bytes % 16 != 0 || p.log_out) return s;
   const OnchipPlan plan = onchip_plan(p.dtype, dev);
   if (!plan.ok) return s;
   const int64_t G = int64_t(plan.cluster) * plan.clusters;
@@ -788,7 +796,7 @@ LocalPlan local_plan(int dtype, const DeviceInfo& dev) {
 OnchipShape onchip_local_shape(const RowProblem& p, const DeviceInfo& dev) {
   OnchipShape s;
   const int64_t row_bytes = p.N * elem_bytes(p.dtype);
-  if (row_bytes % 16 != 0 || p.y == nullptr || p.labels || p.loss || p.log_out) return s;
+  if (row_bytes % 16 != 0 || p.y == nullptr || p.labels || p.loss) return s;
   if ((p.x_pitch && p.x_pitch != row_bytes) || (p.y_pitch && p.y_pitch != row_bytes) || p.scale != 1.f) return s;
   const int64_t units = row_bytes / 16;
   const LocalPlan lp = local_plan(p.dtype, dev);
@@ -808,7 +816,7 @@ OnchipShape onchip_local_shape(const RowProblem& p, const DeviceInfo& dev) {
 }
 
 cudaError_t launch_onchip(const RowProblem& p, const DeviceInfo& dev, const OnchipShape& s, unsigned long long* pub) {
-  OnchipKernel fn = onchip_kernel(p.dtype, s.hold);
+  OnchipKernel fn = onchip_kernel(p.dtype, s.hold, p.log_out);
   cudaError_t err = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(s.smem));
   if (err != cudaSuccess) return err;
   if (s.cluster > 8 &&

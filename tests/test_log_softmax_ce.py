@@ -39,6 +39,8 @@ SHAPES = [
     (synth.F32, 64, 1024), (synth.F32, 1000, 1000), (synth.F32, 300, 4100), (synth.F32, 65, 20000),
     (synth.BF16, 1000, 1000), (synth.BF16, 517, 4104), (synth.BF16, 70, 32768), (synth.BF16, 33, 40000),
     (synth.F32, 400, 20480), (synth.F32, 400, 32764),  # fp32 rows of 80 and ~128 KiB: one row slot a CTA
+    (synth.BF16, 400, 50264),                           # 98 KiB of bf16: x kept packed
+    (synth.F32, 300, 40000), (synth.BF16, 200, 100000), (synth.F32, 260, 200000),  # a cluster per row
 ]
 
 
@@ -78,6 +80,27 @@ def test_log_softmax_masked_and_extreme_rows(variant):
     what = f"log special/{V.VARIANT_NAMES[rwo.last_variant()]}"
     ly_ref = oracle.log_softmax_rows(rows)
     check_log_values(to_host(y), ly_ref, synth.F32, what)
+    _, m_ref, d_ref, lse_ref = oracle.softmax_rows(rows, want_y=False)
+    check_state(m.cpu().numpy(), d.cpu().numpy(), lse.cpu().numpy(), m_ref, d_ref, lse_ref, what)
+
+
+@pytest.mark.parametrize("variant", [V.VARIANT_AUTO, V.VARIANT_ONEREAD_SMEM])
+def test_log_softmax_cluster_rows_special_values(variant):
+    """Rows of 160 KB held on chip by a thread-block cluster, log output: an all -inf row (-inf
+    everywhere), a row whose first quarter is -inf (a CTA's whole segment empty), one huge value,
+    a huge negative row."""
+    M, N = 200, 40000
+    rng = np.random.default_rng(9)
+    rows = (rng.standard_normal((M, N)) * 3).astype(np.float32)
+    rows[0, :] = -np.inf
+    rows[1, :N // 4] = -np.inf
+    rows[2, N - 1] = 1e30
+    rows[3] -= 1e30
+    x = to_device(rows)
+    y, m, d, lse = _run_log(x, variant)
+    assert rwo.last_variant() == V.VARIANT_ONEREAD_SMEM
+    what = f"log cluster special/{V.VARIANT_NAMES[variant]}"
+    check_log_values(to_host(y), oracle.log_softmax_rows(rows), synth.F32, what)
     _, m_ref, d_ref, lse_ref = oracle.softmax_rows(rows, want_y=False)
     check_state(m.cpu().numpy(), d.cpu().numpy(), lse.cpu().numpy(), m_ref, d_ref, lse_ref, what)
 
