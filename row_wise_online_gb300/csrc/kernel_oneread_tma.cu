@@ -91,19 +91,26 @@ __global__ void __launch_bounds__((NCW + 1) * 32) k_oneread_tma(TmaArgs a) {
       uint32_t ph = 0;   // division per row would cost ~0.1 us of this lane's time)
       int64_t r = 0;     // this CTA's row and the chunk of it that copy j carries
       int ch = 0;
-      const int nch = int((a.row_bytes + a.slot_bytes - 1) / a.slot_bytes);
+      // one copy per row where y is written (the row fits a slot); the state-only mode may chunk
+      const int nch = WRITE_Y ? 1 : int((a.row_bytes + a.slot_bytes - 1) / a.slot_bytes);
       const int64_t ncopies = nrows * nch;
       for (int64_t j = 0; j < ncopies; ++j) {
         if (j >= S && !mbar_wait(smem_addr(&freed[s]), ph ^ 1u, a.wait_ns)) timed_out = true;
         const uint32_t bar = smem_addr(&full[s]);
-        const uint32_t off = uint32_t(ch) * a.slot_bytes;
-        const uint32_t bytes = a.row_bytes - off < a.slot_bytes ? a.row_bytes - off : a.slot_bytes;
-        mbar_arrive_expect_tx(bar, bytes);
-        const int64_t row = blockIdx.x + r * gridDim.x;
-        bulk_g2s(smem_addr(slots + size_t(s) * a.slot_bytes), a.x + row * a.x_pitch + off, bytes, bar, pol);
-        if (++ch == nch) {
-          ch = 0;
-          ++r;
+        if constexpr (WRITE_Y) {
+          mbar_arrive_expect_tx(bar, a.row_bytes);
+          const int64_t row = blockIdx.x + j * gridDim.x;
+          bulk_g2s(smem_addr(slots + size_t(s) * a.slot_bytes), a.x + row * a.x_pitch, a.row_bytes, bar, pol);
+        } else {
+          const uint32_t off = uint32_t(ch) * a.slot_bytes;
+          const uint32_t bytes = a.row_bytes - off < a.slot_bytes ? a.row_bytes - off : a.slot_bytes;
+          mbar_arrive_expect_tx(bar, bytes);
+          const int64_t row = blockIdx.x + r * gridDim.x;
+          bulk_g2s(smem_addr(slots + size_t(s) * a.slot_bytes), a.x + row * a.x_pitch + off, bytes, bar, pol);
+          if (++ch == nch) {
+            ch = 0;
+            ++r;
+          }
         }
         if (++s == S) {
           s = 0;
