@@ -75,7 +75,7 @@ enum softmax_variant {
   SOFTMAX_VARIANT_ONEREAD_REG = 1,
   /* One read: bulk copies (cp.async.bulk + mbarrier) stage whole rows in shared memory.  Rows
      up to 8 KiB: each warp owns a row at a time and a private ring of row slots that its lane 0
-     refills; longer rows (up to 64 KiB; fp32 rows up to 128 KiB, 16-bit rows up to 105 KiB, kept
+     refills; longer rows (up to 64 KiB; fp32 rows up to 128 KiB, 16-bit rows up to 120 KiB, kept
      packed): a producer warp feeds a CTA-wide consumer group that copies the row to registers
      and frees the slot at once; longer
      rows (16-byte aligned, up to 1 MiB): a thread-block cluster of 2-8 CTAs per row, each CTA's

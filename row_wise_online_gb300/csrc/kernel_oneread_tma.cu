@@ -353,9 +353,11 @@ constexpr TmaConfig tma_cfg() {
 }
 
 // fp32 rows of 64 - 128 KiB: 10, 12 or 16 vectors a thread over 16 warps (one CTA per SM).
-// 16-bit rows of 64 - 105 KiB: the vectors kept packed, 10, 12 or 14 a thread over 15 warps (16
-// warps in all, so that a thread may take 128 registers: with 17 warps on four sub-partitions it
-// gets 96, and even the packed form spilled).  The state-only mode streams such rows in chunks
+// 16-bit rows of 64 - 120 KiB: the vectors kept packed, 10, 12, 14 or 16 a thread over 15 warps
+// (16 warps in all, so that a thread may take 128 registers: with 17 warps on four sub-partitions
+// it gets 96, and even the packed form spilled; 14 and 16 vectors still spill 28-96 bytes and
+// measured 6.3-6.5 TB/s all the same, bf16 112 / 120 KiB 6.32 / 6.38 against 5.13 / 5.30 on two
+// passes).  The state-only mode streams such rows in chunks
 // through the smaller configurations and has no entry here.
 template <int VPT>
 constexpr TmaConfig tma_cfg_wide() {
@@ -371,7 +373,7 @@ constexpr TmaConfig tma_cfg_packed() {
                     {nullptr, k_oneread_tma<BF16, VPT, 15, kTmaLog, true>, k_oneread_tma<F16, VPT, 15, kTmaLog, true>},
                     {nullptr, nullptr, nullptr}}};
 }
-const TmaConfig kTmaPacked[] = {tma_cfg_packed<10>(), tma_cfg_packed<12>(), tma_cfg_packed<14>()};
+const TmaConfig kTmaPacked[] = {tma_cfg_packed<10>(), tma_cfg_packed<12>(), tma_cfg_packed<14>(), tma_cfg_packed<16>()};
 
 // Ordered by capacity (16-byte units per row = 32 * ncw * vpt).
 const TmaConfig kTma[] = {tma_cfg<2, 4>(),          tma_cfg<4, 4>(),          tma_cfg<4, 8>(),
@@ -413,7 +415,7 @@ size_t tma_smem_bytes(int stages, uint32_t slot_bytes, int ncw) {
 // still overlaps this row's normalisation and stores (measured, 8000 rows, TB/s one slot / two:
 // 16 vectors a thread 64 KiB 5.62 / 6.58, 68 KiB 5.77 / 6.43, 80 KiB 6.10 / 5.83, 112 KiB 6.68 /
 // 5.93; the fitted 10 and 12 vectors with one slot 72 KiB 6.28, 80 KiB 6.47, 88 KiB 6.56, 96 KiB
-// 6.68; 128 KiB (one slot only) 6.38).  16-bit rows of 64 - 105 KiB, x kept packed (bf16, ~1 GB
+// 6.68; 128 KiB (one slot only) 6.38).  16-bit rows of 64 - 120 KiB, x kept packed (bf16, ~1 GB
 // per launch, softmax / log softmax TB/s, one slot against two): 64 KiB + 16 B 5.96 / 5.82
 // against 6.28 / 6.50, 80 KiB 6.20 / 5.98 against 6.18 / 6.25, 88 KiB 6.44 / 6.24 against
 // 6.20 / 6.15, 98 KiB 6.30 / 6.36 against 5.85 / 6.10, 105 KiB 6.43 / 6.48 against 6.09 / 6.20

@@ -184,7 +184,7 @@ def test_host_buffers_staged_pipeline():
     (synth.BF16, 32768, V.VARIANT_ONEREAD_SMEM),  # 64 KiB 16-bit rows: one read
     (synth.F32, 16388, V.VARIANT_ONEREAD_SMEM),   # just over 64 KiB of fp32: bulk copy, 16 warps a row
     (synth.BF16, 32776, V.VARIANT_ONEREAD_SMEM),  # just over 64 KiB of bf16: bulk copy, x kept packed
-    (synth.BF16, 53768, V.VARIANT_TWOPASS),       # just over 105 KiB of bf16: past every one-read kernel
+    (synth.BF16, 61448, V.VARIANT_TWOPASS),       # just over 120 KiB of bf16: past every one-read kernel
 ])
 def test_auto_choice_around_64kib(dtype, N, want):
     w = synth.custom("auto64", dtype, 300, N, seed=N % 101, p1=3.0)
@@ -222,10 +222,11 @@ def test_bulk_copy_fp32_rows_of_64_to_128_kib(N):
 
 
 @pytest.mark.parametrize("dtype,N", [(synth.BF16, 32776), (synth.BF16, 40000), (synth.BF16, 45064),
-                                     (synth.BF16, 53760), (synth.F16, 36872)])
-def test_bulk_copy_16bit_rows_of_64_to_105_kib(dtype, N):
-    """16-bit rows of 64 - 105 KiB on the CTA bulk-copy kernel with x kept packed in registers (15
-    consumer warps, 10, 12 or 14 vectors a thread; one row slot above 80 KiB): softmax with the
+                                     (synth.BF16, 53760), (synth.F16, 36872), (synth.BF16, 61440),
+                                     (synth.F16, 57352)])
+def test_bulk_copy_16bit_rows_of_64_to_120_kib(dtype, N):
+    """16-bit rows of 64 - 120 KiB on the CTA bulk-copy kernel with x kept packed in registers (15
+    consumer warps, 10, 12, 14 or 16 vectors a thread; one row slot above 80 KiB): softmax with the
     state, forced and through AUTO, and log softmax, against the fp64 oracle."""
     w = synth.custom("tma16", dtype, 400, N, seed=N % 79, p1=4.0)
     x_host = synth.generate(w)
