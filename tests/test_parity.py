@@ -247,6 +247,37 @@ def test_bulk_copy_16bit_rows_of_64_to_120_kib(dtype, N):
     check_log_values(to_host(ly), oracle.log_softmax_rows(x_host, dtype=odt), dtype, f"packed log {N}")
 
 
+@pytest.mark.parametrize("dtype,N", [(synth.F32, 20480), (synth.F32, 32768), (synth.BF16, 40000),
+                                     (synth.BF16, 61440), (synth.F16, 45064)])
+def test_bulk_copy_long_rows_special_values(dtype, N):
+    """The bulk-copy configurations for rows above 64 KiB (fp32 in 16 warps, one slot; 16-bit kept
+    packed) on special rows: all -inf (y = 0 / -inf), the first half -inf, one huge value, a huge
+    negative row, a uniform row; softmax with the state and log softmax against the oracle."""
+    M = 160
+    rng = np.random.default_rng(N)
+    rows = (rng.standard_normal((M, N)) * 3).astype(np.float32)
+    big = {synth.F32: 1e30, synth.BF16: 3e38, synth.F16: 65504.0}[dtype]
+    rows[0, :] = -np.inf
+    rows[1, :N // 2] = -np.inf
+    rows[2, N - 7] = big
+    rows[3] -= 1e30 if dtype != synth.F16 else 60000.0
+    rows[4, :] = 0.5
+    x_host = rows if dtype == synth.F32 else synth.f32_to_bf16(rows) if dtype == synth.BF16 else synth.f32_to_f16(rows)
+    odt = {synth.F32: oracle.F32, synth.BF16: oracle.BF16, synth.F16: oracle.F16}[dtype]
+    x = to_device(x_host, dtype)
+    m, d, lse = (torch.full((M,), float("nan"), device="cuda") for _ in range(3))
+    y = rwo.softmax_rows_ex(x, m_out=m, d_out=d, lse_out=lse, variant=V.VARIANT_ONEREAD_SMEM)
+    assert rwo.get_status() == rwo.OK and rwo.last_variant() == V.VARIANT_ONEREAD_SMEM
+    y_ref, m_ref, d_ref, lse_ref = oracle.softmax_rows(x_host, dtype=odt)
+    what = f"bulk copy special {N}"
+    check_y(to_host(y), y_ref, dtype, what)
+    check_rowsums(to_host(y), dtype, ~np.isfinite(m_ref), what)
+    check_state(m.cpu().numpy(), d.cpu().numpy(), lse.cpu().numpy(), m_ref, d_ref, lse_ref, what)
+    ly = rwo.log_softmax_rows(x, variant=V.VARIANT_ONEREAD_SMEM)
+    assert rwo.get_status() == rwo.OK
+    check_log_values(to_host(ly), oracle.log_softmax_rows(x_host, dtype=odt), dtype, what + " log")
+
+
 def test_host_buffers_staged_very_long_rows():
     """Rows of 1 MiB through the staging lanes, whose kernels overlap: AUTO must not take the
     split-row kernel (it needs the whole GPU resident) and the result still matches."""
