@@ -374,6 +374,21 @@ constexpr TmaConfig tma_cfg_packed() {
                     {nullptr, nullptr, nullptr}}};
 }
 const TmaConfig kTmaPacked[] = {tma_cfg_packed<10>(), tma_cfg_packed<12>(), tma_cfg_packed<14>(), tma_cfg_packed<16>()};
+template <int VPT, int NCW>
+constexpr TmaConfig tma_cfg_packed_n() {  // 16-bit types, x kept packed
+  return TmaConfig{NCW, VPT,
+                   {{nullptr, k_oneread_tma<BF16, VPT, NCW, kTmaProb, true>, k_oneread_tma<F16, VPT, NCW, kTmaProb, true>},
+                    {nullptr, k_oneread_tma<BF16, VPT, NCW, kTmaLog, true>, k_oneread_tma<F16, VPT, NCW, kTmaLog, true>},
+                    {nullptr, nullptr, nullptr}}};
+}
+// 16-bit rows of 32 - 54 KiB: packed too, 8, 10, 12 or 14 vectors a thread over 8 consumer warps
+// (measured, bf16, ~1 GB per launch, softmax / log softmax TB/s against the unpacked
+// configurations: 32 KiB 6.08 / 6.14 against 6.04 / 5.65, 36 KiB 6.38 / 6.73 against 5.01 /
+// 4.69, 40 KiB 6.81 against 5.34, 44 KiB 6.61 / 6.73 against 5.74 / 5.39, 48 KiB 6.89 against
+// 6.01, 52 KiB 6.82 / 6.37 against 6.37 / 6.00, 54 KiB 6.55 / 6.29 against 6.50 / 6.16; but
+// 24 KiB 6.18 against 6.33, 56 KiB 6.43 against 6.53, 64 KiB 6.16 against 6.86).
+const TmaConfig kTmaPacked8[] = {tma_cfg_packed_n<8, 8>(), tma_cfg_packed_n<10, 8>(), tma_cfg_packed_n<12, 8>(),
+                                 tma_cfg_packed_n<14, 8>()};
 
 // Ordered by capacity (16-byte units per row = 32 * ncw * vpt).
 const TmaConfig kTma[] = {tma_cfg<2, 4>(),          tma_cfg<4, 4>(),          tma_cfg<4, 8>(),
@@ -382,10 +397,16 @@ const TmaConfig kTma[] = {tma_cfg<2, 4>(),          tma_cfg<4, 4>(),          tm
 constexpr int kTmaWide16 = 7;  // index of the 16-vector fp32 configuration
 
 // The smallest configuration that holds the row, except fp32 rows of 64 - 68 KiB, which take the
-// 16-vector one (with two slots: see plan_tma).
-const TmaConfig* pick_tma(int64_t units, int dtype) {
-  if (dtype == 0 && units > 4096 && units <= 4352) return &kTma[kTmaWide16];  // fp32
-  if (dtype != 0 && units > 4096) {
+// 16-vector one (with two slots: see plan_tma), and 16-bit rows of 32 - 54 KiB and above 64 KiB,
+// kept packed.  The state-only mode (which keeps x packed anyway, and sees at most 32 KiB at a
+// time) takes the plain configurations.
+const TmaConfig* pick_tma(int64_t units, int dtype, bool state) {
+  if (dtype == 0 && !state && units > 4096 && units <= 4352) return &kTma[kTmaWide16];  // fp32
+  if (dtype != 0 && !state && units >= 2048 && units <= 3456) {  // 16-bit rows of 32 - 54 KiB
+    for (const TmaConfig& c : kTmaPacked8)
+      if (units <= int64_t(32) * c.ncw * c.vpt) return &c;
+  }
+  if (dtype != 0 && !state && units > 4096) {
     for (const TmaConfig& c : kTmaPacked)
       if (units <= int64_t(32) * c.ncw * c.vpt) return &c;
     return nullptr;
@@ -437,10 +458,10 @@ TmaPlan plan_tma(const RowProblem& p, const DeviceInfo& dev) {
     // state only: the row streams through the slots in chunks (rows below 4 GiB)
     if (row_bytes >= (int64_t(1) << 32)) return plan;
     copy_bytes = kStateChunk;
-    cfg = pick_tma(kStateChunk / 16, p.dtype);
+    cfg = pick_tma(kStateChunk / 16, p.dtype, true);
   } else {
     if (row_bytes > (int64_t(1) << 20)) return plan;
-    cfg = pick_tma(row_bytes / 16, p.dtype);
+    cfg = pick_tma(row_bytes / 16, p.dtype, p.y == nullptr);
   }
   if (!cfg) return plan;
   const uint32_t slot = uint32_t((copy_bytes + kSlotAlign - 1) / kSlotAlign * kSlotAlign);

@@ -221,12 +221,15 @@ def test_bulk_copy_fp32_rows_of_64_to_128_kib(N):
         assert rwo.last_variant() == V.VARIANT_ONEREAD_SMEM
 
 
-@pytest.mark.parametrize("dtype,N", [(synth.BF16, 32776), (synth.BF16, 40000), (synth.BF16, 45064),
+@pytest.mark.parametrize("dtype,N", [(synth.BF16, 16384), (synth.BF16, 18440), (synth.F16, 22536),
+                                     (synth.BF16, 27648),
+                                     (synth.BF16, 32776), (synth.BF16, 40000), (synth.BF16, 45064),
                                      (synth.BF16, 53760), (synth.F16, 36872), (synth.BF16, 61440),
                                      (synth.F16, 57352)])
-def test_bulk_copy_16bit_rows_of_64_to_120_kib(dtype, N):
-    """16-bit rows of 64 - 120 KiB on the CTA bulk-copy kernel with x kept packed in registers (15
-    consumer warps, 10, 12, 14 or 16 vectors a thread; one row slot above 80 KiB): softmax with the
+def test_bulk_copy_16bit_rows_kept_packed(dtype, N):
+    """16-bit rows of 32 - 54 KiB (8 consumer warps, 8 - 14 vectors a thread) and of 64 - 120 KiB (15
+    consumer warps, 10 - 16 vectors; one row slot above 80 KiB) on the CTA bulk-copy kernel with x
+    kept packed in registers, ragged rows among them: softmax with the
     state, forced and through AUTO, and log softmax, against the fp64 oracle."""
     w = synth.custom("tma16", dtype, 400, N, seed=N % 79, p1=4.0)
     x_host = synth.generate(w)
