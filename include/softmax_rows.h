@@ -71,7 +71,8 @@ enum softmax_status {
 /* Kernel variants (softmax_rows_ex).  AUTO picks one from the shape. */
 enum softmax_variant {
   SOFTMAX_VARIANT_AUTO = 0,
-  /* One read: the row is loaded once into registers with 128-bit loads (rows up to 64 KiB). */
+  /* One read: the row is loaded once into registers with 128-bit loads (rows up to 64 KiB; AUTO
+     takes it for fp32 rows up to 64 KiB and 16-bit rows up to 4 KiB). */
   SOFTMAX_VARIANT_ONEREAD_REG = 1,
   /* One read: bulk copies (cp.async.bulk + mbarrier) stage whole rows in shared memory.  Rows
      up to 8 KiB: each warp owns a row at a time and a private ring of row slots that its lane 0

@@ -142,17 +142,20 @@ int run_variant(RowProblem& p, int variant, const DeviceInfo& dev) {
   const int64_t row_bytes = p.N * elem_bytes(p.dtype);
   if (variant == SOFTMAX_VARIANT_AUTO) {
     if (aligned) {
-      // Measured on GB300: warp-per-row bulk-copy kernel for many rows of 2-8 KiB, register
-      // kernel for shorter rows, for few rows, for 8-16 KiB rows and for fp32 rows up to 64 KiB
-      // (fp32, 8192 rows: 20-32 KiB 6.87-6.90 TB/s against 5.69-5.92 on the bulk-copy kernel,
-      // 40 KiB 6.88 against 6.54, 48 KiB 6.88 against 5.96, 56 KiB 6.86 against 5.79 on two
-      // passes, 64 KiB 6.88 against 6.21; 16-bit rows the other way round: 24-32 KiB 4.8-4.9
-      // against 5.9-6.0, bf16 48 KiB 5.08 against 5.86, 64 KiB 3.94 against 6.70), CTA
-      // bulk-copy kernel for the other rows up to 64 KiB.
-      if (row_bytes > 2048 && row_bytes <= 8192 && p.M >= 4 * int64_t(dev.sm_count) &&
+      // Measured on GB300 (~1 GB per launch): the register kernel for every fp32 row up to 64 KiB
+      // (4-8 KiB 6.95 TB/s against 5.78-6.21 on the warp-per-row bulk-copy kernel, 20-32 KiB
+      // 6.87-6.90 against 5.69-5.92 on the CTA bulk-copy kernel, 40 KiB 6.88 against 6.54, 48 KiB
+      // 6.88 against 5.96, 56 KiB 6.86 against 5.79 on two passes, 64 KiB 6.88 against 6.21) and
+      // for 16-bit rows up to 4 KiB (bf16 4 KiB 6.22 against 5.95); the warp-per-row kernel for
+      // many 16-bit rows of 4-8 KiB (bf16 8 KiB 6.52 against 5.84 in registers); the CTA
+      // bulk-copy kernel for longer 16-bit rows (registers there: bf16 12 / 16 KiB 5.32 / 5.48
+      // against 6.50 / 6.63 with x kept packed, 24-32 KiB 4.8-4.9 against 5.9-6.0, 48 KiB 5.08
+      // against 6.89, 64 KiB 3.94 against 6.70).
+      const bool f32 = p.dtype == SOFTMAX_F32;
+      if (!f32 && row_bytes > 4096 && row_bytes <= 8192 && p.M >= 4 * int64_t(dev.sm_count) &&
           oneread_warp_fits(p, dev))
         variant = SOFTMAX_VARIANT_ONEREAD_SMEM;
-      else if ((row_bytes <= 16384 || (p.dtype == SOFTMAX_F32 && row_bytes <= 65536)) && oneread_reg_fits(p, true))
+      else if (row_bytes <= (f32 ? 65536 : 8192) && oneread_reg_fits(p, true))
         variant = SOFTMAX_VARIANT_ONEREAD_REG;
       else if (oneread_tma_fits(p, dev))
         variant = SOFTMAX_VARIANT_ONEREAD_SMEM;
@@ -389,7 +392,7 @@ int softmax_rows_strided(const void* x, int64_t ldx, void* y, int64_t ldy, float
   if (variant == SOFTMAX_VARIANT_AUTO) {  // the kernels that take a pitch and a scale (and, for
                                           // contiguous rows at scale 1, the cluster kernel)
     if (aligned)
-      variant = (row_bytes <= 16384 || (dtype == SOFTMAX_F32 && row_bytes <= 65536)) && oneread_reg_fits(p, true)
+      variant = row_bytes <= (dtype == SOFTMAX_F32 ? 65536 : 8192) && oneread_reg_fits(p, true)
                     ? SOFTMAX_VARIANT_ONEREAD_REG
                 : oneread_tma_fits(p, *dev) || cluster_local_rows(p, *dev) ? SOFTMAX_VARIANT_ONEREAD_SMEM
                                                                            : SOFTMAX_VARIANT_TWOPASS;

@@ -387,6 +387,14 @@ constexpr TmaConfig tma_cfg_packed_n() {  // 16-bit types, x kept packed
 // 4.69, 40 KiB 6.81 against 5.34, 44 KiB 6.61 / 6.73 against 5.74 / 5.39, 48 KiB 6.89 against
 // 6.01, 52 KiB 6.82 / 6.37 against 6.37 / 6.00, 54 KiB 6.55 / 6.29 against 6.50 / 6.16; but
 // 24 KiB 6.18 against 6.33, 56 KiB 6.43 against 6.53, 64 KiB 6.16 against 6.86).
+// 16-bit rows of 8 - 16 KiB: packed, 8 vectors a thread over 4 consumer warps, with the CTAs per
+// SM chosen so that about 84 KiB of rows are in flight per SM (plan_tma) -- more measured slower.
+// bf16, ~1 GB per launch, TB/s at 2 / 3 / 4 CTAs per SM: 10 KiB 4.72 / 5.64 / 6.17, 12 KiB 5.48 /
+// 6.50 / 6.05, 14 KiB 6.17 / 6.29 / 5.91, 16 KiB 6.63 / 6.04 / 5.99, against 4.87 / 5.67 / 6.22 /
+// 5.98 for the unpacked configurations and 5.32 (12 KiB) / 5.48 (16 KiB) for the register kernel.
+const TmaConfig kTmaPacked4 = tma_cfg_packed_n<8, 4>();
+constexpr int64_t kPacked4InFlight = 86016;
+
 const TmaConfig kTmaPacked8[] = {tma_cfg_packed_n<8, 8>(), tma_cfg_packed_n<10, 8>(), tma_cfg_packed_n<12, 8>(),
                                  tma_cfg_packed_n<14, 8>()};
 
@@ -398,10 +406,11 @@ constexpr int kTmaWide16 = 7;  // index of the 16-vector fp32 configuration
 
 // The smallest configuration that holds the row, except fp32 rows of 64 - 68 KiB, which take the
 // 16-vector one (with two slots: see plan_tma), and 16-bit rows of 32 - 54 KiB and above 64 KiB,
-// kept packed.  The state-only mode (which keeps x packed anyway, and sees at most 32 KiB at a
-// time) takes the plain configurations.
+// kept packed, and 16-bit rows of 8 - 16 KiB (packed over 4 consumer warps).  The state-only mode
+// (which keeps x packed anyway, and sees at most 32 KiB at a time) takes the plain configurations.
 const TmaConfig* pick_tma(int64_t units, int dtype, bool state) {
   if (dtype == 0 && !state && units > 4096 && units <= 4352) return &kTma[kTmaWide16];  // fp32
+  if (dtype != 0 && !state && units > 512 && units <= 1024) return &kTmaPacked4;  // 16-bit, 8 - 16 KiB
   if (dtype != 0 && !state && units >= 2048 && units <= 3456) {  // 16-bit rows of 32 - 54 KiB
     for (const TmaConfig& c : kTmaPacked8)
       if (units <= int64_t(32) * c.ncw * c.vpt) return &c;
@@ -476,6 +485,11 @@ TmaPlan plan_tma(const RowProblem& p, const DeviceInfo& dev) {
     int by_threads = dev.max_threads_per_sm / threads;
     int c = by_smem < by_threads ? by_smem : by_threads;
     if (c > 8) c = 8;
+    if (cfg == &kTmaPacked4) {  // about kPacked4InFlight bytes of rows in flight per SM, 2 - 4 CTAs
+      const int64_t want = kPacked4InFlight / (int64_t(stages) * int64_t(slot));
+      const int w = want < 2 ? 2 : want > 4 ? 4 : int(want);
+      if (c > w) c = w;
+    }
     if (c < 1) continue;
     plan.cfg = cfg;
     plan.stages = stages;

@@ -195,6 +195,25 @@ def test_auto_choice_around_64kib(dtype, N, want):
     check_y(to_host(y), y_ref, dtype, f"auto {N}")
 
 
+@pytest.mark.parametrize("dtype,N,want", [
+    (synth.F32, 1536, V.VARIANT_ONEREAD_REG),     # 6 KiB fp32 rows: registers (warp kernel slower)
+    (synth.F32, 2048, V.VARIANT_ONEREAD_REG),     # 8 KiB fp32 rows: registers
+    (synth.BF16, 2048, V.VARIANT_ONEREAD_REG),    # 4 KiB 16-bit rows: registers
+    (synth.BF16, 4096, V.VARIANT_ONEREAD_SMEM),   # 8 KiB 16-bit rows, many of them: a warp per row
+    (synth.BF16, 6144, V.VARIANT_ONEREAD_SMEM),   # 12 KiB 16-bit rows: CTA bulk copy, x kept packed
+    (synth.F16, 8192, V.VARIANT_ONEREAD_SMEM),    # 16 KiB 16-bit rows: the same
+])
+def test_auto_choice_short_rows(dtype, N, want):
+    w = synth.custom("auto-short", dtype, 700, N, seed=N % 103, p1=3.0)
+    x_host = synth.generate(w)
+    x = to_device(x_host, dtype)
+    y = rwo.softmax_rows_ex(x)
+    assert rwo.get_status() == rwo.OK and rwo.last_variant() == want
+    odt = {synth.F32: oracle.F32, synth.BF16: oracle.BF16, synth.F16: oracle.F16}[dtype]
+    y_ref, *_ = oracle.softmax_rows(x_host, dtype=odt)
+    check_y(to_host(y), y_ref, dtype, f"auto short {N}")
+
+
 @pytest.mark.parametrize("dtype,N", [(synth.F32, 8196), (synth.F32, 10244), (synth.F32, 12288),
                                      (synth.F32, 16380), (synth.F32, 16384), (synth.BF16, 16392),
                                      (synth.BF16, 32768)])
@@ -221,13 +240,16 @@ def test_bulk_copy_fp32_rows_of_64_to_128_kib(N):
         assert rwo.last_variant() == V.VARIANT_ONEREAD_SMEM
 
 
-@pytest.mark.parametrize("dtype,N", [(synth.BF16, 16384), (synth.BF16, 18440), (synth.F16, 22536),
+@pytest.mark.parametrize("dtype,N", [(synth.BF16, 4104), (synth.BF16, 5120), (synth.F16, 6152), (synth.BF16, 7176),
+                                     (synth.BF16, 8192),
+                                     (synth.BF16, 16384), (synth.BF16, 18440), (synth.F16, 22536),
                                      (synth.BF16, 27648),
                                      (synth.BF16, 32776), (synth.BF16, 40000), (synth.BF16, 45064),
                                      (synth.BF16, 53760), (synth.F16, 36872), (synth.BF16, 61440),
                                      (synth.F16, 57352)])
 def test_bulk_copy_16bit_rows_kept_packed(dtype, N):
-    """16-bit rows of 32 - 54 KiB (8 consumer warps, 8 - 14 vectors a thread) and of 64 - 120 KiB (15
+    """16-bit rows of 8 - 16 KiB (4 consumer warps, 8 vectors a thread, 2 - 4 CTAs per SM), of 32 -
+    54 KiB (8 consumer warps, 8 - 14 vectors a thread) and of 64 - 120 KiB (15
     consumer warps, 10 - 16 vectors; one row slot above 80 KiB) on the CTA bulk-copy kernel with x
     kept packed in registers, ragged rows among them: softmax with the
     state, forced and through AUTO, and log softmax, against the fp64 oracle."""
