@@ -170,7 +170,10 @@ constexpr uint32_t kWarpSlotAlign = 128;
 constexpr int64_t kWarpMaxRowBytes = 16384;
 
 // Four slots per warp for rows of at most 2 KB, three above; as many warps as ~200 KB of shared
-// memory per SM holds, at most 16 per CTA.
+// memory per SM holds, at most 16 per CTA -- and for rows above 4 KiB CTAs of 4 warps, several per
+// SM (measured, bf16, TB/s with CTAs of 16 / 8 / 4 warps: 8 KiB rows 6.53 / 6.53 / 6.63 -- the
+// 524,288 x 4096 workload 1.298 -> 1.279 ms --, 6 KiB 5.92 / 5.34 / 6.27; but 4 KiB 5.94 / 5.87 /
+// 5.76 and 3 KiB 6.07 / 6.02 / 5.88).
 WarpPlan plan_warp(const RowProblem& p, const DeviceInfo& dev) {
   WarpPlan plan;
   const int64_t row_bytes = p.N * elem_bytes(p.dtype);
@@ -190,7 +193,8 @@ WarpPlan plan_warp(const RowProblem& p, const DeviceInfo& dev) {
   int warps_sm = int(budget / per_warp);
   if (warps_sm > 32) warps_sm = 32;
   if (warps_sm < 1) return plan;
-  int warps = warps_sm < 16 ? warps_sm : 16;
+  const int cta_warps = row_bytes > 4096 ? 4 : 16;
+  int warps = warps_sm < cta_warps ? warps_sm : cta_warps;
   if (size_t(warps) * per_warp > size_t(dev.max_smem_per_block_optin)) warps = int(dev.max_smem_per_block_optin / per_warp);
   if (warps < 1) return plan;
   plan.cfg = cfg;
