@@ -395,6 +395,13 @@ constexpr TmaConfig tma_cfg_packed_n() {  // 16-bit types, x kept packed
 const TmaConfig kTmaPacked4 = tma_cfg_packed_n<8, 4>();
 constexpr int64_t kPacked4InFlight = 86016;
 
+// fp32 rows of 8 - 16 KiB where y is written: 8 vectors a thread over 4 consumer warps, at most 4
+// CTAs per SM (measured on fp32 4096 x 4096: 22.60 against 23.26 us for 4 vectors over 8 warps;
+// 5 - 8 CTAs per SM 22.65 - 22.85).  Only forced or pitched rows reach it: AUTO keeps fp32 rows up
+// to 64 KiB in registers.
+const TmaConfig kTmaF32Short = tma_cfg<8, 4>();
+constexpr int kF32ShortCtas = 4;
+
 const TmaConfig kTmaPacked8[] = {tma_cfg_packed_n<8, 8>(), tma_cfg_packed_n<10, 8>(), tma_cfg_packed_n<12, 8>(),
                                  tma_cfg_packed_n<14, 8>()};
 
@@ -404,11 +411,12 @@ const TmaConfig kTma[] = {tma_cfg<2, 4>(),          tma_cfg<4, 4>(),          tm
                           tma_cfg_wide<12>(),   tma_cfg_wide<16>()};
 constexpr int kTmaWide16 = 7;  // index of the 16-vector fp32 configuration
 
-// The smallest configuration that holds the row, except fp32 rows of 64 - 68 KiB, which take the
-// 16-vector one (with two slots: see plan_tma), and 16-bit rows of 32 - 54 KiB and above 64 KiB,
+// The smallest configuration that holds the row, except fp32 rows of 8 - 16 KiB (4 consumer warps)
+// and of 64 - 68 KiB, which take the 16-vector one (with two slots: see plan_tma), and 16-bit rows of 32 - 54 KiB and above 64 KiB,
 // kept packed, and 16-bit rows of 8 - 16 KiB (packed over 4 consumer warps).  The state-only mode
 // (which keeps x packed anyway, and sees at most 32 KiB at a time) takes the plain configurations.
 const TmaConfig* pick_tma(int64_t units, int dtype, bool state) {
+  if (dtype == 0 && !state && units > 512 && units <= 1024) return &kTmaF32Short;
   if (dtype == 0 && !state && units > 4096 && units <= 4352) return &kTma[kTmaWide16];  // fp32
   if (dtype != 0 && !state && units > 512 && units <= 1024) return &kTmaPacked4;  // 16-bit, 8 - 16 KiB
   if (dtype != 0 && !state && units >= 2048 && units <= 3456) {  // 16-bit rows of 32 - 54 KiB
@@ -485,6 +493,7 @@ TmaPlan plan_tma(const RowProblem& p, const DeviceInfo& dev) {
     int by_threads = dev.max_threads_per_sm / threads;
     int c = by_smem < by_threads ? by_smem : by_threads;
     if (c > 8) c = 8;
+    if (cfg == &kTmaF32Short && c > kF32ShortCtas) c = kF32ShortCtas;
     if (cfg == &kTmaPacked4) {  // about kPacked4InFlight bytes of rows in flight per SM, 2 - 4 CTAs
       const int64_t want = kPacked4InFlight / (int64_t(stages) * int64_t(slot));
       const int w = want < 2 ? 2 : want > 4 ? 4 : int(want);
