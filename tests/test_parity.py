@@ -198,7 +198,8 @@ def test_auto_choice_around_64kib(dtype, N, want):
 @pytest.mark.parametrize("dtype,N,want", [
     (synth.F32, 1536, V.VARIANT_ONEREAD_REG),     # 6 KiB fp32 rows: registers (warp kernel slower)
     (synth.F32, 2048, V.VARIANT_ONEREAD_REG),     # 8 KiB fp32 rows: registers
-    (synth.BF16, 2048, V.VARIANT_ONEREAD_REG),    # 4 KiB 16-bit rows: registers
+    (synth.BF16, 2048, V.VARIANT_ONEREAD_REG),    # 4 KiB 16-bit rows: registers (two warps a row)
+    (synth.F16, 1600, V.VARIANT_ONEREAD_REG),     # 3.1 KiB 16-bit rows: the same, ragged
     (synth.BF16, 4096, V.VARIANT_ONEREAD_SMEM),   # 8 KiB 16-bit rows, many of them: a warp per row
     (synth.BF16, 6144, V.VARIANT_ONEREAD_SMEM),   # 12 KiB 16-bit rows: CTA bulk copy, x kept packed
     (synth.F16, 8192, V.VARIANT_ONEREAD_SMEM),    # 16 KiB 16-bit rows: the same
