@@ -226,16 +226,20 @@ int run_variant(RowProblem& p, int variant, const DeviceInfo& dev) {
   return SOFTMAX_OK;
 }
 
-// Many rows of 128 KiB - 1 MiB: a thread-block cluster per row, its CTAs' segments held on chip
-// (measured against the cluster-row two passes, fp32: 4000 x 128 KiB 169 against 182 us, 2000 x
-// 256 KiB 168 / 193, 1000 x 512 KiB 161 / 196, 600 x 1 MiB 218 / 242; bf16 1000 x 512 KiB 167 /
-// 206; but 8000 x 80 KB 282 / 252, 800 x 768 KB 238 / 221, and fewer rows of 1 MiB, 100: 46.8 /
-// 46.3, 20: 19.6 / 17.4).  Softmax and log softmax (contiguous rows, scale 1).
+// Many rows of 128 - 512 KiB and of 768 KiB - 1 MiB: a thread-block cluster per row, its CTAs'
+// segments held on chip (measured against the cluster-row two passes, fp32: 4000 x 128 KiB 169
+// against 182 us, 2000 x 256 KiB 168 / 193, 1000 x 512 KiB 161 / 196, 600 x 1 MiB 218 / 242; bf16
+// 1000 x 512 KiB 167 / 206; ~1 GB per launch, TB/s: fp32 / bf16 896 KiB 5.83 / 5.48 against 5.54
+// / 5.27, 1 MiB 5.84 / 5.42 against 5.46 / 5.24; but rows of 576 - 768 KiB, over clusters of 8,
+// fp32 / bf16 576 KiB 4.58 / 4.69 against 5.62 / 5.09, 640 KiB 4.92 / 4.98 against 5.77 / 5.28,
+// 768 KiB 5.44 / 5.42 against 5.68 / 5.22; 8000 x 80 KB 282 / 252 us, and fewer rows of 1 MiB,
+// 100: 46.8 / 46.3, 20: 19.6 / 17.4).  Softmax and log softmax (contiguous rows, scale 1).
 bool cluster_local_rows(const RowProblem& p, const DeviceInfo& dev) {
   const int64_t row_bytes = p.N * elem_bytes(p.dtype);
   return row_bytes >= (int64_t(128) << 10) &&
-         (row_bytes <= (int64_t(512) << 10) ? p.M >= int64_t(dev.sm_count)
-                                            : row_bytes <= (int64_t(1) << 20) && p.M >= 256) &&
+         (row_bytes <= (int64_t(512) << 10)
+              ? p.M >= int64_t(dev.sm_count)
+              : row_bytes > (int64_t(768) << 10) && row_bytes <= (int64_t(1) << 20) && p.M >= 256) &&
          clusterrow_onchip_fits(p, dev);
 }
 

@@ -51,6 +51,18 @@ def test_clusterrow_against_oracle(dtype, M, N, variant):
     check_state(m.cpu().numpy(), d.cpu().numpy(), lse.cpu().numpy(), m_ref, d_ref, lse_ref, what)
 
 
+@pytest.mark.parametrize("N,want", [(160_000, rwo.VARIANT_TWOPASS),      # 625 KiB fp32: two passes measured faster
+                                    (230_000, rwo.VARIANT_ONEREAD_SMEM)])  # 898 KiB: held on chip
+def test_auto_between_512_kib_and_1_mib(N, want):
+    w = synth.custom("crow-mid", synth.F32, 300, N, seed=5, p1=3.0)
+    x_host = synth.generate(w)
+    y = rwo.softmax_rows(to_device(x_host))
+    assert rwo.get_status() == rwo.OK and rwo.last_variant() == want
+    pick = [0, 151, 299]
+    y_ref, *_ = oracle.softmax_rows(x_host[pick])
+    check_y(to_host(y)[pick], y_ref, synth.F32, f"auto {N}")
+
+
 def test_auto_holds_many_long_rows_on_chip():
     """Many 1 MiB rows: AUTO takes a thread-block cluster per row with its segments held on chip
     (reported as ONEREAD_SMEM); forced TWOPASS keeps the cluster-row two passes."""
