@@ -81,7 +81,7 @@ enum softmax_variant {
      and frees the slot at once; longer
      rows (16-byte aligned, up to 1 MiB): a thread-block cluster of 2-8 CTAs per row, each CTA's
      segment held in shared and tensor memory until the row's state, merged over distributed
-     shared memory, is known.  AUTO takes the last for many rows of 128 KiB - 1 MiB. */
+     shared memory, is known.  AUTO takes the last for many rows of 128 - 512 KiB and 768 KiB - 1 MiB. */
   SOFTMAX_VARIANT_ONEREAD_SMEM = 2,
   /* Two passes over global memory: online fold with 128-bit loads, then re-read and normalise
      (any N; the re-read is served from L2 while the row is still resident).  Aligned rows above
@@ -180,7 +180,7 @@ int softmax_rows_strided(const void* x, int64_t ldx, void* y, int64_t ldy, float
  * log(sum_exp), the step before the cross-entropy loss).  Computed as (x_j - m) - ln d from the
  * online state, so x is read once as for softmax.  An all -inf row gives y = -inf everywhere
  * (log 0).  Arguments, layout, outputs and errors as softmax_rows_ex; `variant` may be AUTO,
- * ONEREAD_REG, ONEREAD_SMEM (the bulk-copy kernels, and for many rows of 128 KiB - 1 MiB a
+ * ONEREAD_REG, ONEREAD_SMEM (the bulk-copy kernels, and for many rows of 128 - 512 KiB and 768 KiB - 1 MiB a
  * thread-block cluster per row held on chip) or TWOPASS.  SPLITROW gives
  * SOFTMAX_ERR_UNSUPPORTED; AUTO never picks it (a single very long row runs TWOPASS).
  */
