@@ -484,8 +484,11 @@ TmaPlan plan_tma(const RowProblem& p, const DeviceInfo& dev) {
   const uint32_t slot = uint32_t((copy_bytes + kSlotAlign - 1) / kSlotAlign * kSlotAlign);
   const size_t per_cta_reserved = 1024;  // the runtime's per-block reservation
   const int threads = (cfg->ncw + 1) * 32;
-  // one slot for fp32 rows above 68 KiB and 16-bit rows above 80 KiB
-  const int first = copy_bytes > (p.dtype == 0 ? 69632 : 81920) ? 1 : 2;
+  // one slot for fp32 rows above 68 KiB and 16-bit rows above 80 KiB, and for 16-bit rows of 32 KiB
+  // on the packed 8-warp configuration, which fits two CTAs per SM (bf16, ~1 GB per launch:
+  // softmax / log softmax 6.61 / 6.57 TB/s against 6.01 / 6.12 with two slots; from 34 KiB on,
+  // one CTA per SM, one slot measured 5.1 - 5.9 against 6.2 - 6.9)
+  const int first = copy_bytes > (p.dtype == 0 ? 69632 : 81920) || cfg == &kTmaPacked8[0] ? 1 : 2;
   for (int stages = first; stages >= 1; --stages) {
     const size_t smem = tma_smem_bytes(stages, slot, cfg->ncw);
     if (smem > size_t(dev.max_smem_per_block_optin)) continue;
