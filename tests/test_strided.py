@@ -31,6 +31,10 @@ CASES = [
     (synth.BF16, 64, 32768, 33000, 104, 32768, 0.5),                   # long rows: bulk-copy kernel
     (synth.F16, 500, 2048, 2056, 8, 2048, 1.0 / np.sqrt(64.0)),
     (synth.F32, 40, 20000, 20004, 4, 20000, 2.0),                      # beyond the register kernel
+    # 16-bit rows on the bulk-copy kernel with x kept packed (12, 40 and 78 KiB rows)
+    (synth.BF16, 120, 6144, 6200, 8, 6144, 0.7),
+    (synth.F16, 100, 20000, 20008, 8, 20000, 1.7),
+    (synth.BF16, 80, 40000, 40016, 16, 40008, 0.3),
 ]
 
 
